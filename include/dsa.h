@@ -1,0 +1,183 @@
+/*
+ * dsa.h -- C ABI of libdsa: DeepSeek Sparse Attention with IndexShare reuse on one GPU.
+ *
+ * The library computes the three stages of a DSA layer and the IndexShare schedule that
+ * ties layers together:
+ *   - the lightning indexer scores every preceding key of a query
+ *     (IndexShare explainer, "Why The Indexer Becomes Expensive"; the score formula
+ *      I[t,s] = sum_h w[t,h] * ReLU(q_I[t,h] . k_I[s]) is the project's statement of it);
+ *   - a per-query top-k keeps the k best positions, ties going to the lower position
+ *     (same section; k = 2048 in the GLM-5.2 article, "Where the DSA indexer becomes
+ *      expensive");
+ *   - main attention runs over the selected rows only (same sections);
+ *   - a full (F) layer runs indexer + top-k and keeps the positions; a shared (S) layer
+ *     reuses the most recent F layer's positions with its own Q/KV and outputs
+ *     (explainer, "How IndexShare Works"; article, "What IndexShare reuses"; IndexCache
+ *      notes, section 2: the first layer is always F);
+ *   - the overlap of two layers' selections (explainer, "Why Reusing Indices Can Work").
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller, unless a parameter says
+ *     "host".  The library allocates no device memory; scratch space is the caller's
+ *     workspace `ws` of `ws_bytes` bytes (see dsa_workspace_size).  The workspace must be
+ *     zero-filled once before first use (its first bytes hold the device flag word).
+ *   - `stream` is a cudaStream_t (NULL: the legacy default stream).  Every call only
+ *     enqueues work on it, except topk_overlap (returns a host mean) and
+ *     dsa_read_device_flags, which synchronise that stream.
+ *   - Arguments are validated on the host before anything is launched; a rejected call
+ *     launches nothing and returns a status other than DSA_OK.  dsa_last_error() gives
+ *     a message for the last failure of the calling thread.
+ *   - Faults found in the data on the device (an index outside [-1, S), a NaN score)
+ *     never trap: the element is skipped (attention) or ranked lowest (top-k), and a bit
+ *     is OR-ed into the device flag word, read by dsa_read_device_flags.
+ *   - Tensors are dense and row-major in the shapes given; "[B,T,H,d]" means the last
+ *     index varies fastest.  Query row i of every sequence sits at absolute position
+ *     q_pos0 + i and sees the keys s < q_pos0 + i + diag (clipped to [0, S)).  diag = 0 is
+ *     the strictly-preceding rule of the pages; diag = 1 also admits the query's own key.
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, inconsistent shapes      */
+  DSA_ERR_UNSUPPORTED = 2,  /* a shape the kernels are not built for                     */
+  DSA_ERR_MISALIGNED = 3,   /* a pointer or row stride breaks the 16-byte rule            */
+  DSA_ERR_WORKSPACE = 4,    /* workspace missing or smaller than needed                  */
+  DSA_ERR_SCHEDULE = 5,     /* schedule not 'F'/'S' per layer, or not starting with 'F'  */
+  DSA_ERR_CUDA = 6,         /* a CUDA runtime call or kernel launch failed               */
+  DSA_ERR_DEVICE_FLAG = 7,  /* reserved: returned by callers that treat flags as errors  */
+  DSA_ERR_TIMEOUT = 8       /* a bounded device wait gave up                             */
+} dsa_status;
+
+typedef enum { DSA_BF16 = 0, DSA_E4M3 = 1 } dsa_dtype;
+
+/* Bits of the device flag word. */
+#define DSA_FLAG_BAD_INDEX 0x1u /* attention met an index outside [-1, S): entry skipped  */
+#define DSA_FLAG_NAN_SCORE 0x2u /* top-k met a NaN score: ranked below every number       */
+#define DSA_FLAG_UNSORTED 0x4u  /* topk_overlap met a row that is not ascending           */
+#define DSA_FLAG_TIMEOUT 0x8u   /* a bounded device wait gave up                          */
+
+/* Indexer operands of one layer (lightning indexer, "Why The Indexer Becomes Expensive").
+ *   q       [B,T,H_I,d_I]  bf16 or e4m3 codes                      (16-byte aligned)
+ *   q_scale [B,T]  fp32 per-token dequantisation scale; required for E4M3, NULL for BF16
+ *   w       [B,T,H_I] fp32 head weights (any sign)
+ *   k       [B,S,d_I]  same dtype as q                              (16-byte aligned)
+ *   k_scale [B,S]  fp32; required for E4M3, NULL for BF16
+ * A dequantised operand is scale * code.  Supported: (H_I, d_I) in {(4,64), (64,128)}
+ * for BF16 and {(64,128)} for E4M3. */
+typedef struct {
+  int32_t B, T, S, H_I, d_I;
+  dsa_dtype dtype;
+  const void* q;
+  const float* q_scale;
+  const float* w;
+  const void* k;
+  const float* k_scale;
+  int64_t q_pos0;
+  int32_t diag;
+} dsa_indexer_args;
+
+/* Main-attention operands of one layer, multi-query form: every query head attends over
+ * the same gathered key/value rows (MLA run over its shared latent KV).
+ *   q  [B,T,H,d_qk] bf16                                          (16-byte aligned)
+ *   k  [B,S,k_ld] bf16; key row j of sequence b at (b*S + j)*k_ld, first d_qk used
+ *   v  [B,S,v_ld] bf16; first d_v columns used.  v may equal k (latent KV: the value is
+ *      the first d_v columns of the latent row, so each gathered row serves both).
+ * out = softmax(scale * q K[idx]^T) V[idx] per head.  Supported (H, d_qk, d_v):
+ * (8 or 16, 64, 64) and (64, 576, 512); k_ld and v_ld multiples of 8. */
+typedef struct {
+  int32_t B, T, S, H, d_qk, d_v;
+  float scale;
+  const void* q;
+  const void* k;
+  int64_t k_ld;
+  const void* v;
+  int64_t v_ld;
+} dsa_attn_args;
+
+typedef enum { DSA_TOPK_FROM_SCORES = 0, DSA_TOPK_FROM_INDEXER = 1 } dsa_topk_kind;
+
+/* Source of a top-k: a materialised fp32 score buffer [B,T,ld] (ld >= S; only the visible
+ * prefix of each row is read), or the indexer operands (scores are produced on the fly and
+ * never stored as a full matrix). */
+typedef struct {
+  dsa_topk_kind kind;
+  const float* scores;
+  int64_t ld;
+  const dsa_indexer_args* ix;
+} dsa_topk_src;
+
+/* One layer of an IndexShare group.  `ix` is read for 'F' layers only. */
+typedef struct {
+  dsa_indexer_args ix;
+  dsa_attn_args at;
+  void* out;  /* [B,T,H,d_v] bf16 */
+  float* lse; /* [B,T,H] fp32 natural-log softmax normaliser, or NULL */
+} dsa_layer;
+
+/* Workspace bytes preferred by dsa_topk(FROM_INDEXER) and indexshare_group_forward for
+ * this indexer shape (a smaller workspace also works down to DSA_WS_MIN plus one score row
+ * chunk; calls that need no scratch take DSA_WS_MIN). */
+#define DSA_WS_MIN ((size_t)256)
+size_t dsa_workspace_size(const dsa_indexer_args* ix, int32_t k);
+
+/* Indexer scores, materialised: scores[b,i,s] (row stride ld >= S, fp32) =
+ * sum_h w[b,i,h] * ReLU(q[b,i,h] . k[b,s]) for visible s, -inf for the rest of [0, S). */
+dsa_status dsa_indexer_scores(const dsa_indexer_args* ix, float* scores, int64_t ld, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/* Top-k per query row (IndexShare explainer, "How IndexShare Works": the full layer
+ * "performs the top-k operation").  idx [B,T,k] int32 receives, for each row, the k
+ * visible positions of largest score (equal scores: lower position first), listed in
+ * ascending position order; rows with n < k visible keys list all n and pad with -1.
+ * B, T, S, q_pos0, diag describe the rows; with FROM_INDEXER they must match src->ix.
+ * 1 <= k <= 4096. */
+dsa_status dsa_topk(const dsa_topk_src* src, int32_t B, int32_t T, int32_t S, int64_t q_pos0,
+                    int32_t diag, int32_t k, int32_t* idx, void* ws, size_t ws_bytes,
+                    void* stream);
+
+/* Sparse attention over selected rows (explainer, "Why The Indexer Becomes Expensive":
+ * "the main attention mechanism operates only on this smaller subset").
+ * idx [B,T,k] int32, entries in [-1, S); -1 is skipped.  out [B,T,H,d_v] bf16;
+ * lse [B,T,H] fp32 (natural log) or NULL.  A row with no valid entry gets out = 0,
+ * lse = -inf. */
+dsa_status dsa_sparse_attn(const dsa_attn_args* at, const int32_t* idx, int32_t k, void* out,
+                           float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* IndexShare group forward ("How IndexShare Works"; "What IndexShare reuses").
+ * schedule: one 'F' or 'S' per layer, starting with 'F' (e.g. "FSSS").  For each 'F'
+ * layer number f (0-based count of F layers so far), indexer + top-k write idx_bufs[f]
+ * ([B,T,k] int32, caller-owned).  Every layer then runs dsa_sparse_attn with its own
+ * operands over the most recent F layer's buffer.  All layers share B, T, S. */
+dsa_status indexshare_group_forward(const dsa_layer* layers, int32_t n_layers,
+                                    const char* schedule, int32_t k, int32_t* const* idx_bufs,
+                                    void* ws, size_t ws_bytes, void* stream);
+
+/* Overlap of two index buffers a, b [rows,k] (rows as written by dsa_topk: ascending valid
+ * entries, then -1 padding): per_row[r] = |A_r and B_r| / |A_r| over valid entries (1 when
+ * A_r is empty), fp32 device array or NULL; *mean_out (host) = mean over rows in double.
+ * Synchronises `stream`.  Explainer, "Why Reusing Indices Can Work" (adjacent-layer
+ * overlap). */
+dsa_status topk_overlap(const int32_t* a, const int32_t* b, int32_t rows, int32_t k,
+                        float* per_row, double* mean_out, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* Reads the device flag word of a workspace into *flags_out (host) and clears it.
+ * Synchronises `stream`. */
+dsa_status dsa_read_device_flags(void* ws, uint32_t* flags_out, void* stream);
+
+const char* dsa_status_string(dsa_status s);
+const char* dsa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_H */

@@ -1,0 +1,306 @@
+"""DeepSeek Sparse Attention with IndexShare reuse on one GB300 (sm_103a).
+
+Thin ctypes binding over ``libdsa.so`` (C ABI in ``include/dsa.h``).  The functions here
+only marshal torch tensors into the C structs (device pointers, sizes, the current CUDA
+stream) and allocate outputs; every step of the computation runs in the library's CUDA
+kernels.  There is no CPU fallback: if the library is missing the first call raises.
+
+Calls (same names as the C ABI):
+  indexer_scores(ix)                      -> fp32 scores [B,T,S]
+  dsa_topk(k, ix=... | scores=...)        -> int32 idx [B,T,k]
+  dsa_sparse_attn(at, idx)                -> (out [B,T,H,d_v] bf16, lse [B,T,H] fp32)
+  indexshare_group_forward(layers, schedule, k) -> (outs, lses, idx_bufs)
+  topk_overlap(a, b)                      -> (per_row fp32, mean float)
+Operand dicts use the keys produced by ``synth``: an indexer dict holds q, w, k, q_scale,
+k_scale, q_pos0, diag; an attention dict holds q, k, v (None: latent KV), d_v, scale.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdsa.so")
+
+DSA_BF16, DSA_E4M3 = 0, 1
+TOPK_FROM_SCORES, TOPK_FROM_INDEXER = 0, 1
+FLAG_BAD_INDEX, FLAG_NAN_SCORE, FLAG_UNSORTED, FLAG_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+WS_MIN = 256
+
+_c = ctypes
+_P = _c.c_void_p
+
+
+class IndexerArgs(_c.Structure):
+    _fields_ = [("B", _c.c_int32), ("T", _c.c_int32), ("S", _c.c_int32), ("H_I", _c.c_int32),
+                ("d_I", _c.c_int32), ("dtype", _c.c_int), ("q", _P), ("q_scale", _P), ("w", _P),
+                ("k", _P), ("k_scale", _P), ("q_pos0", _c.c_int64), ("diag", _c.c_int32)]
+
+
+class AttnArgs(_c.Structure):
+    _fields_ = [("B", _c.c_int32), ("T", _c.c_int32), ("S", _c.c_int32), ("H", _c.c_int32),
+                ("d_qk", _c.c_int32), ("d_v", _c.c_int32), ("scale", _c.c_float), ("q", _P),
+                ("k", _P), ("k_ld", _c.c_int64), ("v", _P), ("v_ld", _c.c_int64)]
+
+
+class TopkSrc(_c.Structure):
+    _fields_ = [("kind", _c.c_int), ("scores", _P), ("ld", _c.c_int64),
+                ("ix", _c.POINTER(IndexerArgs))]
+
+
+class Layer(_c.Structure):
+    _fields_ = [("ix", IndexerArgs), ("at", AttnArgs), ("out", _P), ("lse", _P)]
+
+
+class DsaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{status_string(status)}: {msg}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libdsa.so (built by ``build.build()``).  Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"libdsa.so not found at {path}: run "
+                                   "long_context_sparse_tcgen05_gb300.build.build() first")
+            lib = _c.CDLL(path)
+            S = _c.c_int
+            lib.dsa_workspace_size.restype = _c.c_size_t
+            lib.dsa_workspace_size.argtypes = [_c.POINTER(IndexerArgs), _c.c_int32]
+            lib.dsa_indexer_scores.restype = S
+            lib.dsa_indexer_scores.argtypes = [_c.POINTER(IndexerArgs), _P, _c.c_int64, _P,
+                                               _c.c_size_t, _P]
+            lib.dsa_topk.restype = S
+            lib.dsa_topk.argtypes = [_c.POINTER(TopkSrc), _c.c_int32, _c.c_int32, _c.c_int32,
+                                     _c.c_int64, _c.c_int32, _c.c_int32, _P, _P, _c.c_size_t, _P]
+            lib.dsa_sparse_attn.restype = S
+            lib.dsa_sparse_attn.argtypes = [_c.POINTER(AttnArgs), _P, _c.c_int32, _P, _P, _P,
+                                            _c.c_size_t, _P]
+            lib.indexshare_group_forward.restype = S
+            lib.indexshare_group_forward.argtypes = [_c.POINTER(Layer), _c.c_int32, _c.c_char_p,
+                                                     _c.c_int32, _c.POINTER(_P), _P, _c.c_size_t,
+                                                     _P]
+            lib.topk_overlap.restype = S
+            lib.topk_overlap.argtypes = [_P, _P, _c.c_int32, _c.c_int32, _P,
+                                         _c.POINTER(_c.c_double), _P, _c.c_size_t, _P]
+            lib.dsa_read_device_flags.restype = S
+            lib.dsa_read_device_flags.argtypes = [_P, _c.POINTER(_c.c_uint32), _P]
+            lib.dsa_status_string.restype = _c.c_char_p
+            lib.dsa_status_string.argtypes = [S]
+            lib.dsa_last_error.restype = _c.c_char_p
+            lib.dsa_last_error.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def status_string(s: int) -> str:
+    return load_library().dsa_status_string(s).decode()
+
+
+def _check(status: int):
+    if status != 0:
+        raise DsaError(status, load_library().dsa_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else _c.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return _c.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+# --- workspace ----------------------------------------------------------------------
+
+_ws = {}
+
+
+def workspace(nbytes: int = WS_MIN, device=None) -> torch.Tensor:
+    """A zero-initialised uint8 workspace on `device` of at least `nbytes` (cached, grown)."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    t = _ws.get(dev)
+    if t is None or t.numel() < nbytes:
+        if t is not None:
+            torch.cuda.current_stream(dev).synchronize()
+        t = torch.zeros(max(nbytes, WS_MIN), dtype=torch.uint8, device=dev)
+        _ws[dev] = t
+    return t
+
+
+def release_workspace():
+    _ws.clear()
+
+
+# --- struct builders ----------------------------------------------------------------
+
+def indexer_struct(ix: dict) -> IndexerArgs:
+    q, k, w = ix["q"], ix["k"], ix["w"]
+    B, T, HI, DI = q.shape
+    fp8 = q.dtype == torch.float8_e4m3fn
+    for t in (q, k, w):
+        assert t.is_cuda and t.is_contiguous()
+    qs, ks = ix.get("q_scale"), ix.get("k_scale")
+    return IndexerArgs(B, T, k.shape[1], HI, DI, DSA_E4M3 if fp8 else DSA_BF16, q.data_ptr(),
+                       qs.data_ptr() if (fp8 and qs is not None) else None, w.data_ptr(),
+                       k.data_ptr(), ks.data_ptr() if (fp8 and ks is not None) else None,
+                       int(ix.get("q_pos0", 0)), int(ix.get("diag", 0)))
+
+
+def attn_struct(at: dict) -> AttnArgs:
+    q, k = at["q"], at["k"]
+    v = at.get("v")
+    B, T, H, DQK = q.shape
+    for t in (q, k) + ((v,) if v is not None else ()):
+        assert t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16
+    vv = k if v is None else v
+    return AttnArgs(B, T, k.shape[1], H, DQK, int(at["d_v"]), float(at["scale"]), q.data_ptr(),
+                    k.data_ptr(), k.shape[2], vv.data_ptr(), vv.shape[2])
+
+
+# --- calls --------------------------------------------------------------------------
+
+def workspace_size(ix: dict | None, k: int) -> int:
+    if ix is None:
+        return WS_MIN
+    a = indexer_struct(ix)
+    return int(load_library().dsa_workspace_size(_c.byref(a), k))
+
+
+def indexer_scores(ix: dict, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Materialised indexer scores [B,T,S] fp32 (-inf where not visible)."""
+    lib = load_library()
+    a = indexer_struct(ix)
+    if out is None:
+        out = torch.empty((a.B, a.T, a.S), dtype=torch.float32, device=ix["q"].device)
+    ws = workspace(WS_MIN, out.device)
+    _check(lib.dsa_indexer_scores(_c.byref(a), _ptr(out), out.shape[-1], _ptr(ws), ws.numel(),
+                                  _stream()))
+    return out
+
+
+def dsa_topk(k: int, *, ix: dict | None = None, scores: torch.Tensor | None = None,
+             q_pos0: int = 0, diag: int = 0, idx: torch.Tensor | None = None,
+             ws: torch.Tensor | None = None) -> torch.Tensor:
+    """Top-k positions [B,T,k] int32 from indexer operands (fused path) or a score buffer."""
+    lib = load_library()
+    if ix is not None:
+        a = indexer_struct(ix)
+        src = TopkSrc(TOPK_FROM_INDEXER, None, 0, _c.pointer(a))
+        B, T, S, q_pos0, diag = a.B, a.T, a.S, a.q_pos0, a.diag
+        dev = ix["q"].device
+        need = int(lib.dsa_workspace_size(_c.byref(a), k))
+    else:
+        assert scores is not None and scores.dtype == torch.float32 and scores.is_cuda
+        sc = scores if scores.dim() == 3 else scores[None]
+        B, T, S = sc.shape
+        assert sc.stride(2) == 1 and sc.stride(0) == T * sc.stride(1)
+        src = TopkSrc(TOPK_FROM_SCORES, sc.data_ptr(), sc.stride(1), None)
+        dev = scores.device
+        need = WS_MIN
+    if idx is None:
+        idx = torch.empty((B, T, k), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = workspace(need, dev)
+    _check(lib.dsa_topk(_c.byref(src), B, T, S, q_pos0, diag, k, _ptr(idx), _ptr(ws), ws.numel(),
+                        _stream()))
+    return idx
+
+
+def dsa_sparse_attn(at: dict, idx: torch.Tensor, out: torch.Tensor | None = None,
+                    lse: torch.Tensor | bool | None = True):
+    """(out [B,T,H,d_v] bf16, lse [B,T,H] fp32 or None)."""
+    lib = load_library()
+    a = attn_struct(at)
+    dev = at["q"].device
+    assert idx.dtype == torch.int32 and idx.is_contiguous() and idx.shape[:2] == (a.B, a.T)
+    if out is None:
+        out = torch.empty((a.B, a.T, a.H, a.d_v), dtype=torch.bfloat16, device=dev)
+    if lse is True:
+        lse = torch.empty((a.B, a.T, a.H), dtype=torch.float32, device=dev)
+    elif lse is False:
+        lse = None
+    ws = workspace(WS_MIN, dev)
+    _check(lib.dsa_sparse_attn(_c.byref(a), _ptr(idx), idx.shape[-1], _ptr(out), _ptr(lse),
+                               _ptr(ws), ws.numel(), _stream()))
+    return out, lse
+
+
+def indexshare_group_forward(layers, schedule: str, k: int, outs=None, lses=None, idx_bufs=None,
+                             with_lse: bool = True):
+    """Run an F/S schedule over `layers` (dicts with 'ix' (F layers) and 'at').
+
+    Returns (outs, lses, idx_bufs): per-layer outputs and LSEs, one idx buffer per F layer."""
+    lib = load_library()
+    n = len(layers)
+    arr = (Layer * n)()
+    at0 = layers[0]["at"]
+    B, T = at0["q"].shape[:2]
+    dev = at0["q"].device
+    n_full = schedule.count("F")
+    if idx_bufs is None:
+        idx_bufs = [torch.empty((B, T, k), dtype=torch.int32, device=dev) for _ in range(n_full)]
+    if outs is None:
+        outs = []
+        for l in layers:
+            q = l["at"]["q"]
+            outs.append(torch.empty(q.shape[:3] + (int(l["at"]["d_v"]),), dtype=torch.bfloat16, device=dev))
+    if lses is None:
+        lses = [torch.empty(l["at"]["q"].shape[:3], dtype=torch.float32, device=dev) if with_lse else None
+                for l in layers]
+    need = WS_MIN
+    for i, l in enumerate(layers):
+        if i < len(schedule) and schedule[i] == "F" and l.get("ix") is not None:
+            arr[i].ix = indexer_struct(l["ix"])
+            need = max(need, int(lib.dsa_workspace_size(_c.byref(arr[i].ix), k)))
+        arr[i].at = attn_struct(l["at"])
+        arr[i].out = outs[i].data_ptr()
+        arr[i].lse = lses[i].data_ptr() if lses[i] is not None else None
+    bufs = (_P * max(1, n_full))(*[b.data_ptr() for b in idx_bufs])
+    ws = workspace(need, dev)
+    _check(lib.indexshare_group_forward(arr, n, schedule.encode(), k, bufs, _ptr(ws), ws.numel(),
+                                        _stream()))
+    return outs, lses, idx_bufs
+
+
+def topk_overlap(a: torch.Tensor, b: torch.Tensor, per_row: torch.Tensor | bool = True):
+    """(per_row fp32 [rows] or None, mean) of |A and B| / |A| per row.  Synchronises."""
+    lib = load_library()
+    k = a.shape[-1]
+    rows = a.numel() // k
+    assert a.shape == b.shape and a.dtype == b.dtype == torch.int32
+    a2, b2 = a.contiguous(), b.contiguous()
+    if per_row is True:
+        per_row = torch.empty(rows, dtype=torch.float32, device=a.device)
+    elif per_row is False:
+        per_row = None
+    ws = workspace(WS_MIN + (0 if per_row is not None else rows * 4), a.device)
+    mean = _c.c_double()
+    _check(lib.topk_overlap(_ptr(a2), _ptr(b2), rows, k, _ptr(per_row), _c.byref(mean), _ptr(ws),
+                            ws.numel(), _stream()))
+    return per_row, mean.value
+
+
+def read_device_flags(device=None) -> int:
+    """Flag word of the cached workspace (cleared by the read).  Synchronises."""
+    lib = load_library()
+    ws = workspace(WS_MIN, device)
+    v = _c.c_uint32()
+    _check(lib.dsa_read_device_flags(_ptr(ws), _c.byref(v), _stream()))
+    return int(v.value)
+
+
+__all__ = [
+    "indexer_scores", "dsa_topk", "dsa_sparse_attn", "indexshare_group_forward", "topk_overlap",
+    "read_device_flags", "workspace", "workspace_size", "load_library", "DsaError",
+    "IndexerArgs", "AttnArgs", "TopkSrc", "Layer",
+]

@@ -1,0 +1,285 @@
+// Host side of libdsa: argument validation, workspace planning, launch sequencing and the
+// IndexShare schedule walk.  No device memory is allocated here; every buffer belongs to
+// the caller.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "dsa_internal.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+dsa_status fail(dsa_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+dsa_status fail(dsa_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+dsa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+uint32_t* ws_flags(void* ws) { return reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + dsa::kWsFlags); }
+
+dsa_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws) return fail(DSA_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned16(ws)) return fail(DSA_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+  if (ws_bytes < need) return fail(DSA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  return DSA_OK;
+}
+
+dsa_status check_indexer(const dsa_indexer_args* ix) {
+  if (!ix) return fail(DSA_ERR_INVALID_ARG, "indexer args are NULL");
+  if (ix->B <= 0 || ix->T <= 0 || ix->S <= 0 || ix->H_I <= 0 || ix->d_I <= 0)
+    return fail(DSA_ERR_INVALID_ARG, "indexer sizes must be positive (B=%d T=%d S=%d H_I=%d d_I=%d)",
+                ix->B, ix->T, ix->S, ix->H_I, ix->d_I);
+  if (ix->dtype != DSA_BF16 && ix->dtype != DSA_E4M3) return fail(DSA_ERR_INVALID_ARG, "unknown indexer dtype %d", (int)ix->dtype);
+  const bool ok_shape = (ix->H_I == 64 && ix->d_I == 128) || (ix->dtype == DSA_BF16 && ix->H_I == 4 && ix->d_I == 64);
+  if (!ok_shape) return fail(DSA_ERR_UNSUPPORTED, "indexer shape H_I=%d d_I=%d (%s) is not supported", ix->H_I, ix->d_I,
+                             ix->dtype == DSA_E4M3 ? "e4m3" : "bf16");
+  if (!ix->q || !ix->w || !ix->k) return fail(DSA_ERR_INVALID_ARG, "indexer q, w and k must be non-NULL");
+  if (ix->dtype == DSA_E4M3 && (!ix->q_scale || !ix->k_scale))
+    return fail(DSA_ERR_INVALID_ARG, "e4m3 indexer operands need q_scale and k_scale");
+  if (!aligned16(ix->q) || !aligned16(ix->k)) return fail(DSA_ERR_MISALIGNED, "indexer q and k must be 16-byte aligned");
+  if (!aligned16(ix->w)) return fail(DSA_ERR_MISALIGNED, "indexer w must be 16-byte aligned");
+  if (ix->diag < 0 || ix->diag > 1) return fail(DSA_ERR_INVALID_ARG, "diag must be 0 or 1");
+  if (ix->q_pos0 < 0) return fail(DSA_ERR_INVALID_ARG, "q_pos0 must be >= 0");
+  return DSA_OK;
+}
+
+dsa_status check_attn(const dsa_attn_args* at) {
+  if (!at) return fail(DSA_ERR_INVALID_ARG, "attention args are NULL");
+  if (at->B <= 0 || at->T <= 0 || at->S <= 0 || at->H <= 0 || at->d_qk <= 0 || at->d_v <= 0)
+    return fail(DSA_ERR_INVALID_ARG, "attention sizes must be positive");
+  const bool ok = (at->H == 64 && at->d_qk == 576 && at->d_v == 512) ||
+                  (at->H <= 16 && at->d_qk == 64 && at->d_v == 64);
+  if (!ok) return fail(DSA_ERR_UNSUPPORTED, "attention shape H=%d d_qk=%d d_v=%d is not supported", at->H, at->d_qk, at->d_v);
+  if (!at->q || !at->k || !at->v) return fail(DSA_ERR_INVALID_ARG, "attention q, k and v must be non-NULL");
+  if (!aligned16(at->q) || !aligned16(at->k) || !aligned16(at->v)) return fail(DSA_ERR_MISALIGNED, "attention q, k, v must be 16-byte aligned");
+  if (at->k_ld < at->d_qk || at->v_ld < at->d_v || at->k_ld % 8 || at->v_ld % 8)
+    return fail(DSA_ERR_MISALIGNED, "k_ld/v_ld must cover d_qk/d_v and be multiples of 8 elements");
+  if (!(at->scale > 0.f)) return fail(DSA_ERR_INVALID_ARG, "scale must be positive");
+  return DSA_OK;
+}
+
+constexpr int kMaxK = 4096;
+
+// Query rows per chunk of the materialised score buffer that `ws_bytes` can hold.
+int64_t score_chunk_rows(const dsa_indexer_args* ix, size_t ws_bytes) {
+  if (ws_bytes <= dsa::kWsScratch) return 0;
+  const int64_t per_row = (int64_t)ix->B * ix->S * 4;
+  int64_t rows = (int64_t)(ws_bytes - dsa::kWsScratch) / per_row;
+  return rows > ix->T ? ix->T : rows;
+}
+
+dsa_status run_indexer_topk(const dsa_indexer_args* ix, int32_t k, int32_t* idx, void* ws, size_t ws_bytes,
+                            cudaStream_t st) {
+  const int64_t chunk = score_chunk_rows(ix, ws_bytes);
+  if (chunk < 1) return fail(DSA_ERR_WORKSPACE, "workspace too small for one row of indexer scores (%zu bytes)", ws_bytes);
+  float* sc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + dsa::kWsScratch);
+  for (int64_t t0 = 0; t0 < ix->T; t0 += chunk) {
+    const int Tc = (int)((ix->T - t0) < chunk ? (ix->T - t0) : chunk);
+    dsa::IndexerLaunch L{};
+    L.B = ix->B; L.T = ix->T; L.S = ix->S; L.HI = ix->H_I; L.DI = ix->d_I;
+    L.fp8 = ix->dtype == DSA_E4M3;
+    L.q = ix->q; L.q_scale = ix->q_scale; L.w = ix->w; L.k = ix->k; L.k_scale = ix->k_scale;
+    L.q_pos0 = ix->q_pos0; L.diag = ix->diag;
+    L.t0 = (int)t0; L.Tc = Tc;
+    L.out = sc; L.ld = ix->S; L.out_bstride = (int64_t)Tc * ix->S; L.write_masked = 0;
+    cudaError_t e = dsa::launch_indexer_scores(L, st);
+    if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
+    dsa::TopkLaunch P{};
+    P.scores = sc; P.ld = ix->S; P.bstride = (int64_t)Tc * ix->S;
+    P.B = ix->B; P.T = ix->T; P.S = ix->S; P.t0 = (int)t0; P.Tc = Tc;
+    P.q_pos0 = ix->q_pos0; P.diag = ix->diag; P.k = k; P.idx = idx; P.flags = ws_flags(ws);
+    e = dsa::launch_topk_rows(P, st);
+    if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+  }
+  return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dsa_workspace_size(const dsa_indexer_args* ix, int32_t k) {
+  (void)k;
+  if (!ix || ix->B <= 0 || ix->T <= 0 || ix->S <= 0) return DSA_WS_MIN;
+  // Preferred score chunk: up to 4 GiB of fp32 scores, at least one row.
+  const int64_t per_row = (int64_t)ix->B * ix->S * 4;
+  int64_t rows = ((int64_t)4 << 30) / per_row;
+  if (rows < 1) rows = 1;
+  if (rows > ix->T) rows = ix->T;
+  return dsa::kWsScratch + (size_t)(rows * per_row);
+}
+
+dsa_status dsa_indexer_scores(const dsa_indexer_args* ix, float* scores, int64_t ld, void* ws, size_t ws_bytes,
+                              void* stream) {
+  dsa_status s = check_indexer(ix);
+  if (s != DSA_OK) return s;
+  if (!scores) return fail(DSA_ERR_INVALID_ARG, "scores is NULL");
+  if (ld < ix->S) return fail(DSA_ERR_INVALID_ARG, "ld (%lld) < S (%d)", (long long)ld, ix->S);
+  if ((s = check_ws(ws, ws_bytes, DSA_WS_MIN)) != DSA_OK) return s;
+  dsa::IndexerLaunch L{};
+  L.B = ix->B; L.T = ix->T; L.S = ix->S; L.HI = ix->H_I; L.DI = ix->d_I;
+  L.fp8 = ix->dtype == DSA_E4M3;
+  L.q = ix->q; L.q_scale = ix->q_scale; L.w = ix->w; L.k = ix->k; L.k_scale = ix->k_scale;
+  L.q_pos0 = ix->q_pos0; L.diag = ix->diag;
+  L.t0 = 0; L.Tc = ix->T;
+  L.out = scores; L.ld = ld; L.out_bstride = (int64_t)ix->T * ld; L.write_masked = 1;
+  cudaError_t e = dsa::launch_indexer_scores(L, as_stream(stream));
+  return e == cudaSuccess ? DSA_OK : cuda_fail(e, "indexer launch");
+}
+
+dsa_status dsa_topk(const dsa_topk_src* src, int32_t B, int32_t T, int32_t S, int64_t q_pos0, int32_t diag,
+                    int32_t k, int32_t* idx, void* ws, size_t ws_bytes, void* stream) {
+  if (!src) return fail(DSA_ERR_INVALID_ARG, "top-k source is NULL");
+  if (!idx) return fail(DSA_ERR_INVALID_ARG, "idx is NULL");
+  if (B <= 0 || T <= 0 || S <= 0) return fail(DSA_ERR_INVALID_ARG, "B, T, S must be positive");
+  if (k < 1 || k > kMaxK) return fail(DSA_ERR_UNSUPPORTED, "k=%d outside [1, %d]", k, kMaxK);
+  if (diag < 0 || diag > 1) return fail(DSA_ERR_INVALID_ARG, "diag must be 0 or 1");
+  if (q_pos0 < 0) return fail(DSA_ERR_INVALID_ARG, "q_pos0 must be >= 0");
+  dsa_status s = check_ws(ws, ws_bytes, DSA_WS_MIN);
+  if (s != DSA_OK) return s;
+  cudaStream_t st = as_stream(stream);
+  if (src->kind == DSA_TOPK_FROM_SCORES) {
+    if (!src->scores) return fail(DSA_ERR_INVALID_ARG, "scores is NULL");
+    if (src->ld < S) return fail(DSA_ERR_INVALID_ARG, "ld < S");
+    dsa::TopkLaunch P{};
+    P.scores = src->scores; P.ld = src->ld; P.bstride = (int64_t)T * src->ld;
+    P.B = B; P.T = T; P.S = S; P.t0 = 0; P.Tc = T;
+    P.q_pos0 = q_pos0; P.diag = diag; P.k = k; P.idx = idx; P.flags = ws_flags(ws);
+    cudaError_t e = dsa::launch_topk_rows(P, st);
+    return e == cudaSuccess ? DSA_OK : cuda_fail(e, "top-k launch");
+  }
+  if (src->kind != DSA_TOPK_FROM_INDEXER) return fail(DSA_ERR_INVALID_ARG, "unknown top-k source kind");
+  if ((s = check_indexer(src->ix)) != DSA_OK) return s;
+  const dsa_indexer_args* ix = src->ix;
+  if (ix->B != B || ix->T != T || ix->S != S || ix->q_pos0 != q_pos0 || ix->diag != diag)
+    return fail(DSA_ERR_INVALID_ARG, "B/T/S/q_pos0/diag disagree with the indexer args");
+  return run_indexer_topk(ix, k, idx, ws, ws_bytes, st);
+}
+
+dsa_status dsa_sparse_attn(const dsa_attn_args* at, const int32_t* idx, int32_t k, void* out, float* lse, void* ws,
+                           size_t ws_bytes, void* stream) {
+  dsa_status s = check_attn(at);
+  if (s != DSA_OK) return s;
+  if (!idx || !out) return fail(DSA_ERR_INVALID_ARG, "idx and out must be non-NULL");
+  if (k < 1 || k > kMaxK) return fail(DSA_ERR_UNSUPPORTED, "k=%d outside [1, %d]", k, kMaxK);
+  if (!aligned16(out)) return fail(DSA_ERR_MISALIGNED, "out must be 16-byte aligned");
+  if ((s = check_ws(ws, ws_bytes, DSA_WS_MIN)) != DSA_OK) return s;
+  dsa::AttnLaunch L{};
+  L.B = at->B; L.T = at->T; L.S = at->S; L.H = at->H; L.DQK = at->d_qk; L.DV = at->d_v; L.scale = at->scale;
+  L.q = at->q; L.k = at->k; L.k_ld = at->k_ld; L.v = at->v; L.v_ld = at->v_ld;
+  L.idx = idx; L.kk = k; L.out = out; L.lse = lse; L.flags = ws_flags(ws);
+  cudaError_t e = dsa::launch_sparse_attn(L, as_stream(stream));
+  return e == cudaSuccess ? DSA_OK : cuda_fail(e, "attention launch");
+}
+
+dsa_status indexshare_group_forward(const dsa_layer* layers, int32_t n_layers, const char* schedule, int32_t k,
+                                    int32_t* const* idx_bufs, void* ws, size_t ws_bytes, void* stream) {
+  if (!layers || n_layers <= 0) return fail(DSA_ERR_INVALID_ARG, "no layers");
+  if (!schedule) return fail(DSA_ERR_SCHEDULE, "schedule is NULL");
+  if ((int32_t)strlen(schedule) != n_layers)
+    return fail(DSA_ERR_SCHEDULE, "schedule has %zu roles for %d layers", strlen(schedule), n_layers);
+  if (schedule[0] != 'F') return fail(DSA_ERR_SCHEDULE, "the first layer must be full ('F')");
+  int n_full = 0;
+  for (int i = 0; i < n_layers; ++i) {
+    if (schedule[i] != 'F' && schedule[i] != 'S') return fail(DSA_ERR_SCHEDULE, "role '%c' at layer %d is not F or S", schedule[i], i);
+    n_full += schedule[i] == 'F';
+  }
+  if (!idx_bufs) return fail(DSA_ERR_INVALID_ARG, "idx_bufs is NULL");
+  if (k < 1 || k > kMaxK) return fail(DSA_ERR_UNSUPPORTED, "k=%d outside [1, %d]", k, kMaxK);
+  dsa_status s;
+  // Validate every layer before launching anything.
+  const dsa_attn_args& a0 = layers[0].at;
+  for (int i = 0; i < n_layers; ++i) {
+    const dsa_layer& L = layers[i];
+    if ((s = check_attn(&L.at)) != DSA_OK) return fail(s, "layer %d: %s", i, g_last_error.c_str());
+    if (L.at.B != a0.B || L.at.T != a0.T || L.at.S != a0.S) return fail(DSA_ERR_INVALID_ARG, "layer %d: B/T/S differ from layer 0", i);
+    if (!L.out || !aligned16(L.out)) return fail(DSA_ERR_INVALID_ARG, "layer %d: out is NULL or misaligned", i);
+    if (schedule[i] == 'F') {
+      if ((s = check_indexer(&L.ix)) != DSA_OK) return fail(s, "layer %d: %s", i, g_last_error.c_str());
+      if (L.ix.B != a0.B || L.ix.T != a0.T || L.ix.S != a0.S)
+        return fail(DSA_ERR_INVALID_ARG, "layer %d: indexer B/T/S differ from the attention's", i);
+      if (score_chunk_rows(&L.ix, ws_bytes) < 1) return fail(DSA_ERR_WORKSPACE, "layer %d: workspace too small for the indexer", i);
+    }
+  }
+  for (int f = 0; f < n_full; ++f)
+    if (!idx_bufs[f]) return fail(DSA_ERR_INVALID_ARG, "idx_bufs[%d] is NULL", f);
+  if ((s = check_ws(ws, ws_bytes, DSA_WS_MIN)) != DSA_OK) return s;
+
+  cudaStream_t st = as_stream(stream);
+  const int32_t* cur = nullptr;
+  int f = 0;
+  for (int i = 0; i < n_layers; ++i) {
+    const dsa_layer& L = layers[i];
+    if (schedule[i] == 'F') {
+      // Full layer: indexer + top-k, positions kept in this F layer's buffer.
+      if ((s = run_indexer_topk(&L.ix, k, idx_bufs[f], ws, ws_bytes, st)) != DSA_OK) return s;
+      cur = idx_bufs[f++];
+    }
+    // Every layer (full or shared) attends with its own operands over `cur`.
+    if ((s = dsa_sparse_attn(&L.at, cur, k, L.out, L.lse, ws, ws_bytes, stream)) != DSA_OK) return s;
+  }
+  return DSA_OK;
+}
+
+dsa_status topk_overlap(const int32_t* a, const int32_t* b, int32_t rows, int32_t k, float* per_row,
+                        double* mean_out, void* ws, size_t ws_bytes, void* stream) {
+  if (!a || !b || !mean_out) return fail(DSA_ERR_INVALID_ARG, "a, b and mean_out must be non-NULL");
+  if (rows < 0 || k < 1) return fail(DSA_ERR_INVALID_ARG, "rows must be >= 0 and k >= 1");
+  const size_t need = per_row ? DSA_WS_MIN : dsa::kWsScratch + (size_t)rows * 4;
+  dsa_status s = check_ws(ws, ws_bytes, need);
+  if (s != DSA_OK) return s;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  float* pr = per_row ? per_row : reinterpret_cast<float*>(w8 + dsa::kWsScratch);
+  double* mean_dev = reinterpret_cast<double*>(w8 + dsa::kWsMean);
+  cudaStream_t st = as_stream(stream);
+  cudaError_t e = dsa::launch_topk_overlap(a, b, rows, k, pr, mean_dev, ws_flags(ws), st);
+  if (e != cudaSuccess) return cuda_fail(e, "overlap launch");
+  if ((e = cudaMemcpyAsync(mean_out, mean_dev, sizeof(double), cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+    return cuda_fail(e, "overlap mean copy");
+  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "overlap sync");
+  return DSA_OK;
+}
+
+dsa_status dsa_read_device_flags(void* ws, uint32_t* flags_out, void* stream) {
+  if (!ws || !flags_out) return fail(DSA_ERR_INVALID_ARG, "ws and flags_out must be non-NULL");
+  cudaStream_t st = as_stream(stream);
+  cudaError_t e = cudaMemcpyAsync(flags_out, ws_flags(ws), sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws_flags(ws), 0, sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return e == cudaSuccess ? DSA_OK : cuda_fail(e, "reading device flags");
+}
+
+const char* dsa_status_string(dsa_status s) {
+  switch (s) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_MISALIGNED: return "DSA_ERR_MISALIGNED";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
+    case DSA_ERR_SCHEDULE: return "DSA_ERR_SCHEDULE";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+    case DSA_ERR_DEVICE_FLAG: return "DSA_ERR_DEVICE_FLAG";
+    case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
+  }
+  return "DSA_ERR_UNKNOWN";
+}
+
+const char* dsa_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

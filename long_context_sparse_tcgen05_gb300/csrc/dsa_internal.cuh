@@ -1,0 +1,79 @@
+// Internal launch interface between the host API (dsa_api.cu) and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "dsa.h"
+
+namespace dsa {
+
+// Workspace layout: the flag word and a double for reductions live in the first
+// DSA_WS_MIN bytes; scratch buffers start at kWsScratch.
+constexpr size_t kWsFlags = 0;
+constexpr size_t kWsMean = 8;
+constexpr size_t kWsScratch = DSA_WS_MIN;
+
+// Key transform of the selection order: a larger float gives a larger unsigned key.
+// -0 and +0 share one key; NaN maps below -inf.
+__device__ __forceinline__ uint32_t score_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  uint32_t a = u & 0x7fffffffu;
+  if (a > 0x7f800000u) return 0u;  // NaN
+  if (a == 0u) u = 0u;             // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Rows [t0, t0 + Tc) of every sequence of one layer's indexer.
+struct IndexerLaunch {
+  int B, T, S, HI, DI;
+  int fp8;
+  const void* q;
+  const float* q_scale;
+  const float* w;
+  const void* k;
+  const float* k_scale;
+  int64_t q_pos0;
+  int diag;
+  int t0, Tc;
+  float* out;           // out[b*out_bstride + (t - t0)*ld + s]
+  int64_t ld;
+  int64_t out_bstride;
+  int write_masked;     // 1: write -inf over [n_t, S) as well
+};
+cudaError_t launch_indexer_scores(const IndexerLaunch& p, cudaStream_t st);
+
+// Top-k over materialised score rows: rows [t0, t0 + Tc) of every sequence,
+// scores[b*bstride + (t - t0)*ld + s], output idx[(b*T + t)*k + j].
+struct TopkLaunch {
+  const float* scores;
+  int64_t ld, bstride;
+  int B, T, S, t0, Tc;
+  int64_t q_pos0;
+  int diag, k;
+  int32_t* idx;
+  uint32_t* flags;
+};
+cudaError_t launch_topk_rows(const TopkLaunch& p, cudaStream_t st);
+
+struct AttnLaunch {
+  int B, T, S, H, DQK, DV;
+  float scale;
+  const void* q;
+  const void* k;
+  int64_t k_ld;
+  const void* v;
+  int64_t v_ld;
+  const int32_t* idx;
+  int kk;
+  void* out;
+  float* lse;
+  uint32_t* flags;
+};
+cudaError_t launch_sparse_attn(const AttnLaunch& p, cudaStream_t st);
+
+cudaError_t launch_topk_overlap(const int32_t* a, const int32_t* b, int rows, int k,
+                                float* per_row, double* mean_dev, uint32_t* flags,
+                                cudaStream_t st);
+
+}  // namespace dsa

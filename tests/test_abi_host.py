@@ -1,0 +1,202 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared entry point,
+its struct layouts match the Python binding, and host-side validation rejects bad calls
+(before any launch) with the documented status codes."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import long_context_sparse_tcgen05_gb300 as dsa
+from long_context_sparse_tcgen05_gb300 import build as dsa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, WORKSPACE, SCHEDULE = 0, 1, 2, 3, 4, 5
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dsa_build.build()
+    return dsa.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert {"dsa_indexer_scores", "dsa_topk", "dsa_sparse_attn", "indexshare_group_forward",
+            "topk_overlap"} <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", dsa.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(\S+)$", out, flags=re.M))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(lib, n)
+
+
+def test_struct_layouts_match_header(tmp_path):
+    src = tmp_path / "sz.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "dsa.h"\n'
+                   'int main(void){printf("%zu %zu %zu %zu %zu %zu %zu\\n", sizeof(dsa_indexer_args),'
+                   ' sizeof(dsa_attn_args), sizeof(dsa_topk_src), sizeof(dsa_layer),'
+                   ' offsetof(dsa_indexer_args, q_pos0), offsetof(dsa_attn_args, q),'
+                   ' offsetof(dsa_layer, out)); return 0;}\n')
+    exe = tmp_path / "sz"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
+    want = [ctypes.sizeof(dsa.IndexerArgs), ctypes.sizeof(dsa.AttnArgs), ctypes.sizeof(dsa.TopkSrc),
+            ctypes.sizeof(dsa.Layer), dsa.IndexerArgs.q_pos0.offset, dsa.AttnArgs.q.offset,
+            dsa.Layer.out.offset]
+    assert got == want
+
+
+def test_status_strings(lib):
+    assert dsa.status_string(0) == "DSA_OK"
+    assert dsa.status_string(5) == "DSA_ERR_SCHEDULE"
+
+
+# Fake, 16-byte aligned "device" addresses: validation must fail before any launch, so
+# nothing ever dereferences them.
+FAKE = 0x10000000
+
+
+def _ix(**kw):
+    a = dsa.IndexerArgs(1, 64, 64, 64, 128, dsa.DSA_BF16, FAKE, None, FAKE, FAKE, None, 0, 0)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def _at(**kw):
+    a = dsa.AttnArgs(1, 64, 64, 64, 576, 512, 0.04, FAKE, FAKE, 576, FAKE, 576)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def _topk_ix(lib, ix, k=16, ws=FAKE, ws_bytes=1 << 30, **over):
+    src = dsa.TopkSrc(dsa.TOPK_FROM_INDEXER, None, 0, ctypes.pointer(ix))
+    args = dict(B=ix.B, T=ix.T, S=ix.S, q_pos0=ix.q_pos0, diag=ix.diag)
+    args.update(over)
+    return lib.dsa_topk(ctypes.byref(src), args["B"], args["T"], args["S"], args["q_pos0"], args["diag"],
+                        k, ctypes.c_void_p(FAKE), ctypes.c_void_p(ws) if ws else None, ws_bytes, None)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("B", 0, INVALID), ("T", -1, INVALID), ("H_I", 32, UNSUPPORTED), ("d_I", 96, UNSUPPORTED),
+    ("q", None, INVALID), ("q", FAKE + 4, MISALIGNED), ("k", FAKE + 8, MISALIGNED),
+    ("diag", 2, INVALID), ("q_pos0", -5, INVALID), ("dtype", 7, INVALID),
+])
+def test_topk_indexer_arg_validation(lib, field, value, status):
+    ix = _ix(**{field: value})
+    assert _topk_ix(lib, ix) == status
+    assert dsa.load_library().dsa_last_error().decode()
+
+
+def test_topk_e4m3_needs_scales(lib):
+    assert _topk_ix(lib, _ix(dtype=dsa.DSA_E4M3)) == INVALID
+    assert _topk_ix(lib, _ix(dtype=dsa.DSA_E4M3, H_I=4, d_I=64, q_scale=FAKE, k_scale=FAKE)) == UNSUPPORTED
+
+
+@pytest.mark.parametrize("k", [0, -1, 4097])
+def test_topk_k_range(lib, k):
+    assert _topk_ix(lib, _ix(), k=k) == UNSUPPORTED
+
+
+def test_topk_shape_mismatch_and_workspace(lib):
+    assert _topk_ix(lib, _ix(), T=32) == INVALID
+    assert _topk_ix(lib, _ix(), ws=0) == WORKSPACE
+    assert _topk_ix(lib, _ix(), ws=FAKE + 8) == MISALIGNED
+    assert _topk_ix(lib, _ix(), ws_bytes=100) == WORKSPACE
+    assert _topk_ix(lib, _ix(), ws_bytes=300) == WORKSPACE  # not even one score row
+
+
+def test_topk_scores_validation(lib):
+    src = dsa.TopkSrc(dsa.TOPK_FROM_SCORES, None, 64, None)
+    assert lib.dsa_topk(ctypes.byref(src), 1, 4, 64, 0, 0, 8, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1 << 20, None) == INVALID
+    src = dsa.TopkSrc(dsa.TOPK_FROM_SCORES, FAKE, 32, None)
+    assert lib.dsa_topk(ctypes.byref(src), 1, 4, 64, 0, 0, 8, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1 << 20, None) == INVALID
+    src = dsa.TopkSrc(9, FAKE, 64, None)
+    assert lib.dsa_topk(ctypes.byref(src), 1, 4, 64, 0, 0, 8, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1 << 20, None) == INVALID
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("H", 32, UNSUPPORTED), ("d_qk", 128, UNSUPPORTED), ("q", None, INVALID), ("k", FAKE + 2, MISALIGNED),
+    ("k_ld", 570, MISALIGNED), ("v_ld", 100, MISALIGNED), ("scale", 0.0, INVALID), ("S", 0, INVALID),
+])
+def test_attention_arg_validation(lib, field, value, status):
+    at = _at(**{field: value})
+    r = lib.dsa_sparse_attn(ctypes.byref(at), ctypes.c_void_p(FAKE), 16, ctypes.c_void_p(FAKE), None,
+                            ctypes.c_void_p(FAKE), 256, None)
+    assert r == status
+
+
+def test_attention_null_idx_and_bad_k(lib):
+    at = _at()
+    assert lib.dsa_sparse_attn(ctypes.byref(at), None, 16, ctypes.c_void_p(FAKE), None, ctypes.c_void_p(FAKE), 256, None) == INVALID
+    assert lib.dsa_sparse_attn(ctypes.byref(at), ctypes.c_void_p(FAKE), 0, ctypes.c_void_p(FAKE), None, ctypes.c_void_p(FAKE), 256, None) == UNSUPPORTED
+    assert lib.dsa_sparse_attn(ctypes.byref(at), ctypes.c_void_p(FAKE), 16, ctypes.c_void_p(FAKE + 2), None, ctypes.c_void_p(FAKE), 256, None) == MISALIGNED
+
+
+def _group(lib, schedule, n_layers=4, ws_bytes=1 << 30, bufs=True, layer_edit=None):
+    arr = (dsa.Layer * n_layers)()
+    for i in range(n_layers):
+        arr[i].ix = _ix()
+        arr[i].at = _at()
+        arr[i].out = FAKE
+        arr[i].lse = None
+    if layer_edit:
+        layer_edit(arr)
+    b = (ctypes.c_void_p * 4)(FAKE, FAKE, FAKE, FAKE)
+    sched = None if schedule is None else schedule.encode()
+    return lib.indexshare_group_forward(arr, n_layers, sched, 16, b if bufs else None,
+                                        ctypes.c_void_p(FAKE), ws_bytes, None)
+
+
+@pytest.mark.parametrize("schedule", ["SFSS", "FSS", "FSSSS", "FSXS", "", "fsss", None])
+def test_group_schedule_validation(lib, schedule):
+    assert _group(lib, schedule) == SCHEDULE
+
+
+def test_group_layer_validation(lib):
+    def bad_at(arr):
+        arr[2].at.H = 3
+    assert _group(lib, "FSSS", layer_edit=bad_at) == UNSUPPORTED
+
+    def bad_ix_in_f(arr):
+        arr[0].ix.d_I = 3
+    assert _group(lib, "FSSS", layer_edit=bad_ix_in_f) == UNSUPPORTED
+
+    def bad_ix_in_s(arr):  # shared layers' indexer args are ignored
+        arr[1].ix.d_I = 3
+        arr[1].at.T = 64
+    assert _group(lib, "FSSS", layer_edit=bad_ix_in_s, ws_bytes=100) == WORKSPACE
+
+    def mismatched(arr):
+        arr[3].at.T = 8
+    assert _group(lib, "FSSS", layer_edit=mismatched) == INVALID
+    assert _group(lib, "FSSS", bufs=False) == INVALID
+    assert _group(lib, "FSSS", ws_bytes=300) == WORKSPACE
+
+
+def test_overlap_validation(lib):
+    m = ctypes.c_double()
+    assert lib.topk_overlap(None, ctypes.c_void_p(FAKE), 4, 8, None, ctypes.byref(m), ctypes.c_void_p(FAKE), 1 << 20, None) == INVALID
+    assert lib.topk_overlap(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 4, 0, None, ctypes.byref(m), ctypes.c_void_p(FAKE), 1 << 20, None) == INVALID
+    assert lib.topk_overlap(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1000, 8, None, ctypes.byref(m), ctypes.c_void_p(FAKE), 300, None) == WORKSPACE
+
+
+def test_workspace_size_plan(lib):
+    ix = _ix(T=131072, S=131072)
+    n = lib.dsa_workspace_size(ctypes.byref(ix), 2048)
+    assert n >= 256 + 131072 * 4 and n <= 256 + (4 << 30)
+    assert lib.dsa_workspace_size(None, 16) == 256

@@ -1,0 +1,264 @@
+"""CUDA path vs the CPU oracle, element by element, on seeded inputs small enough for the
+oracle to finish in seconds while spanning several tiles and a ragged tail.
+
+Tolerances (stated by the project; reading of the rules in the design doc):
+  * index buffers: bit-exact on small-integer inputs (every fp32 score is then exact), and
+    bit-exact for a top-k over a given fp32 score buffer (same keys on both sides);
+  * Gaussian indexer inputs: top-k recall >= 0.999, every selected position within the
+    fp32 rounding bound of the oracle's k-th score, scores within 1e-2 relative
+    (|err| <= 1e-2 * max(|ref|, 1e-3 * max_row |ref|));
+  * attention outputs: max-abs <= 2e-2 against the fp64 oracle; LSE within 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import long_context_sparse_tcgen05_gb300 as dsa
+import oracle
+from long_context_sparse_tcgen05_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+ATOL_OUT = 2e-2
+ATOL_LSE = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from long_context_sparse_tcgen05_gb300 import build
+    build.build()
+    dsa.load_library()
+    dsa.read_device_flags()  # clear
+
+
+DEV = torch.device("cuda:0")
+
+
+def _wl(HI, DI, dtype, values, T, S=None, k=64, q_pos0=0, diag=0, B=1):
+    base = synth.WORKLOADS["prefill_16k"] if HI == 64 else synth.WORKLOADS["tiny_l1k"]
+    return base.replace(B=B, T=T, S=S or T, q_pos0=q_pos0, diag=diag, idx_dtype=dtype,
+                        values=values, k=k)
+
+
+def _recall_and_validity(got, ref_idx, ref_scores, n_valid, tol_rel=1e-4):
+    recalls = []
+    for r in range(got.shape[0]):
+        g = got[r][got[r] >= 0]
+        e = ref_idx[r][ref_idx[r] >= 0]
+        assert len(g) == len(e) == min(int(n_valid[r]), got.shape[1])
+        assert np.all(np.diff(g) > 0) and np.all(g < n_valid[r])
+        recalls.append(len(np.intersect1d(g, e)) / max(1, len(e)))
+        if len(e) and len(e) < n_valid[r]:
+            tau = np.sort(ref_scores[r, :n_valid[r]])[::-1][len(e) - 1]
+            assert ref_scores[r, g].min() >= tau - tol_rel * max(abs(tau), 1.0)
+    return float(np.mean(recalls)), float(np.min(recalls))
+
+
+# --- top-k over a score buffer --------------------------------------------------------
+
+@pytest.mark.parametrize("kind,n,k", [("int", 1000, 64), ("int", 5000, 2048), ("normal", 3000, 257),
+                                      ("normal", 70000, 2048), ("int", 300, 4096), ("normal", 9000, 1)])
+def test_topk_from_scores_bit_exact(kind, n, k):
+    R = 24
+    sc = synth.scores_input(R, n, DEV, kind, lo=-3, hi=3)
+    for q_pos0, diag in ((n - R, 0), (0, 1), (n // 2, 1)):
+        idx = dsa.dsa_topk(k, scores=sc[None], q_pos0=q_pos0, diag=diag)
+        nv = np.clip(np.arange(R) + q_pos0 + diag, 0, n)
+        ref = oracle.topk_rows(sc.double().cpu().numpy(), nv, k)
+        assert np.array_equal(idx[0].cpu().numpy(), ref), (kind, n, k, q_pos0, diag)
+    assert dsa.read_device_flags() == 0
+
+
+def test_topk_from_scores_ragged_ld_and_batches():
+    B, T, S, ld, k = 3, 7, 777, 800, 100
+    full = synth.scores_input(B * T, ld, DEV, "int", lo=-1, hi=1).reshape(B, T, ld)
+    idx = dsa.dsa_topk(k, scores=full[:, :, :S], q_pos0=S - T, diag=1)
+    nv = np.clip(np.arange(T) + S - T + 1, 0, S)
+    ref = oracle.topk_rows(full[:, :, :S].reshape(B * T, S).double().cpu().numpy(), np.tile(nv, B), k)
+    assert np.array_equal(idx.reshape(B * T, k).cpu().numpy(), ref)
+
+
+def test_topk_nan_scores_rank_lowest_and_raise_flag():
+    R, n, k = 4, 2000, 1990
+    sc = synth.scores_input(R, n, DEV, "normal")
+    sc[:, ::50] = float("nan")
+    dsa.read_device_flags()
+    idx = dsa.dsa_topk(k, scores=sc[None], q_pos0=n, diag=0)
+    assert dsa.read_device_flags() & dsa.FLAG_NAN_SCORE
+    ref = oracle.topk_rows(sc.double().cpu().numpy(), np.full(R, n), k)
+    assert np.array_equal(idx[0].cpu().numpy(), ref)
+
+
+# --- indexer scores ----------------------------------------------------------------------
+
+CASES_INT = [(4, 64, "bf16"), (64, 128, "bf16"), (64, 128, "e4m3")]
+
+
+@pytest.mark.parametrize("HI,DI,dtype", CASES_INT)
+@pytest.mark.parametrize("T,S,q_pos0,diag,B", [(600, 600, 0, 0, 1), (333, 700, 367, 1, 2), (5, 1000, 995, 0, 1)])
+def test_indexer_scores_integer_inputs_bit_exact(HI, DI, dtype, T, S, q_pos0, diag, B):
+    wl = _wl(HI, DI, dtype, "int", T, S, q_pos0=q_pos0, diag=diag, B=B)
+    ix = synth.indexer_inputs(wl, 0, DEV)
+    got = dsa.indexer_scores(ix).reshape(B * T, S).double().cpu().numpy()
+    ref = oracle.indexer_scores(ix)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_indexer_scores_gaussian_within_tolerance(dtype):
+    wl = _wl(64, 128, dtype, "gauss", 520, 520)
+    ix = synth.indexer_inputs(wl, 0, DEV)
+    got = dsa.indexer_scores(ix).reshape(520, 520).double().cpu().numpy()
+    ref = oracle.indexer_scores(ix)
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(got), fin)
+    rowmax = np.max(np.abs(np.where(fin, ref, 0)), axis=1, keepdims=True)
+    bound = 1e-2 * np.maximum(np.abs(ref), 1e-3 * rowmax)
+    assert np.all(np.abs(got - ref)[fin] <= bound[fin])
+
+
+# --- indexer + top-k ---------------------------------------------------------------------
+
+@pytest.mark.parametrize("HI,DI,dtype", CASES_INT)
+@pytest.mark.parametrize("k", [16, 64, 300])
+def test_indexer_topk_integer_inputs_bit_exact(HI, DI, dtype, k):
+    wl = _wl(HI, DI, dtype, "int", 600, 600, k=k)
+    ix = synth.indexer_inputs(wl, 0, DEV)
+    got = dsa.dsa_topk(k, ix=ix).reshape(600, k).cpu().numpy()
+    ref = oracle.indexer_topk(ix, k)
+    assert np.array_equal(got, ref)
+
+
+def test_indexer_topk_chunked_prefill_and_batches_bit_exact():
+    wl = _wl(64, 128, "e4m3", "int", 200, 900, k=128, q_pos0=700, diag=1, B=3)
+    ix = synth.indexer_inputs(wl, 0, DEV)
+    got = dsa.dsa_topk(128, ix=ix).reshape(600, 128).cpu().numpy()
+    assert np.array_equal(got, oracle.indexer_topk(ix, 128))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_indexer_topk_gaussian_recall(dtype):
+    T, k = 1200, 256
+    wl = _wl(64, 128, dtype, "gauss", T, T, k=k)
+    ix = synth.indexer_inputs(wl, 0, DEV)
+    got = dsa.dsa_topk(k, ix=ix).reshape(T, k).cpu().numpy()
+    rows = np.arange(0, T, 3)
+    ref_idx, ref_sc = oracle.indexer_topk(ix, k, rows, return_scores=True)
+    mean, worst = _recall_and_validity(got[rows], ref_idx, ref_sc, np.clip(rows, 0, T))
+    assert mean >= 0.999, (mean, worst)
+
+
+# --- sparse attention ----------------------------------------------------------------------
+
+def _attn_case(H, DQK, DV, latent, T, S, k, seed=0):
+    base = synth.WORKLOADS["prefill_16k"] if DQK == 576 else synth.WORKLOADS["tiny_l1k"]
+    wl = base.replace(T=T, S=S, H=H, DQK=DQK, DV=DV, latent=latent, k=k)
+    at = synth.attn_inputs(wl, seed, DEV)
+    # index rows: a causal top-k of integer scores (ascending, -1 padded)
+    sc = synth.scores_input(T, S, DEV, "int", seed=seed + 3, lo=-4, hi=4)
+    idx = dsa.dsa_topk(k, scores=sc[None], q_pos0=S - T, diag=0)
+    return at, idx
+
+
+@pytest.mark.parametrize("H,DQK,DV,latent,T,S,k", [
+    (8, 64, 64, False, 300, 700, 64), (8, 64, 64, False, 64, 64, 96), (16, 64, 64, True, 100, 400, 128),
+    (64, 576, 512, True, 160, 900, 256), (64, 576, 512, True, 24, 3000, 2048),
+])
+def test_sparse_attn_matches_oracle(H, DQK, DV, latent, T, S, k):
+    at, idx = _attn_case(H, DQK, DV, latent, T, S, k)
+    out, lse = dsa.dsa_sparse_attn(at, idx)
+    ref_o, ref_l = oracle.sparse_attn(at, idx.reshape(T, k).cpu().numpy())
+    got = out.reshape(T, H, DV).float().cpu().numpy()
+    assert np.abs(got - ref_o).max() <= ATOL_OUT
+    gl = lse.reshape(T, H).cpu().numpy()
+    fin = np.isfinite(ref_l)
+    assert np.array_equal(np.isfinite(gl), fin)
+    assert np.abs(gl[fin] - ref_l[fin]).max() <= ATOL_LSE
+
+
+def test_sparse_attn_bad_index_is_skipped_and_flagged():
+    at, idx = _attn_case(64, 576, 512, True, 8, 500, 64)
+    bad = idx.clone()
+    bad[0, 3, 5] = 500          # == S
+    bad[0, 5, 0] = -7           # < -1
+    dsa.read_device_flags()
+    out, lse = dsa.dsa_sparse_attn(at, bad)
+    assert dsa.read_device_flags() & dsa.FLAG_BAD_INDEX
+    fixed = bad.clone()
+    fixed[0, 3, 5] = -1
+    fixed[0, 5, 0] = -1
+    ref_o, _ = oracle.sparse_attn(at, fixed.reshape(8, 64).cpu().numpy())
+    assert np.abs(out.reshape(8, 64, 512).float().cpu().numpy() - ref_o).max() <= ATOL_OUT
+
+
+def test_sparse_attn_empty_rows():
+    at, idx = _attn_case(64, 576, 512, True, 4, 300, 32)
+    idx[:] = -1
+    idx[0, 2, :3] = torch.tensor([1, 5, 9], dtype=torch.int32)
+    out, lse = dsa.dsa_sparse_attn(at, idx)
+    assert (out[0, 0] == 0).all() and torch.isneginf(lse[0, 0]).all()
+    ref_o, ref_l = oracle.sparse_attn(at, idx.reshape(4, 32).cpu().numpy())
+    assert np.abs(out.reshape(4, 64, 512).float().cpu().numpy() - ref_o).max() <= ATOL_OUT
+
+
+# --- IndexShare group ---------------------------------------------------------------------
+
+def test_group_forward_tiny_matches_oracle_and_reuses_indices():
+    wl = synth.WORKLOADS["tiny_l1k"]
+    layers = [synth.layer_inputs(wl, l, DEV) for l in range(4)]
+    outs, lses, bufs = dsa.indexshare_group_forward(layers, "FSSS", wl.k)
+    ref = oracle.group_forward(layers, "FSSS", wl.k)
+    assert np.array_equal(bufs[0].reshape(-1, wl.k).cpu().numpy(), ref[0]["idx"])
+    for l in range(4):
+        o = outs[l].reshape(-1, wl.H, wl.DV).float().cpu().numpy()
+        assert np.abs(o - ref[l]["out"]).max() <= ATOL_OUT
+        # a shared layer's output is exactly sparse attention over the full layer's buffer
+        o2, l2 = dsa.dsa_sparse_attn(layers[l]["at"], bufs[0])
+        assert torch.equal(o2, outs[l]) and torch.equal(l2, lses[l])
+    assert dsa.read_device_flags() == 0
+
+
+def test_group_all_full_and_identical_indexers():
+    wl = synth.WORKLOADS["tiny_l1k"].replace(T=500, S=500)
+    layers = [dict(ix=synth.indexer_inputs(wl, 0, DEV), at=synth.attn_inputs(wl, l, DEV)) for l in range(4)]
+    a, _, ba = dsa.indexshare_group_forward(layers, "FFFF", wl.k)
+    b, _, bb = dsa.indexshare_group_forward(layers, "FSSS", wl.k)
+    assert len(ba) == 4 and len(bb) == 1
+    for l in range(4):
+        assert torch.equal(a[l], b[l]) and torch.equal(ba[l], bb[0])
+    _, mean = dsa.topk_overlap(ba[0], ba[3])
+    assert mean == 1.0
+
+
+def test_group_two_groups_and_lse_optional():
+    wl = synth.WORKLOADS["tiny_l1k"].replace(T=300, S=300, k=32)
+    layers = [synth.layer_inputs(wl.replace(schedule="FSSFSS"), l, DEV) for l in range(6)]
+    outs, lses, bufs = dsa.indexshare_group_forward(layers, "FSSFSS", 32, with_lse=False)
+    ref = oracle.group_forward(layers, "FSSFSS", 32)
+    assert np.array_equal(bufs[1].reshape(-1, 32).cpu().numpy(), ref[3]["idx"])
+    for l in range(6):
+        assert np.abs(outs[l].reshape(300, 8, 64).float().cpu().numpy() - ref[l]["out"]).max() <= ATOL_OUT
+
+
+# --- overlap ------------------------------------------------------------------------------
+
+def test_topk_overlap_matches_oracle():
+    R, S, k = 400, 3000, 128
+    a = dsa.dsa_topk(k, scores=synth.scores_input(R, S, DEV, "normal", seed=31)[None], q_pos0=S - 300)
+    b = dsa.dsa_topk(k, scores=synth.scores_input(R, S, DEV, "normal", seed=32)[None], q_pos0=S - 300)
+    per, mean = dsa.topk_overlap(a, b)
+    rp, rm = oracle.topk_overlap(a.cpu().numpy(), b.cpu().numpy())
+    np.testing.assert_allclose(per.cpu().numpy(), rp, rtol=1e-6)
+    assert mean == pytest.approx(rm, rel=1e-9)
+    _, m2 = dsa.topk_overlap(a, a, per_row=False)
+    assert m2 == 1.0
+
+
+def test_topk_overlap_flags_unsorted_rows():
+    a = torch.tensor([[5, 3, 9, -1]], dtype=torch.int32, device=DEV)
+    b = torch.tensor([[3, 5, 9, -1]], dtype=torch.int32, device=DEV)
+    dsa.read_device_flags()
+    dsa.topk_overlap(a, b)
+    assert dsa.read_device_flags() & dsa.FLAG_UNSORTED
