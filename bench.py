@@ -1,0 +1,420 @@
+#!/usr/bin/env python3
+"""Throughput of the DSA + IndexShare hot path on one GB300 (or N replicas).
+
+A step is one F,S,S,S group forward over a 131,072-token causal prefill (FP8 e4m3 indexer
+with H_I=64, d_I=128, top-2048; four layers of 64-head sparse MQA over a 576-dim latent
+KV), through ``indexshare_group_forward``: the full layer's indexer + top-k, then four
+attention layers over its index buffer.  Inputs are seeded synthetic tensors of that shape
+(see ``synth``), far larger than L2.
+
+Prints one JSON line (rank 0).  ``value`` is group-prefill tokens/s summed over ranks;
+``indexer_topk`` gives the indexer+top-k query rows/s of the same workload.  ``--impl
+reference`` times the CPU oracle instead, on sampled rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from long_context_sparse_tcgen05_gb300 import synth  # noqa: E402
+
+METRIC = "indexer+top-k query rows/s at L=128K; FSSS 4-layer group prefill tokens/s"
+UNIT = "tokens/s"
+GROUP = "FSSS"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill_128k")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle CPU time")
+    return ap.parse_args()
+
+
+# --- distributed plumbing (replicas: each rank runs its own group; barrier + max time) ---
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --- clocks ---------------------------------------------------------------------------
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.gpu)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+                power.append(float(p[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+# --- algorithmic work -------------------------------------------------------------------
+
+def visible_counts(wl) -> np.ndarray:
+    t = np.arange(wl.T, dtype=np.int64)
+    return np.tile(np.clip(wl.q_pos0 + t + wl.diag, 0, wl.S), wl.B)
+
+
+def attn_bytes(wl) -> float:
+    """Algorithmic HBM bytes of one sparse-attention launch: per query row, the gathered
+    latent rows (2*d_qk bytes each, min(k, n_t) of them), Q, O, the index row and LSE."""
+    n = visible_counts(wl)
+    kk = np.minimum(n, wl.k).astype(np.float64)
+    per_row_fixed = wl.H * wl.DQK * 2 + wl.H * wl.DV * 2 + wl.k * 4 + wl.H * 4
+    return float(np.sum(kk * wl.DQK * 2) + len(n) * per_row_fixed)
+
+
+def attn_flops(wl) -> float:
+    n = visible_counts(wl)
+    kk = np.minimum(n, wl.k).astype(np.float64)
+    return float(np.sum(kk) * 2 * wl.H * (wl.DQK + wl.DV))
+
+
+def indexer_flops(wl) -> float:
+    return float(np.sum(visible_counts(wl).astype(np.float64)) * 2 * wl.HI * wl.DI)
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+# --- timing helpers ---------------------------------------------------------------------
+
+def time_loop(fn, steps, warmup, world=1):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        fn()
+    e1.record(st)
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1) / steps
+
+
+# --- CPU oracle on sampled rows --------------------------------------------------------
+
+def oracle_sample(wl, host_ix, host_ats, rows, k):
+    """Oracle time for the sampled rows of one group: (indexer+top-k s, attention s)."""
+    import oracle
+    t0 = time.perf_counter()
+    idx = oracle.indexer_topk(host_ix, k, rows)
+    t1 = time.perf_counter()
+    for at in host_ats:
+        oracle.sparse_attn(at, idx, rows)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
+
+
+def host_sample(wl, ix, ats, rows):
+    """Host copies of what the sampled rows read: their query rows, all keys / KV."""
+    r = torch.as_tensor(rows, device=ix["q"].device)
+
+    def take(t, lead):
+        return None if t is None else t.reshape((-1,) + tuple(t.shape[lead:]))[r].cpu()
+
+    hix = dict(q_rows=take(ix["q"], 2), w_rows=take(ix["w"], 2), q_scale_rows=take(ix.get("q_scale"), 2),
+               k=ix["k"].cpu(), k_scale=None if ix.get("k_scale") is None else ix["k_scale"].cpu(),
+               T=wl.T, S=wl.S, q_pos0=wl.q_pos0, diag=wl.diag)
+    hats = [dict(q_rows=take(at["q"], 2), k=at["k"].cpu(), v=None if at.get("v") is None else at["v"].cpu(),
+                 d_v=at["d_v"], scale=at["scale"], T=wl.T) for at in ats]
+    return hix, hats
+
+
+def extrapolate(wl, rows, t_ix, t_at):
+    n = visible_counts(wl).astype(np.float64)
+    ns = n[np.asarray(rows)]
+    kk, kks = np.minimum(n, wl.k), np.minimum(ns, wl.k)
+    tot_ix = t_ix * n.sum() / max(ns.sum(), 1.0)
+    tot_at = t_at * kk.sum() / max(kks.sum(), 1.0)
+    return tot_ix, tot_at
+
+
+def pick_rows(wl, n_rows, seed=5):
+    g = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([g.integers(0, wl.B * wl.T, n_rows), [wl.B * wl.T - 1]]))
+    return rows.tolist()
+
+
+def cpu_baseline(wl, ix, ats, target_s):
+    """Time the oracle as it stands on a bounded row sample; extrapolate to tokens/s."""
+    import oracle
+    probe = pick_rows(wl, 4, seed=1)
+    hix, hats = host_sample(wl, ix, ats, probe)
+    a, b = oracle_sample(wl, hix, hats, probe, wl.k)
+    n_rows = int(max(4, min(512, len(probe) * target_s / max(a + b, 1e-3))))
+    rows = pick_rows(wl, n_rows)
+    hix, hats = host_sample(wl, ix, ats, rows)
+    t_ix, t_at = oracle_sample(wl, hix, hats, rows, wl.k)
+    tot_ix, tot_at = extrapolate(wl, rows, t_ix, t_at)
+    return {"value": wl.B * wl.T / (tot_ix + tot_at), "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{len(rows)} query rows of {wl.name} (indexer+top-k and 4 attention layers); "
+                      f"{t_ix + t_at:.1f} s measured, extrapolated by visible-key and selected-key counts",
+            "indexer_topk_rows_per_s": wl.B * wl.T / tot_ix}
+
+
+# --- our arm ----------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local):
+    import long_context_sparse_tcgen05_gb300 as dsa
+    from long_context_sparse_tcgen05_gb300 import build
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    build.build()
+    dsa.load_library()
+    wl = synth.WORKLOADS[args.workload]
+    layers = [synth.layer_inputs(wl, l, dev, with_indexer=True) for l in range(4)]
+    group = [dict(ix=layers[0]["ix"], at=layers[l]["at"]) for l in range(4)]
+    ws_need = dsa.workspace_size(layers[0]["ix"], wl.k)
+    dsa.workspace(ws_need, dev)
+    outs = [torch.empty(wl.B, wl.T, wl.H, wl.DV, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    lses = [torch.empty(wl.B, wl.T, wl.H, dtype=torch.float32, device=dev) for _ in range(4)]
+    bufs = [torch.empty(wl.B, wl.T, wl.k, dtype=torch.int32, device=dev) for _ in range(4)]
+
+    def step():
+        dsa.indexshare_group_forward(group, GROUP, wl.k, outs=outs, lses=lses, idx_bufs=bufs[:1])
+
+    clocks = Clocks(local)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    n0 = dsa.launch_count()
+    clocks.start()
+    ms = time_loop(step, args.steps, 0, world)
+    clk = clocks.stop()
+    launches = dsa.launch_count() - n0
+    ms = max_over_ranks(ms, world)
+    tokens = wl.B * wl.T
+    value = tokens * world / (ms / 1e3)
+
+    # components, each timed alone with the same launches the step makes
+    at_ms = time_loop(lambda: dsa.dsa_sparse_attn(group[1]["at"], bufs[0], out=outs[1], lse=lses[1]),
+                      max(3, args.steps // 2), 1)
+    ix_ms = time_loop(lambda: dsa.dsa_topk(wl.k, ix=layers[0]["ix"], idx=bufs[0]), max(3, args.steps // 2), 1)
+    ffff = [dict(ix=layers[l]["ix"], at=layers[l]["at"]) for l in range(4)]
+    ffff_ms = time_loop(lambda: dsa.indexshare_group_forward(ffff, "FFFF", wl.k, outs=outs, lses=lses, idx_bufs=bufs),
+                        max(2, args.steps // 3), 1)
+    _, overlap01 = dsa.topk_overlap(bufs[0], bufs[1], per_row=False)
+    flags = dsa.read_device_flags(dev)
+
+    peaks = load_peaks()
+    a_bytes = attn_bytes(wl)
+    att_gbs = a_bytes / (at_ms / 1e3) / 1e9
+    ix_tf = indexer_flops(wl) / (ix_ms / 1e3) / 1e12
+    fp8_peak = peaks["bf16_tflops"] * 2.0  # FP8 dense = 2x bf16 (nominal 4.5 vs 2.25 PF)
+    attn_total = 4 * at_ms
+    if attn_total >= ix_ms:
+        roof = {"kernel": "sparse attention (k_sparse_attn)", "bound": "hbm", "achieved": round(att_gbs, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(att_gbs / peaks["hbm_gbs"], 4),
+                "traffic": None, "algorithmic_bytes_per_launch": a_bytes, "launch_ms": round(at_ms, 3),
+                "peak_src": peaks["src"]}
+    else:
+        roof = {"kernel": "indexer + top-k (FP8)", "bound": "tensor", "achieved": round(ix_tf, 1),
+                "peak": fp8_peak, "unit": "TFLOP/s", "frac": round(ix_tf / fp8_peak, 4), "traffic": None,
+                "algorithmic_flops_per_call": indexer_flops(wl), "call_ms": round(ix_ms, 3),
+                "peak_src": peaks["src"] + " bf16 x 2 (FP8 nominal ratio)"}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3+bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "L": wl.S, "query_rows": wl.B * wl.T, "k": wl.k, "schedule": GROUP,
+                   "H_I": wl.HI, "d_I": wl.DI, "indexer_dtype": wl.idx_dtype, "H": wl.H, "d_qk": wl.DQK,
+                   "d_v": wl.DV, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (%.1f GB read per step)" % (
+                       (sum(t.numel() * t.element_size() for t in (layers[0]["ix"]["q"], layers[0]["ix"]["k"])) +
+                        4 * layers[0]["at"]["q"].numel() * 2) / 1e9)},
+        "indexer_topk": {"value": round(tokens * world / (ix_ms / 1e3), 1), "unit": "rows/s", "ms": round(ix_ms, 3),
+                         "tflops": round(ix_tf, 1)},
+        "attention_layer_ms": round(at_ms, 3), "attention_gbs": round(att_gbs, 1),
+        "attention_tflops": round(attn_flops(wl) / (at_ms / 1e3) / 1e12, 1),
+        "fsss_vs_ffff": {"fsss_ms": round(ms, 3), "ffff_ms": round(ffff_ms, 3), "speedup": round(ffff_ms / ms, 3),
+                         "adjacent_layer_overlap": round(overlap01, 4)},
+        "roofline": roof, "gpu_launches": int(launches), "clocks": clk, "device_flags": flags,
+    }
+
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(dsa, wl, layers, group, outs, lses, bufs, args, world)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(wl, layers[0]["ix"], [g["at"] for g in group], args.cpu_seconds)
+    return line
+
+
+def run_e2e(dsa, wl, layers, group, outs, lses, bufs, args, world):
+    """Same group forward through the public call, with every input copied in from pinned
+    host memory and every output copied back, inside the timed region."""
+    ix = layers[0]["ix"]
+    dev_inputs = [ix["q"], ix["k"], ix["w"], ix["q_scale"], ix["k_scale"]] + \
+                 [t for g in group for t in (g["at"]["q"], g["at"]["k"])]
+    host_inputs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_inputs]
+    for h, d in zip(host_inputs, dev_inputs):
+        h.copy_(d)
+    dev_outputs = outs + lses
+    host_outputs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_outputs]
+    h2d = sum(t.numel() * t.element_size() for t in host_inputs)
+    d2h = sum(t.numel() * t.element_size() for t in host_outputs)
+
+    def step():
+        for h, d in zip(host_inputs, dev_inputs):
+            d.copy_(h, non_blocking=True)
+        dsa.indexshare_group_forward(group, GROUP, wl.k, outs=outs, lses=lses, idx_bufs=bufs[:1])
+        for h, d in zip(host_outputs, dev_outputs):
+            h.copy_(d, non_blocking=True)
+
+    ms = time_loop(step, max(3, args.steps // 2), 1, world)
+    ms = max_over_ranks(ms, world)
+    del host_inputs, host_outputs
+    return {"value": round(wl.B * wl.T * world / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# --- reference arm: the CPU oracle -------------------------------------------------------
+
+def run_reference(args, rank, world, local):
+    import oracle
+    oracle.build()
+    wl = synth.WORKLOADS[args.workload]
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    rows = pick_rows(wl, 8, seed=3)
+    # inputs: the same seeded tensors; only what the sampled rows read is moved to the host
+    ix = synth.indexer_inputs(wl, 0, dev)
+    hix, _ = host_sample(wl, ix, [], rows)
+    del ix
+    hats = []
+    for l in range(4):
+        at = synth.attn_inputs(wl, l, dev)
+        hats += host_sample(wl, dict(q=at["q"], w=at["q"], k=at["k"]), [at], rows)[1]
+        del at
+    if dev.type == "cuda":
+        torch.cuda.empty_cache()
+
+    def step():
+        a, b = oracle_sample(wl, hix, hats, rows, wl.k)
+        return extrapolate(wl, rows, a, b)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    tot = [step() for _ in range(args.steps)]
+    wall = (time.perf_counter() - t0) / args.steps
+    ext = float(np.mean([a + b for a, b in tot]))
+    value = wl.B * wl.T / ext
+    cores = oracle.num_threads()
+    sample = f"{len(rows)} query rows of {wl.name} per step (indexer+top-k and 4 attention layers), " \
+             f"extrapolated by visible-key and selected-key counts"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ext * 1e3, 1),
+            "sample_wall_ms_per_step": round(wall * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "L": wl.S, "query_rows": wl.B * wl.T, "k": wl.k, "schedule": GROUP},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        line = run_reference(args, rank, world, local)
+        line["n_gpus"] = world
+    else:
+        line = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -174,8 +174,12 @@ dsa_status topk_overlap(const int32_t* a, const int32_t* b, int32_t rows, int32_
  * Synchronises `stream`. */
 dsa_status dsa_read_device_flags(void* ws, uint32_t* flags_out, void* stream);
 
+/* Name of a status code; message of the calling thread's last failure. */
 const char* dsa_status_string(dsa_status s);
 const char* dsa_last_error(void);
+
+/* Number of kernels this library has launched since it was loaded (all threads). */
+uint64_t dsa_launch_count(void);
 
 #ifdef __cplusplus
 }

@@ -99,6 +99,8 @@ def load_library(path: str = LIB_PATH):
             lib.dsa_status_string.argtypes = [S]
             lib.dsa_last_error.restype = _c.c_char_p
             lib.dsa_last_error.argtypes = []
+            lib.dsa_launch_count.restype = _c.c_uint64
+            lib.dsa_launch_count.argtypes = []
             _lib = lib
     return _lib
 
@@ -288,6 +290,11 @@ def topk_overlap(a: torch.Tensor, b: torch.Tensor, per_row: torch.Tensor | bool 
     _check(lib.topk_overlap(_ptr(a2), _ptr(b2), rows, k, _ptr(per_row), _c.byref(mean), _ptr(ws),
                             ws.numel(), _stream()))
     return per_row, mean.value
+
+
+def launch_count() -> int:
+    """Kernels launched by the library since it was loaded."""
+    return int(load_library().dsa_launch_count())
 
 
 def read_device_flags(device=None) -> int:

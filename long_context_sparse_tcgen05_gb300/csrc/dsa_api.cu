@@ -3,10 +3,16 @@
 // the caller.
 #include <cstdarg>
 #include <cstdio>
+#include <atomic>
 #include <cstring>
 #include <string>
 
 #include "dsa_internal.cuh"
+
+namespace dsa {
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace dsa
 
 namespace {
 
@@ -281,5 +287,7 @@ const char* dsa_status_string(dsa_status s) {
 }
 
 const char* dsa_last_error(void) { return g_last_error.c_str(); }
+
+uint64_t dsa_launch_count(void) { return dsa::g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

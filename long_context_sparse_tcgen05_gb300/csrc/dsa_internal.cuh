@@ -14,6 +14,9 @@ constexpr size_t kWsFlags = 0;
 constexpr size_t kWsMean = 8;
 constexpr size_t kWsScratch = DSA_WS_MIN;
 
+// Kernel launches issued by this library since load (diagnostics; see dsa_launch_count).
+void count_launches(uint64_t n);
+
 // Key transform of the selection order: a larger float gives a larger unsigned key.
 // -0 and +0 share one key; NaN maps below -inf.
 __device__ __forceinline__ uint32_t score_key(float f) {

@@ -292,6 +292,7 @@ cudaError_t launch_cfg(const AttnLaunch& p, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
   if (e != cudaSuccess) return e;
   kern<<<p.B * p.T, C::kThreads, C::kSmem, st>>>(p);
+  count_launches(1);
   return cudaGetLastError();
 }
 

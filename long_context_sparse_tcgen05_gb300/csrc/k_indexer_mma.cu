@@ -190,6 +190,7 @@ cudaError_t launch_tb(const IndexerLaunch& p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   dim3 grid((p.S + kKeysPerCta - 1) / kKeysPerCta, (p.Tc + TB - 1) / TB, p.B);
   kern<<<grid, kThreads, C::kSmem, st>>>(p);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -72,10 +72,12 @@ cudaError_t launch_topk_overlap(const int32_t* a, const int32_t* b, int rows, in
   if (rows > 0) {
     const int ctas = (rows + kWarpsPerCta - 1) / kWarpsPerCta;
     k_topk_overlap<<<ctas, kWarpsPerCta * 32, 0, st>>>(a, b, rows, k, per_row, flags);
+    count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   k_mean<<<1, 1024, 0, st>>>(per_row, rows, mean_dev);
+  count_launches(1);
   return cudaGetLastError();
 }
 

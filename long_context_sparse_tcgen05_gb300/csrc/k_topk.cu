@@ -178,6 +178,7 @@ cudaError_t launch_topk_rows(const TopkLaunch& p, cudaStream_t st) {
   const int rows = p.B * p.Tc;
   if (rows <= 0) return cudaSuccess;
   k_topk_rows<<<rows, kThreads, 0, st>>>(p);
+  count_launches(1);
   return cudaGetLastError();
 }
 

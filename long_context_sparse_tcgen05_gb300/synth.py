@@ -94,6 +94,17 @@ def _gen(device, seed: int) -> torch.Generator:
     return g
 
 
+def _draw_chunk(kind, sub, device, seed, chunk, lo, hi):
+    g = _gen(device, seed * 1000003 + chunk)
+    if kind == "normal":
+        return torch.randn(sub, generator=g, device=device)
+    if kind == "uniform":
+        return torch.rand(sub, generator=g, device=device)
+    if kind == "int":
+        return torch.randint(lo, hi + 1, sub, generator=g, device=device).float()
+    raise ValueError(kind)
+
+
 def _draw(kind: str, shape, device, seed: int, lo: int = 0, hi: int = 0) -> torch.Tensor:
     """fp32 tensor of `shape`, drawn chunk by chunk along dim 1 (the token axis)."""
     out = torch.empty(shape, dtype=torch.float32, device=device)
@@ -101,15 +112,23 @@ def _draw(kind: str, shape, device, seed: int, lo: int = 0, hi: int = 0) -> torc
     for c0 in range(0, n, CHUNK):
         c1 = min(n, c0 + CHUNK)
         sub = (shape[0], c1 - c0) + tuple(shape[2:])
-        g = _gen(device, seed * 1000003 + c0 // CHUNK)
-        if kind == "normal":
-            out[:, c0:c1] = torch.randn(sub, generator=g, device=device)
-        elif kind == "uniform":
-            out[:, c0:c1] = torch.rand(sub, generator=g, device=device)
-        elif kind == "int":
-            out[:, c0:c1] = torch.randint(lo, hi + 1, sub, generator=g, device=device).float()
-        else:
-            raise ValueError(kind)
+        out[:, c0:c1] = _draw_chunk(kind, sub, device, seed, c0 // CHUNK, lo, hi)
+    return out
+
+
+def _draw_rows(kind: str, shape, device, seed: int, flat_rows, lo: int = 0, hi: int = 0):
+    """Rows (flat b*shape[1] + t) of the tensor _draw would make, drawing only the chunks
+    that hold them (chunks are seeded independently, so the values are identical)."""
+    n = shape[1]
+    out = torch.empty((len(flat_rows),) + tuple(shape[2:]), dtype=torch.float32, device=device)
+    cache = {}
+    for i, r in enumerate(flat_rows):
+        t = r % n
+        c = t // CHUNK
+        if c not in cache:
+            c0, c1 = c * CHUNK, min(n, (c + 1) * CHUNK)
+            cache[c] = _draw_chunk(kind, (shape[0], c1 - c0) + tuple(shape[2:]), device, seed, c, lo, hi)
+        out[i] = cache[c][r // n, t - c * CHUNK]
     return out
 
 
@@ -177,6 +196,42 @@ def attn_inputs(wl: Workload, layer: int, device="cpu") -> dict:
     else:
         v = _draw("normal", (wl.B, wl.S, wl.DV), device, seed_of(wl, layer, T_V))
         at["v"] = v.to(torch.bfloat16).contiguous()
+    return at
+
+
+def indexer_rows(wl: Workload, layer: int, rows, device="cpu") -> dict:
+    """Indexer operands with only the given query rows drawn: q_rows [n,HI,DI], w_rows,
+    q_scale_rows, plus the full keys; identical values to indexer_inputs at those rows."""
+    assert wl.values in ("gauss", "correlated"), "row subsets are for the Gaussian workloads"
+    qs = (wl.B, wl.T, wl.HI, wl.DI)
+    ws = (wl.B, wl.T, wl.HI)
+    full = indexer_inputs(wl.replace(T=1, q_pos0=0), layer, device)  # keys only matter here
+    if wl.values == "gauss":
+        q = _draw_rows("normal", qs, device, seed_of(wl, layer, T_Q_I), rows)
+        w = _draw_rows("uniform", ws, device, seed_of(wl, layer, T_W), rows) / 8.0
+    else:
+        q = _draw_rows("normal", qs, device, seed_of(wl, 0, T_BASE_Q_I), rows)
+        q += 0.3 * _draw_rows("normal", qs, device, seed_of(wl, layer, T_Q_I), rows)
+        w = _draw_rows("uniform", ws, device, seed_of(wl, 0, T_W), rows) / 8.0
+    ix = dict(k=full["k"], k_scale=full["k_scale"], w_rows=w.contiguous(), T=wl.T, S=wl.S,
+              q_pos0=wl.q_pos0, diag=wl.diag, B=wl.B)
+    if wl.idx_dtype == "bf16":
+        ix["q_rows"], ix["q_scale_rows"] = q.to(torch.bfloat16).contiguous(), None
+    else:
+        ix["q_rows"], ix["q_scale_rows"] = quantize_e4m3_per_token(q, 1)
+    return ix
+
+
+def attn_rows(wl: Workload, layer: int, rows, device="cpu") -> dict:
+    """Attention operands with only the given query rows drawn (q_rows [n,H,DQK]) plus the
+    full KV; identical values to attn_inputs at those rows."""
+    q = _draw_rows("normal", (wl.B, wl.T, wl.H, wl.DQK), device, seed_of(wl, layer, T_Q), rows)
+    at = dict(q_rows=q.to(torch.bfloat16).contiguous(), d_v=wl.DV, scale=wl.scale, T=wl.T)
+    kv = _draw("normal", (wl.B, wl.S, wl.DQK), device, seed_of(wl, layer, T_KV))
+    at["k"] = kv.to(torch.bfloat16).contiguous()
+    at["v"] = None
+    if not wl.latent:
+        at["v"] = _draw("normal", (wl.B, wl.S, wl.DV), device, seed_of(wl, layer, T_V)).to(torch.bfloat16)
     return at
 
 

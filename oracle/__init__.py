@@ -150,17 +150,25 @@ def indexer_scores(ix: dict, rows=None) -> np.ndarray:
 
     ``ix`` holds q [B,T,HI,DI], w [B,T,HI], k [B,S,DI] (bf16 or float8_e4m3fn), optional
     q_scale [B,T] / k_scale [B,S] fp32, q_pos0 (row i sits at position q_pos0 + i), diag."""
-    q, k, w = ix["q"], ix["k"], ix["w"]
-    B, T, HI, DI = q.shape
+    k = ix["k"]
     S = k.shape[1]
-    dt = _dtype_code(q)
+    if "q_rows" in ix:  # operands already restricted to `rows` (flat ids over [B, T])
+        qr, wr, qsr = ix["q_rows"], ix["w_rows"], ix.get("q_scale_rows")
+        T, HI, DI = ix["T"], qr.shape[1], qr.shape[2]
+        r = _rows(rows, 0)
+    else:
+        q, w, qs = ix["q"], ix["w"], ix.get("q_scale")
+        B, T, HI, DI = q.shape
+        r = _rows(rows, B * T)
+        qr, wr = _take_rows(q, r, 2), _take_rows(w, r, 2)
+        qsr = _take_rows(qs, r, 2) if qs is not None else None
+    dt = _dtype_code(qr)
     npdt = np.uint8 if dt == E4M3 else np.uint16
-    r = _rows(rows, B * T)
-    qa = _raw(_take_rows(q, r, 2), npdt)
+    qa = _raw(qr, npdt)
     ka = _raw(k, npdt)
-    wa = _raw(_take_rows(w, r, 2).float(), np.float32)
-    qs, ks = ix.get("q_scale"), ix.get("k_scale")
-    qsa = _raw(_take_rows(qs, r, 2).float(), np.float32) if qs is not None else None
+    wa = _raw(wr.float(), np.float32)
+    ks = ix.get("k_scale")
+    qsa = _raw(qsr.float(), np.float32) if qsr is not None else None
     ksa = _raw(ks.float(), np.float32) if ks is not None else None
     rb = np.ascontiguousarray(r // T)
     rp = np.ascontiguousarray(r % T + int(ix.get("q_pos0", 0)))
@@ -188,6 +196,8 @@ def topk_rows(scores: np.ndarray, n_valid, k: int) -> np.ndarray:
 def row_visible(ix_or_shape: dict, rows) -> np.ndarray:
     """Visible-key count of each flat row b*T+i."""
     T = ix_or_shape["T"] if "T" in ix_or_shape else ix_or_shape["q"].shape[1]
+    if "q_rows" in ix_or_shape:
+        T = ix_or_shape["T"]
     S = ix_or_shape["S"] if "S" in ix_or_shape else ix_or_shape["k"].shape[1]
     q_pos0 = int(ix_or_shape.get("q_pos0", 0))
     diag = int(ix_or_shape.get("diag", 0))
@@ -198,8 +208,7 @@ def row_visible(ix_or_shape: dict, rows) -> np.ndarray:
 
 def indexer_topk(ix: dict, k: int, rows=None, return_scores: bool = False):
     """Index rows [n_rows, k] of a full (F) layer: scores, then top-k."""
-    B, T = ix["q"].shape[:2]
-    r = _rows(rows, B * T)
+    r = _rows(rows, ix["q"].shape[0] * ix["q"].shape[1]) if "q" in ix else _rows(rows, 0)
     sc = indexer_scores(ix, r)
     idx = topk_rows(sc, row_visible(ix, r), k)
     return (idx, sc) if return_scores else idx
@@ -212,13 +221,19 @@ def sparse_attn(at: dict, idx_rows, rows=None):
 
     ``at`` holds q [B,T,H,DQK] bf16, k [B,S,>=DQK] bf16, optional v [B,S,>=DV] bf16
     (absent: v is k, the latent-KV form), d_v, scale.  ``idx_rows`` is [n_rows, kk]."""
-    q, k = at["q"], at["k"]
+    k = at["k"]
     v = at.get("v")
-    B, T, H, DQK = q.shape
     S, k_ld = k.shape[1], k.shape[2]
     DV = int(at["d_v"])
-    r = _rows(rows, B * T)
-    qa = _raw(_take_rows(q, r, 2), np.uint16)
+    if "q_rows" in at:  # queries already restricted to `rows`
+        qr, T = at["q_rows"], at["T"]
+        r = _rows(rows, 0)
+    else:
+        B, T = at["q"].shape[:2]
+        r = _rows(rows, B * T)
+        qr = _take_rows(at["q"], r, 2)
+    H, DQK = qr.shape[1], qr.shape[2]
+    qa = _raw(qr, np.uint16)
     ka = _raw(k, np.uint16)
     if v is None:
         va, v_ld = ka, k_ld

@@ -1,0 +1,87 @@
+"""Full-size workloads through the same call the benchmark times (one F,S,S,S group via
+indexshare_group_forward), checked against the oracle on sampled query rows.
+
+Index rows: bit-exact on the small-integer workload; recall >= 0.999 plus validity (every
+selected position scores within the fp32 rounding bound of the oracle's k-th score) on the
+Gaussian ones.  Attention: the oracle recomputes each sampled row over the GPU's own index
+row (so near-ties of the selection do not leak into the attention check); max-abs <= 2e-2.
+"""
+import numpy as np
+import pytest
+import torch
+
+import long_context_sparse_tcgen05_gb300 as dsa
+import oracle
+from long_context_sparse_tcgen05_gb300 import synth
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from long_context_sparse_tcgen05_gb300 import build
+    build.build()
+    dsa.load_library()
+    dsa.read_device_flags()
+
+
+def _subset_batches(d: dict, keys, bsel):
+    out = dict(d)
+    for k in keys:
+        if out.get(k) is not None:
+            out[k] = out[k][bsel].contiguous()
+    return out
+
+
+@pytest.mark.parametrize("name,n_rows", [("tiny_l1k", 1024), ("prefill_16k", 48), ("prefill_128k", 24),
+                                         ("decode_b32_200k", 8), ("chunked_prefill_1m", 12)])
+def test_workload_group_sampled_rows(name, n_rows):
+    wl = synth.WORKLOADS[name]
+    layers = [synth.layer_inputs(wl, l, DEV) for l in range(4)]
+    outs, lses, bufs = dsa.indexshare_group_forward(layers, "FSSS", wl.k)
+    torch.cuda.synchronize()
+    assert dsa.read_device_flags() == 0
+    idx = bufs[0].reshape(wl.B * wl.T, wl.k)
+
+    if wl.B > 1:  # decode: check whole sequences (one row each), a few of them
+        bsel = torch.linspace(0, wl.B - 1, n_rows).long().tolist()
+        rows = bsel
+        ix = _subset_batches(layers[0]["ix"], ["q", "w", "q_scale", "k", "k_scale"], bsel)
+        ats = [_subset_batches(l["at"], ["q", "k", "v"], bsel) for l in layers]
+        orc_rows = list(range(len(bsel)))
+    else:
+        rows = synth.sample_rows(wl, n_rows)
+        ix, ats, orc_rows = layers[0]["ix"], [l["at"] for l in layers], rows
+
+    got_idx = idx[torch.as_tensor(rows, device=DEV)].cpu().numpy()
+    ref_idx, ref_sc = oracle.indexer_topk(ix, wl.k, orc_rows, return_scores=True)
+    if wl.values == "int":
+        assert np.array_equal(got_idx, ref_idx)
+    else:
+        nv = oracle.row_visible(ix, orc_rows)
+        recalls = []
+        for r in range(len(rows)):
+            g = got_idx[r][got_idx[r] >= 0]
+            e = ref_idx[r][ref_idx[r] >= 0]
+            assert len(g) == len(e) and np.all(np.diff(g) > 0) and np.all(g < nv[r])
+            recalls.append(len(np.intersect1d(g, e)) / len(e) if len(e) else 1.0)
+            if 0 < len(e) < nv[r]:
+                tau = np.sort(ref_sc[r, :nv[r]])[::-1][len(e) - 1]
+                assert ref_sc[r, g].min() >= tau - 1e-4 * abs(tau)
+        assert np.mean(recalls) >= 0.999, (np.mean(recalls), np.min(recalls))
+
+    for l in range(4):
+        ref_o, ref_l = oracle.sparse_attn(ats[l], got_idx, orc_rows)
+        o = outs[l].reshape(wl.B * wl.T, wl.H, wl.DV)[torch.as_tensor(rows, device=DEV)].float().cpu().numpy()
+        assert np.abs(o - ref_o).max() <= 2e-2, (l, np.abs(o - ref_o).max())
+        gl = lses[l].reshape(wl.B * wl.T, wl.H)[torch.as_tensor(rows, device=DEV)].cpu().numpy()
+        fin = np.isfinite(ref_l)
+        assert np.array_equal(np.isfinite(gl), fin)
+        if fin.any():
+            assert np.abs(gl[fin] - ref_l[fin]).max() <= 1e-3
+    del layers, outs, lses, bufs
+    torch.cuda.empty_cache()

@@ -1,0 +1,34 @@
+"""Seeded generators: determinism, row-subset draws equal to full draws, value recipes."""
+import torch
+
+from long_context_sparse_tcgen05_gb300 import synth
+
+
+def test_row_subsets_equal_full_draws():
+    wl = synth.WORKLOADS["prefill_128k"].replace(T=9000, S=9000, H=4, DQK=64, DV=32)
+    rows = [0, 5, 4095, 4096, 8999]
+    full = synth.indexer_inputs(wl, 1)
+    sub = synth.indexer_rows(wl, 1, rows)
+    assert torch.equal(sub["q_rows"].view(torch.uint8), full["q"][0, rows].view(torch.uint8))
+    assert torch.equal(sub["q_scale_rows"], full["q_scale"][0, rows])
+    assert torch.equal(sub["w_rows"], full["w"][0, rows])
+    assert torch.equal(sub["k"].view(torch.uint8), full["k"].view(torch.uint8))
+    at = synth.attn_inputs(wl, 2)
+    ar = synth.attn_rows(wl, 2, rows)
+    assert torch.equal(ar["q_rows"], at["q"][0, rows]) and torch.equal(ar["k"], at["k"])
+
+
+def test_recipes():
+    wl = synth.WORKLOADS["tiny_l1k"]
+    ix = synth.indexer_inputs(wl, 0)
+    q = ix["q"].float()
+    assert q.min() >= -3 and q.max() <= 3 and torch.equal(q, q.round())
+    assert ix["w"].min() >= 1 and ix["w"].max() <= 4
+    ix2 = synth.indexer_inputs(wl, 0)
+    assert torch.equal(ix["q"], ix2["q"])
+    w8 = synth.WORKLOADS["prefill_128k"].replace(T=512, S=512)
+    f = synth.indexer_inputs(w8, 0)
+    assert f["q"].dtype == torch.float8_e4m3fn
+    amax = (f["q"].float().abs().amax(dim=(2, 3)))
+    assert torch.all(amax <= 448) and torch.all(amax >= 416)  # scale = amax / 448
+    assert torch.all(f["w"] >= 0) and torch.all(f["w"] <= 1 / 8)
