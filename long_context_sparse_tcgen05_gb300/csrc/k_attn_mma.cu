@@ -59,10 +59,8 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& lo_r, float& hi_r) {
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  lo_r = __low2float(v);
-  hi_r = __high2float(v);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
@@ -215,11 +213,13 @@ __global__ void __launch_bounds__(AtCfg<HP, DQK, DV, SEPV, NB>::kThreads, 1)
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int key = wn * 16 + nt * 8 + 2 * c;
-      float a0, a1, a2, a3;
-      const uint32_t u01 = pack_bf16(ex2(s[nt][0] - mu0), ex2(s[nt][1] - mu0), a0, a1);
-      const uint32_t u23 = pack_bf16(ex2(s[nt][2] - mu1), ex2(s[nt][3] - mu1), a2, a3);
-      rs0 += a0 + a1;
-      rs1 += a2 + a3;
+      // the row sums use the fp32 weights; P enters the PV product rounded to bf16
+      const float p0 = ex2(s[nt][0] - mu0), p1 = ex2(s[nt][1] - mu0);
+      const float p2 = ex2(s[nt][2] - mu1), p3 = ex2(s[nt][3] - mu1);
+      const uint32_t u01 = pack_bf16(p0, p1);
+      const uint32_t u23 = pack_bf16(p2, p3);
+      rs0 += p0 + p1;
+      rs1 += p2 + p3;
       *reinterpret_cast<uint32_t*>(p_s + hr0 * C::kPPad + key) = u01;
       *reinterpret_cast<uint32_t*>(p_s + hr1 * C::kPPad + key) = u23;
     }
