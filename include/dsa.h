@@ -174,6 +174,23 @@ dsa_status topk_overlap(const int32_t* a, const int32_t* b, int32_t rows, int32_
  * Synchronises `stream`. */
 dsa_status dsa_read_device_flags(void* ws, uint32_t* flags_out, void* stream);
 
+/* Indexer -> top-k without a caller workspace.  The paper has no counterpart to this call;
+ * it exists for callers that cannot allocate device memory where they call the library
+ * (allocator or memory-pool callbacks, runtimes that pre-partition all device memory,
+ * code that must not grow its footprint after start-up).  Results are identical to
+ * dsa_topk with a DSA_TOPK_FROM_INDEXER source.
+ *   ix, k, idx  as for dsa_topk; idx [B,T,k] int32 is the caller's output buffer.
+ *   flags       device uint32 the kernels OR DSA_FLAG_* bits into, or NULL to use a word
+ *               inside the library's array (cleared at the start of every call).
+ * Scratch: a file-scope device array of 64 MiB, held by every GPU that loads the library
+ * until the process exits.  B*S*4 must not exceed 64 MiB - 256 B (DSA_ERR_UNSUPPORTED
+ * otherwise); no cudaMalloc/cudaFree or allocating library routine is called.  The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress); make that
+ * first call before any stream capture.  All calls share the one array: calls whose work
+ * overlaps on the GPU (other streams, other host threads) race on it. */
+dsa_status dsa_topk_indexer_noalloc(const dsa_indexer_args* ix, int32_t k, int32_t* idx,
+                                    uint32_t* flags, void* stream);
+
 /* Name of a status code; message of the calling thread's last failure. */
 const char* dsa_status_string(dsa_status s);
 const char* dsa_last_error(void);

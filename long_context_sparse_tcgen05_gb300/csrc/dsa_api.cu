@@ -118,6 +118,11 @@ dsa_status run_indexer_topk(const dsa_indexer_args* ix, int32_t k, int32_t* idx,
 
 }  // namespace
 
+namespace dsa {
+dsa_status validate_indexer(const dsa_indexer_args* ix) { return check_indexer(ix); }
+dsa_status record_error(dsa_status s, const char* msg) { return fail(s, "%s", msg); }
+}  // namespace dsa
+
 extern "C" {
 
 size_t dsa_workspace_size(const dsa_indexer_args* ix, int32_t k) {

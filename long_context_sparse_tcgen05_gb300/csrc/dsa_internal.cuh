@@ -17,6 +17,11 @@ constexpr size_t kWsScratch = DSA_WS_MIN;
 // Kernel launches issued by this library since load (diagnostics; see dsa_launch_count).
 void count_launches(uint64_t n);
 
+// Host-side helpers shared by the entry points: argument checks of an indexer operand set
+// (sets the thread's last-error message on failure) and recording a failure message.
+dsa_status validate_indexer(const dsa_indexer_args* ix);
+dsa_status record_error(dsa_status s, const char* msg);
+
 // Key transform of the selection order: a larger float gives a larger unsigned key.
 // -0 and +0 share one key; NaN maps below -inf.
 __device__ __forceinline__ uint32_t score_key(float f) {
