@@ -104,6 +104,7 @@ dsa_status run_indexer_topk(const dsa_indexer_args* ix, int32_t k, int32_t* idx,
     L.q_pos0 = ix->q_pos0; L.diag = ix->diag;
     L.t0 = (int)t0; L.Tc = Tc;
     L.out = sc; L.ld = ix->S; L.out_bstride = (int64_t)Tc * ix->S; L.write_masked = 0;
+    L.flags = ws_flags(ws);
     cudaError_t e = dsa::launch_indexer_scores(L, st);
     if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
     dsa::TopkLaunch P{};
@@ -150,6 +151,7 @@ dsa_status dsa_indexer_scores(const dsa_indexer_args* ix, float* scores, int64_t
   L.q_pos0 = ix->q_pos0; L.diag = ix->diag;
   L.t0 = 0; L.Tc = ix->T;
   L.out = scores; L.ld = ld; L.out_bstride = (int64_t)ix->T * ld; L.write_masked = 1;
+  L.flags = ws_flags(ws);
   cudaError_t e = dsa::launch_indexer_scores(L, as_stream(stream));
   return e == cudaSuccess ? DSA_OK : cuda_fail(e, "indexer launch");
 }

@@ -48,8 +48,10 @@ struct IndexerLaunch {
   int64_t ld;
   int64_t out_bstride;
   int write_masked;     // 1: write -inf over [n_t, S) as well
+  uint32_t* flags;      // device flag word (DSA_FLAG_TIMEOUT)
 };
-cudaError_t launch_indexer_scores(const IndexerLaunch& p, cudaStream_t st);
+cudaError_t launch_indexer_scores(const IndexerLaunch& p, cudaStream_t st);     // tcgen05 path
+cudaError_t launch_indexer_scores_mma(const IndexerLaunch& p, cudaStream_t st); // mma.sync path
 
 // Top-k over materialised score rows: rows [t0, t0 + Tc) of every sequence,
 // scores[b*bstride + (t - t0)*ld + s], output idx[(b*T + t)*k + j].

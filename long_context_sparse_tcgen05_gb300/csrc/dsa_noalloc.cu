@@ -77,6 +77,7 @@ extern "C" dsa_status dsa_topk_indexer_noalloc(const dsa_indexer_args* ix, int32
     L.q_pos0 = ix->q_pos0; L.diag = ix->diag;
     L.t0 = (int)t0; L.Tc = Tc;
     L.out = sc; L.ld = ix->S; L.out_bstride = (int64_t)Tc * ix->S; L.write_masked = 0;
+    L.flags = flag_word;
     cudaError_t e = dsa::launch_indexer_scores(L, st);
     if (e != cudaSuccess) return dsa::record_error(DSA_ERR_CUDA, cudaGetErrorString(e));
     dsa::TopkLaunch P{};

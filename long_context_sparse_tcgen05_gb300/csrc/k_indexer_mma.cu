@@ -196,7 +196,7 @@ cudaError_t launch_tb(const IndexerLaunch& p, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_indexer_scores(const IndexerLaunch& p, cudaStream_t st) {
+cudaError_t launch_indexer_scores_mma(const IndexerLaunch& p, cudaStream_t st) {
   if (p.B <= 0 || p.Tc <= 0 || p.S <= 0) return cudaSuccess;
   if (p.HI == 64 && p.DI == 128) return p.fp8 ? launch_tb<64, 128, true, 4>(p, st) : launch_tb<64, 128, false, 4>(p, st);
   if (p.HI == 4 && p.DI == 64 && !p.fp8) return launch_tb<4, 64, false, 32>(p, st);

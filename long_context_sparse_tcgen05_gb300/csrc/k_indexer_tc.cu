@@ -1,0 +1,330 @@
+// Lightning-indexer scores on the 5th-generation tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+//   I[t,s] = sq[t] * sk[s] * sum_h w[t,h] * ReLU(q[t,h] . k[s])
+//
+// One CTA owns a block of query tokens and walks every key tile they can see:
+//   * MMA shape M = 128 keys (A: the key tile, K-major), N = 256 columns = tokens x heads
+//     (B: the stationary query tile, K-major), K = d_I; fp32 accumulators in TMEM, two
+//     256-column buffers so the epilogue of tile i overlaps the MMAs of tile i+1;
+//   * warp 0 streams key tiles with TMA (128-byte swizzle) through a ring of smem stages;
+//   * warp 1 allocates TMEM and issues the MMAs from one thread (tcgen05.commit frees the
+//     stage and publishes the accumulator);
+//   * warps 2..9 read the accumulator rows (TMEM lane = key) with tcgen05.ld, apply ReLU and
+//     the head weights with packed fp32x2 FMAs -- the head sum never leaves the thread --
+//     apply the per-token scales and write the fp32 score row with coalesced stores.
+// Every wait is bounded; a timeout raises DSA_FLAG_TIMEOUT, drains the copies in flight,
+// frees TMEM and returns.
+#include <cuda_bf16.h>
+
+#include <cstdlib>
+#include <mutex>
+
+#include "dsa_internal.cuh"
+#include "sm100.cuh"
+
+namespace dsa {
+namespace {
+using namespace sm100;
+
+constexpr int kM = 128;        // keys per tile
+constexpr int kN = 256;        // token x head columns per tile
+constexpr int kEpiWarps = 8;   // two per TMEM lane quarter, one per column half
+constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr uint32_t kTmemCols = 2 * kN;
+
+template <int HI, int DI, bool FP8>
+struct Cfg {
+  static constexpr int kEsz = FP8 ? 1 : 2;
+  static constexpr int kRowBytes = DI * kEsz;
+  static constexpr int kKBlocks = kRowBytes / 128;  // 128-byte swizzle atoms along d_I
+  static constexpr int kAtomElems = 128 / kEsz;
+  static constexpr int kTB = kN / HI;               // tokens per CTA
+  static constexpr uint32_t kQBlock = kN * 128;
+  static constexpr uint32_t kKBlock = kM * 128;
+  static constexpr uint32_t kQBytes = kN * kRowBytes;
+  static constexpr uint32_t kKTile = kM * kRowBytes;
+  static constexpr int kStages = FP8 ? 6 : 4;
+  static constexpr int kCols = kN / 2;              // columns read by one epilogue warp
+  static constexpr int kBarOff = kQBytes + kStages * kKTile;
+  static constexpr size_t kSmem = 1024 + kBarOff + 256 + (size_t)kTB * HI * 4;
+  static constexpr uint32_t kIdesc = idesc_mn(FP8 ? 0u : 1u, FP8 ? 0u : 1u, kM, kN);
+  static_assert(kRowBytes % 128 == 0, "d_I must fill whole 128-byte rows");
+  static_assert(kN % HI == 0, "heads must tile the N columns");
+};
+
+__device__ __forceinline__ int64_t visible_keys(const IndexerLaunch& p, int t_local) {
+  int64_t n = p.q_pos0 + p.t0 + t_local + p.diag;
+  return n < 0 ? 0 : (n > p.S ? (int64_t)p.S : n);
+}
+
+template <int HI, int DI, bool FP8>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_indexer_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 IndexerLaunch p) {
+  using C = Cfg<HI, DI, FP8>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_s = smem;
+  uint8_t* k_s = smem + C::kQBytes;
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* k_empty = k_full + C::kStages;
+  uint64_t* q_full = k_empty + C::kStages;
+  uint64_t* tm_full = q_full + 1;
+  uint64_t* tm_empty = tm_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tm_empty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* w_s = reinterpret_cast<float*>(smem + C::kBarOff + 256);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nblk = (p.Tc + C::kTB - 1) / C::kTB;
+  const int tb = nblk - 1 - (int)blockIdx.x;  // latest (longest) token blocks first
+  const int b = blockIdx.y;
+  const int tl0 = tb * C::kTB;
+  const int ntok = min(C::kTB, p.Tc - tl0);
+  const int64_t nmax = visible_keys(p, tl0 + ntok - 1);
+  const int ktiles = (int)((nmax + kM - 1) / kM);
+  const int64_t row0 = (int64_t)b * p.T + p.t0 + tl0;  // flat (b, t) of the block's first token
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(k_full + i, 1);
+      mbar_init(k_empty + i, 1);
+    }
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tm_full + i, 1);
+      mbar_init(tm_empty + i, kEpiWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  for (int i = threadIdx.x; i < C::kTB * HI; i += kThreads)
+    w_s[i] = (i / HI < ntok) ? __ldg(p.w + row0 * HI + i) : 0.f;
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0 && ktiles > 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      mbar_arrive_expect_tx(q_full, C::kQBytes);
+      for (int kb = 0; kb < C::kKBlocks; ++kb)
+        tma_load_3d(q_s + kb * C::kQBlock, &tm_q, q_full, kb * C::kAtomElems, (p.t0 + tl0) * HI, b);
+      int issued = 0;
+      for (int kt = 0; kt < ktiles; ++kt) {
+        const int st = kt % C::kStages;
+        const uint32_t ph = (kt / C::kStages) & 1;
+        if (!mbar_wait(k_empty + st, ph ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(k_full + st, C::kKTile);
+        for (int kb = 0; kb < C::kKBlocks; ++kb)
+          tma_load_3d(k_s + st * C::kKTile + kb * C::kKBlock, &tm_k, k_full + st, kb * C::kAtomElems, kt * kM, b);
+        issued = kt + 1;
+      }
+      if (*abort_flag) {  // let every copy still in flight land before the CTA can exit
+        mbar_wait_drain(q_full, 0);
+        for (int kt = issued > C::kStages ? issued - C::kStages : 0; kt < issued; ++kt)
+          mbar_wait_drain(k_full + kt % C::kStages, (kt / C::kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0 && ktiles > 0) {
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      int done = 0;
+      const uint32_t qa = smem_addr(q_s);
+      for (int kt = 0; ok && kt < ktiles; ++kt) {
+        const int st = kt % C::kStages;
+        const uint32_t ph = (kt / C::kStages) & 1;
+        const int buf = kt & 1;
+        const uint32_t bph = (kt >> 1) & 1;
+        if (!mbar_wait(tm_empty + buf, bph ^ 1, abort_flag)) break;
+        if (!mbar_wait(k_full + st, ph, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * kN;
+        const uint32_t ka = smem_addr(k_s + st * C::kKTile);
+#pragma unroll
+        for (int kb = 0; kb < C::kKBlocks; ++kb)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t ad = desc_sw128(ka + kb * C::kKBlock + j * 32);
+            const uint64_t bd = desc_sw128(qa + kb * C::kQBlock + j * 32);
+            if constexpr (FP8)
+              mma_fp8(d, ad, bd, C::kIdesc, (kb | j) != 0);
+            else
+              mma_bf16(d, ad, bd, C::kIdesc, (kb | j) != 0);
+          }
+        mma_commit(k_empty + st);
+        mma_commit(tm_full + buf);
+        done = kt + 1;
+      }
+      if (*abort_flag && done > 0) mbar_wait_drain(tm_full + ((done - 1) & 1), ((done - 1) >> 1) & 1);
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int e = warp - 2;
+    const int lq = warp & 3;                 // TMEM lane quarter this warp may read
+    const int ch = e >> 2;                   // column half
+    const int key_in_tile = lq * 32 + lane;  // TMEM lane = key
+    const uint32_t t_lane = tmem + ((uint32_t)(lq * 32) << 16);
+    float* out_b = p.out + (int64_t)b * p.out_bstride;
+    const float* skg = FP8 ? p.k_scale + (int64_t)b * p.S : nullptr;
+
+    constexpr int kTokW = C::kCols / HI > 0 ? C::kCols / HI : 1;  // tokens per epilogue warp
+    unsigned long long w2[HI >= 64 ? C::kCols / 2 : 1];             // head weights, packed pairs
+    if constexpr (HI >= 64) {
+#pragma unroll
+      for (int c = 0; c < C::kCols / 2; ++c) w2[c] = pack2(w_s[ch * C::kCols + 2 * c], w_s[ch * C::kCols + 2 * c + 1]);
+    }
+
+    auto store = [&](int tok, int key, float v) {  // tok: token index within the CTA block
+      if (tok >= ntok || key >= p.S) return;
+      const int64_t n = visible_keys(p, tl0 + tok);
+      float* dst = out_b + (int64_t)(tl0 + tok) * p.ld + key;
+      if (key < n) {
+        if constexpr (FP8) v *= __ldg(p.q_scale + row0 + tok) * __ldg(skg + key);
+        *dst = v;
+      } else if (p.write_masked) {
+        *dst = -INFINITY;
+      }
+    };
+
+    for (int kt = 0; kt < ktiles; ++kt) {
+      const int buf = kt & 1;
+      const uint32_t bph = (kt >> 1) & 1;
+      if (!mbar_wait(tm_full + buf, bph, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t col0 = t_lane + buf * kN + ch * C::kCols;
+      const int key = kt * kM + key_in_tile;
+      float score[kTokW];
+      if constexpr (HI >= 64) {
+        // 32 columns per load = half of one token's heads
+#pragma unroll
+        for (int tk = 0; tk < kTokW; ++tk) {
+          unsigned long long acc = 0ull;
+#pragma unroll
+          for (int half = 0; half < HI / 32; ++half) {
+            uint32_t r[32];
+            tmem_ld32(col0 + tk * HI + half * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float x0 = fmaxf(__uint_as_float(r[2 * j]), 0.f);
+              const float x1 = fmaxf(__uint_as_float(r[2 * j + 1]), 0.f);
+              acc = fma2(w2[(tk * HI + half * 32) / 2 + j], pack2(x0, x1), acc);
+            }
+          }
+          score[tk] = lo2(acc) + hi2(acc);
+        }
+      } else {
+        // 32 columns per load = 32 / HI whole tokens; weights read from shared memory
+#pragma unroll
+        for (int cb = 0; cb < C::kCols / 32; ++cb) {
+          uint32_t r[32];
+          tmem_ld32(col0 + cb * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int tt = 0; tt < 32 / HI; ++tt) {
+            const int tk = cb * (32 / HI) + tt;
+            const float* wt = w_s + (ch * kTokW + tk) * HI;
+            float acc = 0.f;
+#pragma unroll
+            for (int h = 0; h < HI; ++h) acc += wt[h] * fmaxf(__uint_as_float(r[tt * HI + h]), 0.f);
+            score[tk] = acc;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tm_empty + buf);
+#pragma unroll
+      for (int tk = 0; tk < kTokW; ++tk) store(ch * kTokW + tk, key, score[tk]);
+    }
+    if (p.write_masked && !*abort_flag) {  // keys beyond every visible tile
+      for (int tk = 0; tk < kTokW; ++tk) {
+        const int tok = ch * kTokW + tk;
+        if (tok >= ntok) break;
+        for (int key = ktiles * kM + key_in_tile; key < p.S; key += kM)
+          out_b[(int64_t)(tl0 + tok) * p.ld + key] = -INFINITY;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag && p.flags) atomicOr(p.flags, DSA_FLAG_TIMEOUT);
+}
+
+// ---- host side -------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 3-D map over [dim2][dim1][row_elems] with a box of (atom_elems x box_rows x 1), 128-byte swizzle.
+cudaError_t make_map(CUtensorMap* m, const void* base, bool fp8, int row_elems, int64_t dim1, int64_t dim2,
+                     int atom_elems, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const int esz = fp8 ? 1 : 2;
+  cuuint64_t dims[3] = {(cuuint64_t)row_elems, (cuuint64_t)dim1, (cuuint64_t)dim2};
+  cuuint64_t strides[2] = {(cuuint64_t)row_elems * esz, (cuuint64_t)(row_elems * esz) * (cuuint64_t)dim1};
+  cuuint32_t box[3] = {(cuuint32_t)atom_elems, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int HI, int DI, bool FP8>
+cudaError_t launch_cfg(const IndexerLaunch& p, cudaStream_t st) {
+  using C = Cfg<HI, DI, FP8>;
+  CUtensorMap tq, tk;
+  cudaError_t e = make_map(&tq, p.q, FP8, DI, (int64_t)p.T * HI, p.B, C::kAtomElems, kN);
+  if (e != cudaSuccess) return e;
+  if ((e = make_map(&tk, p.k, FP8, DI, p.S, p.B, C::kAtomElems, kM)) != cudaSuccess) return e;
+  auto kern = k_indexer_tc<HI, DI, FP8>;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem)) != cudaSuccess)
+    return e;
+  dim3 grid((p.Tc + C::kTB - 1) / C::kTB, p.B);
+  kern<<<grid, kThreads, C::kSmem, st>>>(tq, tk, p);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_indexer_scores(const IndexerLaunch& p, cudaStream_t st) {
+  static const bool use_mma = getenv("DSA_INDEXER_MMA") != nullptr;
+  if (use_mma) return launch_indexer_scores_mma(p, st);
+  if (p.B <= 0 || p.Tc <= 0 || p.S <= 0) return cudaSuccess;
+  if (p.HI == 64 && p.DI == 128) return p.fp8 ? launch_cfg<64, 128, true>(p, st) : launch_cfg<64, 128, false>(p, st);
+  if (p.HI == 4 && p.DI == 64 && !p.fp8) return launch_cfg<4, 64, false>(p, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dsa
