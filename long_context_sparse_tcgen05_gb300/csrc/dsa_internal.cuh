@@ -81,6 +81,9 @@ struct AttnLaunch {
   uint32_t* flags;
 };
 cudaError_t launch_sparse_attn(const AttnLaunch& p, cudaStream_t st);
+// tcgen05 sparse MLA kernel for the latent shape (H = 64, d_qk = 576, d_v = 512, v = k)
+bool sparse_mla_tc_supported(const AttnLaunch& p);
+cudaError_t launch_sparse_mla_tc(const AttnLaunch& p, cudaStream_t st);
 
 cudaError_t launch_topk_overlap(const int32_t* a, const int32_t* b, int rows, int k,
                                 float* per_row, double* mean_dev, uint32_t* flags,

@@ -1,0 +1,582 @@
+// Sparse MLA attention over index-selected latent-KV rows on tcgen05 tensor cores.
+//
+// Shapes: H = 64 query heads of width 576 (512 latent + 64 rope) attend, multi-query,
+// over k selected rows of a shared 576-wide latent KV; the value is the first 512 columns
+// of the same row, so each gathered row feeds both products.
+//
+// Persistent CTAs (one per SM) walk query rows.  For each row:
+//   * warps 0..3 load the query tile with TMA and gather the selected KV rows, 32 per block,
+//     with 16-byte cp.async copies into a 128-byte-swizzled ring of four stages (on this
+//     random-row pattern cp.async sustains about 1.8x the rate of TMA tile::gather4), and
+//     keep L2 warm with bulk prefetches of the rows eight blocks ahead;
+//   * warp 4 issues  S = Q K^T  (M = 64 heads, N = 32 keys, K = 576) into TMEM and
+//     O^T += V^T P^T  (M = 128 value dims x 4, N = 64 heads, K = 32 keys) -- the transposed
+//     value product keeps the 64 x 512 fp32 accumulator in 256 TMEM columns; it polls both
+//     queues and issues whichever is ready, so a late gather never holds back a PV product;
+//   * warps 5..8 run the online softmax (one head per TMEM lane, base-2 exponent, fp32 row
+//     sums, bf16 P double-buffered in shared memory).  The running maximum is raised only
+//     when a block exceeds it by more than 2^8; then O^T is rescaled in TMEM.  At the end
+//     they normalise O, write bf16 O and the natural-log LSE.
+// Entries of -1 are skipped (masked), out-of-range entries raise DSA_FLAG_BAD_INDEX and are
+// skipped.  Every wait is bounded (DSA_FLAG_TIMEOUT); TMEM is freed on every exit path.
+#include <cuda_bf16.h>
+
+#include <cstdlib>
+#include <mutex>
+
+#include "dsa_internal.cuh"
+#include "sm100.cuh"
+
+namespace dsa {
+namespace {
+using namespace sm100;
+
+constexpr int kH = 64, kDQK = 576, kDV = 512;
+constexpr int kNB = 32;                    // keys per block
+constexpr int kStages = 4;                 // gathered KV blocks in flight
+constexpr int kPF = 8;                     // blocks prefetched into L2 ahead of the gathers
+constexpr int kAtoms = kDQK / 64;          // 9 swizzle atoms of 64 bf16 per row
+constexpr uint32_t kAtomQ = kH * 128;      // 8 KB
+constexpr uint32_t kAtomKV = kNB * 128;    // 4 KB
+constexpr uint32_t kQBytes = kAtoms * kAtomQ;
+constexpr uint32_t kKVBytes = kAtoms * kAtomKV;
+constexpr uint32_t kPBytes = kH * kNB * 2;  // one P buffer (4 KB)
+constexpr int kProdWarps = 4;              // cp.async gather warps
+constexpr int kMmaWarp = kProdWarps;       // warp 4
+constexpr int kSmWarp0 = kProdWarps + 1;   // warps 5..8: softmax + epilogue
+constexpr int kThreads = (kProdWarps + 5) * 32;
+constexpr int kLag = 3;                    // copy groups left in flight before a block is published
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;              // O^T: 4 chunks x 64 columns
+constexpr uint32_t kColS = 256;            // S: 2 buffers x 32 columns
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.f;
+
+struct Bars {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_full[2], p_empty[2];
+  uint64_t o_full, o_empty;
+  uint64_t info_full[2], info_empty[2];
+};
+
+struct Small {
+  Bars bar;
+  uint32_t tmem;
+  int abort;
+  int nb[2];                       // blocks of the row in flight (by row parity)
+  uint8_t valid[kStages][kNB];     // per stage: key slot holds a valid row
+  float alpha[kH];
+  float lsum[kH];
+  int any_rescale[2][4];          // by block parity, so a fast warp never overwrites an unread flag
+};
+
+constexpr size_t kSmem = 1024 + kQBytes + kStages * kKVBytes + 2 * kPBytes + sizeof(Small);
+
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int r0, int r1,
+                                            int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+// Operand descriptors besides the K-major 128-byte-swizzled form of desc_sw128:
+// MN-major 128-byte swizzled (64-element MN atoms `lbo` bytes apart, 8-row K groups 1024 B
+// apart), and K-major without swizzle (8-row x 16-byte core matrices: `lbo` bytes apart
+// along K, `sbo` bytes apart along M/N).
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = desc_sw128(saddr);
+  d &= ~((uint64_t)0x3FFF << 16);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  return d;
+}
+__device__ __forceinline__ uint64_t desc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
+                    AttnLaunch p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_s = base;
+  uint8_t* kv_s = base + kQBytes;               // kStages stages
+  uint8_t* p_s = kv_s + kStages * kKVBytes;     // 2 buffers
+  Small* sm = reinterpret_cast<Small*>(p_s + 2 * kPBytes);
+  Bars& bar = sm->bar;
+  volatile int* abort_flag = &sm->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows = p.B * p.T;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar.q_full, 1);
+    mbar_init(&bar.q_empty, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bar.kv_full[i], kProdWarps * 32);
+      mbar_init(&bar.kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.s_full[i], 1);
+      mbar_init(&bar.s_empty[i], 4);
+      mbar_init(&bar.p_full[i], 4);
+      mbar_init(&bar.p_empty[i], 1);
+      mbar_init(&bar.info_full[i], 1);
+      mbar_init(&bar.info_empty[i], 2);
+    }
+    mbar_init(&bar.o_full, 1);
+    mbar_init(&bar.o_empty, 4);
+    sm->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&sm->tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem;
+
+  if (warp < kProdWarps) {
+    // ================= producers: row info, Q tile, KV gathers (cp.async), L2 prefetch ==========
+    // Each of the four warps copies 8 of a block's 32 rows: lane l moves 16-byte chunks
+    // l, l+32, l+64 of a 1152-byte row into the 128-byte-swizzled K-major layout the MMAs
+    // read.  A block is published (kv_full) once its copy group has landed, kLag groups later,
+    // after a proxy fence that hands the bytes to the tensor core.
+    const uint8_t* kvg = static_cast<const uint8_t*>(p.k);
+    const int64_t row_bytes = p.k_ld * 2;
+    const bool leader = warp == 0 && lane == 0;
+    int it = 0, qc = 0;
+    long long g = 0;    // global block counter
+    long long pub = 0;  // next block to publish
+    bool ok = true;
+    const bool vec = (p.kk & 3) == 0;
+    auto publish = [&]() {  // copies of block `pub` have landed (wait_group done)
+      fence_async_smem();
+      mbar_arrive(&bar.kv_full[pub % kStages]);
+      ++pub;
+    };
+    for (int row = blockIdx.x; ok && row < rows; row += gridDim.x, ++it) {
+      const int32_t* irow = p.idx + (int64_t)row * p.kk;
+      const int b = row / p.T;
+      const int64_t kvrow0 = (int64_t)b * p.S;
+      // blocks = 1 + (last entry other than -1) / kNB; all loads of the scan issued together
+      int last = -1;
+      if (vec) {
+        const int n4 = p.kk >> 2;
+        for (int c0 = 0; c0 < n4; c0 += 32 * 8) {
+          int4 v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int c = c0 + u * 32 + lane;
+            v[u] = c < n4 ? __ldg(reinterpret_cast<const int4*>(irow) + c) : make_int4(-1, -1, -1, -1);
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int c = 4 * (c0 + u * 32 + lane);
+            if (v[u].x != -1) last = max(last, c);
+            if (v[u].y != -1) last = max(last, c + 1);
+            if (v[u].z != -1) last = max(last, c + 2);
+            if (v[u].w != -1) last = max(last, c + 3);
+          }
+        }
+      } else {
+        for (int j = lane; j < p.kk; j += 32)
+          if (__ldg(irow + j) != -1) last = j;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+      const int nb = (last + kNB) / kNB;
+      if (warp == 0) {
+        if (lane == 0) ok = mbar_wait(&bar.info_empty[it & 1], ((it >> 1) & 1) ^ 1, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok && lane == 0) {
+          sm->nb[it & 1] = nb;
+          mbar_arrive(&bar.info_full[it & 1]);
+        }
+      }
+      if (!ok || *abort_flag) break;
+      if (nb == 0) continue;
+      auto prefetch_block = [&](int jb) {  // warp 0: L2 prefetch of one block's rows
+        const int e = jb * kNB + lane;
+        const int id = e < p.kk ? __ldg(irow + e) : -1;
+        if (id >= 0 && id < p.S) prefetch_l2(kvg + (kvrow0 + id) * row_bytes, kDQK * 2);
+      };
+      if (warp == 0) {
+        for (int jb = 0; jb < kPF && jb < nb; ++jb) prefetch_block(jb);
+        if (lane == 0 && row + (int)gridDim.x < rows)
+          prefetch_l2(static_cast<const __nv_bfloat16*>(p.q) + (int64_t)(row + gridDim.x) * kH * kDQK, kQBytes);
+        if (lane == 0) {
+          ok = mbar_wait(&bar.q_empty, (qc & 1) ^ 1, abort_flag);
+          if (ok) {
+            mbar_arrive_expect_tx(&bar.q_full, kQBytes);
+            for (int a = 0; a < kAtoms; ++a) tma_load_3d(q_s + a * kAtomQ, &tm_q, &bar.q_full, a * 64, 0, row);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+      ++qc;
+      for (int j = 0; ok && j < nb; ++j, ++g) {
+        const int st = (int)(g % kStages);
+        if (warp == 0 && j + kPF < nb) prefetch_block(j + kPF);
+        // ids of this warp's 8 rows
+        const int rl = warp * 8 + (lane & 7);
+        const int e = j * kNB + rl;
+        int id = e < p.kk ? __ldg(irow + e) : -1;
+        const bool valid = id >= 0 && id < p.S;
+        if (lane < 8 && !valid && id != -1) atomicOr(p.flags, DSA_FLAG_BAD_INDEX);
+        if (!valid) id = 0;
+        if (!(ok = mbar_wait(&bar.kv_empty[st], (uint32_t)((g / kStages) & 1) ^ 1, abort_flag))) break;
+        if (lane < 8) sm->valid[st][rl] = valid ? 1 : 0;
+        uint8_t* stage = kv_s + st * kKVBytes;
+#pragma unroll
+        for (int r8 = 0; r8 < 8; ++r8) {
+          const int rid = __shfl_sync(0xffffffffu, id, r8);
+          const bool rv = __shfl_sync(0xffffffffu, valid, r8);
+          const int r = warp * 8 + r8;
+          const uint8_t* src = kvg + (kvrow0 + rid) * row_bytes;
+#pragma unroll
+          for (int u = 0; u < 3; ++u) {
+            const int ch = lane + 32 * u;  // 16-byte chunk of the row
+            if (ch < kDQK * 2 / 16) {
+              const int a = ch >> 3, cc = ch & 7;
+              const uint32_t dst = smem_addr(stage + a * kAtomKV + r * 128 + ((cc ^ (r & 7)) << 4));
+              asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src + ch * 16),
+                           "r"(rv ? 16 : 0)
+                           : "memory");
+            }
+          }
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+        if (g - pub + 1 > kLag) {
+          asm volatile("cp.async.wait_group %0;\n" ::"n"(kLag) : "memory");
+          publish();
+        }
+      }
+      // end of row: publish everything, so the row's last S can run and free the Q tile
+      asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+      while (pub < g) publish();
+    }
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+    (void)leader;
+    if (*abort_flag && warp == 0 && lane == 0 && qc > 0) mbar_wait_drain(&bar.q_full, (uint32_t)((qc - 1) & 1));
+  } else if (warp == kMmaWarp) {
+    // ================= MMA issuer (one thread; never blocks on one stream while another can run) ==
+    const uint32_t id_s = idesc_mn(1, 1, kH, kNB);               // S: M=64 heads, N=32 keys
+    const uint32_t id_o = idesc_mn(1, 1, 128, kH) | (1u << 15);  // O^T: M=128 dims (MN-major A), N=64 heads
+    int it = 0, qc = 0, oc = 0;
+    long long g = 0;
+    bool ok = true;
+    for (int row = blockIdx.x; ok && row < rows; row += gridDim.x, ++it) {
+      int nb = 0;
+      if (lane == 0) {
+        ok = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag);
+        nb = sm->nb[it & 1];
+        mbar_arrive(&bar.info_empty[it & 1]);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      nb = __shfl_sync(0xffffffffu, nb, 0);
+      if (!ok) break;
+      if (nb == 0) continue;
+      if (lane == 0) {
+        ok = mbar_wait(&bar.q_full, qc & 1, abort_flag) && mbar_wait(&bar.o_empty, (oc & 1) ^ 1, abort_flag);
+        const long long g0 = g;
+        int ns = 0, np = 0;  // next S / next PV block of the row
+        long long t0 = clock64();
+        while (ok && np < nb) {
+          bool progressed = false;
+          if (ns < nb) {
+            const long long gs = g0 + ns;
+            const int st = (int)(gs % kStages), sb = (int)(gs & 1);
+            if (mbar_try_wait(&bar.kv_full[st], (uint32_t)((gs / kStages) & 1)) &&
+                mbar_try_wait(&bar.s_empty[sb], (uint32_t)((gs >> 1) & 1) ^ 1)) {
+              tc_fence_after();
+              const uint32_t qa = smem_addr(q_s), ka = smem_addr(kv_s + st * kKVBytes);
+              const uint32_t d = tmem + kColS + sb * kNB;
+              for (int a = 0; a < kAtoms; ++a)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  mma_bf16(d, desc_sw128(qa + a * kAtomQ + k * 32), desc_sw128(ka + a * kAtomKV + k * 32), id_s,
+                           (a | k) != 0);
+              mma_commit(&bar.s_full[sb]);
+              if (ns == nb - 1) mma_commit(&bar.q_empty);  // last use of this row's Q
+              ++ns;
+              progressed = true;
+            }
+          }
+          if (np < ns) {
+            const long long gp = g0 + np;
+            const int st = (int)(gp % kStages), pb = (int)(gp & 1);
+            if (mbar_try_wait(&bar.p_full[pb], (uint32_t)((gp >> 1) & 1))) {
+              tc_fence_after();
+              const uint32_t va = smem_addr(kv_s + st * kKVBytes), pa = smem_addr(p_s + pb * kPBytes);
+#pragma unroll
+              for (int c = 0; c < kDV / 128; ++c)
+#pragma unroll
+                for (int k = 0; k < kNB / 16; ++k)
+                  mma_bf16(tmem + kColO + c * kH, desc_sw128_mn(va + 2 * c * kAtomKV + k * 2048, kAtomKV),
+                           desc_noswz(pa + k * 256, 128, 512), id_o, (np | k) != 0);
+              mma_commit(&bar.kv_empty[st]);
+              mma_commit(&bar.p_empty[pb]);
+              if (np == nb - 1) mma_commit(&bar.o_full);
+              ++np;
+              progressed = true;
+            }
+          }
+          if (progressed) {
+            t0 = clock64();
+          } else if (*abort_flag || clock64() - t0 > kWaitTimeoutCycles) {
+            *abort_flag = 1;
+            ok = false;
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      g += nb;
+      ++qc;
+      ++oc;
+    }
+  } else {
+    // ================= softmax + epilogue (warps 5..8) =================
+    const int q4 = warp & 3;                    // TMEM lane quarter
+    const int sw = warp - kSmWarp0;             // softmax warp index 0..3
+    const bool head_lane = lane < 16;           // M=64 rows live in lanes 0..15 of each quarter
+    const int h = q4 * 16 + lane;               // head of this lane (valid when head_lane)
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const float sl2 = p.scale * kLog2e;
+    int it = 0, oc = 0;
+    long long g = 0;
+    bool ok = true;
+    for (int row = blockIdx.x; ok && row < rows; row += gridDim.x, ++it) {
+      if (!(ok = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag))) break;
+      const int nb = sm->nb[it & 1];
+      named_sync(1, 128);
+      if (threadIdx.x == kSmWarp0 * 32) mbar_arrive(&bar.info_empty[it & 1]);
+      __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * kH * kDV;
+      if (nb == 0) {  // nothing visible: O = 0, LSE = -inf
+        const int t = threadIdx.x - kSmWarp0 * 32;
+        for (int i = t; i < kH * kDV / 8; i += 128) reinterpret_cast<uint4*>(og)[i] = make_uint4(0, 0, 0, 0);
+        if (p.lse && t < kH) p.lse[(int64_t)row * kH + t] = -INFINITY;
+        continue;
+      }
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; ok && j < nb; ++j, ++g) {
+        const int sb = (int)(g & 1), st = (int)(g % kStages);
+        if (!(ok = mbar_wait(&bar.s_full[sb], (uint32_t)((g >> 1) & 1), abort_flag))) break;
+        tc_fence_after();
+        uint32_t sr[32];
+        tmem_ld32(tmem + lane_base + kColS + sb * kNB, sr);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.s_empty[sb]);
+        // scores in base-2 units, masked
+        float s[kNB];
+        float bmax = -INFINITY;
+        const uint32_t* vm = reinterpret_cast<const uint32_t*>(sm->valid[st]);
+#pragma unroll
+        for (int c4 = 0; c4 < kNB / 4; ++c4) {
+          const uint32_t v4 = vm[c4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = c4 * 4 + i;
+            const float x = __uint_as_float(sr[c]) * sl2;
+            s[c] = ((v4 >> (8 * i)) & 0xffu) ? x : -INFINITY;
+            bmax = fmaxf(bmax, s[c]);
+          }
+        }
+        const bool need = head_lane && bmax > m_used + kRescaleLog2;
+        const int any = __any_sync(0xffffffffu, need);
+        if (lane == 0) sm->any_rescale[sb][sw] = any;
+        named_sync(1, 128);
+        const bool rescale =
+            j > 0 && (sm->any_rescale[sb][0] | sm->any_rescale[sb][1] | sm->any_rescale[sb][2] | sm->any_rescale[sb][3]) != 0;
+        const float m_new = need ? bmax : m_used;
+        if (rescale) {
+          // O^T must be complete for the previous block before it is rescaled
+          const long long gp = g - 1;
+          if (!(ok = mbar_wait(&bar.p_empty[gp & 1], (uint32_t)((gp >> 1) & 1), abort_flag))) break;
+          const float alpha = need ? ex2(m_used - m_new) : 1.f;
+          if (head_lane) sm->alpha[h] = alpha;
+          l *= alpha;
+          named_sync(1, 128);
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < kDV / 128; ++c)
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+              uint32_t r[32];
+              const uint32_t ta = tmem + lane_base + kColO + c * kH + half * 32;
+              tmem_ld32(ta, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * sm->alpha[half * 32 + i]);
+              tmem_st32(ta, r);
+            }
+          tmem_wait_st();
+          tc_fence_before();
+        }
+        m_used = m_new;
+        const float mu = m_used == -INFINITY ? 0.f : m_used;
+        // this P buffer is free once the value product of block g-2 is done
+        if (!(ok = mbar_wait(&bar.p_empty[sb], (uint32_t)((g >> 1) & 1) ^ 1, abort_flag))) break;
+        if (head_lane) {
+          // K-major, unswizzled: 8-head x 8-key core matrices, 128 B apart along keys, 512 B along heads
+          uint8_t* prow = p_s + sb * kPBytes + (h >> 3) * 512 + (h & 7) * 16;
+#pragma unroll
+          for (int kg = 0; kg < kNB / 8; ++kg) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float a = ex2(s[kg * 8 + 2 * i] - mu), bq = ex2(s[kg * 8 + 2 * i + 1] - mu);
+              l += a + bq;
+              __nv_bfloat162 v2 = __floats2bfloat162_rn(a, bq);
+              w[i] = *reinterpret_cast<uint32_t*>(&v2);
+            }
+            *reinterpret_cast<uint4*>(prow + kg * 128) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.p_full[sb]);
+      }
+      if (!ok) break;
+      // ---- epilogue: O = O^T / l, LSE ----
+      if (head_lane) {
+        sm->lsum[h] = l > 0.f ? 1.f / l : 0.f;  // reciprocal row sums
+        if (p.lse) p.lse[(int64_t)row * kH + h] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      }
+      if (!(ok = mbar_wait(&bar.o_full, oc & 1, abort_flag))) break;
+      named_sync(1, 128);
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < kDV / 128; ++c) {
+        const int d = c * 128 + q4 * 32 + lane;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + kColO + c * kH + half * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int hh = half * 32 + i;
+            og[(int64_t)hh * kDV + d] = __float2bfloat16_rn(__uint_as_float(r[i]) * sm->lsum[hh]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.o_empty);
+      named_sync(1, 128);  // lsum is reused by the next row
+      ++oc;
+    }
+  }
+
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(p.flags, DSA_FLAG_TIMEOUT);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+
+bool sparse_mla_tc_supported(const AttnLaunch& p) {
+  return p.H == kH && p.DQK == kDQK && p.DV == kDV && p.v == p.k && p.v_ld == p.k_ld && p.k_ld == kDQK &&
+         (int64_t)p.B * p.S < (1ll << 31) && !getenv("DSA_ATTN_MMA");
+}
+
+cudaError_t launch_sparse_mla_tc(const AttnLaunch& p, cudaStream_t st) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap tq, tkv;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)kDQK, (cuuint64_t)kH, (cuuint64_t)p.B * p.T};
+    cuuint64_t strides[2] = {(cuuint64_t)kDQK * 2, (cuuint64_t)kDQK * 2 * kH};
+    cuuint32_t box[3] = {64, (cuuint32_t)kH, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p.q), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)kDQK, (cuuint64_t)p.B * p.S};
+    cuuint64_t strides[1] = {(cuuint64_t)p.k_ld * 2};
+    cuuint32_t box[2] = {64, 1};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.k), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(k_sparse_mla_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  if (e != cudaSuccess) return e;
+  const int rows = p.B * p.T;
+  const int grid = rows < num_sms() ? rows : num_sms();
+  k_sparse_mla_tc<<<grid, kThreads, kSmem, st>>>(tq, tkv, p);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa
