@@ -45,7 +45,6 @@ constexpr int kProdWarps = 4;              // cp.async gather warps
 constexpr int kMmaWarp = kProdWarps;       // warp 4
 constexpr int kSmWarp0 = kProdWarps + 1;   // warps 5..8: softmax + epilogue
 constexpr int kThreads = (kProdWarps + 5) * 32;
-constexpr int kLag = 3;                    // copy groups left in flight before a block is published
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;              // O^T: 4 chunks x 64 columns
 constexpr uint32_t kColS = 256;            // S: 2 buffers x 32 columns
@@ -67,7 +66,6 @@ struct Small {
   uint32_t tmem;
   int abort;
   int nb[2];                       // blocks of the row in flight (by row parity)
-  uint8_t valid[kStages][kNB];     // per stage: key slot holds a valid row
   float alpha[kH];
   float lsum[kH];
   int any_rescale[2][4];          // by block parity, so a fast warp never overwrites an unread flag
@@ -172,21 +170,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= producers: row info, Q tile, KV gathers (cp.async), L2 prefetch ==========
     // Each of the four warps copies 8 of a block's 32 rows: lane l moves 16-byte chunks
     // l, l+32, l+64 of a 1152-byte row into the 128-byte-swizzled K-major layout the MMAs
-    // read.  A block is published (kv_full) once its copy group has landed, kLag groups later,
-    // after a proxy fence that hands the bytes to the tensor core.
+    // read.  Every copying thread then arms an asynchronous arrive on the stage's kv_full
+    // barrier that fires once its own copies have landed, so the producer never waits for
+    // its copies and all stages stay in flight.
     const uint8_t* kvg = static_cast<const uint8_t*>(p.k);
     const int64_t row_bytes = p.k_ld * 2;
     const bool leader = warp == 0 && lane == 0;
     int it = 0, qc = 0;
-    long long g = 0;    // global block counter
-    long long pub = 0;  // next block to publish
+    long long g = 0;  // global block counter
     bool ok = true;
     const bool vec = (p.kk & 3) == 0;
-    auto publish = [&]() {  // copies of block `pub` have landed (wait_group done)
-      fence_async_smem();
-      mbar_arrive(&bar.kv_full[pub % kStages]);
-      ++pub;
-    };
     for (int row = blockIdx.x; ok && row < rows; row += gridDim.x, ++it) {
       const int32_t* irow = p.idx + (int64_t)row * p.kk;
       const int b = row / p.T;
@@ -258,7 +251,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < 8 && !valid && id != -1) atomicOr(p.flags, DSA_FLAG_BAD_INDEX);
         if (!valid) id = 0;
         if (!(ok = mbar_wait(&bar.kv_empty[st], (uint32_t)((g / kStages) & 1) ^ 1, abort_flag))) break;
-        if (lane < 8) sm->valid[st][rl] = valid ? 1 : 0;
         uint8_t* stage = kv_s + st * kKVBytes;
 #pragma unroll
         for (int r8 = 0; r8 < 8; ++r8) {
@@ -278,17 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        asm volatile("cp.async.commit_group;\n" ::: "memory");
-        if (g - pub + 1 > kLag) {
-          asm volatile("cp.async.wait_group %0;\n" ::"n"(kLag) : "memory");
-          publish();
-        }
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_addr(&bar.kv_full[st]))
+                     : "memory");
       }
-      // end of row: publish everything, so the row's last S can run and free the Q tile
-      asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-      while (pub < g) publish();
     }
-    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
     (void)leader;
     if (*abort_flag && warp == 0 && lane == 0 && qc > 0) mbar_wait_drain(&bar.q_full, (uint32_t)((qc - 1) & 1));
   } else if (warp == kMmaWarp) {
@@ -319,8 +305,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ns < nb) {
             const long long gs = g0 + ns;
             const int st = (int)(gs % kStages), sb = (int)(gs & 1);
-            if (mbar_try_wait(&bar.kv_full[st], (uint32_t)((gs / kStages) & 1)) &&
-                mbar_try_wait(&bar.s_empty[sb], (uint32_t)((gs >> 1) & 1) ^ 1)) {
+            if (mbar_test(&bar.kv_full[st], (uint32_t)((gs / kStages) & 1)) &&
+                mbar_test(&bar.s_empty[sb], (uint32_t)((gs >> 1) & 1) ^ 1)) {
+              fence_async_smem();  // the stage was written by cp.async (generic proxy)
               tc_fence_after();
               const uint32_t qa = smem_addr(q_s), ka = smem_addr(kv_s + st * kKVBytes);
               const uint32_t d = tmem + kColS + sb * kNB;
@@ -338,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (np < ns) {
             const long long gp = g0 + np;
             const int st = (int)(gp % kStages), pb = (int)(gp & 1);
-            if (mbar_try_wait(&bar.p_full[pb], (uint32_t)((gp >> 1) & 1))) {
+            if (mbar_test(&bar.p_full[pb], (uint32_t)((gp >> 1) & 1))) {
               tc_fence_after();
               const uint32_t va = smem_addr(kv_s + st * kKVBytes), pa = smem_addr(p_s + pb * kPBytes);
 #pragma unroll
@@ -384,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_sync(1, 128);
       if (threadIdx.x == kSmWarp0 * 32) mbar_arrive(&bar.info_empty[it & 1]);
       __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * kH * kDV;
+      const int32_t* irow = p.idx + (int64_t)row * p.kk;
       if (nb == 0) {  // nothing visible: O = 0, LSE = -inf
         const int t = threadIdx.x - kSmWarp0 * 32;
         for (int i = t; i < kH * kDV / 8; i += 128) reinterpret_cast<uint4*>(og)[i] = make_uint4(0, 0, 0, 0);
@@ -392,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; ok && j < nb; ++j, ++g) {
-        const int sb = (int)(g & 1), st = (int)(g % kStages);
+        const int sb = (int)(g & 1);
         if (!(ok = mbar_wait(&bar.s_full[sb], (uint32_t)((g >> 1) & 1), abort_flag))) break;
         tc_fence_after();
         uint32_t sr[32];
@@ -401,20 +389,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.s_empty[sb]);
-        // scores in base-2 units, masked
+        // scores in base-2 units, masked by the validity of each key slot (lane c checks slot c)
+        const int e = j * kNB + lane;
+        const int id = e < p.kk ? __ldg(irow + e) : -1;
+        const uint32_t vmask = __ballot_sync(0xffffffffu, id >= 0 && id < p.S);
         float s[kNB];
         float bmax = -INFINITY;
-        const uint32_t* vm = reinterpret_cast<const uint32_t*>(sm->valid[st]);
 #pragma unroll
-        for (int c4 = 0; c4 < kNB / 4; ++c4) {
-          const uint32_t v4 = vm[c4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c = c4 * 4 + i;
-            const float x = __uint_as_float(sr[c]) * sl2;
-            s[c] = ((v4 >> (8 * i)) & 0xffu) ? x : -INFINITY;
-            bmax = fmaxf(bmax, s[c]);
-          }
+        for (int c = 0; c < kNB; ++c) {
+          const float x = __uint_as_float(sr[c]) * sl2;
+          s[c] = ((vmask >> c) & 1u) ? x : -INFINITY;
+          bmax = fmaxf(bmax, s[c]);
         }
         const bool need = head_lane && bmax > m_used + kRescaleLog2;
         const int any = __any_sync(0xffffffffu, need);
