@@ -5,16 +5,15 @@
 // of the same row, so each gathered row feeds both products.
 //
 // Persistent CTAs (one per SM) walk query rows.  For each row:
-//   * warps 0..3 load the query tile with TMA and gather the selected KV rows, 32 per block,
-//     with 16-byte cp.async copies into a 128-byte-swizzled ring of four stages (on this
-//     random-row pattern cp.async sustains about 1.8x the rate of TMA tile::gather4), and
-//     keep L2 warm with bulk prefetches of the rows eight blocks ahead;
-//   * warp 4 issues  S = Q K^T  (M = 64 heads, N = 32 keys, K = 576) into TMEM and
-//     O^T += V^T P^T  (M = 128 value dims x 4, N = 64 heads, K = 32 keys) -- the transposed
+//   * warps 0..3 load the query tile with TMA and gather the selected KV rows, 64 per block,
+//     with 16-byte cp.async copies into two 128-byte-swizzled stages (on this random-row
+//     pattern cp.async sustains about 1.8x the rate of TMA tile::gather4);
+//   * warp 4 issues  S = Q K^T  (M = 64 heads, N = 64 keys, K = 576) into TMEM and
+//     O^T += V^T P^T  (M = 128 value dims x 4, N = 64 heads, K = 64 keys) -- the transposed
 //     value product keeps the 64 x 512 fp32 accumulator in 256 TMEM columns; it polls both
 //     queues and issues whichever is ready, so a late gather never holds back a PV product;
 //   * warps 5..8 run the online softmax (one head per TMEM lane, base-2 exponent, fp32 row
-//     sums, bf16 P double-buffered in shared memory).  The running maximum is raised only
+//     sums; bf16 P is written into the block's rope columns, free once S is done).  The running maximum is raised only
 //     when a block exceeds it by more than 2^8; then O^T is rescaled in TMEM.  At the end
 //     they normalise O, write bf16 O and the natural-log LSE.
 // Entries of -1 are skipped (masked), out-of-range entries raise DSA_FLAG_BAD_INDEX and are
@@ -32,22 +31,21 @@ namespace {
 using namespace sm100;
 
 constexpr int kH = 64, kDQK = 576, kDV = 512;
-constexpr int kNB = 32;                    // keys per block
-constexpr int kStages = 4;                 // gathered KV blocks in flight
-constexpr int kPF = 8;                     // blocks prefetched into L2 ahead of the gathers
+constexpr int kNB = 64;                    // keys per block (N of the S product, K of the PV product)
+constexpr int kStages = 2;                 // gathered KV blocks in flight
 constexpr int kAtoms = kDQK / 64;          // 9 swizzle atoms of 64 bf16 per row
 constexpr uint32_t kAtomQ = kH * 128;      // 8 KB
-constexpr uint32_t kAtomKV = kNB * 128;    // 4 KB
+constexpr uint32_t kAtomKV = kNB * 128;    // 8 KB
 constexpr uint32_t kQBytes = kAtoms * kAtomQ;
 constexpr uint32_t kKVBytes = kAtoms * kAtomKV;
-constexpr uint32_t kPBytes = kH * kNB * 2;  // one P buffer (4 KB)
+constexpr int kPAtom = kAtoms - 1;         // P(g) overwrites block g's rope atom once S(g) is done
 constexpr int kProdWarps = 4;              // cp.async gather warps
 constexpr int kMmaWarp = kProdWarps;       // warp 4
 constexpr int kSmWarp0 = kProdWarps + 1;   // warps 5..8: softmax + epilogue
 constexpr int kThreads = (kProdWarps + 5) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;              // O^T: 4 chunks x 64 columns
-constexpr uint32_t kColS = 256;            // S: 2 buffers x 32 columns
+constexpr uint32_t kColS = 256;            // S: 2 buffers x 64 columns
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;
@@ -56,7 +54,7 @@ struct Bars {
   uint64_t q_full, q_empty;
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_full[2], p_empty[2];
+  uint64_t p_full[2];
   uint64_t o_full, o_empty;
   uint64_t info_full[2], info_empty[2];
 };
@@ -71,7 +69,7 @@ struct Small {
   int any_rescale[2][4];          // by block parity, so a fast warp never overwrites an unread flag
 };
 
-constexpr size_t kSmem = 1024 + kQBytes + kStages * kKVBytes + 2 * kPBytes + sizeof(Small);
+constexpr size_t kSmem = 1024 + kQBytes + kStages * kKVBytes + sizeof(Small);
 
 __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int r0, int r1,
                                             int r2, int r3) {
@@ -129,8 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = base;
   uint8_t* kv_s = base + kQBytes;               // kStages stages
-  uint8_t* p_s = kv_s + kStages * kKVBytes;     // 2 buffers
-  Small* sm = reinterpret_cast<Small*>(p_s + 2 * kPBytes);
+  Small* sm = reinterpret_cast<Small*>(kv_s + kStages * kKVBytes);
   Bars& bar = sm->bar;
   volatile int* abort_flag = &sm->abort;
 
@@ -148,7 +145,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar.s_full[i], 1);
       mbar_init(&bar.s_empty[i], 4);
       mbar_init(&bar.p_full[i], 4);
-      mbar_init(&bar.p_empty[i], 1);
       mbar_init(&bar.info_full[i], 1);
       mbar_init(&bar.info_empty[i], 2);
     }
@@ -221,13 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok || *abort_flag) break;
       if (nb == 0) continue;
-      auto prefetch_block = [&](int jb) {  // warp 0: L2 prefetch of one block's rows
-        const int e = jb * kNB + lane;
-        const int id = e < p.kk ? __ldg(irow + e) : -1;
-        if (id >= 0 && id < p.S) prefetch_l2(kvg + (kvrow0 + id) * row_bytes, kDQK * 2);
-      };
       if (warp == 0) {
-        for (int jb = 0; jb < kPF && jb < nb; ++jb) prefetch_block(jb);
         if (lane == 0 && row + (int)gridDim.x < rows)
           prefetch_l2(static_cast<const __nv_bfloat16*>(p.q) + (int64_t)(row + gridDim.x) * kH * kDQK, kQBytes);
         if (lane == 0) {
@@ -242,21 +232,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++qc;
       for (int j = 0; ok && j < nb; ++j, ++g) {
         const int st = (int)(g % kStages);
-        if (warp == 0 && j + kPF < nb) prefetch_block(j + kPF);
-        // ids of this warp's 8 rows
-        const int rl = warp * 8 + (lane & 7);
+        // ids of this warp's 16 rows
+        constexpr int kRowsW = kNB / kProdWarps;
+        const int rl = warp * kRowsW + (lane & (kRowsW - 1));
         const int e = j * kNB + rl;
         int id = e < p.kk ? __ldg(irow + e) : -1;
         const bool valid = id >= 0 && id < p.S;
-        if (lane < 8 && !valid && id != -1) atomicOr(p.flags, DSA_FLAG_BAD_INDEX);
+        if (lane < kRowsW && !valid && id != -1) atomicOr(p.flags, DSA_FLAG_BAD_INDEX);
         if (!valid) id = 0;
         if (!(ok = mbar_wait(&bar.kv_empty[st], (uint32_t)((g / kStages) & 1) ^ 1, abort_flag))) break;
         uint8_t* stage = kv_s + st * kKVBytes;
-#pragma unroll
-        for (int r8 = 0; r8 < 8; ++r8) {
+#pragma unroll 4
+        for (int r8 = 0; r8 < kRowsW; ++r8) {
           const int rid = __shfl_sync(0xffffffffu, id, r8);
           const bool rv = __shfl_sync(0xffffffffu, valid, r8);
-          const int r = warp * 8 + r8;
+          const int r = warp * kRowsW + r8;
           const uint8_t* src = kvg + (kvrow0 + rid) * row_bytes;
 #pragma unroll
           for (int u = 0; u < 3; ++u) {
@@ -279,8 +269,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (*abort_flag && warp == 0 && lane == 0 && qc > 0) mbar_wait_drain(&bar.q_full, (uint32_t)((qc - 1) & 1));
   } else if (warp == kMmaWarp) {
     // ================= MMA issuer (one thread; never blocks on one stream while another can run) ==
-    const uint32_t id_s = idesc_mn(1, 1, kH, kNB);               // S: M=64 heads, N=32 keys
+    const uint32_t id_s = idesc_mn(1, 1, kH, kNB);               // S: M=64 heads, N=64 keys
     const uint32_t id_o = idesc_mn(1, 1, 128, kH) | (1u << 15);  // O^T: M=128 dims (MN-major A), N=64 heads
+    const uint64_t q_desc0 = desc_sw128(smem_addr(q_s));
+    const uint64_t kv_desc0 = desc_sw128(smem_addr(kv_s));
+    const uint64_t v_desc0 = desc_sw128_mn(smem_addr(kv_s), kAtomKV);
+
     int it = 0, qc = 0, oc = 0;
     long long g = 0;
     bool ok = true;
@@ -309,13 +303,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_test(&bar.s_empty[sb], (uint32_t)((gs >> 1) & 1) ^ 1)) {
               fence_async_smem();  // the stage was written by cp.async (generic proxy)
               tc_fence_after();
-              const uint32_t qa = smem_addr(q_s), ka = smem_addr(kv_s + st * kKVBytes);
+              // descriptors: base + compile-time offsets in the 16-byte start-address field
+              const uint64_t qd = q_desc0, kd = kv_desc0 + (uint64_t)((st * kKVBytes) >> 4);
               const uint32_t d = tmem + kColS + sb * kNB;
+#pragma unroll
               for (int a = 0; a < kAtoms; ++a)
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                  mma_bf16(d, desc_sw128(qa + a * kAtomQ + k * 32), desc_sw128(ka + a * kAtomKV + k * 32), id_s,
-                           (a | k) != 0);
+                  mma_bf16(d, qd + (uint64_t)((a * kAtomQ + k * 32) >> 4),
+                           kd + (uint64_t)((a * kAtomKV + k * 32) >> 4), id_s, (a | k) != 0 ? 1u : 0u);
               mma_commit(&bar.s_full[sb]);
               if (ns == nb - 1) mma_commit(&bar.q_empty);  // last use of this row's Q
               ++ns;
@@ -326,16 +322,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long gp = g0 + np;
             const int st = (int)(gp % kStages), pb = (int)(gp & 1);
             if (mbar_test(&bar.p_full[pb], (uint32_t)((gp >> 1) & 1))) {
+              fence_async_smem();
               tc_fence_after();
-              const uint32_t va = smem_addr(kv_s + st * kKVBytes), pa = smem_addr(p_s + pb * kPBytes);
+              const uint64_t vd = v_desc0 + (uint64_t)((st * kKVBytes) >> 4);
+              const uint64_t pd = kv_desc0 + (uint64_t)((st * kKVBytes + kPAtom * kAtomKV) >> 4);
 #pragma unroll
-              for (int c = 0; c < kDV / 128; ++c)
+              for (int k = 0; k < kNB / 16; ++k)
 #pragma unroll
-                for (int k = 0; k < kNB / 16; ++k)
-                  mma_bf16(tmem + kColO + c * kH, desc_sw128_mn(va + 2 * c * kAtomKV + k * 2048, kAtomKV),
-                           desc_noswz(pa + k * 256, 128, 512), id_o, (np | k) != 0);
+                for (int c = 0; c < kDV / 128; ++c)
+                  mma_bf16(tmem + kColO + c * kH, vd + (uint64_t)((2 * c * kAtomKV + k * 2048) >> 4),
+                           pd + (uint64_t)((k * 32) >> 4), id_o, (np | k) != 0 ? 1u : 0u);
               mma_commit(&bar.kv_empty[st]);
-              mma_commit(&bar.p_empty[pb]);
               if (np == nb - 1) mma_commit(&bar.o_full);
               ++np;
               progressed = true;
@@ -383,22 +380,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sb = (int)(g & 1);
         if (!(ok = mbar_wait(&bar.s_full[sb], (uint32_t)((g >> 1) & 1), abort_flag))) break;
         tc_fence_after();
-        uint32_t sr[32];
-        tmem_ld32(tmem + lane_base + kColS + sb * kNB, sr);
+        uint32_t sr[kNB];
+        tmem_ld32(tmem + lane_base + kColS + sb * kNB, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld32(tmem + lane_base + kColS + sb * kNB + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.s_empty[sb]);
-        // scores in base-2 units, masked by the validity of each key slot (lane c checks slot c)
-        const int e = j * kNB + lane;
-        const int id = e < p.kk ? __ldg(irow + e) : -1;
-        const uint32_t vmask = __ballot_sync(0xffffffffu, id >= 0 && id < p.S);
+        // scores in base-2 units, masked by the validity of each key slot (lane c checks c, c+32)
+        const int e0 = j * kNB + lane, e1 = e0 + 32;
+        const int id0 = e0 < p.kk ? __ldg(irow + e0) : -1, id1 = e1 < p.kk ? __ldg(irow + e1) : -1;
+        const uint32_t vm0 = __ballot_sync(0xffffffffu, id0 >= 0 && id0 < p.S);
+        const uint32_t vm1 = __ballot_sync(0xffffffffu, id1 >= 0 && id1 < p.S);
         float s[kNB];
         float bmax = -INFINITY;
 #pragma unroll
         for (int c = 0; c < kNB; ++c) {
           const float x = __uint_as_float(sr[c]) * sl2;
-          s[c] = ((vmask >> c) & 1u) ? x : -INFINITY;
+          s[c] = (((c < 32 ? vm0 : vm1) >> (c & 31)) & 1u) ? x : -INFINITY;
           bmax = fmaxf(bmax, s[c]);
         }
         const bool need = head_lane && bmax > m_used + kRescaleLog2;
@@ -409,9 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             j > 0 && (sm->any_rescale[sb][0] | sm->any_rescale[sb][1] | sm->any_rescale[sb][2] | sm->any_rescale[sb][3]) != 0;
         const float m_new = need ? bmax : m_used;
         if (rescale) {
-          // O^T must be complete for the previous block before it is rescaled
+          // O^T must be complete for the previous block before it is rescaled: the value
+          // product of block g-1 releases its stage
           const long long gp = g - 1;
-          if (!(ok = mbar_wait(&bar.p_empty[gp & 1], (uint32_t)((gp >> 1) & 1), abort_flag))) break;
+          if (!(ok = mbar_wait(&bar.kv_empty[gp % kStages], (uint32_t)((gp / kStages) & 1), abort_flag))) break;
           const float alpha = need ? ex2(m_used - m_new) : 1.f;
           if (head_lane) sm->alpha[h] = alpha;
           l *= alpha;
@@ -434,22 +434,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         m_used = m_new;
         const float mu = m_used == -INFINITY ? 0.f : m_used;
-        // this P buffer is free once the value product of block g-2 is done
-        if (!(ok = mbar_wait(&bar.p_empty[sb], (uint32_t)((g >> 1) & 1) ^ 1, abort_flag))) break;
         if (head_lane) {
-          // K-major, unswizzled: 8-head x 8-key core matrices, 128 B apart along keys, 512 B along heads
-          uint8_t* prow = p_s + sb * kPBytes + (h >> 3) * 512 + (h & 7) * 16;
+          // P row of this head: 64 keys of bf16 = one 128-byte swizzled K-major row, written into
+          // the block's rope atom, which S(g) -- now complete -- was the last to read
+          uint8_t* prow = kv_s + (size_t)(g % kStages) * kKVBytes + kPAtom * kAtomKV + h * 128;
 #pragma unroll
-          for (int kg = 0; kg < kNB / 8; ++kg) {
+          for (int ch = 0; ch < kNB / 8; ++ch) {
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float a = ex2(s[kg * 8 + 2 * i] - mu), bq = ex2(s[kg * 8 + 2 * i + 1] - mu);
+              const float a = ex2(s[ch * 8 + 2 * i] - mu), bq = ex2(s[ch * 8 + 2 * i + 1] - mu);
               l += a + bq;
               __nv_bfloat162 v2 = __floats2bfloat162_rn(a, bq);
               w[i] = *reinterpret_cast<uint32_t*>(&v2);
             }
-            *reinterpret_cast<uint4*>(prow + kg * 128) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(prow + ((ch ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
         fence_async_smem();

@@ -138,7 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && ktiles > 0) {
       bool ok = mbar_wait(q_full, 0, abort_flag);
       int done = 0;
-      const uint32_t qa = smem_addr(q_s);
+      const uint64_t q_desc0 = desc_sw128(smem_addr(q_s));
+      const uint64_t k_desc0 = desc_sw128(smem_addr(k_s));
       for (int kt = 0; ok && kt < ktiles; ++kt) {
         const int st = kt % C::kStages;
         const uint32_t ph = (kt / C::kStages) & 1;
@@ -148,13 +149,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(k_full + st, ph, abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * kN;
-        const uint32_t ka = smem_addr(k_s + st * C::kKTile);
+        const uint64_t kd = k_desc0 + (uint64_t)((st * C::kKTile) >> 4);
 #pragma unroll
         for (int kb = 0; kb < C::kKBlocks; ++kb)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint64_t ad = desc_sw128(ka + kb * C::kKBlock + j * 32);
-            const uint64_t bd = desc_sw128(qa + kb * C::kQBlock + j * 32);
+            // base descriptors + compile-time offsets in the 16-byte start-address field
+            const uint64_t ad = kd + (uint64_t)((kb * C::kKBlock + j * 32) >> 4);
+            const uint64_t bd = q_desc0 + (uint64_t)((kb * C::kQBlock + j * 32) >> 4);
             if constexpr (FP8)
               mma_fp8(d, ad, bd, C::kIdesc, (kb | j) != 0);
             else
