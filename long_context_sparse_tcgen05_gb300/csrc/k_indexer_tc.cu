@@ -5,11 +5,12 @@
 // One CTA owns a block of query tokens and walks every key tile they can see:
 //   * MMA shape M = 128 keys (A: the key tile, K-major), N = 256 columns = tokens x heads
 //     (B: the stationary query tile, K-major), K = d_I; fp32 accumulators in TMEM, two
-//     256-column buffers so the epilogue of tile i overlaps the MMAs of tile i+1;
+//     256-column buffers so the epilogue of tile i overlaps the MMAs of tile i+1 (N = 256
+//     reads each key tile from shared memory once; two N = 128 halves were measured slower);
 //   * warp 0 streams key tiles with TMA (128-byte swizzle) through a ring of smem stages;
 //   * warp 1 allocates TMEM and issues the MMAs from one thread (tcgen05.commit frees the
 //     stage and publishes the accumulator);
-//   * warps 2..9 read the accumulator rows (TMEM lane = key) with tcgen05.ld, apply ReLU and
+//   * warps 2..17 read the accumulator rows (TMEM lane = key) with tcgen05.ld, apply ReLU and
 //     the head weights with packed fp32x2 FMAs -- the head sum never leaves the thread --
 //     apply the per-token scales and write the fp32 score row with coalesced stores.
 // Every wait is bounded; a timeout raises DSA_FLAG_TIMEOUT, drains the copies in flight,
@@ -27,10 +28,11 @@ namespace {
 using namespace sm100;
 
 constexpr int kM = 128;        // keys per tile
-constexpr int kN = 256;        // token x head columns per tile
-constexpr int kEpiWarps = 8;   // two per TMEM lane quarter, one per column half
+constexpr int kN = 256;        // token x head columns per tile and per MMA
+constexpr int kBufs = 2;       // TMEM accumulator buffers of kN columns (512 columns)
+constexpr int kEpiWarps = 16;  // four per TMEM lane quarter, one per 64-column quarter of N
 constexpr int kThreads = 64 + kEpiWarps * 32;
-constexpr uint32_t kTmemCols = 2 * kN;
+constexpr uint32_t kTmemCols = kBufs * kN;
 
 template <int HI, int DI, bool FP8>
 struct Cfg {
@@ -44,7 +46,7 @@ struct Cfg {
   static constexpr uint32_t kQBytes = kN * kRowBytes;
   static constexpr uint32_t kKTile = kM * kRowBytes;
   static constexpr int kStages = FP8 ? 6 : 4;
-  static constexpr int kCols = kN / 2;              // columns read by one epilogue warp
+  static constexpr int kCols = kN / 4;              // columns read by one epilogue warp
   static constexpr int kBarOff = kQBytes + kStages * kKTile;
   static constexpr size_t kSmem = 1024 + kBarOff + 256 + (size_t)kTB * HI * 4;
   static constexpr uint32_t kIdesc = idesc_mn(FP8 ? 0u : 1u, FP8 ? 0u : 1u, kM, kN);
@@ -70,8 +72,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_empty = k_full + C::kStages;
   uint64_t* q_full = k_empty + C::kStages;
   uint64_t* tm_full = q_full + 1;
-  uint64_t* tm_empty = tm_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tm_empty + 2);
+  uint64_t* tm_empty = tm_full + kBufs;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tm_empty + kBufs);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* w_s = reinterpret_cast<float*>(smem + C::kBarOff + 256);
 
@@ -91,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(k_empty + i, 1);
     }
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kBufs; ++i) {
       mbar_init(tm_full + i, 1);
       mbar_init(tm_empty + i, kEpiWarps);
     }
@@ -143,10 +145,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kt = 0; ok && kt < ktiles; ++kt) {
         const int st = kt % C::kStages;
         const uint32_t ph = (kt / C::kStages) & 1;
-        const int buf = kt & 1;
-        const uint32_t bph = (kt >> 1) & 1;
-        if (!mbar_wait(tm_empty + buf, bph ^ 1, abort_flag)) break;
-        if (!mbar_wait(k_full + st, ph, abort_flag)) break;
+        const int buf = kt & (kBufs - 1);
+        if (!(ok = mbar_wait(tm_empty + buf, ((kt / kBufs) & 1) ^ 1, abort_flag))) break;
+        if (!(ok = mbar_wait(k_full + st, ph, abort_flag))) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * kN;
         const uint64_t kd = k_desc0 + (uint64_t)((st * C::kKTile) >> 4);
@@ -166,87 +167,90 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(tm_full + buf);
         done = kt + 1;
       }
-      if (*abort_flag && done > 0) mbar_wait_drain(tm_full + ((done - 1) & 1), ((done - 1) >> 1) & 1);
+      if (*abort_flag && done > 0) mbar_wait_drain(tm_full + ((done - 1) & (kBufs - 1)), ((done - 1) / kBufs) & 1);
     }
   } else {
     // ---------------- epilogue ----------------
     const int e = warp - 2;
     const int lq = warp & 3;                 // TMEM lane quarter this warp may read
-    const int ch = e >> 2;                   // column half
+    const int ch = e >> 2;                   // column quarter (one 64-column slice of N)
     const int key_in_tile = lq * 32 + lane;  // TMEM lane = key
     const uint32_t t_lane = tmem + ((uint32_t)(lq * 32) << 16);
     float* out_b = p.out + (int64_t)b * p.out_bstride;
     const float* skg = FP8 ? p.k_scale + (int64_t)b * p.S : nullptr;
 
     constexpr int kTokW = C::kCols / HI > 0 ? C::kCols / HI : 1;  // tokens per epilogue warp
-    unsigned long long w2[HI >= 64 ? C::kCols / 2 : 1];             // head weights, packed pairs
-    if constexpr (HI >= 64) {
-#pragma unroll
-      for (int c = 0; c < C::kCols / 2; ++c) w2[c] = pack2(w_s[ch * C::kCols + 2 * c], w_s[ch * C::kCols + 2 * c + 1]);
-    }
+    const float* w_warp = w_s + ch * C::kCols;                      // this warp's columns' weights
 
-    auto store = [&](int tok, int key, float v) {  // tok: token index within the CTA block
-      if (tok >= ntok || key >= p.S) return;
-      const int64_t n = visible_keys(p, tl0 + tok);
-      float* dst = out_b + (int64_t)(tl0 + tok) * p.ld + key;
-      if (key < n) {
-        if constexpr (FP8) v *= __ldg(p.q_scale + row0 + tok) * __ldg(skg + key);
-        *dst = v;
-      } else if (p.write_masked) {
-        *dst = -INFINITY;
-      }
+    // per-token constants of this warp's tokens, held in registers
+    int64_t nvis[kTokW];
+    float sq[kTokW];
+#pragma unroll
+    for (int tk = 0; tk < kTokW; ++tk) {
+      const int tok = ch * kTokW + tk;
+      nvis[tk] = tok < ntok ? visible_keys(p, tl0 + tok) : 0;
+      sq[tk] = (FP8 && tok < ntok) ? __ldg(p.q_scale + row0 + tok) : 1.f;
+    }
+    // key scales are fetched one tile ahead so their latency hides behind the tile's work
+    auto key_scale = [&](int kt) -> float {
+      const int key = kt * kM + key_in_tile;
+      return (FP8 && kt < ktiles && key < p.S) ? __ldg(skg + key) : 1.f;
     };
+    float sk_next = key_scale(0);
 
     for (int kt = 0; kt < ktiles; ++kt) {
-      const int buf = kt & 1;
-      const uint32_t bph = (kt >> 1) & 1;
-      if (!mbar_wait(tm_full + buf, bph, abort_flag)) break;
+      const int buf = kt & (kBufs - 1);
+      const float sk = sk_next;
+      sk_next = key_scale(kt + 1);
+      if (!mbar_wait(tm_full + buf, (kt / kBufs) & 1, abort_flag)) break;
       tc_fence_after();
       const uint32_t col0 = t_lane + buf * kN + ch * C::kCols;
-      const int key = kt * kM + key_in_tile;
-      float score[kTokW];
-      if constexpr (HI >= 64) {
-        // 32 columns per load = half of one token's heads
+      // all of this warp's accumulator columns in one go, then the buffer goes back to the MMA
+      uint32_t r[C::kCols / 32][32];
 #pragma unroll
-        for (int tk = 0; tk < kTokW; ++tk) {
-          unsigned long long acc = 0ull;
-#pragma unroll
-          for (int half = 0; half < HI / 32; ++half) {
-            uint32_t r[32];
-            tmem_ld32(col0 + tk * HI + half * 32, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float x0 = fmaxf(__uint_as_float(r[2 * j]), 0.f);
-              const float x1 = fmaxf(__uint_as_float(r[2 * j + 1]), 0.f);
-              acc = fma2(w2[(tk * HI + half * 32) / 2 + j], pack2(x0, x1), acc);
-            }
-          }
-          score[tk] = lo2(acc) + hi2(acc);
-        }
-      } else {
-        // 32 columns per load = 32 / HI whole tokens; weights read from shared memory
-#pragma unroll
-        for (int cb = 0; cb < C::kCols / 32; ++cb) {
-          uint32_t r[32];
-          tmem_ld32(col0 + cb * 32, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int tt = 0; tt < 32 / HI; ++tt) {
-            const int tk = cb * (32 / HI) + tt;
-            const float* wt = w_s + (ch * kTokW + tk) * HI;
-            float acc = 0.f;
-#pragma unroll
-            for (int h = 0; h < HI; ++h) acc += wt[h] * fmaxf(__uint_as_float(r[tt * HI + h]), 0.f);
-            score[tk] = acc;
-          }
-        }
-      }
+      for (int cb = 0; cb < C::kCols / 32; ++cb) tmem_ld32(col0 + cb * 32, r[cb]);
+      tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tm_empty + buf);
+      const int key = kt * kM + key_in_tile;
 #pragma unroll
-      for (int tk = 0; tk < kTokW; ++tk) store(ch * kTokW + tk, key, score[tk]);
+      for (int tk = 0; tk < kTokW; ++tk) {
+        // four independent partial sums per token keep the FMA pipe fed
+        unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
+        float acc1 = 0.f;
+#pragma unroll
+        for (int c4 = 0; c4 < HI / 4; ++c4) {
+          const int c = tk * HI + c4 * 4;  // column within the warp
+          const float4 wv = *reinterpret_cast<const float4*>(w_warp + c);
+          const float x0 = fmaxf(__uint_as_float(r[c >> 5][c & 31]), 0.f);
+          const float x1 = fmaxf(__uint_as_float(r[(c + 1) >> 5][(c + 1) & 31]), 0.f);
+          const float x2 = fmaxf(__uint_as_float(r[(c + 2) >> 5][(c + 2) & 31]), 0.f);
+          const float x3 = fmaxf(__uint_as_float(r[(c + 3) >> 5][(c + 3) & 31]), 0.f);
+          if constexpr (HI >= 8) {
+            acc[(2 * c4) & 3] = fma2(pack2(wv.x, wv.y), pack2(x0, x1), acc[(2 * c4) & 3]);
+            acc[(2 * c4 + 1) & 3] = fma2(pack2(wv.z, wv.w), pack2(x2, x3), acc[(2 * c4 + 1) & 3]);
+          } else {
+            acc1 += wv.x * x0 + wv.y * x1 + wv.z * x2 + wv.w * x3;
+          }
+        }
+        float v;
+        if constexpr (HI >= 8)
+          v = ((lo2(acc[0]) + hi2(acc[0])) + (lo2(acc[1]) + hi2(acc[1]))) +
+              ((lo2(acc[2]) + hi2(acc[2])) + (lo2(acc[3]) + hi2(acc[3])));
+        else
+          v = acc1;
+        const int tok = ch * kTokW + tk;
+        if (tok < ntok && key < p.S) {
+          float* dst = out_b + (int64_t)(tl0 + tok) * p.ld + key;
+          if (key < nvis[tk]) {
+            if constexpr (FP8) v *= sq[tk] * sk;
+            *dst = v;
+          } else if (p.write_masked) {
+            *dst = -INFINITY;
+          }
+        }
+      }
     }
     if (p.write_masked && !*abort_flag) {  // keys beyond every visible tile
       for (int tk = 0; tk < kTokW; ++tk) {
