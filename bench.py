@@ -46,6 +46,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle CPU time")
+    ap.add_argument("--kernel", choices=["attn", "indexer", "topk"], default=None,
+                    help="time one call on a single-kernel case instead of the group step "
+                         "(the case the committed ncu summaries are captured on)")
+    ap.add_argument("--rows", type=int, default=2048, help="--kernel: query rows (the last rows of the sequence)")
+    ap.add_argument("--keys", type=int, default=131072, help="--kernel: sequence length")
     return ap.parse_args()
 
 
@@ -399,8 +404,53 @@ def run_reference(args, rank, world, local):
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_kernel_case(args):
+    """One public call on a synthetic single-kernel case: the last `rows` query rows of a
+    `keys`-token sequence.  attn: sparse MLA attention (k=2048) over index rows from a top-k
+    of Gaussian scores; indexer: FP8 materialised indexer scores; topk: FP8 indexer + top-k."""
+    import long_context_sparse_tcgen05_gb300 as dsa
+    from long_context_sparse_tcgen05_gb300 import build
+    build.build()
+    dsa.load_library()
+    dev = torch.device("cuda:0")
+    T, S = args.rows, args.keys
+    if args.kernel == "attn":
+        wl = synth.WORKLOADS["prefill_16k"].replace(T=T, S=S, q_pos0=S - T)
+        at = synth.attn_inputs(wl, 0, dev)
+        sc = synth.scores_input(T, S, dev, "normal", seed=5)
+        idx = dsa.dsa_topk(2048, scores=sc[None], q_pos0=S - T)
+        del sc
+        out = torch.empty(1, T, 64, 512, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(1, T, 64, dtype=torch.float32, device=dev)
+        fn = lambda: dsa.dsa_sparse_attn(at, idx, out=out, lse=lse)
+        work = f"{T * 2048 * 1152 / 1e9:.2f} GB gathered"
+    else:
+        wl = synth.WORKLOADS["prefill_128k"].replace(T=T, S=S, q_pos0=S - T, values="gauss")
+        ix = synth.indexer_inputs(wl, 0, dev)
+        if args.kernel == "indexer":
+            out = torch.empty(1, T, S, dtype=torch.float32, device=dev)
+            fn = lambda: dsa.indexer_scores(ix, out=out)
+        else:
+            fn = lambda: dsa.dsa_topk(2048, ix=ix)
+        flops = sum(min(S, S - T + t) for t in range(T)) * 2 * 64 * 128
+        work = f"{flops / 1e12:.2f} TFLOP"
+    torch.cuda.synchronize()
+    for r in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        print(json.dumps({"kernel_case": args.kernel, "rows": T, "keys": S, "rep": r,
+                          "ms": round(e0.elapsed_time(e1), 4), "work": work}))
+    print(json.dumps({"device_flags": dsa.read_device_flags(dev)}))
+
+
 def main():
     args = parse()
+    if args.kernel:
+        run_kernel_case(args)
+        return
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         if rank != 0:

@@ -49,6 +49,7 @@ struct IndexerLaunch {
   int64_t out_bstride;
   int write_masked;     // 1: write -inf over [n_t, S) as well
   uint32_t* flags;      // device flag word (DSA_FLAG_TIMEOUT)
+  int ksplit;           // key-range splits per token block (0: chosen by the launcher)
 };
 cudaError_t launch_indexer_scores(const IndexerLaunch& p, cudaStream_t st);     // tcgen05 path
 cudaError_t launch_indexer_scores_mma(const IndexerLaunch& p, cudaStream_t st); // mma.sync path

@@ -2,7 +2,9 @@
 //
 //   I[t,s] = sq[t] * sk[s] * sum_h w[t,h] * ReLU(q[t,h] . k[s])
 //
-// One CTA owns a block of query tokens and walks every key tile they can see:
+// One CTA owns a block of query tokens and walks the key tiles they can see (all of them, or
+// one of `ksplit` equal key ranges when there are too few token blocks to fill the GPU, as in
+// decode):
 //   * MMA shape M = 128 keys (A: the key tile, K-major), N = 256 columns = tokens x heads
 //     (B: the stationary query tile, K-major), K = d_I; fp32 accumulators in TMEM, two
 //     256-column buffers so the epilogue of tile i overlaps the MMAs of tile i+1 (N = 256
@@ -79,12 +81,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nblk = (p.Tc + C::kTB - 1) / C::kTB;
-  const int tb = nblk - 1 - (int)blockIdx.x;  // latest (longest) token blocks first
+  const int tb = nblk - 1 - (int)(blockIdx.x / p.ksplit);  // latest (longest) token blocks first
+  const int split = (int)(blockIdx.x % p.ksplit);
   const int b = blockIdx.y;
   const int tl0 = tb * C::kTB;
   const int ntok = min(C::kTB, p.Tc - tl0);
   const int64_t nmax = visible_keys(p, tl0 + ntok - 1);
-  const int ktiles = (int)((nmax + kM - 1) / kM);
+  // this CTA's key tiles: [kt_lo, kt_lo + ktiles) of the ceil(S / kM) tiles of the row
+  const int tiles_all = (p.S + kM - 1) / kM;
+  const int tps = (tiles_all + p.ksplit - 1) / p.ksplit;
+  const int kt_lo = split * tps;
+  const int kt_vis = (int)((nmax + kM - 1) / kM);
+  const int ktiles = max(0, min(kt_vis, kt_lo + tps) - kt_lo);
+  const int key_hi = min(p.S, (kt_lo + tps) * kM);  // end of this CTA's key range
   const int64_t row0 = (int64_t)b * p.T + p.t0 + tl0;  // flat (b, t) of the block's first token
 
   if (threadIdx.x == 0) {
@@ -126,7 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(k_empty + st, ph ^ 1, abort_flag)) break;
         mbar_arrive_expect_tx(k_full + st, C::kKTile);
         for (int kb = 0; kb < C::kKBlocks; ++kb)
-          tma_load_3d(k_s + st * C::kKTile + kb * C::kKBlock, &tm_k, k_full + st, kb * C::kAtomElems, kt * kM, b);
+          tma_load_3d(k_s + st * C::kKTile + kb * C::kKBlock, &tm_k, k_full + st, kb * C::kAtomElems,
+                      (kt_lo + kt) * kM, b);
         issued = kt + 1;
       }
       if (*abort_flag) {  // let every copy still in flight land before the CTA can exit
@@ -193,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // key scales are fetched one tile ahead so their latency hides behind the tile's work
     auto key_scale = [&](int kt) -> float {
-      const int key = kt * kM + key_in_tile;
+      const int key = (kt_lo + kt) * kM + key_in_tile;
       return (FP8 && kt < ktiles && key < p.S) ? __ldg(skg + key) : 1.f;
     };
     float sk_next = key_scale(0);
@@ -213,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tm_empty + buf);
-      const int key = kt * kM + key_in_tile;
+      const int key = (kt_lo + kt) * kM + key_in_tile;
 #pragma unroll
       for (int tk = 0; tk < kTokW; ++tk) {
         // four independent partial sums per token keep the FMA pipe fed
@@ -256,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tk = 0; tk < kTokW; ++tk) {
         const int tok = ch * kTokW + tk;
         if (tok >= ntok) break;
-        for (int key = ktiles * kM + key_in_tile; key < p.S; key += kM)
+        for (int key = (kt_lo + ktiles) * kM + key_in_tile; key < key_hi; key += kM)
           out_b[(int64_t)(tl0 + tok) * p.ld + key] = -INFINITY;
       }
     }
@@ -316,8 +326,22 @@ cudaError_t launch_cfg(const IndexerLaunch& p, cudaStream_t st) {
   auto kern = k_indexer_tc<HI, DI, FP8>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem)) != cudaSuccess)
     return e;
-  dim3 grid((p.Tc + C::kTB - 1) / C::kTB, p.B);
-  kern<<<grid, kThreads, C::kSmem, st>>>(tq, tk, p);
+  IndexerLaunch q = p;
+  const int nblk = (p.Tc + C::kTB - 1) / C::kTB;
+  if (q.ksplit <= 0) {
+    // split the key range when the token blocks alone would not give about four waves of
+    // CTAs, keeping at least 16 key tiles per split
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long ctas = (long long)nblk * p.B;
+    const int tiles_all = (p.S + kM - 1) / kM;
+    long long want = ctas >= 4LL * sms ? 1 : (4LL * sms + ctas - 1) / ctas;
+    const long long most = tiles_all / 16 > 0 ? tiles_all / 16 : 1;
+    q.ksplit = (int)(want < most ? want : most);
+  }
+  dim3 grid((unsigned)(nblk * q.ksplit), p.B);
+  kern<<<grid, kThreads, C::kSmem, st>>>(tq, tk, q);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -4,7 +4,8 @@
 // One 512-thread CTA owns one row (two CTAs per SM).  Scores are compared through their
 // order-preserving 32-bit keys.
 //   * Rows with at most kCap visible scores are copied to shared memory whole.
-//   * Longer rows: a strided sample of at most kSampleMax keys gives, by an exact radix select
+//   * Longer rows: a sample of at most kSampleMax keys (whole 8-key groups, evenly strided)
+//     gives, by an exact radix select
 //     in shared memory, a threshold theta that about 1.25k of the row's keys exceed; one
 //     streaming pass then appends every key >= theta, in position order (block-wide prefix
 //     sums of warp ballots), to shared memory.  Every key below theta has at least k larger
@@ -205,10 +206,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
     }
     c = n;
   } else {
-    // threshold from a strided sample
-    const int64_t stride = (n + kSampleMax - 1) / kSampleMax;
-    const int64_t m = (n + stride - 1) / stride;
-    for (int64_t i = threadIdx.x; i < m; i += kThreads) sm.key[i] = score_key(__ldg(x + i * stride));
+    // threshold from a sample of whole 8-score groups (one 32-byte sector each), evenly
+    // strided over the row, so the sample touches only every g-th sector
+    const int64_t groups = n / 8;
+    const int64_t gstride = (groups * 8 + kSampleMax - 1) / kSampleMax;  // >= 1 since n > kCap
+    const int64_t mg = (groups + gstride - 1) / gstride;
+    const int64_t m = mg * 8;
+    for (int64_t i = threadIdx.x; i < m; i += kThreads)
+      sm.key[i] = score_key(__ldg(x + (i >> 3) * gstride * 8 + (i & 7)));
     __syncthreads();
     int64_t ks = (int64_t)ceil(1.25 * (double)k * (double)m / (double)n) + 16;
     if (ks > m) ks = m;
