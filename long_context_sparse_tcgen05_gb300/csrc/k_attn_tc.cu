@@ -6,13 +6,15 @@
 //
 // Persistent CTAs (one per SM) walk query rows.  For each row:
 //   * warps 0..3 load the query tile with TMA and gather the selected KV rows, 64 per block,
-//     with 16-byte cp.async copies into two 128-byte-swizzled stages (on this random-row
-//     pattern cp.async sustains about 1.8x the rate of TMA tile::gather4);
-//   * warp 4 issues  S = Q K^T  (M = 64 heads, N = 64 keys, K = 576) into TMEM and
-//     O^T += V^T P^T  (M = 128 value dims x 4, N = 64 heads, K = 64 keys) -- the transposed
-//     value product keeps the 64 x 512 fp32 accumulator in 256 TMEM columns; it polls both
-//     queues and issues whichever is ready, so a late gather never holds back a PV product;
-//   * warps 5..8 run the online softmax (one head per TMEM lane, base-2 exponent, fp32 row
+//     with 16-byte cp.async copies into two 128-byte-swizzled stages.  A stage lands in three
+//     groups (swizzle atoms 0-3, 4-7, 8), each with its own barrier, so the score product
+//     starts on the first columns while the rest are still in flight;
+//   * warp 4 issues  S = Q K^T  (M = 64 heads, N = 64 keys, K = 576) into TMEM, group by group;
+//   * warp 5 issues  O^T += V^T P^T  (M = 128 value dims x 4, N = 64 heads, K = 64 keys) -- the
+//     transposed value product keeps the 64 x 512 fp32 accumulator in 256 TMEM columns.  Two
+//     issuing threads let the tensor pipe interleave the two products (a single issuer stalls
+//     in the 36-instruction score chain while a value product is ready);
+//   * warps 6..9 run the online softmax (one head per TMEM lane, base-2 exponent, fp32 row
 //     sums; bf16 P is written into the block's rope columns, free once S is done).  The running maximum is raised only
 //     when a block exceeds it by more than 2^8; then O^T is rescaled in TMEM.  At the end
 //     they normalise O, write bf16 O and the natural-log LSE.
@@ -39,10 +41,12 @@ constexpr uint32_t kAtomKV = kNB * 128;    // 8 KB
 constexpr uint32_t kQBytes = kAtoms * kAtomQ;
 constexpr uint32_t kKVBytes = kAtoms * kAtomKV;
 constexpr int kPAtom = kAtoms - 1;         // P(g) overwrites block g's rope atom once S(g) is done
+constexpr int kGroups = 3;                 // landing groups of a stage: atoms 0-3, 4-7, 8
 constexpr int kProdWarps = 4;              // cp.async gather warps
-constexpr int kMmaWarp = kProdWarps;       // warp 4
-constexpr int kSmWarp0 = kProdWarps + 1;   // warps 5..8: softmax + epilogue
-constexpr int kThreads = (kProdWarps + 5) * 32;
+constexpr int kMmaWarp = kProdWarps;       // warp 4: score product issuer (and TMEM owner)
+constexpr int kPvWarp = kProdWarps + 1;    // warp 5: value product issuer
+constexpr int kSmWarp0 = kProdWarps + 2;   // warps 6..9: softmax + epilogue
+constexpr int kThreads = (kProdWarps + 6) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;              // O^T: 4 chunks x 64 columns
 constexpr uint32_t kColS = 256;            // S: 2 buffers x 64 columns
@@ -52,11 +56,12 @@ constexpr float kRescaleLog2 = 8.f;
 
 struct Bars {
   uint64_t q_full, q_empty;
-  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t kv_full[kStages][kGroups], kv_empty[kStages];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full[2];
   uint64_t o_full, o_empty;
   uint64_t info_full[2], info_empty[2];
+  uint64_t drain[2];  // end of kernel: each issuer waits for its own products
 };
 
 struct Small {
@@ -138,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar.q_full, 1);
     mbar_init(&bar.q_empty, 1);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&bar.kv_full[i], kProdWarps * 32);
+      for (int gr = 0; gr < kGroups; ++gr) mbar_init(&bar.kv_full[i][gr], kProdWarps * 32);
       mbar_init(&bar.kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -146,7 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar.s_empty[i], 4);
       mbar_init(&bar.p_full[i], 4);
       mbar_init(&bar.info_full[i], 1);
-      mbar_init(&bar.info_empty[i], 2);
+      mbar_init(&bar.info_empty[i], 3);
+      mbar_init(&bar.drain[i], 1);
     }
     mbar_init(&bar.o_full, 1);
     mbar_init(&bar.o_empty, 4);
@@ -242,25 +248,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!valid) id = 0;
         if (!(ok = mbar_wait(&bar.kv_empty[st], (uint32_t)((g / kStages) & 1) ^ 1, abort_flag))) break;
         uint8_t* stage = kv_s + st * kKVBytes;
-#pragma unroll 4
-        for (int r8 = 0; r8 < kRowsW; ++r8) {
-          const int rid = __shfl_sync(0xffffffffu, id, r8);
-          const bool rv = __shfl_sync(0xffffffffu, valid, r8);
-          const int r = warp * kRowsW + r8;
-          const uint8_t* src = kvg + (kvrow0 + rid) * row_bytes;
+        // groups 0 and 1: lane l copies 16-byte chunk 32 * group + l (atoms 4 * group .. + 3) of
+        // each of the warp's rows; group 2 (the rope atom): 8 lanes per row, 4 rows per pass
 #pragma unroll
-          for (int u = 0; u < 3; ++u) {
-            const int ch = lane + 32 * u;  // 16-byte chunk of the row
-            if (ch < kDQK * 2 / 16) {
-              const int a = ch >> 3, cc = ch & 7;
-              const uint32_t dst = smem_addr(stage + a * kAtomKV + r * 128 + ((cc ^ (r & 7)) << 4));
-              asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src + ch * 16),
-                           "r"(rv ? 16 : 0)
-                           : "memory");
-            }
+        for (int gr = 0; gr < 2; ++gr) {
+#pragma unroll 4
+          for (int r8 = 0; r8 < kRowsW; ++r8) {
+            const int rid = __shfl_sync(0xffffffffu, id, r8);
+            const bool rv = __shfl_sync(0xffffffffu, valid, r8);
+            const int r = warp * kRowsW + r8;
+            const int ch = 32 * gr + lane, a = ch >> 3, cc = ch & 7;
+            const uint32_t dst = smem_addr(stage + a * kAtomKV + r * 128 + ((cc ^ (r & 7)) << 4));
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
+                         "l"(kvg + (kvrow0 + rid) * row_bytes + ch * 16), "r"(rv ? 16 : 0)
+                         : "memory");
           }
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_addr(&bar.kv_full[st][gr]))
+                       : "memory");
         }
-        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_addr(&bar.kv_full[st]))
+#pragma unroll
+        for (int pass = 0; pass < kRowsW / 4; ++pass) {
+          const int r4 = pass * 4 + (lane >> 3);
+          const int rid = __shfl_sync(0xffffffffu, id, r4);
+          const bool rv = __shfl_sync(0xffffffffu, valid, r4);
+          const int r = warp * kRowsW + r4;
+          const int ch = 64 + (lane & 7), cc = lane & 7;
+          const uint32_t dst = smem_addr(stage + 8 * kAtomKV + r * 128 + ((cc ^ (r & 7)) << 4));
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
+                       "l"(kvg + (kvrow0 + rid) * row_bytes + ch * 16), "r"(rv ? 16 : 0)
+                       : "memory");
+        }
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_addr(&bar.kv_full[st][2]))
                      : "memory");
       }
     }
@@ -268,14 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     (void)leader;
     if (*abort_flag && warp == 0 && lane == 0 && qc > 0) mbar_wait_drain(&bar.q_full, (uint32_t)((qc - 1) & 1));
   } else if (warp == kMmaWarp) {
-    // ================= MMA issuer (one thread; never blocks on one stream while another can run) ==
-    const uint32_t id_s = idesc_mn(1, 1, kH, kNB);               // S: M=64 heads, N=64 keys
-    const uint32_t id_o = idesc_mn(1, 1, 128, kH) | (1u << 15);  // O^T: M=128 dims (MN-major A), N=64 heads
+    // ================= score product issuer (one thread) =================
+    const uint32_t id_s = idesc_mn(1, 1, kH, kNB);  // S: M=64 heads, N=64 keys
     const uint64_t q_desc0 = desc_sw128(smem_addr(q_s));
     const uint64_t kv_desc0 = desc_sw128(smem_addr(kv_s));
-    const uint64_t v_desc0 = desc_sw128_mn(smem_addr(kv_s), kAtomKV);
-
-    int it = 0, qc = 0, oc = 0;
+    int it = 0, qc = 0;
     long long g = 0;
     bool ok = true;
     for (int row = blockIdx.x; ok && row < rows; row += gridDim.x, ++it) {
@@ -290,69 +305,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (nb == 0) continue;
       if (lane == 0) {
-        ok = mbar_wait(&bar.q_full, qc & 1, abort_flag) && mbar_wait(&bar.o_empty, (oc & 1) ^ 1, abort_flag);
-        const long long g0 = g;
-        int ns = 0, np = 0;  // next S / next PV block of the row
-        long long t0 = clock64();
-        while (ok && np < nb) {
-          bool progressed = false;
-          if (ns < nb) {
-            const long long gs = g0 + ns;
-            const int st = (int)(gs % kStages), sb = (int)(gs & 1);
-            if (mbar_test(&bar.kv_full[st], (uint32_t)((gs / kStages) & 1)) &&
-                mbar_test(&bar.s_empty[sb], (uint32_t)((gs >> 1) & 1) ^ 1)) {
-              fence_async_smem();  // the stage was written by cp.async (generic proxy)
-              tc_fence_after();
-              // descriptors: base + compile-time offsets in the 16-byte start-address field
-              const uint64_t qd = q_desc0, kd = kv_desc0 + (uint64_t)((st * kKVBytes) >> 4);
-              const uint32_t d = tmem + kColS + sb * kNB;
+        ok = mbar_wait(&bar.q_full, qc & 1, abort_flag);
+        for (int j = 0; ok && j < nb; ++j) {
+          const long long gs = g + j;
+          const int st = (int)(gs % kStages), sb = (int)(gs & 1);
+          const uint32_t kvpar = (uint32_t)((gs / kStages) & 1);
+          if (!(ok = mbar_wait(&bar.s_empty[sb], (uint32_t)((gs >> 1) & 1) ^ 1, abort_flag))) break;
+          // descriptors: base + compile-time offsets in the 16-byte start-address field
+          const uint64_t qd = q_desc0, kd = kv_desc0 + (uint64_t)((st * kKVBytes) >> 4);
+          const uint32_t d = tmem + kColS + sb * kNB;
 #pragma unroll
-              for (int a = 0; a < kAtoms; ++a)
+          for (int gr = 0; gr < kGroups; ++gr) {
+            if (!(ok = mbar_wait(&bar.kv_full[st][gr], kvpar, abort_flag))) break;
+            fence_async_smem();  // the stage was written by cp.async (generic proxy)
+            tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  mma_bf16(d, qd + (uint64_t)((a * kAtomQ + k * 32) >> 4),
-                           kd + (uint64_t)((a * kAtomKV + k * 32) >> 4), id_s, (a | k) != 0 ? 1u : 0u);
-              mma_commit(&bar.s_full[sb]);
-              if (ns == nb - 1) mma_commit(&bar.q_empty);  // last use of this row's Q
-              ++ns;
-              progressed = true;
-            }
+            for (int a = 4 * gr; a < (gr == 2 ? kAtoms : 4 * gr + 4); ++a)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_bf16(d, qd + (uint64_t)((a * kAtomQ + k * 32) >> 4), kd + (uint64_t)((a * kAtomKV + k * 32) >> 4),
+                         id_s, (a | k) != 0 ? 1u : 0u);
           }
-          if (np < ns) {
-            const long long gp = g0 + np;
-            const int st = (int)(gp % kStages), pb = (int)(gp & 1);
-            if (mbar_test(&bar.p_full[pb], (uint32_t)((gp >> 1) & 1))) {
-              fence_async_smem();
-              tc_fence_after();
-              const uint64_t vd = v_desc0 + (uint64_t)((st * kKVBytes) >> 4);
-              const uint64_t pd = kv_desc0 + (uint64_t)((st * kKVBytes + kPAtom * kAtomKV) >> 4);
-#pragma unroll
-              for (int k = 0; k < kNB / 16; ++k)
-#pragma unroll
-                for (int c = 0; c < kDV / 128; ++c)
-                  mma_bf16(tmem + kColO + c * kH, vd + (uint64_t)((2 * c * kAtomKV + k * 2048) >> 4),
-                           pd + (uint64_t)((k * 32) >> 4), id_o, (np | k) != 0 ? 1u : 0u);
-              mma_commit(&bar.kv_empty[st]);
-              if (np == nb - 1) mma_commit(&bar.o_full);
-              ++np;
-              progressed = true;
-            }
-          }
-          if (progressed) {
-            t0 = clock64();
-          } else if (*abort_flag || clock64() - t0 > kWaitTimeoutCycles) {
-            *abort_flag = 1;
-            ok = false;
-          }
+          if (!ok) break;
+          mma_commit(&bar.s_full[sb]);
+          if (j == nb - 1) mma_commit(&bar.q_empty);  // last use of this row's Q
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       g += nb;
       ++qc;
+    }
+    if (lane == 0) {  // wait for this thread's own products before TMEM can be freed
+      mma_commit(&bar.drain[0]);
+      mbar_wait_drain(&bar.drain[0], 0);
+    }
+  } else if (warp == kPvWarp) {
+    // ================= value product issuer (one thread) =================
+    const uint32_t id_o = idesc_mn(1, 1, 128, kH) | (1u << 15);  // O^T: M=128 dims (MN-major A), N=64 heads
+    const uint64_t kv_desc0 = desc_sw128(smem_addr(kv_s));
+    const uint64_t v_desc0 = desc_sw128_mn(smem_addr(kv_s), kAtomKV);
+    int it = 0, oc = 0;
+    long long g = 0;
+    bool ok = true;
+    for (int row = blockIdx.x; ok && row < rows; row += gridDim.x, ++it) {
+      int nb = 0;
+      if (lane == 0) {
+        ok = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag);
+        nb = sm->nb[it & 1];
+        mbar_arrive(&bar.info_empty[it & 1]);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      nb = __shfl_sync(0xffffffffu, nb, 0);
+      if (!ok) break;
+      if (nb == 0) continue;
+      if (lane == 0) {
+        ok = mbar_wait(&bar.o_empty, (oc & 1) ^ 1, abort_flag);
+        for (int j = 0; ok && j < nb; ++j) {
+          const long long gp = g + j;
+          const int st = (int)(gp % kStages), pb = (int)(gp & 1);
+          if (!(ok = mbar_wait(&bar.p_full[pb], (uint32_t)((gp >> 1) & 1), abort_flag))) break;
+          fence_async_smem();
+          tc_fence_after();
+          const uint64_t vd = v_desc0 + (uint64_t)((st * kKVBytes) >> 4);
+          const uint64_t pd = kv_desc0 + (uint64_t)((st * kKVBytes + kPAtom * kAtomKV) >> 4);
+#pragma unroll
+          for (int k = 0; k < kNB / 16; ++k)
+#pragma unroll
+            for (int c = 0; c < kDV / 128; ++c)
+              mma_bf16(tmem + kColO + c * kH, vd + (uint64_t)((2 * c * kAtomKV + k * 2048) >> 4),
+                       pd + (uint64_t)((k * 32) >> 4), id_o, (j | k) != 0 ? 1u : 0u);
+          mma_commit(&bar.kv_empty[st]);
+          if (j == nb - 1) mma_commit(&bar.o_full);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      g += nb;
       ++oc;
     }
+    if (lane == 0) {
+      mma_commit(&bar.drain[1]);
+      mbar_wait_drain(&bar.drain[1], 0);
+    }
   } else {
-    // ================= softmax + epilogue (warps 5..8) =================
+    // ================= softmax + epilogue (warps 6..9) =================
     const int q4 = warp & 3;                    // TMEM lane quarter
     const int sw = warp - kSmWarp0;             // softmax warp index 0..3
     const bool head_lane = lane < 16;           // M=64 rows live in lanes 0..15 of each quarter
