@@ -6,16 +6,18 @@
 //
 // Persistent CTAs (one per SM) walk query rows.  For each row:
 //   * warps 0..3 load the query tile with TMA and gather the selected KV rows, 64 per block,
-//     with 16-byte cp.async copies into two 128-byte-swizzled stages.  A stage lands in three
-//     groups (swizzle atoms 0-3, 4-7, 8), each with its own barrier, so the score product
+//     with 16-byte cp.async copies into two 128-byte-swizzled stages.  A stage lands atom by
+//     atom (64 columns of all 64 rows), each atom with its own barrier, so the score product
 //     starts on the first columns while the rest are still in flight;
-//   * warp 4 issues  S = Q K^T  (M = 64 heads, N = 64 keys, K = 576) into TMEM, group by group;
+//   * warp 4 issues  S = Q K^T  (M = 64 heads, N = 64 keys, K = 576) into TMEM, atom by atom;
 //   * warp 5 issues  O^T += V^T P^T  (M = 128 value dims x 4, N = 64 heads, K = 64 keys) -- the
 //     transposed value product keeps the 64 x 512 fp32 accumulator in 256 TMEM columns.  Two
 //     issuing threads let the tensor pipe interleave the two products (a single issuer stalls
 //     in the 36-instruction score chain while a value product is ready);
-//   * warps 6..9 run the online softmax (one head per TMEM lane, base-2 exponent, fp32 row
-//     sums; bf16 P is written into the block's rope columns, free once S is done).  The running maximum is raised only
+//   * warps 6..13 run the online softmax, two warps per TMEM lane quarter, each on 32 of the
+//     block's 64 keys (one head per TMEM lane, base-2 exponent, fp32 row sums; the two halves
+//     of a head exchange block maxima and partial sums through shared memory; bf16 P is written
+//     into the block's rope columns, free once S is done).  The running maximum is raised only
 //     when a block exceeds it by more than 2^8; then O^T is rescaled in TMEM.  At the end
 //     they normalise O, write bf16 O and the natural-log LSE.
 // Entries of -1 are skipped (masked), out-of-range entries raise DSA_FLAG_BAD_INDEX and are
@@ -41,12 +43,14 @@ constexpr uint32_t kAtomKV = kNB * 128;    // 8 KB
 constexpr uint32_t kQBytes = kAtoms * kAtomQ;
 constexpr uint32_t kKVBytes = kAtoms * kAtomKV;
 constexpr int kPAtom = kAtoms - 1;         // P(g) overwrites block g's rope atom once S(g) is done
-constexpr int kGroups = 3;                 // landing groups of a stage: atoms 0-3, 4-7, 8
+constexpr int kGroups = kAtoms;            // a stage lands atom by atom
 constexpr int kProdWarps = 4;              // cp.async gather warps
 constexpr int kMmaWarp = kProdWarps;       // warp 4: score product issuer (and TMEM owner)
 constexpr int kPvWarp = kProdWarps + 1;    // warp 5: value product issuer
-constexpr int kSmWarp0 = kProdWarps + 2;   // warps 6..9: softmax + epilogue
-constexpr int kThreads = (kProdWarps + 6) * 32;
+constexpr int kSmWarp0 = kProdWarps + 2;   // warps 6..13: softmax + epilogue
+constexpr int kSmWarps = 8;
+constexpr int kSmThreads = kSmWarps * 32;
+constexpr int kThreads = (kProdWarps + 2 + kSmWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;              // O^T: 4 chunks x 64 columns
 constexpr uint32_t kColS = 256;            // S: 2 buffers x 64 columns
@@ -71,7 +75,9 @@ struct Small {
   int nb[2];                       // blocks of the row in flight (by row parity)
   float alpha[kH];
   float lsum[kH];
-  int any_rescale[2][4];          // by block parity, so a fast warp never overwrites an unread flag
+  float bmax[2][2][kH];           // [block parity][key half][head]: block maxima of the two halves
+  float lpart[2][kH];             // [key half][head]: partial row sums at the end of a row
+  int any_rescale[2][kSmWarps];   // by block parity, so a fast warp never overwrites an unread flag
 };
 
 constexpr size_t kSmem = 1024 + kQBytes + kStages * kKVBytes + sizeof(Small);
@@ -148,14 +154,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.s_full[i], 1);
-      mbar_init(&bar.s_empty[i], 4);
-      mbar_init(&bar.p_full[i], 4);
+      mbar_init(&bar.s_empty[i], kSmWarps);
+      mbar_init(&bar.p_full[i], kSmWarps);
       mbar_init(&bar.info_full[i], 1);
       mbar_init(&bar.info_empty[i], 3);
       mbar_init(&bar.drain[i], 1);
     }
     mbar_init(&bar.o_full, 1);
-    mbar_init(&bar.o_empty, 4);
+    mbar_init(&bar.o_empty, kSmWarps);
     sm->abort = 0;
     fence_barrier_init();
   }
@@ -248,38 +254,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!valid) id = 0;
         if (!(ok = mbar_wait(&bar.kv_empty[st], (uint32_t)((g / kStages) & 1) ^ 1, abort_flag))) break;
         uint8_t* stage = kv_s + st * kKVBytes;
-        // groups 0 and 1: lane l copies 16-byte chunk 32 * group + l (atoms 4 * group .. + 3) of
-        // each of the warp's rows; group 2 (the rope atom): 8 lanes per row, 4 rows per pass
-#pragma unroll
-        for (int gr = 0; gr < 2; ++gr) {
-#pragma unroll 4
-          for (int r8 = 0; r8 < kRowsW; ++r8) {
-            const int rid = __shfl_sync(0xffffffffu, id, r8);
-            const bool rv = __shfl_sync(0xffffffffu, valid, r8);
-            const int r = warp * kRowsW + r8;
-            const int ch = 32 * gr + lane, a = ch >> 3, cc = ch & 7;
-            const uint32_t dst = smem_addr(stage + a * kAtomKV + r * 128 + ((cc ^ (r & 7)) << 4));
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
-                         "l"(kvg + (kvrow0 + rid) * row_bytes + ch * 16), "r"(rv ? 16 : 0)
-                         : "memory");
-          }
-          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_addr(&bar.kv_full[st][gr]))
-                       : "memory");
-        }
+        // atom by atom: 8 lanes per row (one 16-byte chunk each), 4 rows per pass, 4 passes
+        // cover the warp's 16 rows; the row of each pass is fixed, so its id is fetched once
+        int rid[kRowsW / 4];
+        bool rv[kRowsW / 4];
 #pragma unroll
         for (int pass = 0; pass < kRowsW / 4; ++pass) {
-          const int r4 = pass * 4 + (lane >> 3);
-          const int rid = __shfl_sync(0xffffffffu, id, r4);
-          const bool rv = __shfl_sync(0xffffffffu, valid, r4);
-          const int r = warp * kRowsW + r4;
-          const int ch = 64 + (lane & 7), cc = lane & 7;
-          const uint32_t dst = smem_addr(stage + 8 * kAtomKV + r * 128 + ((cc ^ (r & 7)) << 4));
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
-                       "l"(kvg + (kvrow0 + rid) * row_bytes + ch * 16), "r"(rv ? 16 : 0)
+          rid[pass] = __shfl_sync(0xffffffffu, id, pass * 4 + (lane >> 3));
+          rv[pass] = __shfl_sync(0xffffffffu, valid, pass * 4 + (lane >> 3));
+        }
+        const int cc = lane & 7;
+#pragma unroll
+        for (int a = 0; a < kAtoms; ++a) {
+#pragma unroll
+          for (int pass = 0; pass < kRowsW / 4; ++pass) {
+            const int r = warp * kRowsW + pass * 4 + (lane >> 3);
+            const uint32_t dst = smem_addr(stage + a * kAtomKV + r * 128 + ((cc ^ (r & 7)) << 4));
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
+                         "l"(kvg + (kvrow0 + rid[pass]) * row_bytes + (a * 8 + cc) * 16), "r"(rv[pass] ? 16 : 0)
+                         : "memory");
+          }
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_addr(&bar.kv_full[st][a]))
                        : "memory");
         }
-        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_addr(&bar.kv_full[st][2]))
-                     : "memory");
       }
     }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
@@ -315,16 +312,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t qd = q_desc0, kd = kv_desc0 + (uint64_t)((st * kKVBytes) >> 4);
           const uint32_t d = tmem + kColS + sb * kNB;
 #pragma unroll
-          for (int gr = 0; gr < kGroups; ++gr) {
-            if (!(ok = mbar_wait(&bar.kv_full[st][gr], kvpar, abort_flag))) break;
+          for (int a = 0; a < kAtoms; ++a) {
+            if (!(ok = mbar_wait(&bar.kv_full[st][a], kvpar, abort_flag))) break;
             fence_async_smem();  // the stage was written by cp.async (generic proxy)
             tc_fence_after();
 #pragma unroll
-            for (int a = 4 * gr; a < (gr == 2 ? kAtoms : 4 * gr + 4); ++a)
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_bf16(d, qd + (uint64_t)((a * kAtomQ + k * 32) >> 4), kd + (uint64_t)((a * kAtomKV + k * 32) >> 4),
-                         id_s, (a | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < 4; ++k)
+              mma_bf16(d, qd + (uint64_t)((a * kAtomQ + k * 32) >> 4), kd + (uint64_t)((a * kAtomKV + k * 32) >> 4),
+                       id_s, (a | k) != 0 ? 1u : 0u);
           }
           if (!ok) break;
           mma_commit(&bar.s_full[sb]);
@@ -387,26 +382,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(&bar.drain[1], 0);
     }
   } else {
-    // ================= softmax + epilogue (warps 6..9) =================
+    // ================= softmax + epilogue (warps 6..13) =================
     const int q4 = warp & 3;                    // TMEM lane quarter
-    const int sw = warp - kSmWarp0;             // softmax warp index 0..3
+    const int sw = warp - kSmWarp0;             // softmax warp index 0..7
+    const int kh = sw >> 2;                     // key half: columns 32 * kh .. + 31 of each block
     const bool head_lane = lane < 16;           // M=64 rows live in lanes 0..15 of each quarter
     const int h = q4 * 16 + lane;               // head of this lane (valid when head_lane)
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const float sl2 = p.scale * kLog2e;
+    const int t = threadIdx.x - kSmWarp0 * 32;  // 0..255
     int it = 0, oc = 0;
     long long g = 0;
     bool ok = true;
     for (int row = blockIdx.x; ok && row < rows; row += gridDim.x, ++it) {
       if (!(ok = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag))) break;
       const int nb = sm->nb[it & 1];
-      named_sync(1, 128);
-      if (threadIdx.x == kSmWarp0 * 32) mbar_arrive(&bar.info_empty[it & 1]);
+      named_sync(1, kSmThreads);
+      if (t == 0) mbar_arrive(&bar.info_empty[it & 1]);
       __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * kH * kDV;
       const int32_t* irow = p.idx + (int64_t)row * p.kk;
       if (nb == 0) {  // nothing visible: O = 0, LSE = -inf
-        const int t = threadIdx.x - kSmWarp0 * 32;
-        for (int i = t; i < kH * kDV / 8; i += 128) reinterpret_cast<uint4*>(og)[i] = make_uint4(0, 0, 0, 0);
+        for (int i = t; i < kH * kDV / 8; i += kSmThreads) reinterpret_cast<uint4*>(og)[i] = make_uint4(0, 0, 0, 0);
         if (p.lse && t < kH) p.lse[(int64_t)row * kH + t] = -INFINITY;
         continue;
       }
@@ -415,45 +411,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sb = (int)(g & 1);
         if (!(ok = mbar_wait(&bar.s_full[sb], (uint32_t)((g >> 1) & 1), abort_flag))) break;
         tc_fence_after();
-        uint32_t sr[kNB];
-        tmem_ld32(tmem + lane_base + kColS + sb * kNB, *reinterpret_cast<uint32_t(*)[32]>(sr));
-        tmem_ld32(tmem + lane_base + kColS + sb * kNB + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        uint32_t sr[32];
+        tmem_ld32(tmem + lane_base + kColS + sb * kNB + kh * 32, sr);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.s_empty[sb]);
-        // scores in base-2 units, masked by the validity of each key slot (lane c checks c, c+32)
-        const int e0 = j * kNB + lane, e1 = e0 + 32;
-        const int id0 = e0 < p.kk ? __ldg(irow + e0) : -1, id1 = e1 < p.kk ? __ldg(irow + e1) : -1;
-        const uint32_t vm0 = __ballot_sync(0xffffffffu, id0 >= 0 && id0 < p.S);
-        const uint32_t vm1 = __ballot_sync(0xffffffffu, id1 >= 0 && id1 < p.S);
-        float s[kNB];
+        // scores in base-2 units, masked by the validity of each key slot (lane c checks key c)
+        const int e = j * kNB + kh * 32 + lane;
+        const int id = e < p.kk ? __ldg(irow + e) : -1;
+        const uint32_t vm = __ballot_sync(0xffffffffu, id >= 0 && id < p.S);
+        float s[32];
         float bmax = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kNB; ++c) {
+        for (int c = 0; c < 32; ++c) {
           const float x = __uint_as_float(sr[c]) * sl2;
-          s[c] = (((c < 32 ? vm0 : vm1) >> (c & 31)) & 1u) ? x : -INFINITY;
+          s[c] = ((vm >> c) & 1u) ? x : -INFINITY;
           bmax = fmaxf(bmax, s[c]);
         }
-        const bool need = head_lane && bmax > m_used + kRescaleLog2;
-        const int any = __any_sync(0xffffffffu, need);
+        const bool need_h = head_lane && bmax > m_used + kRescaleLog2;
+        const int any = __any_sync(0xffffffffu, need_h);
+        if (head_lane) sm->bmax[sb][kh][h] = bmax;
         if (lane == 0) sm->any_rescale[sb][sw] = any;
-        named_sync(1, 128);
-        const bool rescale =
-            j > 0 && (sm->any_rescale[sb][0] | sm->any_rescale[sb][1] | sm->any_rescale[sb][2] | sm->any_rescale[sb][3]) != 0;
-        const float m_new = need ? bmax : m_used;
-        if (rescale) {
+        named_sync(1, kSmThreads);
+        int anyr = 0;
+#pragma unroll
+        for (int w = 0; w < kSmWarps; ++w) anyr |= sm->any_rescale[sb][w];
+        const float bm = head_lane ? fmaxf(sm->bmax[sb][0][h], sm->bmax[sb][1][h]) : -INFINITY;
+        const bool need = head_lane && bm > m_used + kRescaleLog2;  // same decision in both halves
+        const float m_new = need ? bm : m_used;
+        if (j > 0 && anyr) {
           // O^T must be complete for the previous block before it is rescaled: the value
           // product of block g-1 releases its stage
           const long long gp = g - 1;
           if (!(ok = mbar_wait(&bar.kv_empty[gp % kStages], (uint32_t)((gp / kStages) & 1), abort_flag))) break;
           const float alpha = need ? ex2(m_used - m_new) : 1.f;
-          if (head_lane) sm->alpha[h] = alpha;
+          if (head_lane && kh == 0) sm->alpha[h] = alpha;
           l *= alpha;
-          named_sync(1, 128);
+          named_sync(1, kSmThreads);
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < kDV / 128; ++c)
+          for (int c = 2 * kh; c < 2 * kh + 2; ++c)  // each key half rescales two of the four chunks
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
               uint32_t r[32];
@@ -470,11 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = m_new;
         const float mu = m_used == -INFINITY ? 0.f : m_used;
         if (head_lane) {
-          // P row of this head: 64 keys of bf16 = one 128-byte swizzled K-major row, written into
-          // the block's rope atom, which S(g) -- now complete -- was the last to read
+          // this half of the head's P row: 32 keys of bf16 = four 16-byte chunks of the 128-byte
+          // swizzled K-major row in the block's rope atom, which S(g) -- now complete -- was the
+          // last to read
           uint8_t* prow = kv_s + (size_t)(g % kStages) * kKVBytes + kPAtom * kAtomKV + h * 128;
 #pragma unroll
-          for (int ch = 0; ch < kNB / 8; ++ch) {
+          for (int ch = 0; ch < 4; ++ch) {
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -483,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               __nv_bfloat162 v2 = __floats2bfloat162_rn(a, bq);
               w[i] = *reinterpret_cast<uint32_t*>(&v2);
             }
-            *reinterpret_cast<uint4*>(prow + ((ch ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(prow + (((kh * 4 + ch) ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
         fence_async_smem();
@@ -492,15 +491,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue: O = O^T / l, LSE ----
-      if (head_lane) {
-        sm->lsum[h] = l > 0.f ? 1.f / l : 0.f;  // reciprocal row sums
-        if (p.lse) p.lse[(int64_t)row * kH + h] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      if (head_lane) sm->lpart[kh][h] = l;
+      named_sync(1, kSmThreads);
+      if (head_lane && kh == 0) {
+        const float lt = sm->lpart[0][h] + sm->lpart[1][h];
+        sm->lsum[h] = lt > 0.f ? 1.f / lt : 0.f;  // reciprocal row sums
+        if (p.lse) p.lse[(int64_t)row * kH + h] = lt > 0.f ? (m_used + log2f(lt)) * kLn2 : -INFINITY;
       }
       if (!(ok = mbar_wait(&bar.o_full, oc & 1, abort_flag))) break;
-      named_sync(1, 128);
+      named_sync(1, kSmThreads);
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < kDV / 128; ++c) {
+      for (int c = 2 * kh; c < 2 * kh + 2; ++c) {
         const int d = c * 128 + q4 * 32 + lane;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
@@ -517,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.o_empty);
-      named_sync(1, 128);  // lsum is reused by the next row
+      named_sync(1, kSmThreads);  // lsum and lpart are reused by the next row
       ++oc;
     }
   }
