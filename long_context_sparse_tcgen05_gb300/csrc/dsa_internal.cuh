@@ -25,11 +25,9 @@ dsa_status record_error(dsa_status s, const char* msg);
 // Key transform of the selection order: a larger float gives a larger unsigned key.
 // -0 and +0 share one key; NaN maps below -inf.
 __device__ __forceinline__ uint32_t score_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  uint32_t a = u & 0x7fffffffu;
-  if (a > 0x7f800000u) return 0u;  // NaN
-  if (a == 0u) u = 0u;             // -0 -> +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  const uint32_t u = __float_as_uint(f + 0.0f);  // -0 + 0 = +0; every other value is unchanged
+  const uint32_t key = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);  // negatives: ~u, else u | sign
+  return f != f ? 0u : key;                      // NaN ranks below every number
 }
 
 // Rows [t0, t0 + Tc) of every sequence of one layer's indexer.

@@ -3,13 +3,16 @@
 //
 // One 512-thread CTA owns one row (two CTAs per SM).  Scores are compared through their
 // order-preserving 32-bit keys.
-//   * Rows with at most kCap visible scores are copied to shared memory whole.
-//   * Longer rows: a sample of at most kSampleMax keys (whole 8-key groups, evenly strided)
-//     gives, by an exact radix select
-//     in shared memory, a threshold theta that about 1.25k of the row's keys exceed; one
-//     streaming pass then appends every key >= theta, in position order (block-wide prefix
-//     sums of warp ballots), to shared memory.  Every key below theta has at least k larger
-//     keys, so the row's top-k lies among the candidates.
+//   * Rows with at most Cap visible scores are copied to shared memory whole.
+//   * Longer rows: a sample of at most Cap keys (whole 8-key groups, evenly strided) gives,
+//     by an exact radix select in shared memory, a threshold theta that about 1.25k of the
+//     row's keys exceed; one streaming pass then appends every key >= theta, in position
+//     order (block-wide prefix sums of per-thread counts), to shared memory.  Every key below
+//     theta has at least k larger keys, so the row's top-k lies among the candidates.  The
+//     pass reads the row through a ring of bulk copies (cp.async.bulk into shared memory,
+//     completion on an mbarrier) of Per scores per thread each, and is bound by its
+//     per-score instruction count: one block-wide scan per Per x 512 scores, 32-bit indices,
+//     no per-score bounds checks on whole chunks, the NaN flag kept in a register.
 //   * An exact radix select (11/11/10-bit histograms) among the candidates finds the k-th key;
 //     a stable compaction writes the selected positions in order.
 // If the sample misjudges the threshold (fewer than k candidates, or more than fit), the CTA
@@ -23,16 +26,22 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
-constexpr int kCap = 8192;         // candidates held in shared memory
-constexpr int kSampleMax = 8192;   // sampled keys of a long row
-constexpr int kPer = 8;            // consecutive scores per thread per streaming step
+constexpr int kPer = 8;                     // consecutive entries per thread per compaction step
+constexpr long long kWaitCycles = 2000000000LL;
 
+// Cap: candidates (and sampled keys) held in shared memory; Ring: bulk-copy slots;
+// Per: consecutive scores per thread per streaming step (a slot holds Per x 512 scores).
+template <int Cap, int Ring, int Per>
 struct TopkSmem {
-  uint32_t key[kCap];
-  int32_t pos[kCap];
+  float ring[Ring][kThreads * Per];
+  uint32_t key[Cap];
+  int32_t pos[Cap];
   uint32_t hist[kBins];
   uint32_t warp_sums[kWarps];
   uint32_t sel_bin, sel_above;
+  uint64_t full[Ring];
+  int abort;
+  uint32_t kmax;  // largest candidate key
 };
 
 // Exclusive block-wide prefix sum; *total receives the block sum.
@@ -62,55 +71,63 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_s
   return base + x - v;
 }
 
-// Warp 0: the bin b (scanning from the top) with above(b) < need <= above(b) + hist[b].
-__device__ __forceinline__ void select_bin(TopkSmem& sm, uint32_t need) {
-  const int lane = threadIdx.x;
-  const int hi = kBins - 64 * lane, lo = hi - 64;
-  uint32_t s = 0;
-  for (int b = lo; b < hi; ++b) s += sm.hist[b];
-  uint32_t incl = s;
+// The bin b (counting from the top) with above(b) < need <= above(b) + hist[b], among the
+// nbins <= 2048 bins: thread t sums the four bins nbins-1-4t .. nbins-4-4t, one block scan
+// gives each thread the count above its bins, and the thread whose bins hold the need-th key
+// writes sel_bin / sel_above.
+template <class Sm>
+__device__ __forceinline__ void select_bin(Sm& sm, uint32_t need, int nbins) {
+  uint32_t h[4], s = 0;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
+  for (int j = 0; j < 4; ++j) {
+    const int b = nbins - 1 - 4 * (int)threadIdx.x - j;
+    h[j] = b >= 0 ? sm.hist[b] : 0u;
+    s += h[j];
   }
-  const uint32_t above = incl - s;
-  if (above < need && need <= incl) {
+  uint32_t tot;
+  const uint32_t above = block_excl_scan(s, sm.warp_sums, &tot);
+  if (above < need && need <= above + s) {
     uint32_t acc = above;
-    for (int b = hi - 1; b >= lo; --b) {
-      const uint32_t h = sm.hist[b];
-      if (acc + h >= need) {
-        sm.sel_bin = (uint32_t)b;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (acc + h[j] >= need) {
+        sm.sel_bin = (uint32_t)(nbins - 1 - 4 * (int)threadIdx.x - j);
         sm.sel_above = acc;
         break;
       }
-      acc += h;
+      acc += h[j];
     }
   }
 }
 
-// The need-th largest key (need >= 1) among keys delivered by get(i), i < n, by three
-// histogram passes.  Returns the key; *ties receives how many keys equal to it are taken.
-template <class Get>
-__device__ uint32_t radix_select(TopkSmem& sm, int64_t n, uint32_t need, Get get, uint32_t* ties) {
-  uint32_t prefix = 0, pmask = 0;
+// Radix select over keys delivered by get(i), i < n, that all carry `prefix` in their bits at
+// and above `top` (prefix has no bits below `top`): histograms of 11-bit digits from bit `top`
+// down to bit `stop` locate the need-th largest key (need >= 1).  Returns its bits at and
+// above `stop` (lower bits zero); with stop = 0 that is the key itself and *ties receives how
+// many keys equal to it are taken.
+template <class Sm, class Get>
+__device__ uint32_t radix_select(Sm& sm, int64_t n, uint32_t need, Get get, uint32_t* ties, uint32_t prefix, int top,
+                                 int stop) {
+  uint32_t pmask = top >= 32 ? 0u : ~((1u << top) - 1u);
 #pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const uint32_t wmask = pass == 2 ? 0x3ffu : 0x7ffu;
-    for (int i = threadIdx.x; i < kBins; i += kThreads) sm.hist[i] = 0;
+  while (top > stop) {
+    const int width = top - stop < 11 ? top - stop : 11;
+    const int shift = top - width;
+    const uint32_t wmask = (1u << width) - 1u;
+    for (int i = threadIdx.x; i < (1 << width); i += kThreads) sm.hist[i] = 0;
     __syncthreads();
     for (int64_t i = threadIdx.x; i < n; i += kThreads) {
       const uint32_t key = get(i);
       if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & wmask], 1u);
     }
     __syncthreads();
-    if (threadIdx.x < 32) select_bin(sm, need);
+    select_bin(sm, need, 1 << width);
     __syncthreads();
     prefix |= sm.sel_bin << shift;
     pmask |= wmask << shift;
     need -= sm.sel_above;
     __syncthreads();
+    top = shift;
   }
   *ties = need;
   return prefix;
@@ -131,8 +148,8 @@ __device__ __forceinline__ void load8(const float* x, int64_t q, int64_t n, bool
 // Stable ordered compaction: writes out[0..k) with the positions of the entries whose key is
 // > tau, plus the first `ties` entries whose key == tau, in stream order.  get(i) gives
 // (key, position) of entry i < n.
-template <class Get>
-__device__ void ordered_output(TopkSmem& sm, int64_t n, uint32_t tau, uint32_t ties, int k, int32_t* out, Get get) {
+template <class Sm, class Get>
+__device__ void ordered_output(Sm& sm, int64_t n, uint32_t tau, uint32_t ties, int k, int32_t* out, Get get) {
   uint32_t out_base = 0, eq_seen = 0;
 #pragma unroll 1
   for (int64_t base = 0; base < n; base += (int64_t)kThreads * kPer) {
@@ -171,10 +188,31 @@ __device__ void ordered_output(TopkSmem& sm, int64_t n, uint32_t tau, uint32_t t
   }
 }
 
+__device__ __forceinline__ uint32_t sa(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(sa(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+template <int Cap, int Ring, int Per>
 __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
-  __shared__ uint32_t s_count;
+  using Sm = TopkSmem<Cap, Ring, Per>;
+  constexpr int kChunk = kThreads * Per;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
   __shared__ int s_nan;
   const int row = blockIdx.x;
   const int b = row / p.Tc, tl = row % p.Tc, t = p.t0 + tl;
@@ -190,14 +228,20 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
   }
   const bool vec = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
   if (threadIdx.x == 0) {
-    s_count = 0;
     s_nan = 0;
+    sm.abort = 0;
+    sm.kmax = 0;
+    for (int i = 0; i < Ring; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(sa(&sm.full[i])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
 
   int64_t c = 0;  // candidates in shared memory
   bool ok = true;
-  if (n <= kCap) {
+  uint32_t theta_s = 0;  // candidate threshold of a long row
+  if (n <= Cap) {
+#pragma unroll 4
     for (int64_t i = threadIdx.x; i < n; i += kThreads) {
       const float v = __ldg(x + i);
       if (isnan(v)) s_nan = 1;
@@ -206,59 +250,144 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
     }
     c = n;
   } else {
+    const int64_t nchunks = (n + kChunk - 1) / kChunk;
+    // ring slot s holds chunk ci; the bulk copy covers the chunk's whole 16-byte units, the
+    // last 1-3 scores of a ragged row tail are read directly
+    auto bulk_len = [&](int64_t ci) -> int64_t {
+      const int64_t len = n - ci * kChunk < kChunk ? n - ci * kChunk : kChunk;
+      return vec ? (len & ~(int64_t)3) : 0;
+    };
+    auto issue = [&](int64_t ci) {
+      const int s = (int)(ci % Ring);
+      const uint32_t bytes = (uint32_t)(bulk_len(ci) * 4);
+      if (bytes) {
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(sa(&sm.full[s])), "r"(bytes)
+                     : "memory");
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                sa(&sm.ring[s][0])),
+            "l"(reinterpret_cast<uint64_t>(x + ci * kChunk)), "r"(bytes), "r"(sa(&sm.full[s]))
+            : "memory");
+      } else {
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(sa(&sm.full[s])) : "memory");
+      }
+    };
+    // the stream starts before the sample is taken, so its latency hides behind the select
+    if (threadIdx.x == 0)
+      for (int64_t ci = 0; ci < Ring && ci < nchunks; ++ci) issue(ci);
     // threshold from a sample of whole 8-score groups (one 32-byte sector each), evenly
     // strided over the row, so the sample touches only every g-th sector
     const int64_t groups = n / 8;
-    const int64_t gstride = (groups * 8 + kSampleMax - 1) / kSampleMax;  // >= 1 since n > kCap
+    const int64_t gstride = (groups * 8 + Cap - 1) / Cap;  // >= 1 since n > Cap
     const int64_t mg = (groups + gstride - 1) / gstride;
     const int64_t m = mg * 8;
+#pragma unroll 4
     for (int64_t i = threadIdx.x; i < m; i += kThreads)
       sm.key[i] = score_key(__ldg(x + (i >> 3) * gstride * 8 + (i & 7)));
     __syncthreads();
     int64_t ks = (int64_t)ceil(1.25 * (double)k * (double)m / (double)n) + 16;
     if (ks > m) ks = m;
+    // the ks-th largest sampled key rounded down to a multiple of 2^10: two digit passes; a
+    // lower threshold only admits more candidates
     uint32_t dummy;
-    const uint32_t theta = radix_select(sm, m, (uint32_t)ks, [&](int64_t i) { return sm.key[i]; }, &dummy);
-    // one streaming pass: append every key >= theta in position order
-    uint32_t count = 0;
+    const uint32_t theta =
+        radix_select(sm, m, (uint32_t)ks, [&](int64_t i) { return sm.key[i]; }, &dummy, 0u, 32, 10);
+    theta_s = theta;
+    // one streaming pass: append every key >= theta in position order (32-bit indices: n < 2^31)
+    const int n32 = (int)n;
+    uint32_t count = 0, kmax = 0;
+    bool nan_seen = false;
 #pragma unroll 1
-    for (int64_t base = 0; base < n; base += (int64_t)kThreads * kPer) {
-      const int64_t q = base + (int64_t)threadIdx.x * kPer;
-      float v[kPer];
-      load8(x, q, n, vec, v);
-      uint32_t key[kPer];
+    for (int64_t ci = 0; ci < nchunks; ++ci) {
+      const int s = (int)(ci % Ring);
+      // a timed-out copy ends the pass for the whole block at once
+      if (__syncthreads_or(!ring_wait(&sm.full[s], (uint32_t)((ci / Ring) & 1), &sm.abort))) break;
+      const int base = (int)ci * kChunk, blen = (int)bulk_len(ci);
+      const int q = base + (int)threadIdx.x * Per;
+      const float* slot = &sm.ring[s][threadIdx.x * Per];
+      uint32_t key[Per];
       uint32_t cnt = 0;
+      if (blen == kChunk) {  // whole chunk in the slot
 #pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        const bool valid = q + j < n;
-        if (valid && isnan(v[j])) s_nan = 1;
-        key[j] = score_key(v[j]);
-        cnt += (valid && key[j] >= theta);
+        for (int j = 0; j < Per; j += 4) {
+          const float4 a4 = *reinterpret_cast<const float4*>(slot + j);
+          const float v4[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            nan_seen |= v4[u] != v4[u];
+            key[j + u] = score_key(v4[u]);
+            cnt += key[j + u] >= theta;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < Per; ++j) {
+          const int i = q + j;
+          const float v = i < base + blen ? slot[j] : (i < n32 ? __ldg(x + i) : 0.f);
+          nan_seen |= i < n32 && v != v;
+          key[j] = i < n32 ? score_key(v) : 0u;
+          cnt += i < n32 && key[j] >= theta;
+        }
       }
       uint32_t tot;
       uint32_t o = count + block_excl_scan(cnt, sm.warp_sums, &tot);
+      // every thread has read slot s (the scan synchronised the block): refill it
+      if (threadIdx.x == 0 && ci + Ring < nchunks) issue(ci + Ring);
+      if (cnt) {
 #pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        if (q + j < n && key[j] >= theta) {
-          if (o < (uint32_t)kCap) {
-            sm.key[o] = key[j];
-            sm.pos[o] = (int32_t)(q + j);
+        for (int j = 0; j < Per; ++j) {
+          // keys past n are 0 and never >= theta (theta is a sampled key, >= 1 unless NaN)
+          if (key[j] >= theta && q + j < n32) {
+            kmax = key[j] > kmax ? key[j] : kmax;
+            if (o < (uint32_t)Cap) {
+              sm.key[o] = key[j];
+              sm.pos[o] = q + j;
+            }
+            ++o;
           }
-          ++o;
         }
       }
       count += tot;
     }
+    if (nan_seen) s_nan = 1;
+    if (kmax) atomicMax(&sm.kmax, kmax);
     __syncthreads();
+    if (sm.abort) {
+      // a copy never completed: let the ones still in flight land before the CTA exits
+      if (threadIdx.x == 0) {
+        for (int64_t ci = nchunks - Ring > 0 ? nchunks - Ring : 0; ci < nchunks; ++ci) {
+          const long long t0 = clock64();
+          uint32_t okw = 0;
+          while (!okw && clock64() - t0 < kWaitCycles)
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, "
+                "p;\n}\n"
+                : "=r"(okw)
+                : "r"(sa(&sm.full[ci % Ring])), "r"((uint32_t)((ci / Ring) & 1))
+                : "memory");
+        }
+        atomicOr(p.flags, DSA_FLAG_TIMEOUT);
+      }
+      return;
+    }
     c = count;
-    ok = count >= (uint32_t)k && count <= (uint32_t)kCap;
+    ok = count >= (uint32_t)k && count <= (uint32_t)Cap;
   }
   __syncthreads();
   if (s_nan && threadIdx.x == 0) atomicOr(p.flags, DSA_FLAG_NAN_SCORE);
 
   if (ok) {
-    uint32_t ties;
-    const uint32_t tau = radix_select(sm, c, (uint32_t)k, [&](int64_t i) { return sm.key[i]; }, &ties);
+    // every candidate key lies in [theta, kmax] (short rows: the whole key range), so the
+    // bits above the highest one where theta and kmax differ are common to all of them
+    uint32_t ties, prefix = 0;
+    int top = 32;
+    if (n > Cap) {
+      const uint32_t diff = theta_s ^ sm.kmax;
+      top = diff ? 32 - __clz(diff) : 0;
+      prefix = top >= 32 ? 0u : (sm.kmax & ~((1u << top) - 1u));
+    }
+    const uint32_t tau =
+        radix_select(sm, c, (uint32_t)k, [&](int64_t i) { return sm.key[i]; }, &ties, prefix, top, 0);
     ordered_output(sm, c, tau, ties, k, out, [&](int64_t i, uint32_t& key, int32_t& ps) {
       key = sm.key[i];
       ps = sm.pos[i];
@@ -267,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
     // the sample misjudged the threshold: three histogram passes over the row in global memory
     auto gkey = [&](int64_t i) { return score_key(__ldg(x + i)); };
     uint32_t ties;
-    const uint32_t tau = radix_select(sm, n, (uint32_t)k, gkey, &ties);
+    const uint32_t tau = radix_select(sm, n, (uint32_t)k, gkey, &ties, 0u, 32, 0);
     ordered_output(sm, n, tau, ties, k, out, [&](int64_t i, uint32_t& key, int32_t& ps) {
       key = gkey(i);
       ps = (int32_t)i;
@@ -275,17 +404,26 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
   }
 }
 
+template <int Cap, int Ring, int Per>
+cudaError_t launch_rows(const TopkLaunch& p, int rows, cudaStream_t st) {
+  const int smem = (int)sizeof(TopkSmem<Cap, Ring, Per>);
+  cudaError_t e =
+      cudaFuncSetAttribute(k_topk_rows<Cap, Ring, Per>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  k_topk_rows<Cap, Ring, Per><<<rows, kThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_topk_rows(const TopkLaunch& p, cudaStream_t st) {
   const int rows = p.B * p.Tc;
   if (rows <= 0) return cudaSuccess;
-  const int smem = (int)sizeof(TopkSmem);
-  cudaError_t e = cudaFuncSetAttribute(k_topk_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  k_topk_rows<<<rows, kThreads, smem, st>>>(p);
+  // about 1.25k + 16 n / Cap candidates are expected: 4096 slots hold them for k <= 2560
+  const cudaError_t e =
+      p.k <= 2560 ? launch_rows<4096, 2, 16>(p, rows, st) : launch_rows<8192, 2, 8>(p, rows, st);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace dsa

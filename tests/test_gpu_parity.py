@@ -59,7 +59,8 @@ def _recall_and_validity(got, ref_idx, ref_scores, n_valid, tol_rel=1e-4):
 # --- top-k over a score buffer --------------------------------------------------------
 
 @pytest.mark.parametrize("kind,n,k", [("int", 1000, 64), ("int", 5000, 2048), ("normal", 3000, 257),
-                                      ("normal", 70000, 2048), ("int", 300, 4096), ("normal", 9000, 1)])
+                                      ("normal", 70000, 2048), ("int", 300, 4096), ("normal", 9000, 1),
+                                      ("normal", 20001, 3000), ("int", 40000, 4096), ("normal", 131072, 2048)])
 def test_topk_from_scores_bit_exact(kind, n, k):
     R = 24
     sc = synth.scores_input(R, n, DEV, kind, lo=-3, hi=3)
@@ -78,6 +79,17 @@ def test_topk_from_scores_ragged_ld_and_batches():
     nv = np.clip(np.arange(T) + S - T + 1, 0, S)
     ref = oracle.topk_rows(full[:, :, :S].reshape(B * T, S).double().cpu().numpy(), np.tile(nv, B), k)
     assert np.array_equal(idx.reshape(B * T, k).cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("ld,S", [(20003, 20001), (9001, 8999)])
+def test_topk_from_scores_unaligned_rows(ld, S):
+    # odd row strides: most rows start off a 16-byte boundary and are streamed without bulk copies
+    T, k = 9, 700
+    full = synth.scores_input(T, ld, DEV, "normal").reshape(1, T, ld)
+    idx = dsa.dsa_topk(k, scores=full[:, :, :S], q_pos0=S - T, diag=1)
+    nv = np.clip(np.arange(T) + S - T + 1, 0, S)
+    ref = oracle.topk_rows(full[0, :, :S].double().cpu().numpy(), nv, k)
+    assert np.array_equal(idx.reshape(T, k).cpu().numpy(), ref)
 
 
 def test_topk_nan_scores_rank_lowest_and_raise_flag():
