@@ -14,6 +14,7 @@ reference`` times the CPU oracle instead, on sampled rows of the same workload.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -156,6 +157,23 @@ def indexer_flops(wl) -> float:
     return float(np.sum(visible_counts(wl).astype(np.float64)) * 2 * wl.HI * wl.DI)
 
 
+def captured_traffic(kernel: str, units: int):
+    """DRAM bytes (read + write) per launch of `kernel` over `units` query rows, scaled from
+    the ncu capture recorded in profiles/traffic.json -- or None when the kernel's source has
+    changed since that capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None, "no capture"
+    rec = json.load(open(p)).get(kernel)
+    if rec is None:
+        return None, "no capture"
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["sha256"]:
+        return None, "kernel changed since " + rec["capture"]
+    return round(rec["dram_bytes_per_query_row"] * units), (
+        f"{rec['capture']}: {rec['dram_bytes'] / 1e9:.2f} GB over {rec['query_rows']} query rows, scaled by rows")
+
+
 def load_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -273,9 +291,17 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     n0 = dsa.launch_count()
     clocks.start()
+    # every launch of the timed steps is bracketed by CUDA events on its stream, so each
+    # kernel's device time is measured inside the timed region itself
+    dsa.trace_enable(256 * args.steps + 64)
     ms = time_loop(step, args.steps, 0, world)
     clk = clocks.stop()
     launches = dsa.launch_count() - n0
+    trace = dsa.trace_read()
+    dsa.trace_disable()
+    by_kind = {}
+    for kind, t in trace:
+        by_kind.setdefault(kind, []).append(t)
     ms = max_over_ranks(ms, world)
     tokens = wl.B * wl.T
     value = tokens * world / (ms / 1e3)
@@ -292,17 +318,22 @@ def run_ours(args, rank, world, local):
 
     peaks = load_peaks()
     a_bytes = attn_bytes(wl)
-    att_gbs = a_bytes / (at_ms / 1e3) / 1e9
+    att_launch_ms = float(np.mean(by_kind["attention"]))  # mean device time in the timed region
+    att_gbs = a_bytes / (att_launch_ms / 1e3) / 1e9
     ix_tf = indexer_flops(wl) / (ix_ms / 1e3) / 1e12
     fp8_peak = peaks["bf16_tflops"] * 2.0  # FP8 dense = 2x bf16 (nominal 4.5 vs 2.25 PF)
     attn_total = 4 * at_ms
     if attn_total >= ix_ms:
-        roof = {"kernel": "sparse attention (k_sparse_attn)", "bound": "hbm", "achieved": round(att_gbs, 1),
+        traffic, traffic_src = captured_traffic("k_sparse_mla_tc", wl.B * wl.T)
+        roof = {"kernel": "sparse MLA attention (k_sparse_mla_tc)", "bound": "hbm", "achieved": round(att_gbs, 1),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(att_gbs / peaks["hbm_gbs"], 4),
-                "traffic": None, "algorithmic_bytes_per_launch": a_bytes, "launch_ms": round(at_ms, 3),
+                "traffic": traffic, "traffic_src": traffic_src, "algorithmic_bytes_per_launch": a_bytes,
+                "launch_ms": round(att_launch_ms, 3), "launches_timed": len(by_kind["attention"]),
                 "peak_src": peaks["src"]}
     else:
-        roof = {"kernel": "indexer + top-k (FP8)", "bound": "tensor", "achieved": round(ix_tf, 1),
+        ixk_ms = float(np.sum(by_kind.get("indexer", [0.0]))) / args.steps
+        ix_tf = indexer_flops(wl) / (ixk_ms / 1e3) / 1e12
+        roof = {"kernel": "indexer (k_indexer_tc, FP8)", "bound": "tensor", "achieved": round(ix_tf, 1),
                 "peak": fp8_peak, "unit": "TFLOP/s", "frac": round(ix_tf / fp8_peak, 4), "traffic": None,
                 "algorithmic_flops_per_call": indexer_flops(wl), "call_ms": round(ix_ms, 3),
                 "peak_src": peaks["src"] + " bf16 x 2 (FP8 nominal ratio)"}
@@ -324,6 +355,7 @@ def run_ours(args, rank, world, local):
         "fsss_vs_ffff": {"fsss_ms": round(ms, 3), "ffff_ms": round(ffff_ms, 3), "speedup": round(ffff_ms / ms, 3),
                          "adjacent_layer_overlap": round(overlap01, 4)},
         "roofline": roof, "gpu_launches": int(launches), "clocks": clk, "device_flags": flags,
+        "kernel_ms_per_step": {k: round(float(np.sum(v)) / args.steps, 3) for k, v in sorted(by_kind.items())},
     }
 
     if not args.no_e2e:

@@ -198,6 +198,24 @@ const char* dsa_last_error(void);
 /* Number of kernels this library has launched since it was loaded (all threads). */
 uint64_t dsa_launch_count(void);
 
+/* Launch tracing, for measuring the device time of each kernel inside a larger timed region.
+ * dsa_trace_enable(max_launches): creates a pool of 2*max_launches CUDA events (host call;
+ *   returns DSA_ERR_INVALID_ARG unless 0 < max_launches <= 2^20, DSA_ERR_CUDA if event
+ *   creation fails) and starts recording: from then on every kernel launch the library makes
+ *   is bracketed by two events recorded on its stream.  Launches beyond the pool are not
+ *   recorded.
+ * dsa_trace_read(kinds, ms, max_records, dropped): waits for the recorded launches to finish
+ *   (host synchronisation on their events), writes up to max_records entries in launch order
+ *   -- kinds[i] is DSA_TRACE_INDEXER, _TOPK, _ATTENTION or _OVERLAP, ms[i] the device time in
+ *   milliseconds (-1 if unavailable) -- returns the number written, stores in *dropped (may
+ *   be NULL) the launches the pool could not record, and clears the records.  Host arrays
+ *   are owned by the caller; kinds or ms may be NULL.
+ * dsa_trace_disable(): stops recording and destroys the pool. */
+enum { DSA_TRACE_INDEXER = 1, DSA_TRACE_TOPK = 2, DSA_TRACE_ATTENTION = 3, DSA_TRACE_OVERLAP = 4 };
+dsa_status dsa_trace_enable(int max_launches);
+int dsa_trace_read(int* kinds, float* ms, int max_records, int* dropped);
+void dsa_trace_disable(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -101,6 +101,13 @@ def load_library(path: str = LIB_PATH):
             lib.dsa_last_error.argtypes = []
             lib.dsa_launch_count.restype = _c.c_uint64
             lib.dsa_launch_count.argtypes = []
+            lib.dsa_trace_enable.restype = S
+            lib.dsa_trace_enable.argtypes = [_c.c_int32]
+            lib.dsa_trace_read.restype = _c.c_int32
+            lib.dsa_trace_read.argtypes = [_c.POINTER(_c.c_int32), _c.POINTER(_c.c_float), _c.c_int32,
+                                           _c.POINTER(_c.c_int32)]
+            lib.dsa_trace_disable.restype = None
+            lib.dsa_trace_disable.argtypes = []
             _lib = lib
     return _lib
 
@@ -295,6 +302,31 @@ def topk_overlap(a: torch.Tensor, b: torch.Tensor, per_row: torch.Tensor | bool 
 def launch_count() -> int:
     """Kernels launched by the library since it was loaded."""
     return int(load_library().dsa_launch_count())
+
+
+TRACE_KINDS = {1: "indexer", 2: "topk", 3: "attention", 4: "overlap"}
+
+
+def trace_enable(max_launches: int = 4096) -> None:
+    """Start bracketing every kernel launch with CUDA events (dsa_trace_enable)."""
+    _check(load_library().dsa_trace_enable(int(max_launches)))
+
+
+def trace_read(max_records: int = 1 << 16) -> list:
+    """[(kind name, device ms), ...] of the launches recorded since the last read, in launch
+    order; waits for them to finish.  Raises if the event pool dropped launches."""
+    lib = load_library()
+    kinds = (_c.c_int32 * max_records)()
+    ms = (_c.c_float * max_records)()
+    dropped = _c.c_int32(0)
+    n = lib.dsa_trace_read(kinds, ms, max_records, _c.byref(dropped))
+    if dropped.value:
+        raise RuntimeError(f"dsa trace: {dropped.value} launches were not recorded (pool too small)")
+    return [(TRACE_KINDS.get(kinds[i], str(kinds[i])), float(ms[i])) for i in range(n)]
+
+
+def trace_disable() -> None:
+    load_library().dsa_trace_disable()
 
 
 def read_device_flags(device=None) -> int:

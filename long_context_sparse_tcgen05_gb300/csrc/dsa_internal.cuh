@@ -17,6 +17,20 @@ constexpr size_t kWsScratch = DSA_WS_MIN;
 // Kernel launches issued by this library since load (diagnostics; see dsa_launch_count).
 void count_launches(uint64_t n);
 
+// Launch tracing (dsa_trace_enable): when on, a scope brackets one launcher's kernels with
+// CUDA events on its stream; durations are read back by dsa_trace_read.
+enum TraceKind { kTraceIndexer = 1, kTraceTopk = 2, kTraceAttention = 3, kTraceOverlap = 4 };
+int trace_open(int kind, cudaStream_t st);
+void trace_close(int slot, cudaStream_t st);
+struct TraceScope {
+  int slot;
+  cudaStream_t st;
+  TraceScope(int kind, cudaStream_t s) : slot(trace_open(kind, s)), st(s) {}
+  ~TraceScope() { trace_close(slot, st); }
+  TraceScope(const TraceScope&) = delete;
+  TraceScope& operator=(const TraceScope&) = delete;
+};
+
 // Host-side helpers shared by the entry points: argument checks of an indexer operand set
 // (sets the thread's last-error message on failure) and recording a failure message.
 dsa_status validate_indexer(const dsa_indexer_args* ix);
@@ -50,7 +64,6 @@ struct IndexerLaunch {
   int ksplit;           // key-range splits per token block (0: chosen by the launcher)
 };
 cudaError_t launch_indexer_scores(const IndexerLaunch& p, cudaStream_t st);     // tcgen05 path
-cudaError_t launch_indexer_scores_mma(const IndexerLaunch& p, cudaStream_t st); // mma.sync path
 
 // Top-k over materialised score rows: rows [t0, t0 + Tc) of every sequence,
 // scores[b*bstride + (t - t0)*ld + s], output idx[(b*T + t)*k + j].

@@ -286,6 +286,7 @@ __global__ void __launch_bounds__(AtCfg<HP, DQK, DV, SEPV, NB>::kThreads, 1)
 
 template <int HP, int DQK, int DV, bool SEPV>
 cudaError_t launch_cfg(const AttnLaunch& p, cudaStream_t st) {
+  TraceScope trace(kTraceAttention, st);
   constexpr int NB = 32;
   using C = AtCfg<HP, DQK, DV, SEPV, NB>;
   auto kern = k_sparse_attn_mma<HP, DQK, DV, SEPV, NB>;

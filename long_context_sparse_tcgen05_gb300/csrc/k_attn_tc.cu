@@ -564,10 +564,11 @@ int num_sms() {
 
 bool sparse_mla_tc_supported(const AttnLaunch& p) {
   return p.H == kH && p.DQK == kDQK && p.DV == kDV && p.v == p.k && p.v_ld == p.k_ld && p.k_ld == kDQK &&
-         (int64_t)p.B * p.S < (1ll << 31) && !getenv("DSA_ATTN_MMA");
+         (int64_t)p.B * p.S < (1ll << 31);
 }
 
 cudaError_t launch_sparse_mla_tc(const AttnLaunch& p, cudaStream_t st) {
+  TraceScope trace(kTraceAttention, st);
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tq, tkv;

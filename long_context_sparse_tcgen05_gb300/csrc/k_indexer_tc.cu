@@ -318,6 +318,7 @@ cudaError_t make_map(CUtensorMap* m, const void* base, bool fp8, int row_elems, 
 
 template <int HI, int DI, bool FP8>
 cudaError_t launch_cfg(const IndexerLaunch& p, cudaStream_t st) {
+  TraceScope trace(kTraceIndexer, st);
   using C = Cfg<HI, DI, FP8>;
   CUtensorMap tq, tk;
   cudaError_t e = make_map(&tq, p.q, FP8, DI, (int64_t)p.T * HI, p.B, C::kAtomElems, kN);
@@ -349,8 +350,6 @@ cudaError_t launch_cfg(const IndexerLaunch& p, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_indexer_scores(const IndexerLaunch& p, cudaStream_t st) {
-  static const bool use_mma = getenv("DSA_INDEXER_MMA") != nullptr;
-  if (use_mma) return launch_indexer_scores_mma(p, st);
   if (p.B <= 0 || p.Tc <= 0 || p.S <= 0) return cudaSuccess;
   if (p.HI == 64 && p.DI == 128) return p.fp8 ? launch_cfg<64, 128, true>(p, st) : launch_cfg<64, 128, false>(p, st);
   if (p.HI == 4 && p.DI == 64 && !p.fp8) return launch_cfg<4, 64, false>(p, st);

@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(1024) k_mean(const float* per_row, int rows, d
 cudaError_t launch_topk_overlap(const int32_t* a, const int32_t* b, int rows, int k,
                                 float* per_row, double* mean_dev, uint32_t* flags,
                                 cudaStream_t st) {
+  TraceScope trace(kTraceOverlap, st);
   if (rows > 0) {
     const int ctas = (rows + kWarpsPerCta - 1) / kWarpsPerCta;
     k_topk_overlap<<<ctas, kWarpsPerCta * 32, 0, st>>>(a, b, rows, k, per_row, flags);

@@ -406,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
 
 template <int Cap, int Ring, int Per>
 cudaError_t launch_rows(const TopkLaunch& p, int rows, cudaStream_t st) {
+  TraceScope trace(kTraceTopk, st);
   const int smem = (int)sizeof(TopkSmem<Cap, Ring, Per>);
   cudaError_t e =
       cudaFuncSetAttribute(k_topk_rows<Cap, Ring, Per>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -200,3 +200,14 @@ def test_workspace_size_plan(lib):
     n = lib.dsa_workspace_size(ctypes.byref(ix), 2048)
     assert n >= 256 + 131072 * 4 and n <= 256 + (4 << 30)
     assert lib.dsa_workspace_size(None, 16) == 256
+
+
+def test_trace_enable_validation_and_empty_read(lib):
+    assert lib.dsa_trace_enable(0) == INVALID
+    assert lib.dsa_trace_enable(-5) == INVALID
+    assert lib.dsa_trace_enable((1 << 20) + 1) == INVALID
+    dropped = ctypes.c_int32(7)
+    # nothing recorded: no records, no drops, nothing dereferenced in the null arrays
+    assert lib.dsa_trace_read(None, None, 0, ctypes.byref(dropped)) == 0
+    assert dropped.value == 0
+    lib.dsa_trace_disable()

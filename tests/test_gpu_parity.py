@@ -254,6 +254,27 @@ def test_group_two_groups_and_lse_optional():
         assert np.abs(outs[l].reshape(300, 8, 64).float().cpu().numpy() - ref[l]["out"]).max() <= ATOL_OUT
 
 
+def test_trace_records_every_launch_of_a_group():
+    # the schedule FSSS launches the indexer and the top-k of the F layer (one chunk at this
+    # size) and four attention kernels; the trace sees each with a positive device time
+    wl = synth.WORKLOADS["tiny_l1k"]
+    layers = [synth.layer_inputs(wl, l, DEV) for l in range(4)]
+    dsa.indexshare_group_forward(layers, "FSSS", wl.k)  # warm (workspace, tensor maps)
+    torch.cuda.synchronize()
+    n0 = dsa.launch_count()
+    dsa.trace_enable(64)
+    try:
+        dsa.indexshare_group_forward(layers, "FSSS", wl.k)
+        rec = dsa.trace_read()
+    finally:
+        dsa.trace_disable()
+    kinds = [k for k, _ in rec]
+    assert kinds.count("attention") == 4 and kinds.count("indexer") == 1 and kinds.count("topk") == 1
+    assert len(rec) == dsa.launch_count() - n0
+    assert all(ms > 0 for _, ms in rec)
+    assert dsa.trace_read() == []  # cleared by the read
+
+
 # --- overlap ------------------------------------------------------------------------------
 
 def test_topk_overlap_matches_oracle():
