@@ -133,6 +133,49 @@ __device__ uint32_t radix_select(Sm& sm, int64_t n, uint32_t need, Get get, uint
   return prefix;
 }
 
+// Keeps, in place and in position order, the exact top-k of the first `count` candidates
+// (count >= k; ties go to the lower position, i.e. the earlier entry) and returns the k-th key.
+template <class Sm>
+__device__ uint32_t compact_top(Sm& sm, uint32_t count, int k) {
+  uint32_t ties;
+  const uint32_t tau =
+      radix_select(sm, (int64_t)count, (uint32_t)k, [&](int64_t i) { return sm.key[i]; }, &ties, 0u, 32, 0);
+  uint32_t out_base = 0, eq_seen = 0;
+#pragma unroll 1
+  for (uint32_t base = 0; base < count; base += (uint32_t)kThreads * kPer) {
+    const uint32_t q = base + threadIdx.x * kPer;
+    uint32_t kk[kPer];
+    int32_t ps[kPer];
+    uint32_t cg = 0, ce = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const bool valid = q + j < count;
+      kk[j] = valid ? sm.key[q + j] : 0u;
+      ps[j] = valid ? sm.pos[q + j] : -1;
+      cg += valid && kk[j] > tau;
+      ce += valid && kk[j] == tau;
+    }
+    uint32_t tot;  // every entry of this pass is in registers once the scan returns
+    const uint32_t ex = block_excl_scan((cg << 16) | ce, sm.warp_sums, &tot);
+    const uint32_t rem = ties > eq_seen ? ties - eq_seen : 0u;
+    uint32_t o = out_base + (ex >> 16) + ((ex & 0xffffu) < rem ? (ex & 0xffffu) : rem);
+    uint32_t eq_idx = eq_seen + (ex & 0xffffu);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      if (ps[j] < 0) continue;
+      if (kk[j] > tau || (kk[j] == tau && eq_idx++ < ties)) {
+        sm.key[o] = kk[j];
+        sm.pos[o] = ps[j];
+        ++o;
+      }
+    }
+    out_base += (tot >> 16) + ((tot & 0xffffu) < rem ? (tot & 0xffffu) : rem);
+    eq_seen += tot & 0xffffu;
+  }
+  __syncthreads();
+  return tau;
+}
+
 __device__ __forceinline__ void load8(const float* x, int64_t q, int64_t n, bool vec, float v[kPer]) {
   if (vec && q + kPer <= n) {
     const float4 a = __ldg(reinterpret_cast<const float4*>(x + q));
@@ -285,14 +328,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
     for (int64_t i = threadIdx.x; i < m; i += kThreads)
       sm.key[i] = score_key(__ldg(x + (i >> 3) * gstride * 8 + (i & 7)));
     __syncthreads();
-    int64_t ks = (int64_t)ceil(1.25 * (double)k * (double)m / (double)n) + 16;
+    // aim at about 1.5k candidates: too few (< k) costs a fallback, too many only a compaction
+    int64_t ks = (int64_t)ceil(1.5 * (double)k * (double)m / (double)n) + 8;
     if (ks > m) ks = m;
     // the ks-th largest sampled key rounded down to a multiple of 2^10: two digit passes; a
     // lower threshold only admits more candidates
     uint32_t dummy;
-    const uint32_t theta =
+    uint32_t theta =
         radix_select(sm, m, (uint32_t)ks, [&](int64_t i) { return sm.key[i]; }, &dummy, 0u, 32, 10);
-    theta_s = theta;
+    theta_s = theta;  // lower bound of every candidate key
     // one streaming pass: append every key >= theta in position order (32-bit indices: n < 2^31)
     const int n32 = (int)n;
     uint32_t count = 0, kmax = 0;
@@ -333,10 +377,21 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
       uint32_t o = count + block_excl_scan(cnt, sm.warp_sums, &tot);
       // every thread has read slot s (the scan synchronised the block): refill it
       if (threadIdx.x == 0 && ci + Ring < nchunks) issue(ci + Ring);
+      if (count + tot > (uint32_t)Cap && count >= (uint32_t)k) {
+        // the buffer would overflow: keep only its exact top-k and raise the threshold to the
+        // k-th key -- a later key equal to it loses the tie to every kept one -- then recount
+        const uint32_t tau = compact_top(sm, count, k);
+        count = (uint32_t)k;
+        theta_s = tau;
+        theta = tau == 0xffffffffu ? tau : tau + 1u;
+        cnt = 0;
+#pragma unroll
+        for (int j = 0; j < Per; ++j) cnt += q + j < n32 && key[j] >= theta;
+        o = count + block_excl_scan(cnt, sm.warp_sums, &tot);
+      }
       if (cnt) {
 #pragma unroll
         for (int j = 0; j < Per; ++j) {
-          // keys past n are 0 and never >= theta (theta is a sampled key, >= 1 unless NaN)
           if (key[j] >= theta && q + j < n32) {
             kmax = key[j] > kmax ? key[j] : kmax;
             if (o < (uint32_t)Cap) {

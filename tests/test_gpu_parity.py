@@ -60,7 +60,8 @@ def _recall_and_validity(got, ref_idx, ref_scores, n_valid, tol_rel=1e-4):
 
 @pytest.mark.parametrize("kind,n,k", [("int", 1000, 64), ("int", 5000, 2048), ("normal", 3000, 257),
                                       ("normal", 70000, 2048), ("int", 300, 4096), ("normal", 9000, 1),
-                                      ("normal", 20001, 3000), ("int", 40000, 4096), ("normal", 131072, 2048)])
+                                      ("normal", 20001, 3000), ("int", 40000, 4096), ("normal", 131072, 2048),
+                                      ("normal", 600000, 2048)])
 def test_topk_from_scores_bit_exact(kind, n, k):
     R = 24
     sc = synth.scores_input(R, n, DEV, kind, lo=-3, hi=3)
@@ -79,6 +80,20 @@ def test_topk_from_scores_ragged_ld_and_batches():
     nv = np.clip(np.arange(T) + S - T + 1, 0, S)
     ref = oracle.topk_rows(full[:, :, :S].reshape(B * T, S).double().cpu().numpy(), np.tile(nv, B), k)
     assert np.array_equal(idx.reshape(B * T, k).cpu().numpy(), ref)
+
+
+def test_topk_from_scores_monotone_ties():
+    # scores rise with position in plateaus of 64 equal values: the top-k sits at the end of
+    # each row, and every row's k-th value is shared by many positions (ties to the lower one)
+    R, n, k = 6, 700000, 2048
+    sc = (torch.arange(n, device=DEV, dtype=torch.float32) // 64).repeat(R, 1)
+    sc[1::2] = sc[1::2].flip(1)  # odd rows fall instead
+    for q_pos0, diag in ((n - R, 1), (n // 3, 0)):
+        idx = dsa.dsa_topk(k, scores=sc[None], q_pos0=q_pos0, diag=diag)
+        nv = np.clip(np.arange(R) + q_pos0 + diag, 0, n)
+        ref = oracle.topk_rows(sc.double().cpu().numpy(), nv, k)
+        assert np.array_equal(idx[0].cpu().numpy(), ref)
+    assert dsa.read_device_flags() == 0
 
 
 @pytest.mark.parametrize("ld,S", [(20003, 20001), (9001, 8999)])
