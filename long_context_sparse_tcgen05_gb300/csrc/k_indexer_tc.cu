@@ -12,9 +12,13 @@
 //   * warp 0 streams key tiles with TMA (128-byte swizzle) through a ring of smem stages;
 //   * warp 1 allocates TMEM and issues the MMAs from one thread (tcgen05.commit frees the
 //     stage and publishes the accumulator);
-//   * warps 2..17 read the accumulator rows (TMEM lane = key) with tcgen05.ld, apply ReLU and
-//     the head weights with packed fp32x2 FMAs -- the head sum never leaves the thread --
-//     apply the per-token scales and write the fp32 score row with coalesced stores.
+//   * warps 2..17 read the accumulator (TMEM lane = key) with tcgen05.ld, apply ReLU and the
+//     head weights with packed fp32x2 FMAs, apply the per-token scales and write the fp32 score
+//     row with coalesced stores.  With 64 heads per token a warp owns one token's 64 columns
+//     of its 32 TMEM lanes and reads them with the 16x256b shape, so a thread holds 4 keys x
+//     16 heads: its 16 head weights stay in registers for the whole CTA (re-reading them from
+//     shared memory every tile saturated the LSU pipe), and a 3-shuffle reduce-scatter over
+//     the 4 threads that share the keys leaves each thread one key's sum.
 // Every wait is bounded; a timeout raises DSA_FLAG_TIMEOUT, drains the copies in flight,
 // frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -55,6 +59,19 @@ struct Cfg {
   static_assert(kRowBytes % 128 == 0, "d_I must fill whole 128-byte rows");
   static_assert(kN % HI == 0, "heads must tile the N columns");
 };
+
+// Thread t of a warp receives, for each of the x8 repetitions j, TMEM lanes base + t/4 and
+// base + t/4 + 8 at columns 8j + 2(t%4) and 8j + 2(t%4) + 1, in that order (r[4j .. 4j+3]).
+__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
 
 __device__ __forceinline__ int64_t visible_keys(const IndexerLaunch& p, int t_local) {
   int64_t n = p.q_pos0 + p.t0 + t_local + p.diag;
@@ -208,56 +225,117 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     float sk_next = key_scale(0);
 
-    for (int kt = 0; kt < ktiles; ++kt) {
-      const int buf = kt & (kBufs - 1);
-      const float sk = sk_next;
-      sk_next = key_scale(kt + 1);
-      if (!mbar_wait(tm_full + buf, (kt / kBufs) & 1, abort_flag)) break;
-      tc_fence_after();
-      const uint32_t col0 = t_lane + buf * kN + ch * C::kCols;
-      // all of this warp's accumulator columns in one go, then the buffer goes back to the MMA
-      uint32_t r[C::kCols / 32][32];
+    if constexpr (HI == 64) {
+      // one token per warp; thread t: keys kq + t/4 + {0, 8, 16, 24}, heads 8j + 2(t%4) + {0, 1}
+      const int m = lane & 3, rq = lane >> 2;
+      const int my_key = lq * 32 + (m >> 1) * 16 + (m & 1) * 8 + rq;  // the key this thread stores
+      unsigned long long wp[8];
 #pragma unroll
-      for (int cb = 0; cb < C::kCols / 32; ++cb) tmem_ld32(col0 + cb * 32, r[cb]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tm_empty + buf);
-      const int key = (kt_lo + kt) * kM + key_in_tile;
-#pragma unroll
-      for (int tk = 0; tk < kTokW; ++tk) {
-        // four independent partial sums per token keep the FMA pipe fed
+      for (int j = 0; j < 8; ++j) wp[j] = pack2(w_warp[8 * j + 2 * m], w_warp[8 * j + 2 * m + 1]);
+      auto key_scale16 = [&](int kt) -> float {
+        const int key = (kt_lo + kt) * kM + my_key;
+        return (FP8 && kt < ktiles && key < p.S) ? __ldg(skg + key) : 1.f;
+      };
+      float sk16_next = key_scale16(0);
+      for (int kt = 0; kt < ktiles; ++kt) {
+        const int buf = kt & (kBufs - 1);
+        const float sk = sk16_next;
+        sk16_next = key_scale16(kt + 1);
+        if (!mbar_wait(tm_full + buf, (kt / kBufs) & 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t col0 = tmem + ((uint32_t)(lq * 32) << 16) + buf * kN + ch * C::kCols;
+        uint32_t r[2][32];
+        tmem_ld_16x256b_x8(col0, r[0]);
+        tmem_ld_16x256b_x8(col0 + (16u << 16), r[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tm_empty + buf);
+        // acc[2a + e]: key a*16 + e*8 + rq, as two partial sums (even / odd head of each pair)
         unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
-        float acc1 = 0.f;
 #pragma unroll
-        for (int c4 = 0; c4 < HI / 4; ++c4) {
-          const int c = tk * HI + c4 * 4;  // column within the warp
-          const float4 wv = *reinterpret_cast<const float4*>(w_warp + c);
-          const float x0 = fmaxf(__uint_as_float(r[c >> 5][c & 31]), 0.f);
-          const float x1 = fmaxf(__uint_as_float(r[(c + 1) >> 5][(c + 1) & 31]), 0.f);
-          const float x2 = fmaxf(__uint_as_float(r[(c + 2) >> 5][(c + 2) & 31]), 0.f);
-          const float x3 = fmaxf(__uint_as_float(r[(c + 3) >> 5][(c + 3) & 31]), 0.f);
-          if constexpr (HI >= 8) {
-            acc[(2 * c4) & 3] = fma2(pack2(wv.x, wv.y), pack2(x0, x1), acc[(2 * c4) & 3]);
-            acc[(2 * c4 + 1) & 3] = fma2(pack2(wv.z, wv.w), pack2(x2, x3), acc[(2 * c4 + 1) & 3]);
-          } else {
-            acc1 += wv.x * x0 + wv.y * x1 + wv.z * x2 + wv.w * x3;
-          }
-        }
-        float v;
-        if constexpr (HI >= 8)
-          v = ((lo2(acc[0]) + hi2(acc[0])) + (lo2(acc[1]) + hi2(acc[1]))) +
-              ((lo2(acc[2]) + hi2(acc[2])) + (lo2(acc[3]) + hi2(acc[3])));
-        else
-          v = acc1;
-        const int tok = ch * kTokW + tk;
-        if (tok < ntok && key < p.S) {
-          float* dst = out_b + (int64_t)(tl0 + tok) * p.ld + key;
-          if (key < nvis[tk]) {
-            if constexpr (FP8) v *= sq[tk] * sk;
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+          for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float x0 = fmaxf(__uint_as_float(r[a][4 * j + 2 * e]), 0.f);
+              const float x1 = fmaxf(__uint_as_float(r[a][4 * j + 2 * e + 1]), 0.f);
+              acc[2 * a + e] = fma2(pack2(x0, x1), wp[j], acc[2 * a + e]);
+            }
+        float v4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v4[i] = lo2(acc[i]) + hi2(acc[i]);
+        // reduce-scatter over the 4 threads of a key group: thread m ends with key index m
+        const bool hi1 = (m & 2) != 0, hi0 = (m & 1) != 0;
+        const float s0 = hi1 ? v4[0] : v4[2], s1 = hi1 ? v4[1] : v4[3];
+        const float k0 = hi1 ? v4[2] : v4[0], k1 = hi1 ? v4[3] : v4[1];
+        const float u0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 2);
+        const float u1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 2);
+        float v = (hi0 ? u1 : u0) + __shfl_xor_sync(0xffffffffu, hi0 ? u0 : u1, 1);
+        const int key = (kt_lo + kt) * kM + my_key;
+        if (ntok > ch && key < p.S) {
+          float* dst = out_b + (int64_t)(tl0 + ch) * p.ld + key;
+          if (key < nvis[0]) {
+            if constexpr (FP8) v *= sq[0] * sk;
             *dst = v;
           } else if (p.write_masked) {
             *dst = -INFINITY;
+          }
+        }
+      }
+    } else {
+    for (int kt = 0; kt < ktiles; ++kt) {
+        const int buf = kt & (kBufs - 1);
+        const float sk = sk_next;
+        sk_next = key_scale(kt + 1);
+        if (!mbar_wait(tm_full + buf, (kt / kBufs) & 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t col0 = t_lane + buf * kN + ch * C::kCols;
+        // all of this warp's accumulator columns in one go, then the buffer goes back to the MMA
+        uint32_t r[C::kCols / 32][32];
+#pragma unroll
+        for (int cb = 0; cb < C::kCols / 32; ++cb) tmem_ld32(col0 + cb * 32, r[cb]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tm_empty + buf);
+        const int key = (kt_lo + kt) * kM + key_in_tile;
+#pragma unroll
+        for (int tk = 0; tk < kTokW; ++tk) {
+          // four independent partial sums per token keep the FMA pipe fed
+          unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
+          float acc1 = 0.f;
+#pragma unroll
+          for (int c4 = 0; c4 < HI / 4; ++c4) {
+            const int c = tk * HI + c4 * 4;  // column within the warp
+            const float4 wv = *reinterpret_cast<const float4*>(w_warp + c);
+            const float x0 = fmaxf(__uint_as_float(r[c >> 5][c & 31]), 0.f);
+            const float x1 = fmaxf(__uint_as_float(r[(c + 1) >> 5][(c + 1) & 31]), 0.f);
+            const float x2 = fmaxf(__uint_as_float(r[(c + 2) >> 5][(c + 2) & 31]), 0.f);
+            const float x3 = fmaxf(__uint_as_float(r[(c + 3) >> 5][(c + 3) & 31]), 0.f);
+            if constexpr (HI >= 8) {
+              acc[(2 * c4) & 3] = fma2(pack2(wv.x, wv.y), pack2(x0, x1), acc[(2 * c4) & 3]);
+              acc[(2 * c4 + 1) & 3] = fma2(pack2(wv.z, wv.w), pack2(x2, x3), acc[(2 * c4 + 1) & 3]);
+            } else {
+              acc1 += wv.x * x0 + wv.y * x1 + wv.z * x2 + wv.w * x3;
+            }
+          }
+          float v;
+          if constexpr (HI >= 8)
+            v = ((lo2(acc[0]) + hi2(acc[0])) + (lo2(acc[1]) + hi2(acc[1]))) +
+                ((lo2(acc[2]) + hi2(acc[2])) + (lo2(acc[3]) + hi2(acc[3])));
+          else
+            v = acc1;
+          const int tok = ch * kTokW + tk;
+          if (tok < ntok && key < p.S) {
+            float* dst = out_b + (int64_t)(tl0 + tok) * p.ld + key;
+            if (key < nvis[tk]) {
+              if constexpr (FP8) v *= sq[tk] * sk;
+              *dst = v;
+            } else if (p.write_masked) {
+              *dst = -INFINITY;
+            }
           }
         }
       }
