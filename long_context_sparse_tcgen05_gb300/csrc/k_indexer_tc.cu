@@ -229,9 +229,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // one token per warp; thread t: keys kq + t/4 + {0, 8, 16, 24}, heads 8j + 2(t%4) + {0, 1}
       const int m = lane & 3, rq = lane >> 2;
       const int my_key = lq * 32 + (m >> 1) * 16 + (m & 1) * 8 + rq;  // the key this thread stores
+      // halved weights: w * ReLU(x) = (w / 2) * (x + |x|), both factors exact, so the product
+      // rounds exactly as w * max(x, 0) does (finite x); the add runs on the FMA pipe with a
+      // free |.| operand, where a max would take an ALU-pipe slot
       unsigned long long wp[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) wp[j] = pack2(w_warp[8 * j + 2 * m], w_warp[8 * j + 2 * m + 1]);
+      for (int j = 0; j < 8; ++j)
+        wp[j] = pack2(0.5f * w_warp[8 * j + 2 * m], 0.5f * w_warp[8 * j + 2 * m + 1]);
       auto key_scale16 = [&](int kt) -> float {
         const int key = (kt_lo + kt) * kM + my_key;
         return (FP8 && kt < ktiles && key < p.S) ? __ldg(skg + key) : 1.f;
@@ -259,9 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int a = 0; a < 2; ++a)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const float x0 = fmaxf(__uint_as_float(r[a][4 * j + 2 * e]), 0.f);
-              const float x1 = fmaxf(__uint_as_float(r[a][4 * j + 2 * e + 1]), 0.f);
-              acc[2 * a + e] = fma2(pack2(x0, x1), wp[j], acc[2 * a + e]);
+              const float y0 = __uint_as_float(r[a][4 * j + 2 * e]);
+              const float y1 = __uint_as_float(r[a][4 * j + 2 * e + 1]);
+              acc[2 * a + e] = fma2(pack2(y0 + fabsf(y0), y1 + fabsf(y1)), wp[j], acc[2 * a + e]);
             }
         float v4[4];
 #pragma unroll
