@@ -366,31 +366,56 @@ def run_ours(args, rank, world, local):
 
 
 def run_e2e(dsa, wl, layers, group, outs, lses, bufs, args, world):
-    """Same group forward through the public call, with every input copied in from pinned
-    host memory and every output copied back, inside the timed region."""
+    """The same F,S,S,S group through the public calls, with every input copied in from pinned
+    host memory and every output copied back inside the timed region.  The layers consume
+    their inputs in order, so the copies are pipelined against the compute: each layer's
+    inputs go in on a copy stream ahead of its attention call, each layer's output goes back
+    on a second copy stream as soon as it is written, and a step ends when its last output is
+    on the host.  The calls are the ones indexshare_group_forward makes (the F layer's top-k
+    from indexer operands, then one attention call per layer over its index buffer)."""
     ix = layers[0]["ix"]
-    dev_inputs = [ix["q"], ix["k"], ix["w"], ix["q_scale"], ix["k_scale"]] + \
-                 [t for g in group for t in (g["at"]["q"], g["at"]["k"])]
-    host_inputs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_inputs]
-    for h, d in zip(host_inputs, dev_inputs):
-        h.copy_(d)
-    dev_outputs = outs + lses
-    host_outputs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_outputs]
-    h2d = sum(t.numel() * t.element_size() for t in host_inputs)
-    d2h = sum(t.numel() * t.element_size() for t in host_outputs)
+    ix_dev = [ix["q"], ix["k"], ix["w"], ix["q_scale"], ix["k_scale"]]
+    at_dev = [[g["at"]["q"], g["at"]["k"]] for g in group]
+    pin = lambda ts: [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in ts]
+    ix_host = pin(ix_dev)
+    at_host = [pin(ts) for ts in at_dev]
+    out_dev = [[outs[l], lses[l]] for l in range(4)]
+    out_host = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ts] for ts in out_dev]
+    h2d = sum(t.numel() * t.element_size() for t in ix_host) + sum(t.numel() * t.element_size() for ts in at_host for t in ts)
+    d2h = sum(t.numel() * t.element_size() for ts in out_host for t in ts)
+    comp = torch.cuda.current_stream()
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
 
     def step():
-        for h, d in zip(host_inputs, dev_inputs):
-            d.copy_(h, non_blocking=True)
-        dsa.indexshare_group_forward(group, GROUP, wl.k, outs=outs, lses=lses, idx_bufs=bufs[:1])
-        for h, d in zip(host_outputs, dev_outputs):
-            h.copy_(d, non_blocking=True)
+        cin.wait_stream(comp)  # the previous step no longer reads the input buffers
+        ready = []
+        with torch.cuda.stream(cin):
+            for h, d in zip(ix_host, ix_dev):
+                d.copy_(h, non_blocking=True)
+            for l in range(4):
+                for h, d in zip(at_host[l], at_dev[l]):
+                    d.copy_(h, non_blocking=True)
+                ready.append(torch.cuda.Event())
+                ready[-1].record(cin)
+        comp.wait_event(ready[0])
+        dsa.dsa_topk(wl.k, ix=ix, idx=bufs[0])
+        for l in range(4):
+            comp.wait_event(ready[l])
+            dsa.dsa_sparse_attn(group[l]["at"], bufs[0], out=outs[l], lse=lses[l])
+            done = torch.cuda.Event()
+            done.record(comp)
+            cout.wait_event(done)
+            with torch.cuda.stream(cout):
+                for h, d in zip(out_host[l], out_dev[l]):
+                    h.copy_(d, non_blocking=True)
+        comp.wait_stream(cout)  # the step's outputs are on the host when it ends
 
     ms = time_loop(step, max(3, args.steps // 2), 1, world)
     ms = max_over_ranks(ms, world)
-    del host_inputs, host_outputs
+    del ix_host, at_host, out_host
     return {"value": round(wl.B * wl.T * world / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "overlap": "per-layer inputs in and outputs out on two copy streams, pipelined against compute"}
 
 
 # --- reference arm: the CPU oracle -------------------------------------------------------
