@@ -215,7 +215,8 @@ def dsa_topk(k: int, *, ix: dict | None = None, scores: torch.Tensor | None = No
         assert sc.stride(2) == 1 and sc.stride(0) == T * sc.stride(1)
         src = TopkSrc(TOPK_FROM_SCORES, sc.data_ptr(), sc.stride(1), None)
         dev = scores.device
-        need = WS_MIN
+        # few rows may be split across CTAs: room for up to 16 segment lists per row
+        need = WS_MIN + (B * T * 16 * (k * 8 + 4) if B * T < 256 else 0)
     if idx is None:
         idx = torch.empty((B, T, k), dtype=torch.int32, device=dev)
     if ws is None:

@@ -82,6 +82,27 @@ dsa_status check_attn(const dsa_attn_args* at) {
 
 constexpr int kMaxK = 4096;
 
+// Few long rows: split each across CTAs (dsa::topk_parts) when the workspace from byte `off` on
+// holds the segments' lists; otherwise one CTA per row.
+void plan_topk_parts(dsa::TopkLaunch& P, int64_t rows, int64_t n_max, void* ws, size_t off, size_t ws_bytes) {
+  P.parts = 1;
+  const int parts = dsa::topk_parts(rows, n_max);
+  if (parts <= 1) return;
+  const size_t per = (size_t)rows * parts;
+  const size_t need = per * ((size_t)P.k * 8 + 4);
+  if (off > ws_bytes || ws_bytes - off < need) return;
+  uint8_t* w = static_cast<uint8_t*>(ws) + off;
+  P.parts = parts;
+  P.part_pos = reinterpret_cast<int32_t*>(w);
+  P.part_key = reinterpret_cast<uint32_t*>(w + per * P.k * 4);
+  P.part_cnt = reinterpret_cast<int32_t*>(w + per * P.k * 8);
+}
+
+int64_t max_visible(int64_t q_pos0, int T, int diag, int S) {
+  const int64_t n = q_pos0 + T - 1 + diag;
+  return n < 0 ? 0 : (n > S ? S : n);
+}
+
 // Query rows per chunk of the materialised score buffer that `ws_bytes` can hold.
 int64_t score_chunk_rows(const dsa_indexer_args* ix, size_t ws_bytes) {
   if (ws_bytes <= dsa::kWsScratch) return 0;
@@ -111,6 +132,8 @@ dsa_status run_indexer_topk(const dsa_indexer_args* ix, int32_t k, int32_t* idx,
     P.scores = sc; P.ld = ix->S; P.bstride = (int64_t)Tc * ix->S;
     P.B = ix->B; P.T = ix->T; P.S = ix->S; P.t0 = (int)t0; P.Tc = Tc;
     P.q_pos0 = ix->q_pos0; P.diag = ix->diag; P.k = k; P.idx = idx; P.flags = ws_flags(ws);
+    plan_topk_parts(P, (int64_t)ix->B * Tc, max_visible(ix->q_pos0, ix->T, ix->diag, ix->S), ws,
+                    dsa::kWsScratch + (size_t)(chunk * ix->B * ix->S * 4), ws_bytes);
     e = dsa::launch_topk_rows(P, st);
     if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
   }
@@ -127,14 +150,18 @@ dsa_status record_error(dsa_status s, const char* msg) { return fail(s, "%s", ms
 extern "C" {
 
 size_t dsa_workspace_size(const dsa_indexer_args* ix, int32_t k) {
-  (void)k;
   if (!ix || ix->B <= 0 || ix->T <= 0 || ix->S <= 0) return DSA_WS_MIN;
   // Preferred score chunk: up to 4 GiB of fp32 scores, at least one row.
   const int64_t per_row = (int64_t)ix->B * ix->S * 4;
   int64_t rows = ((int64_t)4 << 30) / per_row;
   if (rows < 1) rows = 1;
   if (rows > ix->T) rows = ix->T;
-  return dsa::kWsScratch + (size_t)(rows * per_row);
+  size_t bytes = dsa::kWsScratch + (size_t)(rows * per_row);
+  // a chunk of few rows may have them split across CTAs: room for the segments' lists
+  const int64_t chunk_rows = rows * ix->B;
+  if (chunk_rows < 256 && k >= 1 && k <= kMaxK)
+    bytes += (size_t)chunk_rows * dsa::kMaxTopkParts * ((size_t)k * 8 + 4);
+  return bytes;
 }
 
 dsa_status dsa_indexer_scores(const dsa_indexer_args* ix, float* scores, int64_t ld, void* ws, size_t ws_bytes,
@@ -174,6 +201,7 @@ dsa_status dsa_topk(const dsa_topk_src* src, int32_t B, int32_t T, int32_t S, in
     P.scores = src->scores; P.ld = src->ld; P.bstride = (int64_t)T * src->ld;
     P.B = B; P.T = T; P.S = S; P.t0 = 0; P.Tc = T;
     P.q_pos0 = q_pos0; P.diag = diag; P.k = k; P.idx = idx; P.flags = ws_flags(ws);
+    plan_topk_parts(P, (int64_t)B * T, max_visible(q_pos0, T, diag, S), ws, dsa::kWsScratch, ws_bytes);
     cudaError_t e = dsa::launch_topk_rows(P, st);
     return e == cudaSuccess ? DSA_OK : cuda_fail(e, "top-k launch");
   }

@@ -75,8 +75,19 @@ struct TopkLaunch {
   int diag, k;
   int32_t* idx;
   uint32_t* flags;
+  // few long rows: each row split into `parts` segments (> 1), one CTA each; segment s of row
+  // r = b*Tc + tl writes its exact top-k, sorted by position, with the keys, to
+  // part_pos / part_key[(r*parts + s)*k ..] and its length to part_cnt[r*parts + s]; a merge
+  // kernel then writes idx
+  int parts;
+  int32_t* part_pos;
+  uint32_t* part_key;
+  int32_t* part_cnt;
 };
 cudaError_t launch_topk_rows(const TopkLaunch& p, cudaStream_t st);
+constexpr int kMaxTopkParts = 16;
+// Segments per row for `rows` rows of up to `n` visible scores (1: no split).
+int topk_parts(int64_t rows, int64_t n);
 
 struct AttnLaunch {
   int B, T, S, H, DQK, DV;

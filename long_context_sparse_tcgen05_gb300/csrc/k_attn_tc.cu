@@ -82,14 +82,6 @@ struct Small {
 
 constexpr size_t kSmem = 1024 + kQBytes + kStages * kKVBytes + sizeof(Small);
 
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int r0, int r1,
-                                            int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_addr(bar))
-      : "memory");
-}
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
                : "memory");
@@ -112,28 +104,17 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
-// Operand descriptors besides the K-major 128-byte-swizzled form of desc_sw128:
-// MN-major 128-byte swizzled (64-element MN atoms `lbo` bytes apart, 8-row K groups 1024 B
-// apart), and K-major without swizzle (8-row x 16-byte core matrices: `lbo` bytes apart
-// along K, `sbo` bytes apart along M/N).
+// MN-major 128-byte-swizzled operand descriptor: 64-element MN atoms `lbo` bytes apart, 8-row
+// K groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t lbo) {
   uint64_t d = desc_sw128(saddr);
   d &= ~((uint64_t)0x3FFF << 16);
   d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
   return d;
 }
-__device__ __forceinline__ uint64_t desc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
-  d |= (uint64_t)1 << 46;
-  return d;
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
-    k_sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-                    AttnLaunch p) {
+    k_sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, AttnLaunch p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = base;
@@ -176,10 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kProdWarps) {
     // ================= producers: row info, Q tile, KV gathers (cp.async), L2 prefetch ==========
-    // Each of the four warps copies 8 of a block's 32 rows: lane l moves 16-byte chunks
-    // l, l+32, l+64 of a 1152-byte row into the 128-byte-swizzled K-major layout the MMAs
-    // read.  Every copying thread then arms an asynchronous arrive on the stage's kv_full
-    // barrier that fires once its own copies have landed, so the producer never waits for
+    // Each of the four warps copies 16 of a block's 64 rows, atom by atom (8 lanes per row,
+    // one 16-byte chunk each), into the 128-byte-swizzled K-major layout the MMAs read.  After
+    // each atom every copying thread arms an asynchronous arrive on that atom's kv_full
+    // barrier, which fires once its own copies have landed, so the producer never waits for
     // its copies and all stages stay in flight.
     const uint8_t* kvg = static_cast<const uint8_t*>(p.k);
     const int64_t row_bytes = p.k_ld * 2;
@@ -571,7 +552,7 @@ cudaError_t launch_sparse_mla_tc(const AttnLaunch& p, cudaStream_t st) {
   TraceScope trace(kTraceAttention, st);
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  CUtensorMap tq, tkv;
+  CUtensorMap tq;
   {
     cuuint64_t dims[3] = {(cuuint64_t)kDQK, (cuuint64_t)kH, (cuuint64_t)p.B * p.T};
     cuuint64_t strides[2] = {(cuuint64_t)kDQK * 2, (cuuint64_t)kDQK * 2 * kH};
@@ -582,21 +563,11 @@ cudaError_t launch_sparse_mla_tc(const AttnLaunch& p, cudaStream_t st) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)kDQK, (cuuint64_t)p.B * p.S};
-    cuuint64_t strides[1] = {(cuuint64_t)p.k_ld * 2};
-    cuuint32_t box[2] = {64, 1};
-    cuuint32_t es[2] = {1, 1};
-    if (enc(&tkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.k), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
   cudaError_t e = cudaFuncSetAttribute(k_sparse_mla_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (e != cudaSuccess) return e;
   const int rows = p.B * p.T;
   const int grid = rows < num_sms() ? rows : num_sms();
-  k_sparse_mla_tc<<<grid, kThreads, kSmem, st>>>(tq, tkv, p);
+  k_sparse_mla_tc<<<grid, kThreads, kSmem, st>>>(tq, p);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -176,23 +176,12 @@ __device__ uint32_t compact_top(Sm& sm, uint32_t count, int k) {
   return tau;
 }
 
-__device__ __forceinline__ void load8(const float* x, int64_t q, int64_t n, bool vec, float v[kPer]) {
-  if (vec && q + kPer <= n) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(x + q));
-    const float4 b = __ldg(reinterpret_cast<const float4*>(x + q + 4));
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  } else {
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) v[j] = (q + j < n) ? __ldg(x + q + j) : 0.f;
-  }
-}
-
 // Stable ordered compaction: writes out[0..k) with the positions of the entries whose key is
 // > tau, plus the first `ties` entries whose key == tau, in stream order.  get(i) gives
 // (key, position) of entry i < n.
 template <class Sm, class Get>
-__device__ void ordered_output(Sm& sm, int64_t n, uint32_t tau, uint32_t ties, int k, int32_t* out, Get get) {
+__device__ void ordered_output(Sm& sm, int64_t n, uint32_t tau, uint32_t ties, int k, int32_t* out, Get get,
+                               int32_t pos_off = 0, uint32_t* kout = nullptr) {
   uint32_t out_base = 0, eq_seen = 0;
 #pragma unroll 1
   for (int64_t base = 0; base < n; base += (int64_t)kThreads * kPer) {
@@ -219,9 +208,13 @@ __device__ void ordered_output(Sm& sm, int64_t n, uint32_t tau, uint32_t ties, i
     for (int j = 0; j < kPer; ++j) {
       if (ps[j] < 0) continue;
       if (key[j] > tau) {
-        out[o++] = ps[j];
+        if (kout) kout[o] = key[j];
+        out[o++] = ps[j] + pos_off;
       } else if (key[j] == tau) {
-        if (eq_idx < ties) out[o++] = ps[j];
+        if (eq_idx < ties) {
+          if (kout) kout[o] = key[j];
+          out[o++] = ps[j] + pos_off;
+        }
         ++eq_idx;
       }
     }
@@ -257,16 +250,38 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
   __shared__ int s_nan;
-  const int row = blockIdx.x;
+  const int parts = p.parts > 1 ? p.parts : 1;
+  const int row = (int)(blockIdx.x / parts), part = (int)(blockIdx.x % parts);
   const int b = row / p.Tc, tl = row % p.Tc, t = p.t0 + tl;
   const float* x = p.scores + (int64_t)b * p.bstride + (int64_t)tl * p.ld;
   int32_t* out = p.idx + ((int64_t)b * p.T + t) * p.k;
   int64_t n = p.q_pos0 + t + p.diag;
   n = n < 0 ? 0 : (n > p.S ? p.S : n);
   const int k = p.k;
+  // a split row: this CTA's segment [seg0, seg0 + n), whole 4,096-score pieces but the last
+  int32_t seg0 = 0;
+  uint32_t* kout = nullptr;
+  if (parts > 1) {
+    const int64_t seg_len = ((n + parts - 1) / parts + 4095) / 4096 * 4096;
+    const int64_t s0 = (int64_t)part * seg_len, s1 = s0 + seg_len < n ? s0 + seg_len : n;
+    seg0 = (int32_t)s0;
+    n = s1 > s0 ? s1 - s0 : 0;
+    x += s0;
+    const int64_t slot = (int64_t)row * parts + part;
+    out = p.part_pos + slot * k;
+    kout = p.part_key + slot * k;
+    if (threadIdx.x == 0) p.part_cnt[slot] = (int32_t)(n < k ? n : k);
+  }
 
   if (n <= k) {
-    for (int j = threadIdx.x; j < k; j += kThreads) out[j] = j < n ? j : -1;
+    for (int j = threadIdx.x; j < k; j += kThreads) {
+      out[j] = j < n ? seg0 + j : -1;
+      if (kout && j < n) {
+        const float v = __ldg(x + j);
+        if (isnan(v)) atomicOr(p.flags, DSA_FLAG_NAN_SCORE);
+        kout[j] = score_key(v);
+      }
+    }
     return;
   }
   const bool vec = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
@@ -446,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
     ordered_output(sm, c, tau, ties, k, out, [&](int64_t i, uint32_t& key, int32_t& ps) {
       key = sm.key[i];
       ps = sm.pos[i];
-    });
+    }, seg0, kout);
   } else {
     // the sample misjudged the threshold: three histogram passes over the row in global memory
     auto gkey = [&](int64_t i) { return score_key(__ldg(x + i)); };
@@ -455,8 +470,55 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
     ordered_output(sm, n, tau, ties, k, out, [&](int64_t i, uint32_t& key, int32_t& ps) {
       key = gkey(i);
       ps = (int32_t)i;
-    });
+    }, seg0, kout);
   }
+}
+
+struct MergeSmem {
+  uint32_t hist[kBins];
+  uint32_t warp_sums[kWarps];
+  uint32_t sel_bin, sel_above;
+  int32_t pre[kMaxTopkParts + 1];  // start of each segment's list in the concatenation
+};
+
+// One split row: the exact top-k of its segments' lists, concatenated in segment order (so in
+// position order).
+__global__ void __launch_bounds__(kThreads) k_topk_merge(TopkLaunch p) {
+  __shared__ MergeSmem sm;
+  const int row = blockIdx.x, parts = p.parts, k = p.k;
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int s = 0; s < parts; ++s) {
+      sm.pre[s] = acc;
+      acc += p.part_cnt[(int64_t)row * parts + s];
+    }
+    sm.pre[parts] = acc;
+  }
+  __syncthreads();
+  const int64_t n = sm.pre[parts];
+  const int b = row / p.Tc, tl = row % p.Tc;
+  int32_t* out = p.idx + ((int64_t)b * p.T + p.t0 + tl) * k;
+  const int64_t base = (int64_t)row * parts * k;
+  auto locate = [&](int64_t i) -> int64_t {  // entry i of the concatenation -> list offset
+    int lo = 0, hi = parts;                  // largest s with pre[s] <= i
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sm.pre[mid] <= i) lo = mid; else hi = mid;
+    }
+    return base + (int64_t)lo * k + (i - sm.pre[lo]);
+  };
+  if (n <= k) {
+    for (int j = threadIdx.x; j < k; j += kThreads) out[j] = j < n ? p.part_pos[locate(j)] : -1;
+    return;
+  }
+  uint32_t ties;
+  const uint32_t tau =
+      radix_select(sm, n, (uint32_t)k, [&](int64_t i) { return p.part_key[locate(i)]; }, &ties, 0u, 32, 0);
+  ordered_output(sm, n, tau, ties, k, out, [&](int64_t i, uint32_t& key, int32_t& ps) {
+    const int64_t o = locate(i);
+    key = p.part_key[o];
+    ps = p.part_pos[o];
+  });
 }
 
 template <int Cap, int Ring, int Per>
@@ -466,20 +528,38 @@ cudaError_t launch_rows(const TopkLaunch& p, int rows, cudaStream_t st) {
   cudaError_t e =
       cudaFuncSetAttribute(k_topk_rows<Cap, Ring, Per>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k_topk_rows<Cap, Ring, Per><<<rows, kThreads, smem, st>>>(p);
+  k_topk_rows<Cap, Ring, Per><<<rows * (p.parts > 1 ? p.parts : 1), kThreads, smem, st>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+int topk_parts(int64_t rows, int64_t n) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (rows <= 0 || rows >= sms) return 1;
+  int64_t parts = (2LL * sms) / rows;        // about two CTAs per SM
+  const int64_t by_len = n / 32768;           // segments of at least 32K scores
+  if (parts > by_len) parts = by_len;
+  if (parts > kMaxTopkParts) parts = kMaxTopkParts;
+  return parts < 2 ? 1 : (int)parts;
+}
+
 cudaError_t launch_topk_rows(const TopkLaunch& p, cudaStream_t st) {
   const int rows = p.B * p.Tc;
   if (rows <= 0) return cudaSuccess;
+  if (p.parts > kMaxTopkParts || (p.parts > 1 && !(p.part_pos && p.part_key && p.part_cnt)))
+    return cudaErrorInvalidValue;
   // about 1.25k + 16 n / Cap candidates are expected: 4096 slots hold them for k <= 2560
-  const cudaError_t e =
+  cudaError_t e =
       p.k <= 2560 ? launch_rows<4096, 2, 16>(p, rows, st) : launch_rows<8192, 2, 8>(p, rows, st);
   count_launches(1);
-  return e;
+  if (e != cudaSuccess || p.parts <= 1) return e;
+  TraceScope trace(kTraceTopk, st);
+  k_topk_merge<<<rows, kThreads, 0, st>>>(p);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 }  // namespace dsa
