@@ -124,8 +124,12 @@ typedef struct {
 } dsa_layer;
 
 /* Workspace bytes preferred by dsa_topk(FROM_INDEXER) and indexshare_group_forward for
- * this indexer shape (a smaller workspace also works down to DSA_WS_MIN plus one score row
- * chunk; calls that need no scratch take DSA_WS_MIN). */
+ * this indexer shape: a chunk of fp32 score rows (up to 4 GiB) and, when the chunk has fewer
+ * than 256 query rows, room for splitting each row's top-k across CTAs (16 lists of k
+ * positions and keys per row).  A smaller workspace also works, down to DSA_WS_MIN plus one
+ * score row chunk; without the split room the top-k runs one CTA per row.  dsa_topk over a
+ * score buffer uses, beyond DSA_WS_MIN, the same split room when given it.  Calls that need
+ * no scratch take DSA_WS_MIN. */
 #define DSA_WS_MIN ((size_t)256)
 size_t dsa_workspace_size(const dsa_indexer_args* ix, int32_t k);
 

@@ -4,20 +4,25 @@
 // One 512-thread CTA owns one row (two CTAs per SM).  Scores are compared through their
 // order-preserving 32-bit keys.
 //   * Rows with at most Cap visible scores are copied to shared memory whole.
-//   * Longer rows: a sample of at most Cap keys (whole 8-key groups, evenly strided) gives,
-//     by an exact radix select in shared memory, a threshold theta that about 1.25k of the
-//     row's keys exceed; one streaming pass then appends every key >= theta, in position
-//     order (block-wide prefix sums of per-thread counts), to shared memory.  Every key below
-//     theta has at least k larger keys, so the row's top-k lies among the candidates.  The
-//     pass reads the row through a ring of bulk copies (cp.async.bulk into shared memory,
-//     completion on an mbarrier) of Per scores per thread each, and is bound by its
-//     per-score instruction count: one block-wide scan per Per x 512 scores, 32-bit indices,
-//     no per-score bounds checks on whole chunks, the NaN flag kept in a register.
-//   * An exact radix select (11/11/10-bit histograms) among the candidates finds the k-th key;
-//     a stable compaction writes the selected positions in order.
-// If the sample misjudges the threshold (fewer than k candidates, or more than fit), the CTA
-// falls back to three histogram passes over the row in global memory and a final ordered
-// compaction pass.  Either way DRAM sees about one read of the row.
+//   * Longer rows: a sample of at most Cap keys (whole 8-key groups, evenly strided) gives, by
+//     two 11-bit radix passes in shared memory, a threshold theta that about 1.5k of the row's
+//     keys exceed; one streaming pass then appends every key >= theta, in position order
+//     (block-wide prefix sums of per-thread counts), to shared memory.  Every key below theta
+//     has at least k larger keys, so the row's top-k lies among the candidates.  The pass
+//     reads the row through a ring of bulk copies (cp.async.bulk into shared memory,
+//     completion on an mbarrier) of Per scores per thread each, and is bound by its per-score
+//     instruction count: one block-wide scan per Per x 512 scores, 32-bit indices, no
+//     per-score bounds checks on whole chunks, the NaN flag kept in a register.  A buffer
+//     about to overflow is compacted in place to its exact top-k and theta raised to the k-th
+//     key (a later equal key loses the tie).
+//   * An exact radix select among the candidates, starting at the first bit where theta and
+//     the largest candidate differ, finds the k-th key; a stable compaction writes the
+//     selected positions in order.
+//   * Fewer rows than SMs (decode): each row is split into segments of at least 32K scores,
+//     one CTA each; a segment writes its exact top-k with the keys, sorted by position, and
+//     k_topk_merge selects the row's top-k from the concatenated lists.
+// If the sample overestimates the threshold (fewer than k candidates), the CTA falls back to
+// histogram passes over the row in global memory and a final ordered compaction pass.
 #include "dsa_internal.cuh"
 
 namespace dsa {

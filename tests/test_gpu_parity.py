@@ -118,6 +118,24 @@ def test_topk_nan_scores_rank_lowest_and_raise_flag():
     assert np.array_equal(idx[0].cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("n,k,nan_every", [(300000, 2048, 0), (300000, 2048, 997), (250000, 1, 0),
+                                            (140000, 3000, 0)])
+def test_topk_few_long_rows_split_across_ctas(n, k, nan_every):
+    # fewer rows than SMs: every row is split into segments, one CTA each, merged per row
+    R = 5
+    sc = synth.scores_input(R, n, DEV, "normal", seed=11)
+    if nan_every:
+        sc[:, ::nan_every] = float("nan")
+    dsa.read_device_flags()
+    for q_pos0, diag in ((n - R, 1), (n // 2, 0)):
+        idx = dsa.dsa_topk(k, scores=sc[None], q_pos0=q_pos0, diag=diag)
+        nv = np.clip(np.arange(R) + q_pos0 + diag, 0, n)
+        ref = oracle.topk_rows(sc.double().cpu().numpy(), nv, k)
+        assert np.array_equal(idx[0].cpu().numpy(), ref), (n, k, q_pos0, diag)
+    flags = dsa.read_device_flags()
+    assert bool(flags & dsa.FLAG_NAN_SCORE) == bool(nan_every) and not flags & ~dsa.FLAG_NAN_SCORE
+
+
 # --- indexer scores ----------------------------------------------------------------------
 
 CASES_INT = [(4, 64, "bf16"), (64, 128, "bf16"), (64, 128, "e4m3")]
