@@ -239,7 +239,9 @@ def dsa_sparse_attn(at: dict, idx: torch.Tensor, out: torch.Tensor | None = None
         lse = torch.empty((a.B, a.T, a.H), dtype=torch.float32, device=dev)
     elif lse is False:
         lse = None
-    ws = workspace(WS_MIN, dev)
+    # few rows may be split over CTAs (up to 8 parts per row, fp32 outputs + LSE)
+    rows = a.B * a.T
+    ws = workspace(WS_MIN + (rows * 8 * a.H * (a.d_v + 1) * 4 if rows < 128 else 0), dev)
     _check(lib.dsa_sparse_attn(_c.byref(a), _ptr(idx), idx.shape[-1], _ptr(out), _ptr(lse),
                                _ptr(ws), ws.numel(), _stream()))
     return out, lse

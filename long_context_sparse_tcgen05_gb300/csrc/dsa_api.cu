@@ -225,6 +225,18 @@ dsa_status dsa_sparse_attn(const dsa_attn_args* at, const int32_t* idx, int32_t 
   L.B = at->B; L.T = at->T; L.S = at->S; L.H = at->H; L.DQK = at->d_qk; L.DV = at->d_v; L.scale = at->scale;
   L.q = at->q; L.k = at->k; L.k_ld = at->k_ld; L.v = at->v; L.v_ld = at->v_ld;
   L.idx = idx; L.kk = k; L.out = out; L.lse = lse; L.flags = ws_flags(ws);
+  // few rows: split each row's blocks over CTAs when the workspace holds the parts
+  const int splits = dsa::attn_splits(L);
+  if (splits > 1) {
+    const size_t parts = (size_t)at->B * at->T * splits;
+    const size_t need = parts * (size_t)at->H * ((size_t)at->d_v + 1) * 4;
+    if (ws_bytes > dsa::kWsScratch && ws_bytes - dsa::kWsScratch >= need) {
+      uint8_t* w = static_cast<uint8_t*>(ws) + dsa::kWsScratch;
+      L.splits = splits;
+      L.part_o = reinterpret_cast<float*>(w);
+      L.part_lse = reinterpret_cast<float*>(w + parts * (size_t)at->H * at->d_v * 4);
+    }
+  }
   cudaError_t e = dsa::launch_sparse_attn(L, as_stream(stream));
   return e == cudaSuccess ? DSA_OK : cuda_fail(e, "attention launch");
 }

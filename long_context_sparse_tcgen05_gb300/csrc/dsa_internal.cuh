@@ -102,8 +102,17 @@ struct AttnLaunch {
   void* out;
   float* lse;
   uint32_t* flags;
+  // few rows (decode): each row's selected blocks split into `splits` (> 1) parts, one CTA
+  // each; part s of row r writes its output normalised by its own row sums, fp32,
+  // part_o[((r*splits + s)*H + h)*DV ..], and its LSE part_lse[(r*splits + s)*H + h]; a
+  // combine kernel merges them into out / lse
+  int splits;
+  float* part_o;
+  float* part_lse;
 };
 cudaError_t launch_sparse_attn(const AttnLaunch& p, cudaStream_t st);
+constexpr int kMaxAttnSplits = 8;
+int attn_splits(const AttnLaunch& p);  // parts per row the 64-head MLA kernel would use (1: none)
 // tcgen05 sparse MLA kernel for the latent shape (H = 64, d_qk = 576, d_v = 512, v = k)
 bool sparse_mla_tc_supported(const AttnLaunch& p);
 cudaError_t launch_sparse_mla_tc(const AttnLaunch& p, cudaStream_t st);

@@ -20,6 +20,9 @@
 //     into the block's rope columns, free once S is done).  The running maximum is raised only
 //     when a block exceeds it by more than 2^8; then O^T is rescaled in TMEM.  At the end
 //     they normalise O, write bf16 O and the natural-log LSE.
+// With fewer rows than SMs (decode) a row's blocks are split over several CTAs: each writes
+// its part normalised by its own row sums, in fp32, with its LSE, and k_attn_combine merges
+// the parts (weights exp(LSE_part - LSE_row)).
 // Entries of -1 are skipped (masked), out-of-range entries raise DSA_FLAG_BAD_INDEX and are
 // skipped.  Every wait is bounded (DSA_FLAG_TIMEOUT); TMEM is freed on every exit path.
 #include <cuda_bf16.h>
@@ -72,7 +75,8 @@ struct Small {
   Bars bar;
   uint32_t tmem;
   int abort;
-  int nb[2];                       // blocks of the row in flight (by row parity)
+  int nb[2];                       // blocks of the work item in flight (by item parity)
+  int j0[2];                       // its first block within the row
   float alpha[kH];
   float lsum[kH];
   float bmax[2][2][kH];           // [block parity][key half][head]: block maxima of the two halves
@@ -125,6 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows = p.B * p.T;
+  const int splits = p.splits > 1 ? p.splits : 1;  // work item = (row, part of its blocks)
+  const int items = rows * splits;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar.q_full, 1);
@@ -169,7 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long g = 0;  // global block counter
     bool ok = true;
     const bool vec = (p.kk & 3) == 0;
-    for (int row = blockIdx.x; ok && row < rows; row += gridDim.x, ++it) {
+    for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
+      const int row = item / splits;
       const int32_t* irow = p.idx + (int64_t)row * p.kk;
       const int b = row / p.T;
       const int64_t kvrow0 = (int64_t)b * p.S;
@@ -199,20 +206,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-      const int nb = (last + kNB) / kNB;
+      const int nbr = (last + kNB) / kNB;  // blocks of the row
+      const int split = item % splits;
+      const int j0 = split * nbr / splits, nb = (split + 1) * nbr / splits - j0;  // this item's blocks
       if (warp == 0) {
         if (lane == 0) ok = mbar_wait(&bar.info_empty[it & 1], ((it >> 1) & 1) ^ 1, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (ok && lane == 0) {
           sm->nb[it & 1] = nb;
+          sm->j0[it & 1] = j0;
           mbar_arrive(&bar.info_full[it & 1]);
         }
       }
       if (!ok || *abort_flag) break;
       if (nb == 0) continue;
       if (warp == 0) {
-        if (lane == 0 && row + (int)gridDim.x < rows)
-          prefetch_l2(static_cast<const __nv_bfloat16*>(p.q) + (int64_t)(row + gridDim.x) * kH * kDQK, kQBytes);
+        const int next_row = (item + (int)gridDim.x) / splits;
+        if (lane == 0 && next_row < rows && next_row != row)
+          prefetch_l2(static_cast<const __nv_bfloat16*>(p.q) + (int64_t)next_row * kH * kDQK, kQBytes);
         if (lane == 0) {
           ok = mbar_wait(&bar.q_empty, (qc & 1) ^ 1, abort_flag);
           if (ok) {
@@ -228,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ids of this warp's 16 rows
         constexpr int kRowsW = kNB / kProdWarps;
         const int rl = warp * kRowsW + (lane & (kRowsW - 1));
-        const int e = j * kNB + rl;
+        const int e = (j0 + j) * kNB + rl;
         int id = e < p.kk ? __ldg(irow + e) : -1;
         const bool valid = id >= 0 && id < p.S;
         if (lane < kRowsW && !valid && id != -1) atomicOr(p.flags, DSA_FLAG_BAD_INDEX);
@@ -271,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0, qc = 0;
     long long g = 0;
     bool ok = true;
-    for (int row = blockIdx.x; ok && row < rows; row += gridDim.x, ++it) {
+    for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
       int nb = 0;
       if (lane == 0) {
         ok = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag);
@@ -323,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0, oc = 0;
     long long g = 0;
     bool ok = true;
-    for (int row = blockIdx.x; ok && row < rows; row += gridDim.x, ++it) {
+    for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
       int nb = 0;
       if (lane == 0) {
         ok = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag);
@@ -375,16 +386,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0, oc = 0;
     long long g = 0;
     bool ok = true;
-    for (int row = blockIdx.x; ok && row < rows; row += gridDim.x, ++it) {
+    for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
+      const int row = item / splits;
       if (!(ok = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag))) break;
-      const int nb = sm->nb[it & 1];
+      const int nb = sm->nb[it & 1], j0 = sm->j0[it & 1];
       named_sync(1, kSmThreads);
       if (t == 0) mbar_arrive(&bar.info_empty[it & 1]);
       __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * kH * kDV;
+      float* po = splits > 1 ? p.part_o + (int64_t)item * kH * kDV : nullptr;  // this part's output
       const int32_t* irow = p.idx + (int64_t)row * p.kk;
       if (nb == 0) {  // nothing visible: O = 0, LSE = -inf
-        for (int i = t; i < kH * kDV / 8; i += kSmThreads) reinterpret_cast<uint4*>(og)[i] = make_uint4(0, 0, 0, 0);
-        if (p.lse && t < kH) p.lse[(int64_t)row * kH + t] = -INFINITY;
+        if (po) {
+          for (int i = t; i < kH * kDV / 4; i += kSmThreads) reinterpret_cast<float4*>(po)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (t < kH) p.part_lse[(int64_t)item * kH + t] = -INFINITY;
+        } else {
+          for (int i = t; i < kH * kDV / 8; i += kSmThreads) reinterpret_cast<uint4*>(og)[i] = make_uint4(0, 0, 0, 0);
+          if (p.lse && t < kH) p.lse[(int64_t)row * kH + t] = -INFINITY;
+        }
         continue;
       }
       float m_used = -INFINITY, l = 0.f;
@@ -399,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.s_empty[sb]);
         // scores in base-2 units, masked by the validity of each key slot (lane c checks key c)
-        const int e = j * kNB + kh * 32 + lane;
+        const int e = (j0 + j) * kNB + kh * 32 + lane;
         const int id = e < p.kk ? __ldg(irow + e) : -1;
         const uint32_t vm = __ballot_sync(0xffffffffu, id >= 0 && id < p.S);
         float s[32];
@@ -477,7 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (head_lane && kh == 0) {
         const float lt = sm->lpart[0][h] + sm->lpart[1][h];
         sm->lsum[h] = lt > 0.f ? 1.f / lt : 0.f;  // reciprocal row sums
-        if (p.lse) p.lse[(int64_t)row * kH + h] = lt > 0.f ? (m_used + log2f(lt)) * kLn2 : -INFINITY;
+        const float lse_v = lt > 0.f ? (m_used + log2f(lt)) * kLn2 : -INFINITY;
+        if (po) p.part_lse[(int64_t)item * kH + h] = lse_v;
+        else if (p.lse) p.lse[(int64_t)row * kH + h] = lse_v;
       }
       if (!(ok = mbar_wait(&bar.o_full, oc & 1, abort_flag))) break;
       named_sync(1, kSmThreads);
@@ -490,10 +510,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t r[32];
           tmem_ld32(tmem + lane_base + kColO + c * kH + half * 32, r);
           tmem_wait_ld();
+          if (po) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int hh = half * 32 + i;
-            og[(int64_t)hh * kDV + d] = __float2bfloat16_rn(__uint_as_float(r[i]) * sm->lsum[hh]);
+            for (int i = 0; i < 32; ++i) {
+              const int hh = half * 32 + i;
+              po[(int64_t)hh * kDV + d] = __uint_as_float(r[i]) * sm->lsum[hh];
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int hh = half * 32 + i;
+              og[(int64_t)hh * kDV + d] = __float2bfloat16_rn(__uint_as_float(r[i]) * sm->lsum[hh]);
+            }
           }
         }
       }
@@ -511,6 +539,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
   if (threadIdx.x == 0 && *abort_flag) atomicOr(p.flags, DSA_FLAG_TIMEOUT);
+}
+
+// Merge of a split row's parts: O = sum_s w_s O_s, w_s = exp(LSE_s - LSE), LSE = log sum_s exp(LSE_s).
+__global__ void __launch_bounds__(256) k_attn_combine(AttnLaunch p) {
+  __shared__ float wgt[kMaxAttnSplits][kH];
+  const int row = blockIdx.x, S = p.splits;
+  const float* pl = p.part_lse + (int64_t)row * S * kH;
+  if (threadIdx.x < kH) {
+    const int h = threadIdx.x;
+    float mx = -INFINITY;
+    for (int s = 0; s < S; ++s) mx = fmaxf(mx, pl[s * kH + h]);
+    float sum = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const float w = mx == -INFINITY ? 0.f : expf(pl[s * kH + h] - mx);
+      wgt[s][h] = w;
+      sum += w;
+    }
+    for (int s = 0; s < S; ++s) wgt[s][h] = sum > 0.f ? wgt[s][h] / sum : 0.f;
+    if (p.lse) p.lse[(int64_t)row * kH + h] = sum > 0.f ? mx + logf(sum) : -INFINITY;
+  }
+  __syncthreads();
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + (int64_t)row * S * kH * kDV);
+  __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * kH * kDV;
+  for (int i = threadIdx.x; i < kH * kDV / 4; i += 256) {
+    const int h = (i * 4) / kDV;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < S; ++s) {
+      const float4 v = po[(int64_t)s * kH * kDV / 4 + i];
+      const float w = wgt[s][h];
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
+    }
+    __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y), b = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    reinterpret_cast<uint2*>(og)[i] = u;
+  }
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -549,6 +617,7 @@ bool sparse_mla_tc_supported(const AttnLaunch& p) {
 }
 
 cudaError_t launch_sparse_mla_tc(const AttnLaunch& p, cudaStream_t st) {
+  if (p.splits > kMaxAttnSplits || (p.splits > 1 && !(p.part_o && p.part_lse))) return cudaErrorInvalidValue;
   TraceScope trace(kTraceAttention, st);
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
@@ -566,10 +635,25 @@ cudaError_t launch_sparse_mla_tc(const AttnLaunch& p, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(k_sparse_mla_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (e != cudaSuccess) return e;
   const int rows = p.B * p.T;
-  const int grid = rows < num_sms() ? rows : num_sms();
+  const int items = rows * (p.splits > 1 ? p.splits : 1);
+  const int grid = items < num_sms() ? items : num_sms();
   k_sparse_mla_tc<<<grid, kThreads, kSmem, st>>>(tq, p);
   count_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess || p.splits <= 1) return e;
+  k_attn_combine<<<rows, 256, 0, st>>>(p);
+  count_launches(1);
   return cudaGetLastError();
+}
+
+int attn_splits(const AttnLaunch& p) {
+  if (!sparse_mla_tc_supported(p)) return 1;
+  const int rows = p.B * p.T, sms = num_sms();
+  if (rows <= 0 || rows * 2 > sms) return 1;
+  int s = sms / rows;                                       // about one CTA per SM
+  const int by_len = (p.kk + 4 * kNB - 1) / (4 * kNB);      // parts of at least 4 blocks
+  if (s > by_len) s = by_len;
+  if (s > kMaxAttnSplits) s = kMaxAttnSplits;
+  return s < 2 ? 1 : s;
 }
 
 }  // namespace dsa
