@@ -43,6 +43,7 @@ struct TopkSmem {
   int32_t pos[Cap];
   uint32_t hist[kBins];
   uint32_t warp_sums[kWarps];
+  uint32_t stream_sums[2][kWarps];  // per-warp totals of the streaming pass, by chunk parity
   uint32_t sel_bin, sel_above;
   uint64_t full[Ring];
   int abort;
@@ -74,6 +75,30 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* warp_s
   *total = warp_sums[kWarps - 1];
   __syncthreads();
   return base + x - v;
+}
+
+// The same prefix sum with a single barrier: after it every warp scans the kWarps warp totals
+// itself. Consecutive calls must alternate between two sums arrays, so that a warp writing the
+// next call's totals cannot overwrite ones that a slower warp has still to read.
+__device__ __forceinline__ uint32_t block_excl_scan1(uint32_t v, uint32_t* sums, uint32_t* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sums[wid] = x;
+  __syncthreads();
+  uint32_t s = lane < kWarps ? sums[lane] : 0u;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
+    if (lane >= o) s += y;
+  }
+  *total = __shfl_sync(0xffffffffu, s, kWarps - 1);
+  const uint32_t before = __shfl_sync(0xffffffffu, s, wid > 0 ? wid - 1 : 0);
+  return (wid > 0 ? before : 0u) + x - v;
 }
 
 // The bin b (counting from the top) with above(b) < need <= above(b) + hist[b], among the
@@ -252,6 +277,7 @@ template <int Cap, int Ring, int Per>
 __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
   using Sm = TopkSmem<Cap, Ring, Per>;
   constexpr int kChunk = kThreads * Per;
+  static_assert(kChunk < (1 << 16), "a chunk's candidate count must stay below the timeout flag");
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
   __shared__ int s_nan;
@@ -364,8 +390,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
 #pragma unroll 1
     for (int64_t ci = 0; ci < nchunks; ++ci) {
       const int s = (int)(ci % Ring);
-      // a timed-out copy ends the pass for the whole block at once
-      if (__syncthreads_or(!ring_wait(&sm.full[s], (uint32_t)((ci / Ring) & 1), &sm.abort))) break;
+      // a thread whose copy wait timed out adds 2^16 to the block sum below (a chunk holds at
+      // most 8,192 candidates), and the whole block leaves the pass after that sum
+      const bool landed = ring_wait(&sm.full[s], (uint32_t)((ci / Ring) & 1), &sm.abort);
       const int base = (int)ci * kChunk, blen = (int)bulk_len(ci);
       const int q = base + (int)threadIdx.x * Per;
       const float* slot = &sm.ring[s][threadIdx.x * Per];
@@ -394,7 +421,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
         }
       }
       uint32_t tot;
-      uint32_t o = count + block_excl_scan(cnt, sm.warp_sums, &tot);
+      uint32_t o = count + block_excl_scan1(cnt + (landed ? 0u : 1u << 16), sm.stream_sums[ci & 1], &tot);
+      if (tot >> 16) break;
       // every thread has read slot s (the scan synchronised the block): refill it
       if (threadIdx.x == 0 && ci + Ring < nchunks) issue(ci + Ring);
       if (count + tot > (uint32_t)Cap && count >= (uint32_t)k) {
