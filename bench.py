@@ -423,10 +423,43 @@ def run_e2e(dsa, wl, layers, group, outs, lses, bufs, args, world):
 
     ms = time_loop(step, max(3, args.steps // 2), 1, world)
     ms = max_over_ranks(ms, world)
+    link = host_copy_gbs(at_host[0][0], at_dev[0][0], out_host[0][0], out_dev[0][0], cin, cout)
     del ix_host, at_host, out_host
     return {"value": round(wl.B * wl.T * world / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "overlap": "per-layer inputs in and outputs out on two copy streams, pipelined against compute"}
+            "overlap": "per-layer inputs in and outputs out on two copy streams, pipelined against compute",
+            "host_copy_gbs": link, "copy_bound_ms": round((h2d + d2h) / (link["both"] * 1e9) * 1e3, 1)}
+
+
+def host_copy_gbs(h_in, d_in, h_out, d_out, cin, cout, nbytes=1 << 30, reps=3):
+    """Pinned host <-> device copy rates of this machine (GB/s, median of reps): in alone, out
+    alone, and both directions at once on the two copy streams the end-to-end step uses.  The
+    host link differs between machines, and it bounds the end-to-end step from below."""
+    hi, di = h_in.view(-1)[:nbytes // h_in.element_size()], d_in.view(-1)[:nbytes // h_in.element_size()]
+    ho, do = h_out.view(-1)[:nbytes // h_out.element_size()], d_out.view(-1)[:nbytes // h_out.element_size()]
+    b_in, b_out = hi.numel() * hi.element_size(), ho.numel() * ho.element_size()
+    comp = torch.cuda.current_stream()
+    res = {}
+    for name in ("h2d", "d2h", "both"):
+        ts = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(comp)
+            cin.wait_stream(comp)
+            cout.wait_stream(comp)
+            for st, go, dst, src in ((cin, name != "d2h", di, hi), (cout, name != "h2d", ho, do)):
+                if go:
+                    with torch.cuda.stream(st):
+                        dst.copy_(src, non_blocking=True)
+            comp.wait_stream(cin)
+            comp.wait_stream(cout)
+            e1.record(comp)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / 1e3)
+        moved = (b_in if name != "d2h" else 0) + (b_out if name != "h2d" else 0)
+        res[name] = round(moved / sorted(ts)[len(ts) // 2] / 1e9, 1)
+    return res
 
 
 # --- reference arm: the CPU oracle -------------------------------------------------------
