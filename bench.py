@@ -51,7 +51,10 @@ def parse():
                     help="time one call on a single-kernel case instead of the group step "
                          "(the case the committed ncu summaries are captured on)")
     ap.add_argument("--rows", type=int, default=2048, help="--kernel: query rows (the last rows of the sequence)")
-    ap.add_argument("--keys", type=int, default=131072, help="--kernel: sequence length")
+    ap.add_argument("--keys", type=int, default=131072, help="--kernel/--heatmap: sequence length")
+    ap.add_argument("--heatmap", action="store_true",
+                    help="all-F pass over the 16 layers of heatmap_128k, the layer-overlap matrix, "
+                         "the best schedule per number of full layers and measured group times")
     return ap.parse_args()
 
 
@@ -553,10 +556,103 @@ def run_kernel_case(args):
     print(json.dumps({"device_flags": dsa.read_device_flags(dev)}))
 
 
+def run_heatmap(args):
+    """The layer-overlap heatmap of an all-F pass and the schedules it suggests.  Every layer
+    of heatmap_128k runs its own indexer + top-k (dsa_topk), topk_overlap_matrix gives the mean
+    overlap of every pair of layers, indexshare_schedule_search the best schedule for each
+    number of full layers, and indexshare_group_forward times the uniform F,S,S,S x 4 schedule
+    against the best one with as many full layers.  The layers' attention operands are one
+    shared set (attention time does not depend on which rows are selected), so the group times
+    hold 16 layers of attention without 16 copies of Q and the latent KV."""
+    import long_context_sparse_tcgen05_gb300 as dsa
+    from long_context_sparse_tcgen05_gb300 import build
+    build.build()
+    dsa.load_library()
+    dev = torch.device("cuda:0")
+    wl = synth.WORKLOADS["heatmap_128k"]
+    if args.keys != wl.S:
+        wl = wl.replace(T=args.keys, S=args.keys)
+    n, T, k = wl.n_layers, wl.B * wl.T, wl.k
+
+    def timed(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    # all-F pass: one indexer + top-k per layer, each into its own index buffer
+    bufs = [torch.empty((wl.B, wl.T, k), dtype=torch.int32, device=dev) for _ in range(n)]
+    f_ms = []
+    for l in range(n):
+        ix = synth.indexer_inputs(wl, l, dev)
+        if l == 0:
+            dsa.dsa_topk(k, ix=ix, idx=bufs[0])  # warm-up
+        f_ms.append(timed(lambda: dsa.dsa_topk(k, ix=ix, idx=bufs[l])))
+        del ix
+    torch.cuda.empty_cache()
+
+    # the overlap matrix, timed by the launch tracer (its kernels on the current stream)
+    M, _ = dsa.topk_overlap_matrix(bufs)
+    dsa.trace_enable(64)
+    for _ in range(3):
+        M, _ = dsa.topk_overlap_matrix(bufs)
+    m_ms = statistics.median(ms for kind, ms in dsa.trace_read() if kind == "overlap")
+    dsa.trace_disable()
+    idx_bytes = n * T * k * 4
+
+    # attention time of one layer, then the schedules
+    at = synth.attn_inputs(wl, 0, dev)
+    out = torch.empty((wl.B, wl.T, wl.H, wl.DV), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((wl.B, wl.T, wl.H), dtype=torch.float32, device=dev)
+    dsa.dsa_sparse_attn(at, bufs[0], out=out, lse=lse)
+    a_ms = timed(lambda: dsa.dsa_sparse_attn(at, bufs[0], out=out, lse=lse))
+    t_f = statistics.mean(f_ms)
+    schedules = []
+    for m in range(1, n + 1):
+        sched, score = dsa.indexshare_schedule_search(M, m)
+        schedules.append({"n_full": m, "schedule": sched, "score": round(score, 4),
+                          "model_ms": round(m * t_f + n * a_ms, 1)})
+    uniform = "FSSS" * (n // 4)
+    best = schedules[uniform.count("F") - 1]["schedule"]
+    del bufs
+    torch.cuda.empty_cache()
+
+    def group_ms(sched):
+        layers = [dict(ix=synth.indexer_inputs(wl, l, dev) if sched[l] == "F" else None, at=at)
+                  for l in range(n)]
+        run = lambda: dsa.indexshare_group_forward(layers, sched, k, outs=[out] * n, lses=[lse] * n)
+        run()
+        ms = statistics.median(timed(run) for _ in range(2))
+        del layers
+        torch.cuda.empty_cache()
+        return round(ms, 1)
+
+    groups = {s: group_ms(s) for s in dict.fromkeys([uniform, best, "F" * n])}
+    line = {
+        "workload": wl.name, "L": wl.S, "query_rows": T, "k": k, "layers": n,
+        "clusters": list(wl.clusters), "cluster_share": synth.CLUSTER_SHARE,
+        "heatmap": [[round(v, 4) for v in row] for row in M],
+        "adjacent_overlap": [round(M[l][l + 1], 4) for l in range(n - 1)],
+        "indexer_topk_ms_per_layer": round(t_f, 2), "attention_ms_per_layer": round(a_ms, 2),
+        "overlap_matrix": {"ms": round(m_ms, 3), "idx_bytes": idx_bytes,
+                           "gbs": round(idx_bytes / (m_ms * 1e-3) / 1e9, 1)},
+        "schedules": schedules,
+        "measured_group_ms": {s: groups[s] for s in groups},
+        "uniform": {"schedule": uniform, "score": round(dsa.indexshare_schedule_score(M, uniform), 4)},
+        "device_flags": dsa.read_device_flags(dev),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.kernel:
         run_kernel_case(args)
+        return
+    if args.heatmap:
+        run_heatmap(args)
         return
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":

@@ -174,6 +174,44 @@ dsa_status topk_overlap(const int32_t* a, const int32_t* b, int32_t rows, int32_
                         float* per_row, double* mean_out, void* ws, size_t ws_bytes,
                         void* stream);
 
+/* All-pairs overlap of n index buffers of the same query rows -- the layer-overlap heatmap
+ * of an all-F pass (IndexCache notes, section 2: pairwise overlap of the layers' top-k
+ * sets, 70-100% between adjacent layers, with blocks of layers that pick nearly the same
+ * tokens).  matrix_out[i*n + j] (host, n*n doubles) = the mean over rows of
+ * |A^i_r and A^j_r| / |A^i_r| over valid entries (1 for a row whose A^i_r is empty; 1 for
+ * every entry when rows = 0): what topk_overlap(bufs[i], bufs[j]) returns, for every ordered
+ * pair at once; the diagonal is 1.
+ *   bufs    HOST array of n DEVICE pointers, each [rows,k] int32 in the form dsa_topk
+ *           writes (ascending valid entries, then -1 padding); 1 <= n <= 16.
+ *   counts  DEVICE int32 [rows,n,n] receiving |A^i_r and A^j_r| (diagonal: |A^i_r|), or NULL.
+ *   ws      at least topk_overlap_matrix_workspace_size(n) bytes.
+ * One CTA holds a row of all n buffers in shared memory: n * (k + k/64 + 1) * 4 bytes must
+ * not exceed DSA_OVERLAP_MATRIX_MAX_SMEM (n = 16 allows k <= 3,072), else
+ * DSA_ERR_UNSUPPORTED.  A row not in dsa_topk's form raises DSA_FLAG_UNSORTED.  The sum over
+ * rows runs in a fixed order (deterministic).  Synchronises `stream`. */
+#define DSA_OVERLAP_MATRIX_MAX_SMEM ((size_t)204800)
+dsa_status topk_overlap_matrix(const int32_t* const* bufs, int32_t n, int32_t rows, int32_t k,
+                               int32_t* counts, double* matrix_out, void* ws, size_t ws_bytes,
+                               void* stream);
+size_t topk_overlap_matrix_workspace_size(int32_t n);
+
+/* F/S schedules judged by an overlap matrix (host only, no GPU work).  A shared layer l
+ * reuses the positions of the most recent full layer f(l) (f(l) = l for a full layer), so
+ * the fraction of its own top-k it keeps is overlap[l*n + f(l)] (GLM-5.2 IndexShare
+ * article: the released schedule repeats F,S,S,S after a few initial exceptions; IndexCache
+ * notes, section 2: the first layer is always F).
+ *   indexshare_schedule_score:  *score_out = mean over the n layers of overlap[l*n + f(l)].
+ *   indexshare_schedule_search: among schedules with exactly n_full 'F' (the first layer
+ *     one of them), one of largest score, written to schedule_out (n characters + NUL) with
+ *     its score; ties go to the schedule whose later full layers sit earliest.
+ * overlap: host n*n doubles, row-major (e.g. from topk_overlap_matrix).  n <=
+ * DSA_SCHEDULE_MAX_LAYERS.  A bad schedule string returns DSA_ERR_SCHEDULE. */
+#define DSA_SCHEDULE_MAX_LAYERS 256
+dsa_status indexshare_schedule_score(const double* overlap, int32_t n, const char* schedule,
+                                     double* score_out);
+dsa_status indexshare_schedule_search(const double* overlap, int32_t n, int32_t n_full,
+                                      char* schedule_out, double* score_out);
+
 /* Reads the device flag word of a workspace into *flags_out (host) and clears it.
  * Synchronises `stream`. */
 dsa_status dsa_read_device_flags(void* ws, uint32_t* flags_out, void* stream);

@@ -11,6 +11,9 @@ Calls (same names as the C ABI):
   dsa_sparse_attn(at, idx)                -> (out [B,T,H,d_v] bf16, lse [B,T,H] fp32)
   indexshare_group_forward(layers, schedule, k) -> (outs, lses, idx_bufs)
   topk_overlap(a, b)                      -> (per_row fp32, mean float)
+  topk_overlap_matrix(bufs)               -> (n x n mean overlaps, counts [rows,n,n] or None)
+  indexshare_schedule_score(M, schedule)  -> float (host only)
+  indexshare_schedule_search(M, n_full)   -> (schedule str, score) (host only)
 Operand dicts use the keys produced by ``synth``: an indexer dict holds q, w, k, q_scale,
 k_scale, q_pos0, diag; an attention dict holds q, k, v (None: latent KV), d_v, scale.
 """
@@ -93,6 +96,17 @@ def load_library(path: str = LIB_PATH):
             lib.topk_overlap.restype = S
             lib.topk_overlap.argtypes = [_P, _P, _c.c_int32, _c.c_int32, _P,
                                          _c.POINTER(_c.c_double), _P, _c.c_size_t, _P]
+            lib.topk_overlap_matrix.restype = S
+            lib.topk_overlap_matrix.argtypes = [_c.POINTER(_P), _c.c_int32, _c.c_int32, _c.c_int32, _P,
+                                                _c.POINTER(_c.c_double), _P, _c.c_size_t, _P]
+            lib.topk_overlap_matrix_workspace_size.restype = _c.c_size_t
+            lib.topk_overlap_matrix_workspace_size.argtypes = [_c.c_int32]
+            lib.indexshare_schedule_score.restype = S
+            lib.indexshare_schedule_score.argtypes = [_c.POINTER(_c.c_double), _c.c_int32, _c.c_char_p,
+                                                      _c.POINTER(_c.c_double)]
+            lib.indexshare_schedule_search.restype = S
+            lib.indexshare_schedule_search.argtypes = [_c.POINTER(_c.c_double), _c.c_int32, _c.c_int32,
+                                                       _c.c_char_p, _c.POINTER(_c.c_double)]
             lib.dsa_read_device_flags.restype = S
             lib.dsa_read_device_flags.argtypes = [_P, _c.POINTER(_c.c_uint32), _P]
             lib.dsa_status_string.restype = _c.c_char_p
@@ -302,6 +316,49 @@ def topk_overlap(a: torch.Tensor, b: torch.Tensor, per_row: torch.Tensor | bool 
     return per_row, mean.value
 
 
+def topk_overlap_matrix(bufs, counts: bool = False):
+    """All-pairs overlap of n index buffers of the same rows (the layer-overlap heatmap of an
+    all-F pass): (M, counts) with M[i][j] = mean over rows of |A_i and A_j| / |A_i| as nested
+    Python lists of floats, and counts an int32 [rows, n, n] device tensor of the per-row
+    intersection sizes when asked for (else None).  Synchronises."""
+    lib = load_library()
+    n = len(bufs)
+    k = bufs[0].shape[-1]
+    rows = bufs[0].numel() // k
+    for b in bufs:
+        assert b.shape == bufs[0].shape and b.dtype == torch.int32 and b.is_contiguous()
+    dev = bufs[0].device
+    cnt = torch.empty((rows, n, n), dtype=torch.int32, device=dev) if counts else None
+    arr = (_P * n)(*[b.data_ptr() for b in bufs])
+    ws = workspace(int(lib.topk_overlap_matrix_workspace_size(n)), dev)
+    out = (_c.c_double * (n * n))()
+    _check(lib.topk_overlap_matrix(arr, n, rows, k, _ptr(cnt), out, _ptr(ws), ws.numel(), _stream()))
+    return [[out[i * n + j] for j in range(n)] for i in range(n)], cnt
+
+
+def _matrix_arg(M):
+    n = len(M)
+    flat = (_c.c_double * (n * n))(*[float(M[i][j]) for i in range(n) for j in range(n)])
+    return n, flat
+
+
+def indexshare_schedule_score(M, schedule: str) -> float:
+    """Mean over layers of the overlap each layer keeps under `schedule` (host only)."""
+    n, flat = _matrix_arg(M)
+    v = _c.c_double()
+    _check(load_library().indexshare_schedule_score(flat, n, schedule.encode(), _c.byref(v)))
+    return v.value
+
+
+def indexshare_schedule_search(M, n_full: int):
+    """(schedule, score): a best schedule with n_full full layers under overlap matrix M."""
+    n, flat = _matrix_arg(M)
+    buf = _c.create_string_buffer(n + 1)
+    v = _c.c_double()
+    _check(load_library().indexshare_schedule_search(flat, n, int(n_full), buf, _c.byref(v)))
+    return buf.value.decode(), v.value
+
+
 def launch_count() -> int:
     """Kernels launched by the library since it was loaded."""
     return int(load_library().dsa_launch_count())
@@ -343,6 +400,7 @@ def read_device_flags(device=None) -> int:
 
 __all__ = [
     "indexer_scores", "dsa_topk", "dsa_sparse_attn", "indexshare_group_forward", "topk_overlap",
+    "topk_overlap_matrix", "indexshare_schedule_score", "indexshare_schedule_search",
     "read_device_flags", "workspace", "workspace_size", "load_library", "DsaError",
     "IndexerArgs", "AttnArgs", "TopkSrc", "Layer",
 ]

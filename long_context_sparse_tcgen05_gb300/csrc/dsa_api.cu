@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cstring>
 #include <string>
+#include <vector>
 
 #include "dsa_internal.cuh"
 
@@ -306,6 +307,104 @@ dsa_status topk_overlap(const int32_t* a, const int32_t* b, int32_t rows, int32_
   if ((e = cudaMemcpyAsync(mean_out, mean_dev, sizeof(double), cudaMemcpyDeviceToHost, st)) != cudaSuccess)
     return cuda_fail(e, "overlap mean copy");
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "overlap sync");
+  return DSA_OK;
+}
+
+dsa_status topk_overlap_matrix(const int32_t* const* bufs, int32_t n, int32_t rows, int32_t k,
+                               int32_t* counts, double* matrix_out, void* ws, size_t ws_bytes, void* stream) {
+  if (!bufs || !matrix_out) return fail(DSA_ERR_INVALID_ARG, "bufs and matrix_out must be non-NULL");
+  if (n < 1 || n > dsa::kMaxOverlapLayers)
+    return fail(DSA_ERR_INVALID_ARG, "n = %d buffers; 1 <= n <= %d", n, dsa::kMaxOverlapLayers);
+  if (rows < 0 || k < 1) return fail(DSA_ERR_INVALID_ARG, "rows must be >= 0 and k >= 1");
+  for (int i = 0; i < n; ++i)
+    if (!bufs[i]) return fail(DSA_ERR_INVALID_ARG, "bufs[%d] is NULL", i);
+  if (dsa::overlap_matrix_smem(n, k) > DSA_OVERLAP_MATRIX_MAX_SMEM)
+    return fail(DSA_ERR_UNSUPPORTED, "n = %d rows of k = %d do not fit in one CTA's shared memory", n, k);
+  dsa_status s = check_ws(ws, ws_bytes, topk_overlap_matrix_workspace_size(n));
+  if (s != DSA_OK) return s;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  double* matrix_dev = reinterpret_cast<double*>(w8 + dsa::kWsScratch);
+  dsa::OverlapMatrixLaunch P{};
+  for (int i = 0; i < n; ++i) P.bufs[i] = bufs[i];
+  P.n = n;
+  P.k = k;
+  P.rows = rows;
+  P.counts = counts;
+  P.part = matrix_dev + dsa::kMaxOverlapLayers * dsa::kMaxOverlapLayers;
+  P.flags = ws_flags(ws);
+  cudaStream_t st = as_stream(stream);
+  cudaError_t e = dsa::launch_overlap_matrix(P, matrix_dev, st);
+  if (e != cudaSuccess) return cuda_fail(e, "overlap matrix launch");
+  if ((e = cudaMemcpyAsync(matrix_out, matrix_dev, sizeof(double) * n * n, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+    return cuda_fail(e, "overlap matrix copy");
+  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "overlap matrix sync");
+  return DSA_OK;
+}
+
+size_t topk_overlap_matrix_workspace_size(int32_t n) {
+  const size_t nn = n > 0 ? (size_t)n * (size_t)n : 0;
+  return dsa::kWsScratch + sizeof(double) * (dsa::kMaxOverlapLayers * dsa::kMaxOverlapLayers + dsa::kMaxOverlapCtas * nn);
+}
+
+// --- F/S schedules scored by a measured overlap matrix (host only) ---------------------
+
+namespace {
+
+bool valid_schedule(const char* sched, int n) {
+  if (!sched || (int)strnlen(sched, (size_t)n + 1) != n || sched[0] != 'F') return false;
+  for (int i = 0; i < n; ++i)
+    if (sched[i] != 'F' && sched[i] != 'S') return false;
+  return true;
+}
+
+}  // namespace
+
+dsa_status indexshare_schedule_score(const double* overlap, int32_t n, const char* schedule, double* score_out) {
+  if (!overlap || !score_out) return fail(DSA_ERR_INVALID_ARG, "overlap and score_out must be non-NULL");
+  if (n < 1) return fail(DSA_ERR_INVALID_ARG, "n must be >= 1");
+  if (!valid_schedule(schedule, n))
+    return fail(DSA_ERR_SCHEDULE, "schedule must be %d characters of 'F'/'S' starting with 'F'", n);
+  double sum = 0.0;
+  int f = 0;
+  for (int l = 0; l < n; ++l) {
+    if (schedule[l] == 'F') f = l;
+    sum += overlap[(size_t)l * n + f];
+  }
+  *score_out = sum / n;
+  return DSA_OK;
+}
+
+dsa_status indexshare_schedule_search(const double* overlap, int32_t n, int32_t n_full, char* schedule_out,
+                                      double* score_out) {
+  if (!overlap || !schedule_out || !score_out) return fail(DSA_ERR_INVALID_ARG, "pointers must be non-NULL");
+  if (n < 1 || n > DSA_SCHEDULE_MAX_LAYERS)
+    return fail(DSA_ERR_INVALID_ARG, "n = %d layers; 1 <= n <= %d", n, DSA_SCHEDULE_MAX_LAYERS);
+  if (n_full < 1 || n_full > n) return fail(DSA_ERR_INVALID_ARG, "n_full = %d; 1 <= n_full <= n = %d", n_full, n);
+  // seg(a, b): layers a .. b-1 served by an F layer at a = sum of overlap[l][a]
+  // best[m][b]: the largest sum over layers 0 .. b-1 split into m such runs, the first at 0
+  const int N = n + 1;
+  std::vector<double> best((size_t)(n_full + 1) * N, -1.0), seg((size_t)n * N, 0.0);
+  std::vector<int> from((size_t)(n_full + 1) * N, -1);
+  for (int a = 0; a < n; ++a)
+    for (int b = a + 1; b <= n; ++b) seg[(size_t)a * N + b] = seg[(size_t)a * N + b - 1] + overlap[(size_t)(b - 1) * n + a];
+  for (int b = 1; b <= n; ++b) best[(size_t)1 * N + b] = seg[b];
+  for (int m = 2; m <= n_full; ++m)
+    for (int b = m; b <= n; ++b)
+      for (int a = m - 1; a < b; ++a) {  // the m-th run starts at layer a; earlier a wins ties
+        const double v = best[(size_t)(m - 1) * N + a] + seg[(size_t)a * N + b];
+        if (from[(size_t)m * N + b] < 0 || v > best[(size_t)m * N + b]) {
+          best[(size_t)m * N + b] = v;
+          from[(size_t)m * N + b] = a;
+        }
+      }
+  for (int l = 0; l < n; ++l) schedule_out[l] = 'S';
+  schedule_out[n] = '\0';
+  for (int m = n_full, b = n; m >= 1; --m) {
+    const int a = m == 1 ? 0 : from[(size_t)m * N + b];
+    schedule_out[a] = 'F';
+    b = a;
+  }
+  *score_out = best[(size_t)n_full * N + n] / n;
   return DSA_OK;
 }
 

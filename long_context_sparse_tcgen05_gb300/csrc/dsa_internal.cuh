@@ -121,4 +121,19 @@ cudaError_t launch_topk_overlap(const int32_t* a, const int32_t* b, int rows, in
                                 float* per_row, double* mean_dev, uint32_t* flags,
                                 cudaStream_t st);
 
+// All-pairs overlap of n index buffers over the same rows.  part: kMaxOverlapCtas * n * n
+// doubles of per-CTA sums; counts: [rows, n, n] int32 or nullptr.
+constexpr int kMaxOverlapLayers = 16;
+constexpr int kMaxOverlapCtas = 1024;
+struct OverlapMatrixLaunch {
+  const int32_t* bufs[kMaxOverlapLayers];
+  int n, k;
+  int64_t rows;
+  int32_t* counts;
+  double* part;
+  uint32_t* flags;
+};
+size_t overlap_matrix_smem(int n, int k);  // dynamic shared memory of one CTA
+cudaError_t launch_overlap_matrix(const OverlapMatrixLaunch& p, double* matrix_dev, cudaStream_t st);
+
 }  // namespace dsa

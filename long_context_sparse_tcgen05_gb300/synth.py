@@ -15,6 +15,8 @@ the workloads the project is measured on:
                          16 layers (four F,S,S,S groups).
 * ``chunked_prefill_1m`` the last 4,096 rows of a 1,048,576-token sequence against the full
                          causal cache, FP8 indexer, correlated inputs, 16 layers.
+* ``heatmap_128k``       the 128K shapes over 16 layers run all-F, for the layer-overlap
+                         heatmap: indexer inputs correlated in clusters of layers.
 
 Every tensor is drawn from its own Philox stream, seeded by
 ``20261202 + 1000*workload_id + 10*layer + tensor_id``; tensors longer than one chunk are
@@ -35,6 +37,8 @@ CHUNK = 4096  # tokens per independently seeded chunk
 
 T_Q_I, T_K_I, T_W, T_Q, T_KV, T_V = 0, 1, 2, 3, 4, 5
 T_BASE_Q_I, T_BASE_K_I = 7, 8
+T_CLUSTER_Q_I, T_CLUSTER_K_I = 6, 9  # drawn per cluster (the cluster id takes the layer slot)
+CLUSTER_SHARE = 0.75                 # share of a layer's noise variance common to its cluster
 
 
 @dataclasses.dataclass(frozen=True)
@@ -56,6 +60,7 @@ class Workload:
     DV: int             # value dim
     latent: bool        # True: V is the first DV columns of the KV row (one buffer)
     diag: int = 0       # keys s < q_pos + diag are visible
+    clusters: tuple = ()  # "clustered" values: cluster id of each layer
 
     @property
     def n_layers(self) -> int:
@@ -81,6 +86,9 @@ WORKLOADS = {
     "chunked_prefill_1m": Workload("chunked_prefill_1m", 4, 1, 4096, 1048576, 1048576 - 4096,
                                    64, 128, "e4m3", "correlated", 2048, "FSSS" * 4, 64, 576, 512,
                                    True),
+    "heatmap_128k": Workload("heatmap_128k", 5, 1, 131072, 131072, 0, 64, 128, "e4m3", "clustered",
+                             2048, "F" * 16, 64, 576, 512, True,
+                             clusters=(0, 1, 1, 2, 2, 2, 3, 3, 3, 3, 3, 3, 3, 3, 3, 3)),
 }
 
 
@@ -161,6 +169,19 @@ def indexer_inputs(wl: Workload, layer: int, device="cpu") -> dict:
         k = _draw("normal", ks, device, seed_of(wl, 0, T_BASE_K_I))
         k += 0.3 * _draw("normal", ks, device, seed_of(wl, layer, T_K_I))
         w = _draw("uniform", ws, device, seed_of(wl, 0, T_W)) / 8.0
+    elif wl.values == "clustered":
+        # shared base + 0.3 * (unit-variance noise), the noise mixing a component drawn once
+        # per cluster of layers with the layer's own: each layer's values are distributed as
+        # in "correlated", and layers of one cluster share CLUSTER_SHARE of their noise
+        a, b = math.sqrt(CLUSTER_SHARE), math.sqrt(1.0 - CLUSTER_SHARE)
+        c = wl.clusters[layer]
+        q = _draw("normal", qs, device, seed_of(wl, 0, T_BASE_Q_I))
+        q += (0.3 * a) * _draw("normal", qs, device, seed_of(wl, c, T_CLUSTER_Q_I))
+        q += (0.3 * b) * _draw("normal", qs, device, seed_of(wl, layer, T_Q_I))
+        k = _draw("normal", ks, device, seed_of(wl, 0, T_BASE_K_I))
+        k += (0.3 * a) * _draw("normal", ks, device, seed_of(wl, c, T_CLUSTER_K_I))
+        k += (0.3 * b) * _draw("normal", ks, device, seed_of(wl, layer, T_K_I))
+        w = _draw("uniform", ws, device, seed_of(wl, 0, T_W)) / 8.0
     else:
         raise ValueError(wl.values)
     ix = dict(w=w.contiguous(), q_pos0=wl.q_pos0, diag=wl.diag)
@@ -202,16 +223,23 @@ def attn_inputs(wl: Workload, layer: int, device="cpu") -> dict:
 def indexer_rows(wl: Workload, layer: int, rows, device="cpu") -> dict:
     """Indexer operands with only the given query rows drawn: q_rows [n,HI,DI], w_rows,
     q_scale_rows, plus the full keys; identical values to indexer_inputs at those rows."""
-    assert wl.values in ("gauss", "correlated"), "row subsets are for the Gaussian workloads"
+    assert wl.values in ("gauss", "correlated", "clustered"), "row subsets are for the Gaussian workloads"
     qs = (wl.B, wl.T, wl.HI, wl.DI)
     ws = (wl.B, wl.T, wl.HI)
     full = indexer_inputs(wl.replace(T=1, q_pos0=0), layer, device)  # keys only matter here
     if wl.values == "gauss":
         q = _draw_rows("normal", qs, device, seed_of(wl, layer, T_Q_I), rows)
         w = _draw_rows("uniform", ws, device, seed_of(wl, layer, T_W), rows) / 8.0
-    else:
+    elif wl.values == "correlated":
         q = _draw_rows("normal", qs, device, seed_of(wl, 0, T_BASE_Q_I), rows)
         q += 0.3 * _draw_rows("normal", qs, device, seed_of(wl, layer, T_Q_I), rows)
+        w = _draw_rows("uniform", ws, device, seed_of(wl, 0, T_W), rows) / 8.0
+    else:
+        a, b = math.sqrt(CLUSTER_SHARE), math.sqrt(1.0 - CLUSTER_SHARE)
+        c = wl.clusters[layer]
+        q = _draw_rows("normal", qs, device, seed_of(wl, 0, T_BASE_Q_I), rows)
+        q += (0.3 * a) * _draw_rows("normal", qs, device, seed_of(wl, c, T_CLUSTER_Q_I), rows)
+        q += (0.3 * b) * _draw_rows("normal", qs, device, seed_of(wl, layer, T_Q_I), rows)
         w = _draw_rows("uniform", ws, device, seed_of(wl, 0, T_W), rows) / 8.0
     ix = dict(k=full["k"], k_scale=full["k_scale"], w_rows=w.contiguous(), T=wl.T, S=wl.S,
               q_pos0=wl.q_pos0, diag=wl.diag, B=wl.B)

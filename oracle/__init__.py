@@ -289,3 +289,51 @@ def topk_overlap(a, b):
     per = np.empty(aa.shape[0], dtype=np.float64)
     mean = _load().orc_topk_overlap(_ptr(aa), _ptr(bb), aa.shape[0], k, _ptr(per))
     return per, float(mean)
+
+
+def overlap_matrix(bufs):
+    """M[i][j] = topk_overlap(bufs[i], bufs[j]) mean, for every ordered pair of n index
+    buffers over the same rows (the pairwise-overlap heatmap of the IndexCache notes,
+    section 2), plus the per-row fractions [rows, n, n]."""
+    n = len(bufs)
+    M = np.ones((n, n), dtype=np.float64)
+    per = None
+    for i in range(n):
+        for j in range(n):
+            pr, m = topk_overlap(bufs[i], bufs[j])
+            if per is None:
+                per = np.empty((pr.shape[0], n, n), dtype=np.float64)
+            per[:, i, j] = pr
+            M[i, j] = m
+    return M, per
+
+
+def schedule_score(M, schedule: str) -> float:
+    """A shared layer reuses the most recent full layer's positions (explainer, "How
+    IndexShare Works"), so it keeps the fraction M[l][f] of its own top-k, f being that full
+    layer; a full layer keeps all of it.  The score is the mean of that over the layers."""
+    M = np.asarray(M, dtype=np.float64)
+    check_schedule(schedule, M.shape[0])
+    total = 0.0
+    f = 0
+    for l, role in enumerate(schedule):
+        if role == "F":
+            f = l
+        total += M[l, f]
+    return total / M.shape[0]
+
+
+def schedule_search(M, n_full: int):
+    """(best score, every schedule reaching it) over all schedules with n_full full layers,
+    the first layer among them: plain enumeration."""
+    import itertools
+    n = np.asarray(M).shape[0]
+    best, arg = None, []
+    for rest in itertools.combinations(range(1, n), n_full - 1):
+        sched = "".join("F" if (l == 0 or l in rest) else "S" for l in range(n))
+        v = schedule_score(M, sched)
+        if best is None or v > best + 1e-12:
+            best, arg = v, [sched]
+        elif abs(v - best) <= 1e-12:
+            arg.append(sched)
+    return best, arg

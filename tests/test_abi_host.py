@@ -211,3 +211,41 @@ def test_trace_enable_validation_and_empty_read(lib):
     assert lib.dsa_trace_read(None, None, 0, ctypes.byref(dropped)) == 0
     assert dropped.value == 0
     lib.dsa_trace_disable()
+
+
+def test_overlap_matrix_validation(lib):
+    P = ctypes.c_void_p
+    m = (ctypes.c_double * 256)()
+    bufs = (P * 16)(*([FAKE] * 16))
+    need4 = lib.topk_overlap_matrix_workspace_size(4)
+    assert need4 == 256 + 8 * (16 * 16 + 1024 * 16)
+
+    def call(b, n, rows, k, ws_bytes, out=m):
+        return lib.topk_overlap_matrix(b, n, rows, k, None, out, P(FAKE), ws_bytes, None)
+
+    assert call(None, 4, 10, 8, need4) == INVALID
+    assert call(bufs, 4, 10, 8, need4, out=None) == INVALID
+    assert call(bufs, 0, 10, 8, need4) == INVALID
+    assert call(bufs, 17, 10, 8, 1 << 30) == INVALID
+    assert call(bufs, 4, -1, 8, need4) == INVALID
+    assert call(bufs, 4, 10, 0, need4) == INVALID
+    assert call((P * 4)(FAKE, None, FAKE, FAKE), 4, 10, 8, need4) == INVALID
+    # one CTA holds a row of every buffer: 16 x 3,072 fits, 16 x 4,096 does not, 12 x 4,096 does
+    assert call(bufs, 16, 10, 4096, 1 << 30) == UNSUPPORTED
+    assert call(bufs, 4, 10, 8, need4 - 8) == WORKSPACE
+    assert call(bufs, 16, 10, 3072, lib.topk_overlap_matrix_workspace_size(16) - 1) == WORKSPACE
+    assert call(bufs, 12, 10, 4096, lib.topk_overlap_matrix_workspace_size(12) - 1) == WORKSPACE
+
+
+def test_schedule_validation(lib):
+    M = [[1.0, 0.5], [0.5, 1.0]]
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.indexshare_schedule_score(M, "SF")
+    assert e.value.status == SCHEDULE
+    for bad in ("F", "FSS", "FX"):
+        with pytest.raises(dsa.DsaError):
+            dsa.indexshare_schedule_score(M, bad)
+    for n_full in (0, 3):
+        with pytest.raises(dsa.DsaError) as e:
+            dsa.indexshare_schedule_search(M, n_full)
+        assert e.value.status == INVALID

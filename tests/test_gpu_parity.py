@@ -328,3 +328,60 @@ def test_topk_overlap_flags_unsorted_rows():
     dsa.read_device_flags()
     dsa.topk_overlap(a, b)
     assert dsa.read_device_flags() & dsa.FLAG_UNSORTED
+
+
+def _index_buffers(n, R, k, universe, seed, empty_every=0):
+    """n index buffers [R,k] in top-k form over the same rows: every row draws a pool of
+    positions and each buffer an ascending subset of it of the row's valid count (so the
+    buffers overlap heavily but not fully); rows with valid count 0 are all -1."""
+    g = torch.Generator().manual_seed(seed)
+    bufs = [np.full((R, k), -1, np.int32) for _ in range(n)]
+    for r in range(R):
+        nv = 0 if empty_every and r % empty_every == 0 else int(torch.randint(1, k + 1, (1,), generator=g))
+        pool = torch.randperm(universe, generator=g)[:min(universe, nv + nv // 3 + 1)]
+        for b in bufs:
+            b[r, :nv] = np.sort(pool[torch.randperm(len(pool), generator=g)[:nv]].numpy())
+    return bufs
+
+
+@pytest.mark.parametrize("n,R,k,universe", [(5, 300, 64, 200), (16, 150, 2048, 6000), (16, 40, 3072, 9000),
+                                            (12, 30, 4096, 20000), (1, 10, 8, 16), (2, 333, 100, 150)])
+def test_topk_overlap_matrix_matches_oracle(n, R, k, universe):
+    host = _index_buffers(n, R, k, universe, seed=40 + n + k, empty_every=37)
+    bufs = [torch.from_numpy(b).to(DEV) for b in host]
+    M, cnt = dsa.topk_overlap_matrix(bufs, counts=True)
+    assert dsa.read_device_flags() == 0
+    cnt = cnt.cpu().numpy().astype(np.int64)
+    Mo, per = oracle.overlap_matrix(host)
+    valid = np.stack([(b >= 0).sum(1) for b in host], 1)           # [R, n]
+    assert np.array_equal(cnt[:, np.arange(n), np.arange(n)], valid)  # diagonal: |A_i|
+    assert np.array_equal(cnt, cnt.transpose(0, 2, 1))               # |A_i and A_j| symmetric
+    frac = np.where(valid[:, :, None] == 0, 1.0, cnt / np.maximum(valid[:, :, None], 1))
+    assert np.array_equal(frac, per)  # the same integers divided in double: bit-exact
+    np.testing.assert_allclose(np.array(M), Mo, rtol=1e-12, atol=0)
+    assert all(M[i][i] == 1.0 for i in range(n))
+
+
+def test_topk_overlap_matrix_of_an_all_full_pass():
+    # four layers of the clustered workload, each with its own indexer + top-k; layers 1 and
+    # 2 share a cluster, layers 0 and 3 do not share one with anything else here
+    wl = synth.WORKLOADS["heatmap_128k"].replace(T=1536, S=1536, k=256)
+    bufs = [dsa.dsa_topk(wl.k, ix=synth.indexer_inputs(wl, l, DEV)) for l in range(4)]
+    M, _ = dsa.topk_overlap_matrix(bufs)
+    Mo, _ = oracle.overlap_matrix([b.cpu().numpy() for b in bufs])
+    np.testing.assert_allclose(np.array(M), Mo, rtol=1e-12, atol=0)
+    assert M[1][2] > M[0][1] + 0.05 and M[1][2] > M[2][3] + 0.05
+    # the pairwise call agrees with the matrix entry
+    assert dsa.topk_overlap(bufs[1], bufs[2], per_row=False)[1] == pytest.approx(M[1][2], rel=1e-12)
+
+
+def test_topk_overlap_matrix_flags_rows_not_in_topk_form():
+    good = torch.tensor([[1, 4, 9, -1], [2, 3, -1, -1]], dtype=torch.int32, device=DEV)
+    for bad in ([[1, 4, 9, -1], [3, 2, -1, -1]],    # descending
+                [[1, 4, 9, -1], [2, -1, 5, -1]],    # padding before a valid entry
+                [[1, 4, 4, -1], [2, 3, -1, -1]]):   # repeated position
+        dsa.read_device_flags()
+        dsa.topk_overlap_matrix([good, torch.tensor(bad, dtype=torch.int32, device=DEV)])
+        assert dsa.read_device_flags() & dsa.FLAG_UNSORTED
+    dsa.topk_overlap_matrix([good, good])
+    assert dsa.read_device_flags() == 0

@@ -85,3 +85,44 @@ def test_workload_group_sampled_rows(name, n_rows):
             assert np.abs(gl[fin] - ref_l[fin]).max() <= 1e-3
     del layers, outs, lses, bufs
     torch.cuda.empty_cache()
+
+
+def test_heatmap_all_full_pass_and_overlap_matrix_sampled_rows():
+    """The launch configuration of bench.py --heatmap: 16 layers of the 128K clustered
+    workload, each with its own indexer + top-k, then the all-pairs overlap matrix.  Per layer
+    the index rows of three sampled queries are checked against the oracle (recall, validity);
+    the matrix's per-row intersection counts are checked exactly on sampled rows against set
+    intersections of the GPU's own index rows, and its means against the mean over all rows
+    of count / valid count computed from those counts."""
+    wl = synth.WORKLOADS["heatmap_128k"]
+    n, R, k = wl.n_layers, wl.B * wl.T, wl.k
+    check_rows = [5, 2048, 20000]
+    bufs = []
+    for l in range(n):
+        ix = synth.indexer_inputs(wl, l, DEV)
+        bufs.append(dsa.dsa_topk(k, ix=ix))
+        got = bufs[-1].reshape(R, k)[torch.as_tensor(check_rows, device=DEV)].cpu().numpy()
+        ref, _ = oracle.indexer_topk(ix, k, check_rows, return_scores=True)
+        rec = [len(np.intersect1d(g[g >= 0], e[e >= 0])) / max(1, (e >= 0).sum()) for g, e in zip(got, ref)]
+        assert np.mean(rec) >= 0.999, (l, rec)
+        del ix
+        torch.cuda.empty_cache()
+    M, cnt = dsa.topk_overlap_matrix(bufs, counts=True)
+    assert dsa.read_device_flags() == 0
+    rows = synth.sample_rows(wl, 12)
+    sel = torch.as_tensor(rows, device=DEV)
+    host = [b.reshape(R, k)[sel].cpu().numpy() for b in bufs]
+    c = cnt[sel].cpu().numpy()
+    for r in range(len(rows)):
+        sets = [set(h[r][h[r] >= 0].tolist()) for h in host]
+        want = np.array([[len(sets[i] & sets[j]) for j in range(n)] for i in range(n)])
+        assert np.array_equal(c[r], want), rows[r]
+    # means: the matrix equals the mean of count/valid over all rows
+    cf = cnt.double()
+    diag = torch.diagonal(cf, dim1=1, dim2=2)[:, :, None]
+    frac = torch.where(diag == 0, torch.ones_like(cf), cf / diag.clamp(min=1))
+    np.testing.assert_allclose(np.array(M), frac.mean(0).cpu().numpy(), rtol=1e-9, atol=0)
+    # clusters: (1,2), (3,4,5), (6..15) overlap more inside than across
+    assert M[1][2] > M[0][1] and M[4][5] > M[2][3] and M[7][8] > M[5][6]
+    del bufs, cnt
+    torch.cuda.empty_cache()

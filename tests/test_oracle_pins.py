@@ -339,3 +339,63 @@ def test_overlap_brute_force_and_extremes():
     assert oracle.topk_overlap(a, a)[1] == 1.0
     disj = np.arange(2 * k, dtype=np.int32).reshape(2, k)
     assert oracle.topk_overlap(disj[:1], disj[1:])[1] == 0.0
+
+
+def _random_index_rows(g, R, k, universe, n_bufs):
+    """n_bufs [R,k] buffers in top-k form; every buffer of a row has the same valid count
+    (the same query sees the same keys in every layer)."""
+    bufs = [np.full((R, k), -1, np.int32) for _ in range(n_bufs)]
+    for r in range(R):
+        nv = int(torch.randint(0, k + 1, (1,), generator=g))
+        for b in bufs:
+            b[r, :nv] = np.sort(torch.randperm(universe, generator=g)[:nv].numpy())
+    return bufs
+
+
+def test_overlap_matrix_brute_force_sets():
+    g = torch.Generator().manual_seed(33)
+    bufs = _random_index_rows(g, 40, 16, 40, 5)
+    M, per = oracle.overlap_matrix(bufs)
+    for i in range(5):
+        for j in range(5):
+            fr = []
+            for r in range(40):
+                si = set(bufs[i][r][bufs[i][r] >= 0].tolist())
+                sj = set(bufs[j][r][bufs[j][r] >= 0].tolist())
+                fr.append(1.0 if not si else len(si & sj) / len(si))
+                assert per[r, i, j] == fr[-1]
+            assert M[i, j] == pytest.approx(sum(fr) / len(fr), rel=1e-12)
+    # equal valid counts per row make the matrix symmetric; every layer overlaps itself fully
+    assert np.allclose(M, M.T, rtol=0, atol=1e-15)
+    assert np.all(np.diag(M) == 1.0)
+
+
+# A 4-layer overlap matrix worked by hand: layer 1 is close to 0, layer 3 to 2.
+HAND_M = [[1.0, 0.9, 0.5, 0.2],
+          [0.9, 1.0, 0.6, 0.3],
+          [0.5, 0.6, 1.0, 0.7],
+          [0.2, 0.3, 0.7, 1.0]]
+
+
+@pytest.mark.parametrize("sched,want", [
+    ("FSSS", (1.0 + 0.9 + 0.5 + 0.2) / 4),   # layers 1..3 reuse layer 0
+    ("FSFS", (1.0 + 0.9 + 1.0 + 0.7) / 4),   # layer 1 reuses 0, layer 3 reuses 2
+    ("FFSS", (1.0 + 1.0 + 0.6 + 0.3) / 4),   # layers 2, 3 reuse layer 1
+    ("FSSF", (1.0 + 0.9 + 0.5 + 1.0) / 4),
+    ("FFFF", 1.0),
+])
+def test_schedule_score_hand_worked(sched, want):
+    assert oracle.schedule_score(HAND_M, sched) == pytest.approx(want, abs=1e-15)
+
+
+def test_schedule_search_hand_worked():
+    # two full layers: FSFS (0.9) beats FSSF (0.85), FFSS (0.725)
+    best, arg = oracle.schedule_search(HAND_M, 2)
+    assert arg == ["FSFS"] and best == pytest.approx(0.9, abs=1e-15)
+    best, arg = oracle.schedule_search(HAND_M, 1)
+    assert arg == ["FSSS"] and best == pytest.approx(0.65, abs=1e-15)
+    best, arg = oracle.schedule_search(HAND_M, 4)
+    assert arg == ["FFFF"] and best == 1.0
+    # three full layers: FFFS (1+1+1+0.7)/4 = 0.925, FSFF (1+0.9+1+1)/4 = 0.975, FFSF 0.9
+    best, arg = oracle.schedule_search(HAND_M, 3)
+    assert arg == ["FSFF"] and best == pytest.approx(0.975, abs=1e-15)

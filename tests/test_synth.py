@@ -32,3 +32,21 @@ def test_recipes():
     amax = (f["q"].float().abs().amax(dim=(2, 3)))
     assert torch.all(amax <= 448) and torch.all(amax >= 416)  # scale = amax / 448
     assert torch.all(f["w"] >= 0) and torch.all(f["w"] <= 1 / 8)
+
+
+def test_clustered_layers_share_noise_inside_a_cluster():
+    # every layer is base + 0.3 * unit noise; inside a cluster 3/4 of the noise variance is
+    # shared: corr = (1 + 0.09 * 0.75) / 1.09 inside, 1 / 1.09 across clusters
+    wl = synth.WORKLOADS["heatmap_128k"].replace(T=256, S=256)
+    assert len(wl.clusters) == wl.n_layers == 16
+    deq = []
+    for l in (0, 1, 2, 6):
+        ix = synth.indexer_inputs(wl, l)
+        deq.append((ix["q"].float() * ix["q_scale"][..., None, None]).flatten().double())
+    corr = lambda a, b: float(torch.corrcoef(torch.stack([a, b]))[0, 1])
+    inside = corr(deq[1], deq[2])            # layers 1, 2: cluster 1
+    across = corr(deq[0], deq[1])            # clusters 0 and 1
+    assert abs(inside - (1 + 0.09 * 0.75) / 1.09) < 0.01
+    assert abs(across - 1 / 1.09) < 0.01
+    assert abs(corr(deq[2], deq[3]) - 1 / 1.09) < 0.01  # clusters 1 and 3
+    assert abs(float(deq[3].std()) - 1.09 ** 0.5) < 0.02
