@@ -8,7 +8,7 @@
 // section 2) takes n buffers of the same query rows.  One CTA holds a row of every buffer in
 // shared memory; each warp takes whole pairs (i < j) and each lane a contiguous run of the
 // shorter list, found in the other list by one binary search and then a forward walk (both
-// lists ascend).  Lists are stored with one pad word per 64 entries, so the lanes' runs of 64
+// lists ascend).  A row of each buffer arrives by cp.async, word by word.  Lists are stored with one pad word per 64 entries, so the lanes' runs of 64
 // start in different banks.  Per-row fractions |A_i and A_j| / |A_i| are summed in double by
 // the thread that owns the ordered pair (i, j); per-CTA sums are reduced in a fixed order.
 #include <algorithm>
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(1024) k_mean(const float* per_row, int rows, d
 
 // --- all pairs ---------------------------------------------------------------------
 
-constexpr int kMatThreads = 512;
+constexpr int kMatThreads = 1024;
 constexpr int kMatWarps = kMatThreads / 32;
 
 __device__ __forceinline__ int padded(int e) { return e + (e >> 6); }
@@ -111,10 +111,17 @@ __global__ void __launch_bounds__(kMatThreads) k_overlap_matrix(OverlapMatrixLau
   double acc = 0.0;  // sum over this CTA's rows of the fraction of ordered pair threadIdx.x
   bool unsorted = false;
   for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
-    for (int e = threadIdx.x; e < n * k; e += kMatThreads) {
-      const int i = e / k, j = e - i * k;
-      lists[i * stride + padded(j)] = __ldg(p.bufs[i] + row * k + j);
+    // the row of every buffer, copied asynchronously word by word (rows need not be 16-byte
+    // aligned), then one wait
+    for (int i = 0; i < n; ++i) {
+      const int32_t* src = p.bufs[i] + row * k;
+      const uint32_t dst = (uint32_t)__cvta_generic_to_shared(lists + i * stride);
+      for (int j = threadIdx.x; j < k; j += kMatThreads)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst + 4u * (uint32_t)padded(j)),
+                     "l"(src + j)
+                     : "memory");
     }
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
     __syncthreads();
     // the previous row's counts were read before the barrier above
     for (int t = threadIdx.x; t < kMaxOverlapLayers * kMaxOverlapLayers; t += kMatThreads) cnt[t] = 0;
@@ -128,10 +135,10 @@ __global__ void __launch_bounds__(kMatThreads) k_overlap_matrix(OverlapMatrixLau
       vlen[threadIdx.x] = lo;
     }
     // form check: ascending valid entries, then only padding
-    for (int e = threadIdx.x; e < n * k; e += kMatThreads) {
-      const int i = e / k, j = e - i * k;
-      if (j + 1 < k) {
-        const int32_t a = lists[i * stride + padded(j)], b = lists[i * stride + padded(j + 1)];
+    for (int i = 0; i < n; ++i) {
+      const int32_t* l = lists + i * stride;
+      for (int j = threadIdx.x; j + 1 < k; j += kMatThreads) {
+        const int32_t a = l[padded(j)], b = l[padded(j + 1)];
         if (b >= 0 && (a < 0 || b <= a)) unsorted = true;
       }
     }
@@ -150,14 +157,13 @@ __global__ void __launch_bounds__(kMatThreads) k_overlap_matrix(OverlapMatrixLau
       const int e0 = lane * run, e1 = min(na, e0 + run);
       int c = 0;
       if (e0 < e1) {
-        int b = lower_bound_padded(lb, nb, la[padded(e0)]);
-        for (int e = e0; e < e1 && b < nb; ++e) {
-          const int32_t x = la[padded(e)];
-          while (b < nb && lb[padded(b)] < x) ++b;
-          if (b < nb && lb[padded(b)] == x) {
-            ++c;
-            ++b;
-          }
+        // merge walk without branches: advance the smaller side (both on a match)
+        int b = lower_bound_padded(lb, nb, la[padded(e0)]), e = e0;
+        while (e < e1 && b < nb) {
+          const int32_t x = la[padded(e)], y = lb[padded(b)];
+          c += x == y;
+          e += x <= y;
+          b += y <= x;
         }
       }
 #pragma unroll
