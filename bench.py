@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle CPU time")
-    ap.add_argument("--kernel", choices=["attn", "indexer", "topk", "ixtopk"], default=None,
+    ap.add_argument("--kernel", choices=["attn", "indexer", "topk", "ixtopk", "quant"], default=None,
                     help="time one call on a single-kernel case instead of the group step "
                          "(the case the committed ncu summaries are captured on)")
     ap.add_argument("--rows", type=int, default=2048, help="--kernel: query rows (the last rows of the sequence)")
@@ -544,14 +544,25 @@ def run_kernel_case(args):
     """One public call on a synthetic single-kernel case: the last `rows` query rows of a
     `keys`-token sequence.  attn: sparse MLA attention (k=2048) over index rows from a top-k
     of Gaussian scores; indexer: FP8 materialised indexer scores; topk: top-2048 over those
-    scores (computed once, outside the timed call); ixtopk: FP8 indexer + top-k."""
+    scores (computed once, outside the timed call); ixtopk: FP8 indexer + top-k; quant: e4m3
+    quantisation of `rows` query tokens of the indexer (64 heads x 128 dims, one scale per
+    token) into a cache."""
     import long_context_sparse_tcgen05_gb300 as dsa
     from long_context_sparse_tcgen05_gb300 import build
     build.build()
     dsa.load_library()
     dev = torch.device("cuda:0")
     T, S = args.rows, args.keys
-    if args.kernel == "attn":
+    if args.kernel == "quant":
+        width = 64 * 128
+        g = torch.Generator(device=dev)
+        g.manual_seed(synth.SEED_BASE + 17)
+        x = torch.randn((1, T, width), generator=g, device=dev).to(torch.bfloat16)
+        codes = torch.empty((1, T, width), dtype=torch.uint8, device=dev)
+        scales = torch.empty((1, T), dtype=torch.float32, device=dev)
+        fn = lambda: dsa.dsa_quantize_e4m3_append(x, codes, scales)
+        work = f"{T * (3 * width + 4) / 1e9:.3f} GB moved"
+    elif args.kernel == "attn":
         wl = synth.WORKLOADS["prefill_16k"].replace(T=T, S=S, q_pos0=S - T)
         at = synth.attn_inputs(wl, 0, dev)
         sc = synth.scores_input(T, S, dev, "normal", seed=5)

@@ -212,6 +212,27 @@ dsa_status indexshare_schedule_score(const double* overlap, int32_t n, const cha
 dsa_status indexshare_schedule_search(const double* overlap, int32_t n, int32_t n_full,
                                       char* schedule_out, double* score_out);
 
+/* FP8 e4m3 quantisation with one fp32 scale per row, appended into an indexer cache (the
+ * step before the FP8 indexer, which reads e4m3 codes with per-token scales: IndexCache notes,
+ * section 1, "few heads, low-rank, FP8").  For each new row of `width` values:
+ * scale = amax / 448 over the row (1 when every value is 0) and code = e4m3(x / scale), the
+ * e4m3 value nearest to the fp32 quotient (ties to even), saturated to +-448; the scale and
+ * the quotient are fp32 roundings (IEEE division).  A dequantised value is scale * code.
+ *   x          [B, n, width] bf16; sequence b starts at x + b * x_stride_b (elements), its n
+ *              rows contiguous.  8-byte aligned; x_stride_b a multiple of 4.
+ *   codes      [B, S_cap, width] e4m3 cache (4-byte aligned); new row i of sequence b is
+ *              written to row pos_b + i.
+ *   scales     [B, S_cap] fp32 (4-byte aligned), same rows.
+ *   positions  DEVICE int64 [B] giving pos_b, or NULL for pos_b = pos0 in every sequence.
+ * width: a multiple of 4 in [4, 65536] -- d_I for the key cache (one scale per key), H_I * d_I
+ * for queries (one scale per token over all heads).  With positions NULL, pos0 + n <= S_cap
+ * is checked on the host; a device position outside [0, S_cap - n] skips that sequence and
+ * raises DSA_FLAG_BAD_INDEX.  Needs DSA_WS_MIN bytes of workspace (the flag word). */
+dsa_status dsa_quantize_e4m3_append(const void* x, int32_t B, int32_t n, int32_t width,
+                                    int64_t x_stride_b, uint8_t* codes, float* scales,
+                                    int32_t S_cap, int64_t pos0, const int64_t* positions,
+                                    void* ws, size_t ws_bytes, void* stream);
+
 /* Reads the device flag word of a workspace into *flags_out (host) and clears it.
  * Synchronises `stream`. */
 dsa_status dsa_read_device_flags(void* ws, uint32_t* flags_out, void* stream);

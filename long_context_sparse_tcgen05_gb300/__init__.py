@@ -14,6 +14,7 @@ Calls (same names as the C ABI):
   topk_overlap_matrix(bufs)               -> (n x n mean overlaps, counts [rows,n,n] or None)
   indexshare_schedule_score(M, schedule)  -> float (host only)
   indexshare_schedule_search(M, n_full)   -> (schedule str, score) (host only)
+  dsa_quantize_e4m3_append(x, codes, scales, pos0 | positions) -> e4m3 rows + scales in a cache
 Operand dicts use the keys produced by ``synth``: an indexer dict holds q, w, k, q_scale,
 k_scale, q_pos0, diag; an attention dict holds q, k, v (None: latent KV), d_v, scale.
 """
@@ -107,6 +108,9 @@ def load_library(path: str = LIB_PATH):
             lib.indexshare_schedule_search.restype = S
             lib.indexshare_schedule_search.argtypes = [_c.POINTER(_c.c_double), _c.c_int32, _c.c_int32,
                                                        _c.c_char_p, _c.POINTER(_c.c_double)]
+            lib.dsa_quantize_e4m3_append.restype = S
+            lib.dsa_quantize_e4m3_append.argtypes = [_P, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int64, _P, _P,
+                                                     _c.c_int32, _c.c_int64, _P, _P, _c.c_size_t, _P]
             lib.dsa_read_device_flags.restype = S
             lib.dsa_read_device_flags.argtypes = [_P, _c.POINTER(_c.c_uint32), _P]
             lib.dsa_status_string.restype = _c.c_char_p
@@ -359,6 +363,25 @@ def indexshare_schedule_search(M, n_full: int):
     return buf.value.decode(), v.value
 
 
+def dsa_quantize_e4m3_append(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, pos0: int = 0,
+                             positions: torch.Tensor | None = None):
+    """Quantise x [B, n, width] bf16 to e4m3 with one fp32 scale per row and write the rows into
+    codes [B, S_cap, width] (uint8 or float8_e4m3fn) / scales [B, S_cap] at row pos0 (or at
+    positions[b], an int64 device tensor [B]) of every sequence."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 3 and x.stride(2) == 1 and x.stride(1) == x.shape[2]
+    assert codes.dtype in (torch.uint8, torch.float8_e4m3fn) and codes.is_contiguous()
+    assert scales.dtype == torch.float32 and scales.is_contiguous()
+    B, n, width = x.shape
+    assert codes.shape[0] == B and codes.shape[2] == width and scales.shape == codes.shape[:2]
+    if positions is not None:
+        assert positions.dtype == torch.int64 and positions.numel() == B and positions.is_contiguous()
+    ws = workspace(WS_MIN, x.device)
+    _check(load_library().dsa_quantize_e4m3_append(_ptr(x), B, n, width, x.stride(0), _ptr(codes), _ptr(scales),
+                                                   codes.shape[1], int(pos0), _ptr(positions), _ptr(ws),
+                                                   ws.numel(), _stream()))
+    return codes, scales
+
+
 def launch_count() -> int:
     """Kernels launched by the library since it was loaded."""
     return int(load_library().dsa_launch_count())
@@ -401,6 +424,7 @@ def read_device_flags(device=None) -> int:
 __all__ = [
     "indexer_scores", "dsa_topk", "dsa_sparse_attn", "indexshare_group_forward", "topk_overlap",
     "topk_overlap_matrix", "indexshare_schedule_score", "indexshare_schedule_search",
+    "dsa_quantize_e4m3_append",
     "read_device_flags", "workspace", "workspace_size", "load_library", "DsaError",
     "IndexerArgs", "AttnArgs", "TopkSrc", "Layer",
 ]

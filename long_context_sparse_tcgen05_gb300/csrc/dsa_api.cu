@@ -341,6 +341,40 @@ dsa_status topk_overlap_matrix(const int32_t* const* bufs, int32_t n, int32_t ro
   return DSA_OK;
 }
 
+dsa_status dsa_quantize_e4m3_append(const void* x, int32_t B, int32_t n, int32_t width, int64_t x_stride_b,
+                                    uint8_t* codes, float* scales, int32_t S_cap, int64_t pos0,
+                                    const int64_t* positions, void* ws, size_t ws_bytes, void* stream) {
+  if (!x || !codes || !scales) return fail(DSA_ERR_INVALID_ARG, "x, codes and scales must be non-NULL");
+  if (B < 1 || n < 0 || S_cap < 1) return fail(DSA_ERR_INVALID_ARG, "B >= 1, n >= 0 and S_cap >= 1 are required");
+  if (width < 4 || width > 65536 || width % 4)
+    return fail(DSA_ERR_UNSUPPORTED, "width = %d; a multiple of 4 in [4, 65536] is required", width);
+  if (x_stride_b < (int64_t)n * width)
+    return fail(DSA_ERR_INVALID_ARG, "x_stride_b = %lld is smaller than n * width", (long long)x_stride_b);
+  if ((reinterpret_cast<uintptr_t>(x) & 7u) || (x_stride_b & 3) || (reinterpret_cast<uintptr_t>(codes) & 3u) ||
+      (reinterpret_cast<uintptr_t>(scales) & 3u))
+    return fail(DSA_ERR_MISALIGNED, "x needs 8-byte alignment (and x_stride_b a multiple of 4), codes and "
+                                    "scales 4-byte alignment");
+  if (!positions && (pos0 < 0 || pos0 > (int64_t)S_cap - n))
+    return fail(DSA_ERR_INVALID_ARG, "rows [%lld, %lld) fall outside the cache of %d rows", (long long)pos0,
+                (long long)pos0 + n, S_cap);
+  dsa_status s = check_ws(ws, ws_bytes, DSA_WS_MIN);
+  if (s != DSA_OK) return s;
+  dsa::QuantLaunch P{};
+  P.x = static_cast<const uint16_t*>(x);
+  P.B = B;
+  P.n = n;
+  P.width = width;
+  P.x_stride_b = x_stride_b;
+  P.codes = codes;
+  P.scales = scales;
+  P.S_cap = S_cap;
+  P.pos0 = pos0;
+  P.positions = positions;
+  P.flags = ws_flags(ws);
+  cudaError_t e = dsa::launch_quant_e4m3_rows(P, as_stream(stream));
+  return e == cudaSuccess ? DSA_OK : cuda_fail(e, "quantisation launch");
+}
+
 size_t topk_overlap_matrix_workspace_size(int32_t n) {
   const size_t nn = n > 0 ? (size_t)n * (size_t)n : 0;
   return dsa::kWsScratch + sizeof(double) * (dsa::kMaxOverlapLayers * dsa::kMaxOverlapLayers + dsa::kMaxOverlapCtas * nn);

@@ -136,4 +136,20 @@ struct OverlapMatrixLaunch {
 size_t overlap_matrix_smem(int n, int k);  // dynamic shared memory of one CTA
 cudaError_t launch_overlap_matrix(const OverlapMatrixLaunch& p, double* matrix_dev, cudaStream_t st);
 
+// Per-row e4m3 quantisation into a cache: rows (b, i) of x [B, n, width] bf16 (sequence stride
+// x_stride_b elements) go to row (b, pos_b + i) of codes [B, S_cap, width] and scales [B, S_cap],
+// pos_b = positions[b] (device) or pos0.
+struct QuantLaunch {
+  const uint16_t* x;
+  int B, n, width;
+  int64_t x_stride_b;
+  uint8_t* codes;
+  float* scales;
+  int S_cap;
+  int64_t pos0;
+  const int64_t* positions;
+  uint32_t* flags;
+};
+cudaError_t launch_quant_e4m3_rows(const QuantLaunch& p, cudaStream_t st);
+
 }  // namespace dsa

@@ -16,6 +16,8 @@ What it follows:
     shared layers keep their own queries, attention weights and outputs.
   * The score formula I[t,s] = sum_h w[t,h] * ReLU(q_I[t,h] . k_I[s]) is the project's
     statement of the indexer (the pages do not print one).
+  * IndexCache notes, section 1: the indexer runs in FP8; its operands are e4m3 codes with one
+    fp32 scale per token (the OCP E4M3 format, encoded and decoded here from its definition).
 
 The numeric work sits in ``dsa_oracle.c`` (plain loops, double precision); this module
 only marshals arrays and writes out the schedule walk.  Every function is pinned by
@@ -74,6 +76,10 @@ def _load():
             lib.orc_sparse_attn.argtypes = [_I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_double, _I64, _P, _P, _P, _I64, _P, _I64,
                                             _P, ctypes.c_int, _P, _P]
+            lib.orc_encode_e4m3.restype = ctypes.c_uint8
+            lib.orc_encode_e4m3.argtypes = [ctypes.c_float]
+            lib.orc_encode_e4m3_array.argtypes = [_P, _P, _I64]
+            lib.orc_quantize_e4m3_rows.argtypes = [_P, _I64, ctypes.c_int, _P, _P]
             lib.orc_topk_overlap.restype = ctypes.c_double
             lib.orc_topk_overlap.argtypes = [_P, _P, _I64, ctypes.c_int, _P]
             _lib = lib
@@ -120,6 +126,25 @@ def e4m3_to_double(codes) -> np.ndarray:
     out = np.empty(c.size, dtype=np.float64)
     _load().orc_decode_e4m3(_ptr(c), _ptr(out), c.size)
     return out
+
+
+def encode_e4m3(values) -> np.ndarray:
+    """E4M3 codes of fp32 values: nearest representable value, ties to even, saturated."""
+    v = np.ascontiguousarray(np.asarray(values, dtype=np.float32).reshape(-1))
+    out = np.empty(v.size, dtype=np.uint8)
+    _load().orc_encode_e4m3_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def quantize_e4m3_rows(x, width: int):
+    """(codes uint8 [rows, width], scales fp32 [rows]) of bf16 rows: scale = amax / 448 per
+    row (1 for an all-zero row), code = e4m3(x / scale) in fp32."""
+    c = _raw(x, np.uint16).reshape(-1, width)
+    c = np.ascontiguousarray(c)
+    codes = np.empty(c.shape, dtype=np.uint8)
+    scales = np.empty(c.shape[0], dtype=np.float32)
+    _load().orc_quantize_e4m3_rows(_ptr(c), c.shape[0], width, _ptr(codes), _ptr(scales))
+    return codes, scales
 
 
 def visible(S: int, q_pos: int, diag: int = 0) -> int:

@@ -64,6 +64,55 @@ double orc_e4m3_to_double(uint8_t b) {
   return sign ? -v : v;
 }
 
+/* The E4M3 code of the representable value nearest to v, ties to the even mantissa,
+ * magnitudes beyond the largest finite value (448) saturated to it; NaN gives the NaN code.
+ * Representable magnitudes are m * 2^(e-3) for m in [8, 16) and exponent e in [-6, 8], and
+ * m * 2^-9 for m in [0, 8) (subnormals). */
+uint8_t orc_encode_e4m3(float v) {
+  if (v != v) return 0x7F;
+  const uint8_t sign = signbit(v) ? 0x80 : 0;
+  const double a = fabs((double)v);
+  if (a >= 448.0) return sign | 0x7E;
+  int e;
+  frexp(a, &e); /* a in [2^(e-1), 2^e) */
+  int ex = e - 1;
+  if (ex < -6) ex = -6;
+  const double quantum = ldexp(1.0, ex - 3);
+  const double r = nearbyint(a / quantum) * quantum; /* default rounding: ties to even */
+  if (r == 0.0) return sign;
+  if (r < ldexp(1.0, -6)) return sign | (uint8_t)(r / ldexp(1.0, -9));
+  int e2;
+  frexp(r, &e2);
+  const int E = e2 - 1; /* r in [2^E, 2^(E+1)) */
+  const int mant = (int)((r / ldexp(1.0, E) - 1.0) * 8.0);
+  return sign | (uint8_t)(((E + 7) << 3) | mant);
+}
+
+void orc_encode_e4m3_array(const float* src, uint8_t* dst, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) dst[i] = orc_encode_e4m3(src[i]);
+}
+
+/* Per-row FP8 quantisation as the FP8 indexer consumes it (one scale per token row):
+ * scale = amax / 448 (1 for an all-zero row), code = e4m3(x / scale); the scale and the
+ * quotient are fp32 roundings (C float arithmetic). */
+void orc_quantize_e4m3_rows(const uint16_t* x, int64_t rows, int width, uint8_t* codes, float* scales) {
+  for (int64_t r = 0; r < rows; ++r) {
+    const uint16_t* xr = x + r * (int64_t)width;
+    float amax = 0.0f;
+    for (int j = 0; j < width; ++j) {
+      const float v = (float)orc_bf16_to_double(xr[j]);
+      if (fabsf(v) > amax) amax = fabsf(v);
+    }
+    const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int j = 0; j < width; ++j) {
+      const float v = (float)orc_bf16_to_double(xr[j]);
+      const float y = v / scale;
+      codes[r * (int64_t)width + j] = orc_encode_e4m3(y);
+    }
+    scales[r] = scale;
+  }
+}
+
 void orc_decode_bf16(const uint16_t* src, double* dst, int64_t n) {
   for (int64_t i = 0; i < n; ++i) dst[i] = orc_bf16_to_double(src[i]);
 }

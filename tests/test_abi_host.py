@@ -249,3 +249,28 @@ def test_schedule_validation(lib):
         with pytest.raises(dsa.DsaError) as e:
             dsa.indexshare_schedule_search(M, n_full)
         assert e.value.status == INVALID
+
+
+def test_quantize_append_validation(lib):
+    P = ctypes.c_void_p
+
+    def call(x=FAKE, B=2, n=3, width=128, stride=384, codes=FAKE, scales=FAKE, S_cap=10, pos0=0,
+             positions=None, ws_bytes=1 << 20):
+        return lib.dsa_quantize_e4m3_append(P(x) if x else None, B, n, width, stride, P(codes) if codes else None,
+                                            P(scales) if scales else None, S_cap, pos0,
+                                            P(positions) if positions else None, P(FAKE), ws_bytes, None)
+
+    assert call(x=0) == INVALID
+    assert call(codes=0) == INVALID
+    assert call(scales=0) == INVALID
+    assert call(B=0) == INVALID
+    assert call(S_cap=0) == INVALID
+    assert call(width=130, stride=390) == UNSUPPORTED
+    assert call(width=65540, stride=3 * 65540) == UNSUPPORTED
+    assert call(stride=383) == INVALID
+    assert call(x=FAKE + 4) == MISALIGNED
+    assert call(stride=386) == MISALIGNED
+    assert call(codes=FAKE + 2) == MISALIGNED
+    assert call(pos0=8) == INVALID          # rows 8..10 do not fit 10
+    assert call(pos0=-1) == INVALID
+    assert call(ws_bytes=100) == WORKSPACE

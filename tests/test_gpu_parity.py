@@ -385,3 +385,55 @@ def test_topk_overlap_matrix_flags_rows_not_in_topk_form():
         assert dsa.read_device_flags() & dsa.FLAG_UNSORTED
     dsa.topk_overlap_matrix([good, good])
     assert dsa.read_device_flags() == 0
+
+
+# --- FP8 quantisation into a cache ---------------------------------------------------------
+
+def _quant_rows(B, n, width, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(B, n, width, generator=g) * torch.exp2(torch.randint(-18, 14, (B, n, 1), generator=g).float())
+    x[0, 0] = 0.0                      # an all-zero row: scale 1, codes 0
+    if n > 1:
+        x[-1, 1, ::3] = 0.0
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("B,n,width,S_cap,pos0", [(3, 5, 128, 20, 7), (2, 4, 8192, 4, 0), (1, 9, 4, 9, 0),
+                                                  (4, 3, 132, 11, 8), (32, 1, 128, 200001, 200000)])
+def test_quantize_e4m3_append_matches_oracle(B, n, width, S_cap, pos0):
+    xb = _quant_rows(B, n, width, seed=width + n)
+    codes = torch.full((B, S_cap, width), 0x55, dtype=torch.uint8, device=DEV)
+    scales = torch.full((B, S_cap), -7.0, dtype=torch.float32, device=DEV)
+    dsa.dsa_quantize_e4m3_append(xb.to(DEV), codes, scales, pos0=pos0)
+    assert dsa.read_device_flags() == 0
+    want_c, want_s = oracle.quantize_e4m3_rows(xb.reshape(-1, width), width)
+    got_c = codes[:, pos0:pos0 + n].reshape(-1, width).cpu().numpy()
+    got_s = scales[:, pos0:pos0 + n].reshape(-1).cpu().numpy()
+    assert np.array_equal(got_c, want_c)
+    assert np.array_equal(got_s, want_s)
+    # nothing outside the appended rows is touched
+    mask = torch.ones(S_cap, dtype=torch.bool)
+    mask[pos0:pos0 + n] = False
+    assert bool((codes[:, mask.to(DEV)] == 0x55).all()) and bool((scales[:, mask.to(DEV)] == -7.0).all())
+
+
+def test_quantize_e4m3_append_per_sequence_positions_and_bad_position():
+    B, n, width, S_cap = 4, 2, 128, 10
+    xb = _quant_rows(B, n, width, seed=77)
+    codes = torch.zeros((B, S_cap, width), dtype=torch.uint8, device=DEV)
+    scales = torch.zeros((B, S_cap), dtype=torch.float32, device=DEV)
+    pos = torch.tensor([0, 8, 3, 9], dtype=torch.int64, device=DEV)  # 9 + 2 > 10: skipped, flagged
+    dsa.read_device_flags()
+    dsa.dsa_quantize_e4m3_append(xb.to(DEV), codes, scales, positions=pos)
+    assert dsa.read_device_flags() & dsa.FLAG_BAD_INDEX
+    want_c, want_s = oracle.quantize_e4m3_rows(xb.reshape(-1, width), width)
+    want_c = want_c.reshape(B, n, width)
+    want_s = want_s.reshape(B, n)
+    for b, p in enumerate([0, 8, 3]):
+        assert np.array_equal(codes[b, p:p + n].cpu().numpy(), want_c[b])
+        assert np.array_equal(scales[b, p:p + n].cpu().numpy(), want_s[b])
+    assert int(codes[3].count_nonzero()) == 0 and int(scales[3].count_nonzero()) == 0
+    # the codes feed the FP8 indexer: e4m3 view, dequantised = scale * code
+    deq = codes[0, :n].view(torch.float8_e4m3fn).float() * scales[0, :n, None]
+    ref = xb[0].to(DEV).float()
+    assert bool(((deq - ref).abs() <= ref.abs().amax(-1, keepdim=True) / 16).all())

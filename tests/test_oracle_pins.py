@@ -399,3 +399,50 @@ def test_schedule_search_hand_worked():
     # three full layers: FFFS (1+1+1+0.7)/4 = 0.925, FSFF (1+0.9+1+1)/4 = 0.975, FFSF 0.9
     best, arg = oracle.schedule_search(HAND_M, 3)
     assert arg == ["FSFF"] and best == pytest.approx(0.975, abs=1e-15)
+
+
+# --- FP8 quantisation ----------------------------------------------------------------------
+
+def _torch_e4m3(v):
+    """torch's own fp32 -> e4m3fn conversion (round to nearest even) after clamping to the
+    finite range: the library routine the encoder is pinned to."""
+    t = torch.as_tensor(np.asarray(v, dtype=np.float32))
+    return t.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_encoder_matches_torch_on_every_value_tie_and_range():
+    finite = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float()
+    finite = finite[torch.isfinite(finite)].numpy().astype(np.float32)
+    mags = np.unique(np.abs(finite))
+    mids = ((mags[1:].astype(np.float64) + mags[:-1]) / 2).astype(np.float32)  # exact ties
+    near = np.concatenate([np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1e9))])
+    g = np.random.default_rng(3)
+    rand = (g.standard_normal(20000) * np.exp2(g.integers(-14, 10, 20000))).astype(np.float32)
+    big = np.array([448.0, 449.0, 464.0, 465.0, 480.0, 1e6, 3.4e38], dtype=np.float32)
+    tiny = np.array([2.0 ** -10, 2.0 ** -11, 3 * 2.0 ** -11, 1e-30, 0.0], dtype=np.float32)
+    v = np.concatenate([finite, mids, -mids, near, -near, rand, big, -big, tiny, -tiny])
+    assert np.array_equal(oracle.encode_e4m3(v), _torch_e4m3(v))
+    # round trip: every finite code decodes and re-encodes to itself
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    assert np.array_equal(oracle.encode_e4m3(oracle.e4m3_to_double(codes)), codes)
+
+
+def test_row_quantiser_matches_torch_ops():
+    g = torch.Generator().manual_seed(8)
+    rows, width = 64, 136
+    x = torch.randn(rows, width, generator=g) * torch.exp2(torch.randint(-20, 12, (rows, 1), generator=g).float())
+    x[5] = 0.0
+    x[9, :] = 0.0
+    x[9, 3] = -2.0 ** -30
+    xb = x.to(torch.bfloat16)
+    codes, scales = oracle.quantize_e4m3_rows(xb, width)
+    xf = xb.float()
+    amax = xf.abs().amax(-1)
+    sc = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    want = (xf / sc[:, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(scales, sc.numpy())
+    assert np.array_equal(codes, want)
+    assert scales[5] == 1.0 and np.all(codes[5] == 0)
+    # dequantised rows keep their largest magnitude: amax maps to the code of 448
+    big = np.abs(xf.numpy()).argmax(1)
+    assert np.all((codes[np.arange(rows), big] & 0x7F)[amax.numpy() > 0] == 0x7E)
