@@ -399,7 +399,9 @@ def _quant_rows(B, n, width, seed):
 
 
 @pytest.mark.parametrize("B,n,width,S_cap,pos0", [(3, 5, 128, 20, 7), (2, 4, 8192, 4, 0), (1, 9, 4, 9, 0),
-                                                  (4, 3, 132, 11, 8), (32, 1, 128, 200001, 200000)])
+                                                  (4, 3, 132, 11, 8), (32, 1, 128, 200001, 200000),
+                                                  (2, 3, 1000, 5, 1), (2, 2, 2048, 2, 0), (3, 70, 5000, 80, 3),
+                                                  (1, 2, 8196, 3, 1)])
 def test_quantize_e4m3_append_matches_oracle(B, n, width, S_cap, pos0):
     xb = _quant_rows(B, n, width, seed=width + n)
     codes = torch.full((B, S_cap, width), 0x55, dtype=torch.uint8, device=DEV)
