@@ -277,7 +277,7 @@ def run_ours(args, rank, world, local):
     build.build()
     dsa.load_library()
     wl = synth.WORKLOADS[args.workload]
-    layers = [synth.layer_inputs(wl, l, dev, with_indexer=True) for l in range(4)]
+    layers = synth.group_inputs(wl, 4, dev, with_indexer=True)
     group = [dict(ix=layers[0]["ix"], at=layers[l]["at"]) for l in range(4)]
     ws_need = dsa.workspace_size(layers[0]["ix"], wl.k)
     dsa.workspace(ws_need, dev)
@@ -378,7 +378,13 @@ def run_e2e(dsa, wl, layers, group, outs, lses, bufs, args, world):
     from indexer operands, then one attention call per layer over its index buffer)."""
     ix = layers[0]["ix"]
     ix_dev = [ix["q"], ix["k"], ix["w"], ix["q_scale"], ix["k_scale"]]
-    at_dev = [[g["at"]["q"], g["at"]["k"]] for g in group]
+    # each distinct device tensor goes in once, before the first layer that reads it (the
+    # draft steps of a multi-token-prediction layer share one cache)
+    seen = {ix["k"].data_ptr()}
+    at_dev = []
+    for g in group:
+        at_dev.append([t for t in (g["at"]["q"], g["at"]["k"]) if t.data_ptr() not in seen])
+        seen.update(t.data_ptr() for t in at_dev[-1])
     # host buffers of exactly the tensors' sizes, page-locked in place (the caching pinned
     # allocator would round each one up to a power of two: 131 GB locked instead of 75 GB)
     cudart = torch.cuda.cudart()

@@ -17,6 +17,9 @@ the workloads the project is measured on:
                          causal cache, FP8 indexer, correlated inputs, 16 layers.
 * ``heatmap_128k``       the 128K shapes over 16 layers run all-F, for the layer-overlap
                          heatmap: indexer inputs correlated in clusters of layers.
+* ``mtp_draft_b32_200k`` four draft steps of a multi-token-prediction layer over the 32 x
+                         200,000-token decode cache: every step has its own queries, all share
+                         the layer's caches (indexer keys and latent KV) and see the same keys.
 
 Every tensor is drawn from its own Philox stream, seeded by
 ``20261202 + 1000*workload_id + 10*layer + tensor_id``; tensors longer than one chunk are
@@ -61,6 +64,7 @@ class Workload:
     latent: bool        # True: V is the first DV columns of the KV row (one buffer)
     diag: int = 0       # keys s < q_pos + diag are visible
     clusters: tuple = ()  # "clustered" values: cluster id of each layer
+    shared_cache: bool = False  # every "layer" (draft step) reads layer 0's keys and KV
 
     @property
     def n_layers(self) -> int:
@@ -86,6 +90,8 @@ WORKLOADS = {
     "chunked_prefill_1m": Workload("chunked_prefill_1m", 4, 1, 4096, 1048576, 1048576 - 4096,
                                    64, 128, "e4m3", "correlated", 2048, "FSSS" * 4, 64, 576, 512,
                                    True),
+    "mtp_draft_b32_200k": Workload("mtp_draft_b32_200k", 6, 32, 1, 200000, 200000, 64, 128, "e4m3",
+                                   "gauss", 2048, "FSSS", 64, 576, 512, True, shared_cache=True),
     "heatmap_128k": Workload("heatmap_128k", 5, 1, 131072, 131072, 0, 64, 128, "e4m3", "clustered",
                              2048, "F" * 16, 64, 576, 512, True,
                              clusters=(0, 1, 1, 2, 2, 2, 3, 3, 3, 3, 3, 3, 3, 3, 3, 3)),
@@ -94,6 +100,11 @@ WORKLOADS = {
 
 def seed_of(wl: Workload, layer: int, tensor_id: int) -> int:
     return SEED_BASE + 1000 * wl.wid + 10 * layer + tensor_id
+
+
+def _cache_layer(wl: Workload, layer: int) -> int:
+    """Layer whose seeds draw this layer's keys and KV (layer 0 for a shared cache)."""
+    return 0 if wl.shared_cache else layer
 
 
 def _gen(device, seed: int) -> torch.Generator:
@@ -156,18 +167,18 @@ def indexer_inputs(wl: Workload, layer: int, device="cpu") -> dict:
     ws = (wl.B, wl.T, wl.HI)
     if wl.values == "int":
         q = _draw("int", qs, device, seed_of(wl, layer, T_Q_I), -3, 3)
-        k = _draw("int", ks, device, seed_of(wl, layer, T_K_I), -3, 3)
+        k = _draw("int", ks, device, seed_of(wl, _cache_layer(wl, layer), T_K_I), -3, 3)
         w = _draw("int", ws, device, seed_of(wl, layer, T_W), 1, 4)
     elif wl.values == "gauss":
         q = _draw("normal", qs, device, seed_of(wl, layer, T_Q_I))
-        k = _draw("normal", ks, device, seed_of(wl, layer, T_K_I))
+        k = _draw("normal", ks, device, seed_of(wl, _cache_layer(wl, layer), T_K_I))
         w = _draw("uniform", ws, device, seed_of(wl, layer, T_W)) / 8.0
     elif wl.values == "correlated":
         # shared base + 0.3 * independent per-layer noise; w is drawn once for all layers
         q = _draw("normal", qs, device, seed_of(wl, 0, T_BASE_Q_I))
         q += 0.3 * _draw("normal", qs, device, seed_of(wl, layer, T_Q_I))
         k = _draw("normal", ks, device, seed_of(wl, 0, T_BASE_K_I))
-        k += 0.3 * _draw("normal", ks, device, seed_of(wl, layer, T_K_I))
+        k += 0.3 * _draw("normal", ks, device, seed_of(wl, _cache_layer(wl, layer), T_K_I))
         w = _draw("uniform", ws, device, seed_of(wl, 0, T_W)) / 8.0
     elif wl.values == "clustered":
         # shared base + 0.3 * (unit-variance noise), the noise mixing a component drawn once
@@ -180,7 +191,7 @@ def indexer_inputs(wl: Workload, layer: int, device="cpu") -> dict:
         q += (0.3 * b) * _draw("normal", qs, device, seed_of(wl, layer, T_Q_I))
         k = _draw("normal", ks, device, seed_of(wl, 0, T_BASE_K_I))
         k += (0.3 * a) * _draw("normal", ks, device, seed_of(wl, c, T_CLUSTER_K_I))
-        k += (0.3 * b) * _draw("normal", ks, device, seed_of(wl, layer, T_K_I))
+        k += (0.3 * b) * _draw("normal", ks, device, seed_of(wl, _cache_layer(wl, layer), T_K_I))
         w = _draw("uniform", ws, device, seed_of(wl, 0, T_W)) / 8.0
     else:
         raise ValueError(wl.values)
@@ -203,19 +214,23 @@ def indexer_inputs(wl: Workload, layer: int, device="cpu") -> dict:
     return ix
 
 
-def attn_inputs(wl: Workload, layer: int, device="cpu") -> dict:
+def attn_inputs(wl: Workload, layer: int, device="cpu", kv_of=None) -> dict:
     """Attention operands of one layer: q [B,T,H,DQK] bf16 and either a latent KV
-    [B,S,DQK] (V = its first DV columns) or separate K [B,S,DQK] and V [B,S,DV]."""
+    [B,S,DQK] (V = its first DV columns) or separate K [B,S,DQK] and V [B,S,DV].  kv_of: an
+    attention dict whose KV tensors this layer shares (a shared cache) instead of drawing."""
     q = _draw("normal", (wl.B, wl.T, wl.H, wl.DQK), device, seed_of(wl, layer, T_Q))
     at = dict(q=q.to(torch.bfloat16).contiguous(), d_v=wl.DV, scale=wl.scale)
     del q
-    kv = _draw("normal", (wl.B, wl.S, wl.DQK), device, seed_of(wl, layer, T_KV))
+    if kv_of is not None:
+        at["k"], at["v"] = kv_of["k"], kv_of["v"]
+        return at
+    kv = _draw("normal", (wl.B, wl.S, wl.DQK), device, seed_of(wl, _cache_layer(wl, layer), T_KV))
     at["k"] = kv.to(torch.bfloat16).contiguous()
     del kv
     if wl.latent:
         at["v"] = None
     else:
-        v = _draw("normal", (wl.B, wl.S, wl.DV), device, seed_of(wl, layer, T_V))
+        v = _draw("normal", (wl.B, wl.S, wl.DV), device, seed_of(wl, _cache_layer(wl, layer), T_V))
         at["v"] = v.to(torch.bfloat16).contiguous()
     return at
 
@@ -255,12 +270,31 @@ def attn_rows(wl: Workload, layer: int, rows, device="cpu") -> dict:
     full KV; identical values to attn_inputs at those rows."""
     q = _draw_rows("normal", (wl.B, wl.T, wl.H, wl.DQK), device, seed_of(wl, layer, T_Q), rows)
     at = dict(q_rows=q.to(torch.bfloat16).contiguous(), d_v=wl.DV, scale=wl.scale, T=wl.T)
-    kv = _draw("normal", (wl.B, wl.S, wl.DQK), device, seed_of(wl, layer, T_KV))
+    kv = _draw("normal", (wl.B, wl.S, wl.DQK), device, seed_of(wl, _cache_layer(wl, layer), T_KV))
     at["k"] = kv.to(torch.bfloat16).contiguous()
     at["v"] = None
     if not wl.latent:
-        at["v"] = _draw("normal", (wl.B, wl.S, wl.DV), device, seed_of(wl, layer, T_V)).to(torch.bfloat16)
+        v = _draw("normal", (wl.B, wl.S, wl.DV), device, seed_of(wl, _cache_layer(wl, layer), T_V))
+        at["v"] = v.to(torch.bfloat16)
     return at
+
+
+def group_inputs(wl: Workload, n_layers: int, device="cpu", with_indexer=None) -> list:
+    """layer_inputs of layers 0 .. n_layers-1; with a shared cache the key and KV tensors of
+    layer 0 are reused by every layer (the values are identical; they are drawn once)."""
+    out = []
+    for l in range(n_layers):
+        if not wl.shared_cache or l == 0:
+            out.append(layer_inputs(wl, l, device, with_indexer))
+            continue
+        need_ix = wl.schedule[l] == "F" if with_indexer is None else with_indexer
+        ix = None
+        if need_ix:
+            ix = indexer_inputs(wl.replace(S=1), l, device)  # this step's queries only
+            src = out[0]["ix"] if out[0]["ix"] is not None else indexer_inputs(wl, 0, device)
+            ix["k"], ix["k_scale"] = src["k"], src["k_scale"]
+        out.append(dict(ix=ix, at=attn_inputs(wl, l, device, kv_of=out[0]["at"])))
+    return out
 
 
 def layer_inputs(wl: Workload, layer: int, device="cpu", with_indexer=None) -> dict:

@@ -38,10 +38,11 @@ def _subset_batches(d: dict, keys, bsel):
 
 
 @pytest.mark.parametrize("name,n_rows", [("tiny_l1k", 1024), ("prefill_16k", 48), ("prefill_128k", 24),
-                                         ("decode_b32_200k", 8), ("chunked_prefill_1m", 12)])
+                                         ("decode_b32_200k", 8), ("chunked_prefill_1m", 12),
+                                         ("mtp_draft_b32_200k", 8)])
 def test_workload_group_sampled_rows(name, n_rows):
     wl = synth.WORKLOADS[name]
-    layers = [synth.layer_inputs(wl, l, DEV) for l in range(4)]
+    layers = synth.group_inputs(wl, 4, DEV)
     outs, lses, bufs = dsa.indexshare_group_forward(layers, "FSSS", wl.k)
     torch.cuda.synchronize()
     assert dsa.read_device_flags() == 0

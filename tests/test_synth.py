@@ -50,3 +50,18 @@ def test_clustered_layers_share_noise_inside_a_cluster():
     assert abs(across - 1 / 1.09) < 0.01
     assert abs(corr(deq[2], deq[3]) - 1 / 1.09) < 0.01  # clusters 1 and 3
     assert abs(float(deq[3].std()) - 1.09 ** 0.5) < 0.02
+
+
+def test_shared_cache_steps_share_keys_and_kv_but_not_queries():
+    wl = synth.WORKLOADS["mtp_draft_b32_200k"].replace(B=2, S=300, q_pos0=300)
+    g = synth.group_inputs(wl, 4, with_indexer=True)
+    for l in range(1, 4):
+        assert g[l]["at"]["k"] is g[0]["at"]["k"] and g[l]["ix"]["k"] is g[0]["ix"]["k"]
+        assert not torch.equal(g[l]["at"]["q"], g[0]["at"]["q"])
+        assert not torch.equal(g[l]["ix"]["q"].view(torch.uint8), g[0]["ix"]["q"].view(torch.uint8))
+        # the same values layer_inputs draws for that step
+        one = synth.layer_inputs(wl, l, with_indexer=True)
+        assert torch.equal(one["at"]["k"], g[l]["at"]["k"]) and torch.equal(one["at"]["q"], g[l]["at"]["q"])
+        assert torch.equal(one["ix"]["q"].view(torch.uint8), g[l]["ix"]["q"].view(torch.uint8))
+        assert torch.equal(one["ix"]["k"].view(torch.uint8), g[l]["ix"]["k"].view(torch.uint8))
+        assert torch.equal(one["ix"]["q_scale"], g[l]["ix"]["q_scale"])
