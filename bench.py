@@ -52,6 +52,9 @@ def parse():
                          "(the case the committed ncu summaries are captured on)")
     ap.add_argument("--rows", type=int, default=2048, help="--kernel: query rows (the last rows of the sequence)")
     ap.add_argument("--keys", type=int, default=131072, help="--kernel/--heatmap: sequence length")
+    ap.add_argument("--varlen", action="store_true",
+                    help="one F,S,S,S group over eight packed prompts of 1K..64K tokens "
+                         "(indexshare_group_forward_varlen) against the same prompts one call each")
     ap.add_argument("--heatmap", action="store_true",
                     help="all-F pass over the 16 layers of heatmap_128k, the layer-overlap matrix, "
                          "the best schedule per number of full layers and measured group times")
@@ -714,6 +717,46 @@ def run_heatmap(args):
     print(json.dumps(line), flush=True)
 
 
+def run_varlen(args):
+    """Packed prompts of different lengths through one indexshare_group_forward_varlen call:
+    eight prefills of 64K, 32K, 16K, 8K, 8K, 4K, 2K and 1K tokens with the 128K workload's
+    operands (FP8 indexer, top-2,048, 64-head MLA), against one indexshare_group_forward call
+    per prompt."""
+    import long_context_sparse_tcgen05_gb300 as dsa
+    from long_context_sparse_tcgen05_gb300 import build
+    build.build()
+    dsa.load_library()
+    dev = torch.device("cuda:0")
+    lens = [65536, 32768, 16384, 8192, 8192, 4096, 2048, 1024]
+    base = synth.WORKLOADS["prefill_128k"]
+    wls = [base.replace(T=n, S=n, q_pos0=0, wid=30 + i) for i, n in enumerate(lens)]
+    per_seq = [synth.group_inputs(wl, 4, dev) for wl in wls]
+    packed = []
+    for l in range(4):
+        at = dict(per_seq[0][l]["at"])
+        at["q"] = torch.cat([p[l]["at"]["q"] for p in per_seq], dim=1)
+        at["k"] = torch.cat([p[l]["at"]["k"] for p in per_seq], dim=1)
+        ix = None
+        if GROUP[l] == "F":
+            ix = dict(per_seq[0][l]["ix"])
+            for key in ("q", "w", "q_scale", "k", "k_scale"):
+                ix[key] = torch.cat([p[l]["ix"][key] for p in per_seq], dim=1)
+        packed.append(dict(ix=ix, at=at))
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    q0 = [0] * len(lens)
+    packed_run = lambda: dsa.indexshare_group_forward_varlen(packed, GROUP, base.k, cu, cu, q0)
+    outs = [dsa.indexshare_group_forward(p, GROUP, base.k) for p in per_seq]  # buffers for the loop
+    loop_run = lambda: [dsa.indexshare_group_forward(p, GROUP, base.k, outs=o[0], lses=o[1], idx_bufs=o[2])
+                        for p, o in zip(per_seq, outs)]
+    t_packed = time_loop(packed_run, args.steps, max(3, args.warmup))
+    t_loop = time_loop(loop_run, args.steps, max(3, args.warmup))
+    tokens = sum(lens)
+    print(json.dumps({"varlen": {"lengths": lens, "tokens": tokens, "schedule": GROUP,
+                                 "packed_ms": round(t_packed, 3), "packed_tokens_per_s": round(tokens / t_packed * 1e3, 1),
+                                 "one_call_per_prompt_ms": round(t_loop, 3),
+                                 "device_flags": dsa.read_device_flags(dev)}}), flush=True)
+
+
 def main():
     args = parse()
     if args.kernel:
@@ -721,6 +764,9 @@ def main():
         return
     if args.heatmap:
         run_heatmap(args)
+        return
+    if args.varlen:
+        run_varlen(args)
         return
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":

@@ -165,6 +165,35 @@ dsa_status indexshare_group_forward(const dsa_layer* layers, int32_t n_layers,
                                     const char* schedule, int32_t k, int32_t* const* idx_bufs,
                                     void* ws, size_t ws_bytes, void* stream);
 
+/* Variable-length sequences packed along the row axis (host arrays).  Sequence b owns the
+ * packed query rows cu_q[b] .. cu_q[b+1]-1 and the packed key rows cu_k[b] .. cu_k[b+1]-1;
+ * its first query row sits at absolute position q_pos0[b] (a full prefill: q_pos0 = 0 with
+ * as many rows as keys; a chunk: the last rows of a longer cache).  cu_q and cu_k hold
+ * n_seqs + 1 non-decreasing entries starting at 0; every sequence has at least one key. */
+typedef struct {
+  int32_t n_seqs;
+  const int64_t* cu_q;
+  const int64_t* cu_k;
+  const int64_t* q_pos0;
+} dsa_varlen;
+
+/* indexshare_group_forward over packed variable-length sequences (batched serving of
+ * prompts of different lengths; the pages describe one sequence at a time, so this only
+ * extends the boundary).  Every layer's operands describe the packed tensors as one
+ * sequence: B = 1, T = cu_q[n_seqs] query rows, S = cu_k[n_seqs] key rows (q, w, q_scale,
+ * out, lse and each idx_bufs[f] [1,T,k] packed by query row; k, k_scale and the KV packed
+ * by key row); the indexer's own q_pos0 is ignored.  Each sequence runs the schedule on
+ * its own rows and keys -- its scores, selections and attention never reach another
+ * sequence -- with the results of indexshare_group_forward on that sequence alone.  Every
+ * sequence's view is checked (shapes, alignment of its offsets, workspace) before anything
+ * launches; sequences with no query rows are skipped.  ws: at least
+ * dsa_workspace_size_varlen bytes are preferred (the largest sequence's need). */
+dsa_status indexshare_group_forward_varlen(const dsa_layer* layers, int32_t n_layers,
+                                           const char* schedule, int32_t k,
+                                           const dsa_varlen* seqs, int32_t* const* idx_bufs,
+                                           void* ws, size_t ws_bytes, void* stream);
+size_t dsa_workspace_size_varlen(const dsa_indexer_args* ix, const dsa_varlen* seqs, int32_t k);
+
 /* Overlap of two index buffers a, b [rows,k] (rows as written by dsa_topk: ascending valid
  * entries, then -1 padding): per_row[r] = |A_r and B_r| / |A_r| over valid entries (1 when
  * A_r is empty), fp32 device array or NULL; *mean_out (host) = mean over rows in double.

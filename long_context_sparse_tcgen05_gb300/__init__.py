@@ -10,6 +10,7 @@ Calls (same names as the C ABI):
   dsa_topk(k, ix=... | scores=...)        -> int32 idx [B,T,k]
   dsa_sparse_attn(at, idx)                -> (out [B,T,H,d_v] bf16, lse [B,T,H] fp32)
   indexshare_group_forward(layers, schedule, k) -> (outs, lses, idx_bufs)
+  indexshare_group_forward_varlen(layers, schedule, k, cu_q, cu_k, q_pos0) -> same, packed rows
   topk_overlap(a, b)                      -> (per_row fp32, mean float)
   topk_overlap_matrix(bufs)               -> (n x n mean overlaps, counts [rows,n,n] or None)
   indexshare_schedule_score(M, schedule)  -> float (host only)
@@ -59,6 +60,11 @@ class Layer(_c.Structure):
     _fields_ = [("ix", IndexerArgs), ("at", AttnArgs), ("out", _P), ("lse", _P)]
 
 
+class Varlen(_c.Structure):
+    _fields_ = [("n_seqs", _c.c_int32), ("cu_q", _c.POINTER(_c.c_int64)), ("cu_k", _c.POINTER(_c.c_int64)),
+                ("q_pos0", _c.POINTER(_c.c_int64))]
+
+
 class DsaError(RuntimeError):
     def __init__(self, status: int, msg: str):
         super().__init__(f"{status_string(status)}: {msg}")
@@ -94,6 +100,11 @@ def load_library(path: str = LIB_PATH):
             lib.indexshare_group_forward.argtypes = [_c.POINTER(Layer), _c.c_int32, _c.c_char_p,
                                                      _c.c_int32, _c.POINTER(_P), _P, _c.c_size_t,
                                                      _P]
+            lib.indexshare_group_forward_varlen.restype = S
+            lib.indexshare_group_forward_varlen.argtypes = [_c.POINTER(Layer), _c.c_int32, _c.c_char_p, _c.c_int32,
+                                                            _c.POINTER(Varlen), _c.POINTER(_P), _P, _c.c_size_t, _P]
+            lib.dsa_workspace_size_varlen.restype = _c.c_size_t
+            lib.dsa_workspace_size_varlen.argtypes = [_c.POINTER(IndexerArgs), _c.POINTER(Varlen), _c.c_int32]
             lib.topk_overlap.restype = S
             lib.topk_overlap.argtypes = [_P, _P, _c.c_int32, _c.c_int32, _P,
                                          _c.POINTER(_c.c_double), _P, _c.c_size_t, _P]
@@ -265,11 +276,7 @@ def dsa_sparse_attn(at: dict, idx: torch.Tensor, out: torch.Tensor | None = None
     return out, lse
 
 
-def indexshare_group_forward(layers, schedule: str, k: int, outs=None, lses=None, idx_bufs=None,
-                             with_lse: bool = True):
-    """Run an F/S schedule over `layers` (dicts with 'ix' (F layers) and 'at').
-
-    Returns (outs, lses, idx_bufs): per-layer outputs and LSEs, one idx buffer per F layer."""
+def _group_structs(layers, schedule: str, k: int, outs, lses, idx_bufs, with_lse: bool):
     lib = load_library()
     n = len(layers)
     arr = (Layer * n)()
@@ -296,9 +303,42 @@ def indexshare_group_forward(layers, schedule: str, k: int, outs=None, lses=None
         arr[i].out = outs[i].data_ptr()
         arr[i].lse = lses[i].data_ptr() if lses[i] is not None else None
     bufs = (_P * max(1, n_full))(*[b.data_ptr() for b in idx_bufs])
+    return arr, bufs, need, outs, lses, idx_bufs, dev
+
+
+def indexshare_group_forward(layers, schedule: str, k: int, outs=None, lses=None, idx_bufs=None,
+                             with_lse: bool = True):
+    """Run an F/S schedule over `layers` (dicts with 'ix' (F layers) and 'at').
+
+    Returns (outs, lses, idx_bufs): per-layer outputs and LSEs, one idx buffer per F layer."""
+    arr, bufs, need, outs, lses, idx_bufs, dev = _group_structs(layers, schedule, k, outs, lses, idx_bufs,
+                                                                with_lse)
     ws = workspace(need, dev)
-    _check(lib.indexshare_group_forward(arr, n, schedule.encode(), k, bufs, _ptr(ws), ws.numel(),
-                                        _stream()))
+    _check(load_library().indexshare_group_forward(arr, len(layers), schedule.encode(), k, bufs, _ptr(ws),
+                                                   ws.numel(), _stream()))
+    return outs, lses, idx_bufs
+
+
+def indexshare_group_forward_varlen(layers, schedule: str, k: int, cu_q, cu_k, q_pos0, outs=None, lses=None,
+                                    idx_bufs=None, with_lse: bool = True):
+    """indexshare_group_forward over sequences packed along the row axis: the layers' tensors
+    are [1, total rows, ...] (queries, weights, outputs) and [1, total keys, ...] (keys, KV);
+    sequence b owns query rows cu_q[b]:cu_q[b+1] and key rows cu_k[b]:cu_k[b+1], its first
+    query at position q_pos0[b] (host integer sequences)."""
+    lib = load_library()
+    n_seqs = len(q_pos0)
+    cq = (_c.c_int64 * (n_seqs + 1))(*[int(x) for x in cu_q])
+    ck = (_c.c_int64 * (n_seqs + 1))(*[int(x) for x in cu_k])
+    qp = (_c.c_int64 * n_seqs)(*[int(x) for x in q_pos0])
+    seqs = Varlen(n_seqs, cq, ck, qp)
+    arr, bufs, _, outs, lses, idx_bufs, dev = _group_structs(layers, schedule, k, outs, lses, idx_bufs, with_lse)
+    need = WS_MIN
+    for i, l in enumerate(layers):
+        if schedule[i] == "F" and l.get("ix") is not None:
+            need = max(need, int(lib.dsa_workspace_size_varlen(_c.byref(arr[i].ix), _c.byref(seqs), k)))
+    ws = workspace(need, dev)
+    _check(lib.indexshare_group_forward_varlen(arr, len(layers), schedule.encode(), k, _c.byref(seqs), bufs,
+                                               _ptr(ws), ws.numel(), _stream()))
     return outs, lses, idx_bufs
 
 
@@ -424,7 +464,7 @@ def read_device_flags(device=None) -> int:
 __all__ = [
     "indexer_scores", "dsa_topk", "dsa_sparse_attn", "indexshare_group_forward", "topk_overlap",
     "topk_overlap_matrix", "indexshare_schedule_score", "indexshare_schedule_search",
-    "dsa_quantize_e4m3_append",
+    "dsa_quantize_e4m3_append", "indexshare_group_forward_varlen", "Varlen",
     "read_device_flags", "workspace", "workspace_size", "load_library", "DsaError",
     "IndexerArgs", "AttnArgs", "TopkSrc", "Layer",
 ]

@@ -3,7 +3,9 @@
 // the caller.
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -242,8 +244,11 @@ dsa_status dsa_sparse_attn(const dsa_attn_args* at, const int32_t* idx, int32_t 
   return e == cudaSuccess ? DSA_OK : cuda_fail(e, "attention launch");
 }
 
-dsa_status indexshare_group_forward(const dsa_layer* layers, int32_t n_layers, const char* schedule, int32_t k,
-                                    int32_t* const* idx_bufs, void* ws, size_t ws_bytes, void* stream) {
+namespace {
+
+// Validation of one group call: every layer, the schedule and the buffers; nothing launches.
+dsa_status group_check(const dsa_layer* layers, int32_t n_layers, const char* schedule, int32_t k,
+                       int32_t* const* idx_bufs, void* ws, size_t ws_bytes) {
   if (!layers || n_layers <= 0) return fail(DSA_ERR_INVALID_ARG, "no layers");
   if (!schedule) return fail(DSA_ERR_SCHEDULE, "schedule is NULL");
   if ((int32_t)strlen(schedule) != n_layers)
@@ -257,7 +262,6 @@ dsa_status indexshare_group_forward(const dsa_layer* layers, int32_t n_layers, c
   if (!idx_bufs) return fail(DSA_ERR_INVALID_ARG, "idx_bufs is NULL");
   if (k < 1 || k > kMaxK) return fail(DSA_ERR_UNSUPPORTED, "k=%d outside [1, %d]", k, kMaxK);
   dsa_status s;
-  // Validate every layer before launching anything.
   const dsa_attn_args& a0 = layers[0].at;
   for (int i = 0; i < n_layers; ++i) {
     const dsa_layer& L = layers[i];
@@ -273,8 +277,13 @@ dsa_status indexshare_group_forward(const dsa_layer* layers, int32_t n_layers, c
   }
   for (int f = 0; f < n_full; ++f)
     if (!idx_bufs[f]) return fail(DSA_ERR_INVALID_ARG, "idx_bufs[%d] is NULL", f);
-  if ((s = check_ws(ws, ws_bytes, DSA_WS_MIN)) != DSA_OK) return s;
+  return check_ws(ws, ws_bytes, DSA_WS_MIN);
+}
 
+// The schedule walk of a checked group.
+dsa_status group_run(const dsa_layer* layers, int32_t n_layers, const char* schedule, int32_t k,
+                     int32_t* const* idx_bufs, void* ws, size_t ws_bytes, void* stream) {
+  dsa_status s;
   cudaStream_t st = as_stream(stream);
   const int32_t* cur = nullptr;
   int f = 0;
@@ -289,6 +298,105 @@ dsa_status indexshare_group_forward(const dsa_layer* layers, int32_t n_layers, c
     if ((s = dsa_sparse_attn(&L.at, cur, k, L.out, L.lse, ws, ws_bytes, stream)) != DSA_OK) return s;
   }
   return DSA_OK;
+}
+
+// Sequence b of a packed group as a one-sequence group: every pointer advanced to its first
+// query row / key row, T and S its own, its indexer queries at q_pos0[b].
+void varlen_view(const dsa_layer* layers, int32_t n_layers, const char* schedule, int32_t k, const dsa_varlen* v,
+                 int b, int32_t* const* idx_bufs, std::vector<dsa_layer>& out, std::vector<int32_t*>& bufs) {
+  const int64_t q0 = v->cu_q[b], k0 = v->cu_k[b];
+  const int32_t T = (int32_t)(v->cu_q[b + 1] - q0), S = (int32_t)(v->cu_k[b + 1] - k0);
+  out.assign(layers, layers + n_layers);
+  int f = 0;
+  bufs.clear();
+  for (int i = 0; i < n_layers; ++i) {
+    dsa_layer& L = out[i];
+    dsa_attn_args& a = L.at;
+    a.T = T;
+    a.S = S;
+    a.q = static_cast<const uint16_t*>(a.q) + q0 * a.H * a.d_qk;
+    a.k = static_cast<const uint16_t*>(a.k) + k0 * a.k_ld;
+    a.v = a.v ? static_cast<const uint16_t*>(a.v) + k0 * a.v_ld : a.v;
+    L.out = static_cast<uint16_t*>(L.out) + q0 * a.H * a.d_v;
+    if (L.lse) L.lse += q0 * a.H;
+    if (schedule[i] == 'F') {
+      dsa_indexer_args& x = L.ix;
+      const int64_t elt = x.dtype == DSA_E4M3 ? 1 : 2;
+      x.T = T;
+      x.S = S;
+      x.q = static_cast<const uint8_t*>(x.q) + q0 * x.H_I * x.d_I * elt;
+      if (x.q_scale) x.q_scale += q0;
+      x.w += q0 * x.H_I;
+      x.k = static_cast<const uint8_t*>(x.k) + k0 * x.d_I * elt;
+      if (x.k_scale) x.k_scale += k0;
+      x.q_pos0 = v->q_pos0[b];
+      bufs.push_back(idx_bufs[f++] + q0 * k);
+    }
+  }
+}
+
+dsa_status check_varlen(const dsa_layer* layers, const dsa_varlen* v) {
+  if (!v || v->n_seqs < 1 || !v->cu_q || !v->cu_k || !v->q_pos0)
+    return fail(DSA_ERR_INVALID_ARG, "seqs needs n_seqs >= 1 and the cu_q, cu_k and q_pos0 arrays");
+  if (v->cu_q[0] != 0 || v->cu_k[0] != 0) return fail(DSA_ERR_INVALID_ARG, "cu_q[0] and cu_k[0] must be 0");
+  for (int b = 0; b < v->n_seqs; ++b) {
+    const int64_t T = v->cu_q[b + 1] - v->cu_q[b], S = v->cu_k[b + 1] - v->cu_k[b];
+    if (T < 0 || S < 1 || T > INT32_MAX || S > INT32_MAX)
+      return fail(DSA_ERR_INVALID_ARG, "sequence %d: %lld query rows and %lld keys", b, (long long)T, (long long)S);
+  }
+  if (layers && (layers[0].at.B != 1 || v->cu_q[v->n_seqs] != layers[0].at.T || v->cu_k[v->n_seqs] != layers[0].at.S))
+    return fail(DSA_ERR_INVALID_ARG, "packed layers must describe B = 1, T = cu_q[n_seqs], S = cu_k[n_seqs]");
+  return DSA_OK;
+}
+
+}  // namespace
+
+dsa_status indexshare_group_forward(const dsa_layer* layers, int32_t n_layers, const char* schedule, int32_t k,
+                                    int32_t* const* idx_bufs, void* ws, size_t ws_bytes, void* stream) {
+  dsa_status s = group_check(layers, n_layers, schedule, k, idx_bufs, ws, ws_bytes);
+  if (s != DSA_OK) return s;
+  return group_run(layers, n_layers, schedule, k, idx_bufs, ws, ws_bytes, stream);
+}
+
+dsa_status indexshare_group_forward_varlen(const dsa_layer* layers, int32_t n_layers, const char* schedule,
+                                           int32_t k, const dsa_varlen* seqs, int32_t* const* idx_bufs, void* ws,
+                                           size_t ws_bytes, void* stream) {
+  // the packed layers are only read through the per-sequence views, which are fully checked
+  if (!layers || n_layers <= 0) return fail(DSA_ERR_INVALID_ARG, "no layers");
+  if (!schedule || (int32_t)strlen(schedule) != n_layers)
+    return fail(DSA_ERR_SCHEDULE, "schedule must have one role per layer");
+  if (!idx_bufs) return fail(DSA_ERR_INVALID_ARG, "idx_bufs is NULL");
+  dsa_status s = check_varlen(layers, seqs);
+  if (s != DSA_OK) return s;
+  std::vector<dsa_layer> view;
+  std::vector<int32_t*> bufs;
+  // every sequence is checked before the first one launches
+  for (int b = 0; b < seqs->n_seqs; ++b) {
+    if (seqs->cu_q[b + 1] == seqs->cu_q[b]) continue;
+    varlen_view(layers, n_layers, schedule, k, seqs, b, idx_bufs, view, bufs);
+    if ((s = group_check(view.data(), n_layers, schedule, k, bufs.data(), ws, ws_bytes)) != DSA_OK)
+      return fail(s, "sequence %d: %s", b, g_last_error.c_str());
+  }
+  for (int b = 0; b < seqs->n_seqs; ++b) {
+    if (seqs->cu_q[b + 1] == seqs->cu_q[b]) continue;
+    varlen_view(layers, n_layers, schedule, k, seqs, b, idx_bufs, view, bufs);
+    if ((s = group_run(view.data(), n_layers, schedule, k, bufs.data(), ws, ws_bytes, stream)) != DSA_OK) return s;
+  }
+  return DSA_OK;
+}
+
+size_t dsa_workspace_size_varlen(const dsa_indexer_args* ix, const dsa_varlen* seqs, int32_t k) {
+  if (!ix || check_varlen(nullptr, seqs) != DSA_OK) return DSA_WS_MIN;
+  size_t best = DSA_WS_MIN;
+  for (int b = 0; b < seqs->n_seqs; ++b) {
+    dsa_indexer_args x = *ix;
+    x.B = 1;
+    x.T = (int32_t)(seqs->cu_q[b + 1] - seqs->cu_q[b]);
+    x.S = (int32_t)(seqs->cu_k[b + 1] - seqs->cu_k[b]);
+    if (x.T < 1) continue;
+    best = std::max(best, dsa_workspace_size(&x, k));
+  }
+  return best;
 }
 
 dsa_status topk_overlap(const int32_t* a, const int32_t* b, int32_t rows, int32_t k, float* per_row,

@@ -274,3 +274,53 @@ def test_quantize_append_validation(lib):
     assert call(pos0=8) == INVALID          # rows 8..10 do not fit 10
     assert call(pos0=-1) == INVALID
     assert call(ws_bytes=100) == WORKSPACE
+
+
+def test_varlen_struct_layout(tmp_path):
+    src = tmp_path / "vl.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "dsa.h"\n'
+                   'int main(void){printf("%zu %zu %zu %zu\\n", sizeof(dsa_varlen), offsetof(dsa_varlen, cu_q),'
+                   ' offsetof(dsa_varlen, cu_k), offsetof(dsa_varlen, q_pos0)); return 0;}\n')
+    exe = tmp_path / "vl"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
+    assert got == [ctypes.sizeof(dsa.Varlen), dsa.Varlen.cu_q.offset, dsa.Varlen.cu_k.offset,
+                   dsa.Varlen.q_pos0.offset]
+
+
+def _varlen(lib, cu_q, cu_k, q_pos0, schedule="FSSS", T=None, S=None, layer_edit=None, seqs=True, ws_bytes=1 << 30):
+    n_layers = len(schedule) if schedule else 4
+    arr = (dsa.Layer * n_layers)()
+    for i in range(n_layers):
+        arr[i].ix = _ix(T=T if T is not None else cu_q[-1], S=S if S is not None else cu_k[-1])
+        arr[i].at = _at(T=T if T is not None else cu_q[-1], S=S if S is not None else cu_k[-1])
+        arr[i].out = FAKE
+        arr[i].lse = None
+    if layer_edit:
+        layer_edit(arr)
+    n = len(q_pos0)
+    v = dsa.Varlen(n, (ctypes.c_int64 * len(cu_q))(*cu_q), (ctypes.c_int64 * len(cu_k))(*cu_k),
+                   (ctypes.c_int64 * max(1, n))(*q_pos0))
+    b = (ctypes.c_void_p * 4)(FAKE, FAKE, FAKE, FAKE)
+    return lib.indexshare_group_forward_varlen(arr, n_layers, schedule.encode() if schedule else None, 16,
+                                               ctypes.byref(v) if seqs else None, b, ctypes.c_void_p(FAKE),
+                                               ws_bytes, None)
+
+
+def test_varlen_validation(lib):
+    ok = ([0, 64, 96], [0, 64, 160], [0, 32])
+    assert _varlen(lib, *ok, seqs=False) == INVALID
+    assert _varlen(lib, [4, 64, 96], [0, 64, 160], [0, 32]) == INVALID      # cu_q[0] != 0
+    assert _varlen(lib, [0, 64, 60], [0, 64, 160], [0, 32]) == INVALID      # decreasing
+    assert _varlen(lib, [0, 64, 96], [0, 64, 64], [0, 32]) == INVALID       # a sequence with no key
+    assert _varlen(lib, *ok, T=100) == INVALID                              # packed rows != cu_q[n]
+    assert _varlen(lib, *ok, S=100) == INVALID
+    assert _varlen(lib, *ok, schedule="FSS") != OK and _varlen(lib, *ok, schedule="SFSS") == SCHEDULE
+
+    def odd_k(arr):  # key rows of 64 bf16 values: sequence 1 starts 64 rows in, 16-byte aligned
+        for i in range(4):
+            arr[i].at.H = 3
+    assert _varlen(lib, *ok, layer_edit=odd_k) == UNSUPPORTED
+    # a sequence whose q_pos0 leaves its last rows without a key in the cache
+    assert _varlen(lib, *ok[:2], [0, -1]) == INVALID
+    assert _varlen(lib, *ok, ws_bytes=300) == WORKSPACE

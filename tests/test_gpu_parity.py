@@ -439,3 +439,73 @@ def test_quantize_e4m3_append_per_sequence_positions_and_bad_position():
     deq = codes[0, :n].view(torch.float8_e4m3fn).float() * scales[0, :n, None]
     ref = xb[0].to(DEV).float()
     assert bool(((deq - ref).abs() <= ref.abs().amax(-1, keepdim=True) / 16).all())
+
+
+# --- packed variable-length sequences ------------------------------------------------------
+
+def _pack(seqs_layers, schedule):
+    """Concatenate per-sequence layer dicts (B = 1 each) along the row axis."""
+    packed = []
+    for l in range(len(schedule)):
+        at = dict(seqs_layers[0][l]["at"])
+        for key in ("q", "k", "v"):
+            if at[key] is not None:
+                at[key] = torch.cat([s[l]["at"][key] for s in seqs_layers], dim=1).contiguous()
+        ix = None
+        if schedule[l] == "F":
+            ix = dict(seqs_layers[0][l]["ix"])
+            for key in ("q", "w", "q_scale", "k", "k_scale"):
+                if ix[key] is not None:
+                    ix[key] = torch.cat([s[l]["ix"][key] for s in seqs_layers], dim=1).contiguous()
+            ix["q_pos0"] = 0
+        packed.append(dict(ix=ix, at=at))
+    return packed
+
+
+@pytest.mark.parametrize("base,shapes,k", [
+    ("tiny_l1k", [(300, 300, 0), (128, 500, 372), (0, 50, 50), (1, 200, 200), (77, 77, 0)], 64),
+    ("prefill_128k", [(700, 700, 0), (256, 3000, 2744), (33, 33, 0), (1, 5000, 5000)], 512),
+])
+def test_group_forward_varlen_equals_each_sequence_alone(base, shapes, k):
+    schedule = "FSSS"
+    wls = [synth.WORKLOADS[base].replace(T=T, S=S, q_pos0=p0, k=k, wid=20 + i, values=(
+        "int" if base == "tiny_l1k" else "gauss")) for i, (T, S, p0) in enumerate(shapes)]
+    per_seq = [[synth.layer_inputs(wl, l, DEV) for l in range(4)] if wl.T > 0 else None for wl in wls]
+    # an empty sequence still owns keys: give it tensors with 0 query rows
+    for i, wl in enumerate(wls):
+        if wl.T == 0:
+            full = [synth.layer_inputs(wl.replace(T=1), l, DEV) for l in range(4)]
+            for l in range(4):
+                full[l]["at"]["q"] = full[l]["at"]["q"][:, :0]
+                if full[l]["ix"] is not None:
+                    for key in ("q", "w", "q_scale"):
+                        if full[l]["ix"][key] is not None:
+                            full[l]["ix"][key] = full[l]["ix"][key][:, :0]
+            per_seq[i] = full
+    packed = _pack(per_seq, schedule)
+    cu_q = np.concatenate([[0], np.cumsum([wl.T for wl in wls])]).tolist()
+    cu_k = np.concatenate([[0], np.cumsum([wl.S for wl in wls])]).tolist()
+    outs, lses, bufs = dsa.indexshare_group_forward_varlen(packed, schedule, k, cu_q, cu_k, [wl.q_pos0 for wl in wls])
+    torch.cuda.synchronize()
+    assert dsa.read_device_flags() == 0
+    for i, wl in enumerate(wls):
+        if wl.T == 0:
+            continue
+        r0, r1 = cu_q[i], cu_q[i + 1]
+        o1, l1, b1 = dsa.indexshare_group_forward(per_seq[i], schedule, k)
+        assert torch.equal(bufs[0][:, r0:r1], b1[0])
+        for l in range(4):
+            assert torch.equal(outs[l][:, r0:r1], o1[l]) and torch.equal(lses[l][:, r0:r1], l1[l])
+        # and the oracle on a few rows of this sequence
+        rows = sorted({0, wl.T // 2, wl.T - 1})
+        got = b1[0].reshape(wl.T, k)[rows].cpu().numpy()
+        ref = oracle.indexer_topk(per_seq[i][0]["ix"], k, rows)
+        if wl.values == "int":
+            assert np.array_equal(got, ref)
+        else:
+            rec = [len(np.intersect1d(g[g >= 0], e[e >= 0])) / max(1, (e >= 0).sum()) for g, e in zip(got, ref)]
+            assert np.mean(rec) >= 0.999
+        for l in range(4):
+            ref_o, _ = oracle.sparse_attn(per_seq[i][l]["at"], got, rows)
+            o = o1[l].reshape(wl.T, wl.H, wl.DV)[rows].float().cpu().numpy()
+            assert np.abs(o - ref_o).max() <= ATOL_OUT
