@@ -616,14 +616,34 @@ def run_kernel_case(args):
         else:
             fn = lambda: dsa.dsa_topk(2048, ix=ix)
     torch.cuda.synchronize()
+    times = []
     for r in range(args.steps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         fn()
         e1.record()
         torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
         print(json.dumps({"kernel_case": args.kernel, "rows": T, "keys": S, "rep": r,
-                          "ms": round(e0.elapsed_time(e1), 4), "work": work}))
+                          "ms": round(times[-1], 4), "work": work}))
+    if args.kernel == "quant" and len(times) > 1:
+        # HBM roofline of the warm launches, and the oracle's quantiser on a sample beside it
+        import oracle
+        ms = statistics.median(times[1:])
+        nbytes = T * (3 * width + 4)
+        peaks = load_peaks()
+        sample = min(T, 256)
+        xs = x[0, :sample].cpu()
+        t0 = time.perf_counter()
+        oracle.quantize_e4m3_rows(xs, width)
+        cpu_s = time.perf_counter() - t0
+        print(json.dumps({"kernel_case": "quant", "tokens_per_s": round(T / (ms * 1e-3), 1), "ms": round(ms, 4),
+                          "roofline": {"bound": "hbm", "achieved": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                       "frac": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                                       "peak_src": peaks["src"]},
+                          "cpu_baseline": {"value": round(sample / cpu_s, 1), "unit": "tokens/s", "cores": 1,
+                                           "kind": "oracle", "sample": f"{sample} tokens of {width} values"}}))
     print(json.dumps({"device_flags": dsa.read_device_flags(dev)}))
 
 
@@ -687,6 +707,7 @@ def run_heatmap(args):
                           "model_ms": round(m * t_f + n * a_ms, 1)})
     uniform = "FSSS" * (n // 4)
     best = schedules[uniform.count("F") - 1]["schedule"]
+    bufs_keep = [b.reshape(T, k)[torch.linspace(0, T - 1, min(T, 512)).long().to(dev)].clone() for b in bufs]
     del bufs
     torch.cuda.empty_cache()
 
@@ -701,6 +722,15 @@ def run_heatmap(args):
         return round(ms, 1)
 
     groups = {s: group_ms(s) for s in dict.fromkeys([uniform, best, "F" * n])}
+    # the oracle's all-pairs overlap on a row sample beside the kernel
+    import oracle
+    sample = min(T, 512)
+    host = [b.cpu().numpy() for b in bufs_keep]
+    t0 = time.perf_counter()
+    oracle.overlap_matrix(host)
+    cpu_s = time.perf_counter() - t0
+    del bufs_keep
+    peaks = load_peaks()
     line = {
         "workload": wl.name, "L": wl.S, "query_rows": T, "k": k, "layers": n,
         "clusters": list(wl.clusters), "cluster_share": synth.CLUSTER_SHARE,
@@ -708,7 +738,15 @@ def run_heatmap(args):
         "adjacent_overlap": [round(M[l][l + 1], 4) for l in range(n - 1)],
         "indexer_topk_ms_per_layer": round(t_f, 2), "attention_ms_per_layer": round(a_ms, 2),
         "overlap_matrix": {"ms": round(m_ms, 3), "idx_bytes": idx_bytes,
-                           "gbs": round(idx_bytes / (m_ms * 1e-3) / 1e9, 1)},
+                           "gbs": round(idx_bytes / (m_ms * 1e-3) / 1e9, 1),
+                           "rows_per_s": round(T / (m_ms * 1e-3), 1),
+                           "roofline": {"bound": "hbm", "achieved": round(idx_bytes / (m_ms * 1e-3) / 1e9, 1),
+                                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                        "frac": round(idx_bytes / (m_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                                        "note": "HBM floor; the kernel is bound by shared-memory issue"},
+                           "cpu_baseline": {"value": round(sample / cpu_s, 1), "unit": "rows/s",
+                                            "cores": oracle.num_threads(), "kind": "oracle",
+                                            "sample": f"{sample} rows of the {n} buffers, every ordered pair"}},
         "schedules": schedules,
         "measured_group_ms": {s: groups[s] for s in groups},
         "uniform": {"schedule": uniform, "score": round(dsa.indexshare_schedule_score(M, uniform), 4)},
