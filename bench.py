@@ -407,17 +407,14 @@ def run_e2e(dsa, wl, layers, group, outs, lses, bufs, args, world):
     for g in group:
         at_dev.append([t for t in (g["at"]["q"], g["at"]["k"]) if t.data_ptr() not in seen])
         seen.update(t.data_ptr() for t in at_dev[-1])
-    # host buffers of exactly the tensors' sizes, page-locked in place (the caching pinned
-    # allocator would round each one up to a power of two: 131 GB locked instead of 75 GB)
-    cudart = torch.cuda.cudart()
-    locked = []
+    # page-locked host buffers of exactly the tensors' sizes, allocated by the CUDA driver
+    # (cuMemHostAlloc); torch's caching pinned allocator would round each one up to a power of
+    # two (131 GB locked instead of 75 GB).  Registering malloc'd pages in place instead
+    # (cudaHostRegister) was measured too: host-to-device copies from them fell to 20 GB/s.
+    pinned = HostPinned()
 
     def host_like(t, fill):
-        h = torch.empty(t.shape, dtype=t.dtype)
-        err = cudart.cudaHostRegister(h.data_ptr(), h.numel() * h.element_size(), 0)
-        if int(err) != 0:
-            raise RuntimeError(f"cudaHostRegister failed ({int(err)})")
-        locked.append(h)
+        h = pinned.empty(t.shape, t.dtype)
         return h.copy_(t) if fill else h
 
     ix_host = [host_like(t, True) for t in ix_dev]
@@ -483,15 +480,51 @@ def run_e2e(dsa, wl, layers, group, outs, lses, bufs, args, world):
     ms = max_over_ranks(evs[0].elapsed_time(evs[-1]) / steps, world)
     link1 = host_copy_gbs(at_host[0][0], at_dev[0][0], out_host[0][0], out_dev[0][0], cin, cout)
     torch.cuda.synchronize()
-    for h in locked:
-        cudart.cudaHostUnregister(h.data_ptr())
-    del ix_host, at_host, out_host, locked
+    del ix_host, at_host, out_host
+    host_alloc = pinned.kind
+    pinned.free()
     return {"value": round(wl.B * wl.T * world / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "overlap": "per-layer inputs in and outputs out on two copy streams, pipelined against compute",
-            "step_ms": [round(x, 1) for x in per_step],
+            "step_ms": [round(x, 1) for x in per_step], "host_alloc": host_alloc,
             "host_copy_gbs": {"before": link0, "after": link1},
             "copy_bound_ms": round((h2d + d2h) / (min(link0["both"], link1["both"]) * 1e9) * 1e3, 1)}
+
+
+class HostPinned:
+    """Page-locked host tensors of exact size from the CUDA driver (cuMemHostAlloc in the
+    current context), or torch's pinned allocator when the driver call is unavailable."""
+
+    def __init__(self):
+        import ctypes
+        self._ct = ctypes
+        self._ptrs = []
+        self.kind = "cuMemHostAlloc"
+        try:
+            self._cuda = ctypes.CDLL("libcuda.so.1")
+            self._cuda.cuMemHostAlloc.restype = ctypes.c_int
+            self._cuda.cuMemHostAlloc.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t, ctypes.c_uint]
+            self._cuda.cuMemFreeHost.restype = ctypes.c_int
+            self._cuda.cuMemFreeHost.argtypes = [ctypes.c_void_p]
+        except OSError:
+            self._cuda, self.kind = None, "torch pinned"
+
+    def empty(self, shape, dtype):
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        if self._cuda is not None and n > 0:
+            p = self._ct.c_void_p()
+            if self._cuda.cuMemHostAlloc(self._ct.byref(p), n, 0) == 0:
+                self._ptrs.append(p.value)
+                buf = (self._ct.c_uint8 * n).from_address(p.value)
+                return torch.frombuffer(buf, dtype=torch.uint8).view(dtype).view(shape)
+            self.kind = "torch pinned"
+        return torch.empty(shape, dtype=dtype, pin_memory=True)
+
+    def free(self):
+        torch.cuda.synchronize()
+        for p in self._ptrs:
+            self._cuda.cuMemFreeHost(p)
+        self._ptrs = []
 
 
 def host_copy_gbs(h_in, d_in, h_out, d_out, cin, cout, nbytes=1 << 30, reps=3):
