@@ -394,12 +394,15 @@ def run_e2e(dsa, wl, layers, group, outs, lses, bufs, args, world):
     """The same F,S,S,S group through the public calls, with every input copied in from pinned
     host memory and every output copied back inside the timed region.  The layers consume
     their inputs in order, so the copies are pipelined against the compute: each layer's
-    inputs go in on a copy stream ahead of its attention call, each layer's output goes back
-    on a second copy stream as soon as it is written, and a step ends when its last output is
-    on the host.  The calls are the ones indexshare_group_forward makes (the F layer's top-k
-    from indexer operands, then one attention call per layer over its index buffer)."""
+    inputs go in on a copy stream ahead of its attention call and each layer's output goes
+    back on a second copy stream as soon as it is written.  Alternate steps use two sets of
+    device input and output buffers, so one step's copies also overlap its neighbours'
+    compute (the next step's inputs stream in while this one computes; its outputs drain
+    while the next one computes).  A step ends when its last output is on the host.  The
+    calls are the ones indexshare_group_forward makes (the F layer's top-k from indexer
+    operands, then one attention call per layer over its index buffer)."""
     ix = layers[0]["ix"]
-    ix_dev = [ix["q"], ix["k"], ix["w"], ix["q_scale"], ix["k_scale"]]
+    ix_keys = ["q", "k", "w", "q_scale", "k_scale"]
     # each distinct device tensor goes in once, before the first layer that reads it (the
     # draft steps of a multi-token-prediction layer share one cache)
     seen = {ix["k"].data_ptr()}
@@ -407,6 +410,19 @@ def run_e2e(dsa, wl, layers, group, outs, lses, bufs, args, world):
     for g in group:
         at_dev.append([t for t in (g["at"]["q"], g["at"]["k"]) if t.data_ptr() not in seen])
         seen.update(t.data_ptr() for t in at_dev[-1])
+    ix_dev = [ix[key] for key in ix_keys]
+
+    # the second set of device buffers: every copied tensor and every output, cloned
+    twin = {}
+    for t in ix_dev + [t for ts in at_dev for t in ts]:
+        twin.setdefault(t.data_ptr(), torch.empty_like(t))
+    swap = lambda t: twin.get(t.data_ptr(), t) if torch.is_tensor(t) else t
+    sets = [dict(ix=ix, ix_dev=ix_dev, at=[g["at"] for g in group], at_dev=at_dev, outs=outs, lses=lses)]
+    sets.append(dict(ix={key: swap(v) for key, v in ix.items()}, ix_dev=[swap(t) for t in ix_dev],
+                     at=[{key: swap(v) for key, v in g["at"].items()} for g in group],
+                     at_dev=[[swap(t) for t in ts] for ts in at_dev],
+                     outs=[torch.empty_like(o) for o in outs], lses=[torch.empty_like(x) for x in lses]))
+
     # page-locked host buffers of exactly the tensors' sizes, allocated by the CUDA driver
     # (cuMemHostAlloc); torch's caching pinned allocator would round each one up to a power of
     # two (131 GB locked instead of 75 GB).  Registering malloc'd pages in place instead
@@ -419,8 +435,7 @@ def run_e2e(dsa, wl, layers, group, outs, lses, bufs, args, world):
 
     ix_host = [host_like(t, True) for t in ix_dev]
     at_host = [[host_like(t, True) for t in ts] for ts in at_dev]
-    out_dev = [[outs[l], lses[l]] for l in range(4)]
-    out_host = [[host_like(t, False) for t in ts] for ts in out_dev]
+    out_host = [[host_like(outs[l], False), host_like(lses[l], False)] for l in range(4)]
     h2d = sum(t.numel() * t.element_size() for t in ix_host) + sum(t.numel() * t.element_size() for ts in at_host for t in ts)
     d2h = sum(t.numel() * t.element_size() for ts in out_host for t in ts)
     comp = torch.cuda.current_stream()
@@ -429,63 +444,79 @@ def run_e2e(dsa, wl, layers, group, outs, lses, bufs, args, world):
     # the last layer runs in row chunks so that only its last chunk's copy-back trails the compute
     nchunk = 4 if wl.T % 4 == 0 else 1
     rc = wl.T // nchunk
+    computed = [None, None]   # per set: the compute of the last step that used it
+    drained = [None, None]    # per set: the copy-back of the last step that used it
 
-    def step():
-        cin.wait_stream(comp)  # the previous step no longer reads the input buffers
+    def step(i):
+        S = sets[i % 2]
+        if computed[i % 2] is not None:
+            cin.wait_event(computed[i % 2])  # that step no longer reads these input buffers
         ready = []
         with torch.cuda.stream(cin):
-            for h, d in zip(ix_host, ix_dev):
+            for h, d in zip(ix_host, S["ix_dev"]):
                 d.copy_(h, non_blocking=True)
             ready_ix = torch.cuda.Event()
             ready_ix.record(cin)
             for l in range(4):
-                for h, d in zip(at_host[l], at_dev[l]):
+                for h, d in zip(at_host[l], S["at_dev"][l]):
                     d.copy_(h, non_blocking=True)
                 ready.append(torch.cuda.Event())
                 ready[-1].record(cin)
         comp.wait_event(ready_ix)  # the F layer's indexer starts while the attention inputs stream in
-        dsa.dsa_topk(wl.k, ix=ix, idx=bufs[0])
+        dsa.dsa_topk(wl.k, ix=S["ix"], idx=bufs[0])
+        if drained[i % 2] is not None:
+            comp.wait_event(drained[i % 2])  # that step's outputs have left these buffers
         for l in range(4):
             comp.wait_event(ready[l])
             parts = [(0, wl.T)] if l < 3 else [(c * rc, (c + 1) * rc) for c in range(nchunk)]
             for r0, r1 in parts:
-                at = group[l]["at"]
+                at = S["at"][l]
                 if (r0, r1) != (0, wl.T):
                     at = dict(at, q=at["q"][:, r0:r1])
-                dsa.dsa_sparse_attn(at, bufs[0][:, r0:r1], out=outs[l][:, r0:r1], lse=lses[l][:, r0:r1])
+                o, x = S["outs"][l], S["lses"][l]
+                dsa.dsa_sparse_attn(at, bufs[0][:, r0:r1], out=o[:, r0:r1], lse=x[:, r0:r1])
                 done = torch.cuda.Event()
                 done.record(comp)
                 cout.wait_event(done)
                 with torch.cuda.stream(cout):
-                    for h, d in zip(out_host[l], out_dev[l]):
+                    for h, d in zip(out_host[l], (o, x)):
                         h[:, r0:r1].copy_(d[:, r0:r1], non_blocking=True)
-        comp.wait_stream(cout)  # the step's outputs are on the host when it ends
+        computed[i % 2] = torch.cuda.Event()
+        computed[i % 2].record(comp)
+        drained[i % 2] = torch.cuda.Event(enable_timing=True)
+        drained[i % 2].record(cout)
+        return drained[i % 2]
 
-    link0 = host_copy_gbs(at_host[0][0], at_dev[0][0], out_host[0][0], out_dev[0][0], cin, cout)
-    # one warm-up step, then timed steps with an event after each (a step ends when its last
-    # output is on the host, so consecutive events bound single steps)
+    link0 = host_copy_gbs(at_host[0][0], at_dev[0][0], out_host[0][0], outs[0], cin, cout)
+    # two warm-up steps (both buffer sets), then timed steps; a step's end is the event after
+    # its last copy-back, so consecutive ends bound single steps of the running pipeline
     steps = max(3, args.steps // 2)
-    step()
+    step(0)
+    step(1)
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-    evs[0].record(comp)
-    for i in range(steps):
-        step()
-        evs[i + 1].record(comp)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(comp)
+    cin.wait_stream(comp)
+    cout.wait_stream(comp)
+    ends = [step(i) for i in range(steps)]
+    comp.wait_stream(cout)
+    comp.wait_stream(cin)
+    e1.record(comp)
     torch.cuda.synchronize()
     barrier(world)
-    per_step = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
-    ms = max_over_ranks(evs[0].elapsed_time(evs[-1]) / steps, world)
-    link1 = host_copy_gbs(at_host[0][0], at_dev[0][0], out_host[0][0], out_dev[0][0], cin, cout)
+    per_step = [e0.elapsed_time(ends[0])] + [ends[i - 1].elapsed_time(ends[i]) for i in range(1, steps)]
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    link1 = host_copy_gbs(at_host[0][0], at_dev[0][0], out_host[0][0], outs[0], cin, cout)
     torch.cuda.synchronize()
-    del ix_host, at_host, out_host
+    del ix_host, at_host, out_host, sets, twin
     host_alloc = pinned.kind
     pinned.free()
     return {"value": round(wl.B * wl.T * world / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "overlap": "per-layer inputs in and outputs out on two copy streams, pipelined against compute",
+            "overlap": "per-layer inputs in and outputs out on two copy streams, pipelined against compute; "
+                       "alternate steps on two device buffer sets",
             "step_ms": [round(x, 1) for x in per_step], "host_alloc": host_alloc,
             "host_copy_gbs": {"before": link0, "after": link1},
             "copy_bound_ms": round((h2d + d2h) / (min(link0["both"], link1["both"]) * 1e9) * 1e3, 1)}
