@@ -1,7 +1,7 @@
 """CUDA path vs the CPU oracle, element by element, on seeded inputs small enough for the
 oracle to finish in seconds while spanning several tiles and a ragged tail.
 
-Tolerances (stated by the project; reading of the rules in the design doc):
+Tolerances (the ones the project states; recall and the score bound defined as below):
   * index buffers: bit-exact on small-integer inputs (every fp32 score is then exact), and
     bit-exact for a top-k over a given fp32 score buffer (same keys on both sides);
   * Gaussian indexer inputs: top-k recall >= 0.999, every selected position within the
