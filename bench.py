@@ -596,7 +596,8 @@ def run_reference(args, rank, world, local):
     oracle.build()
     wl = synth.WORKLOADS[args.workload]
     dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
-    rows = pick_rows(wl, 8, seed=3)
+    # one sampled row per oracle thread (rows are the oracle's unit of parallel work)
+    rows = pick_rows(wl, max(1, oracle.num_threads() - 1), seed=3)
     # inputs: the same seeded tensors; only what the sampled rows read is moved to the host
     ix = synth.indexer_inputs(wl, 0, dev)
     hix, _ = host_sample(wl, ix, [], rows)
