@@ -324,3 +324,18 @@ def test_varlen_validation(lib):
     # a sequence whose q_pos0 leaves its last rows without a key in the cache
     assert _varlen(lib, *ok[:2], [0, -1]) == INVALID
     assert _varlen(lib, *ok, ws_bytes=300) == WORKSPACE
+
+
+def test_varlen_workspace_is_the_largest_sequence_need(lib):
+    cu = [0, 1000, 1000 + 131072, 1000 + 131072 + 5]
+    v = dsa.Varlen(3, (ctypes.c_int64 * 4)(*cu), (ctypes.c_int64 * 4)(*cu), (ctypes.c_int64 * 3)(0, 0, 0))
+    ix = _ix(T=cu[-1], S=cu[-1])
+    got = lib.dsa_workspace_size_varlen(ctypes.byref(ix), ctypes.byref(v), 2048)
+    want = 0
+    for b in range(3):
+        one = _ix(T=cu[b + 1] - cu[b], S=cu[b + 1] - cu[b])
+        want = max(want, lib.dsa_workspace_size(ctypes.byref(one), 2048))
+    assert got == want
+    # malformed sequences fall back to the minimum
+    bad = dsa.Varlen(1, (ctypes.c_int64 * 2)(3, 9), (ctypes.c_int64 * 2)(0, 9), (ctypes.c_int64 * 1)(0))
+    assert lib.dsa_workspace_size_varlen(ctypes.byref(ix), ctypes.byref(bad), 2048) == 256
