@@ -103,6 +103,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = blockIdx.y;
   const int tl0 = tb * C::kTB;
   const int ntok = min(C::kTB, p.Tc - tl0);
+  // epilogue warps own one column quarter each; quarters that hold none of this block's
+  // tokens (decode: one token per block) have no work, so they sit the tiles out and the
+  // accumulator buffers wait only for the others
+  constexpr int kTokWarp = C::kCols / HI > 0 ? C::kCols / HI : 1;
+  const int active_ch = min(kEpiWarps / 4, (ntok + kTokWarp - 1) / kTokWarp);
   const int64_t nmax = visible_keys(p, tl0 + ntok - 1);
   // this CTA's key tiles: [kt_lo, kt_lo + ktiles) of the ceil(S / kM) tiles of the row
   const int tiles_all = (p.S + kM - 1) / kM;
@@ -121,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     for (int i = 0; i < kBufs; ++i) {
       mbar_init(tm_full + i, 1);
-      mbar_init(tm_empty + i, kEpiWarps);
+      mbar_init(tm_empty + i, 4 * active_ch);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -196,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (*abort_flag && done > 0) mbar_wait_drain(tm_full + ((done - 1) & (kBufs - 1)), ((done - 1) / kBufs) & 1);
     }
-  } else {
+  } else if (((warp - 2) >> 2) < active_ch) {
     // ---------------- epilogue ----------------
     const int e = warp - 2;
     const int lq = warp & 3;                 // TMEM lane quarter this warp may read
