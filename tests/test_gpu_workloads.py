@@ -127,3 +127,52 @@ def test_heatmap_all_full_pass_and_overlap_matrix_sampled_rows():
     assert M[1][2] > M[0][1] and M[4][5] > M[2][3] and M[7][8] > M[5][6]
     del bufs, cnt
     torch.cuda.empty_cache()
+
+
+def test_fp8_append_of_the_128k_queries_sampled_rows():
+    """The launch configuration of bench.py --kernel quant: the queries of 131,072 tokens
+    (64 heads x 128 dims, one scale per token) quantised into a cache in one call; sampled
+    tokens bit-exact against the oracle's quantiser."""
+    T, width = 131072, 64 * 128
+    g = torch.Generator(device=DEV)
+    g.manual_seed(synth.SEED_BASE + 17)
+    x = torch.randn((1, T, width), generator=g, device=DEV).to(torch.bfloat16)
+    codes = torch.empty((1, T, width), dtype=torch.uint8, device=DEV)
+    scales = torch.empty((1, T), dtype=torch.float32, device=DEV)
+    dsa.dsa_quantize_e4m3_append(x, codes, scales)
+    assert dsa.read_device_flags() == 0
+    rows = torch.as_tensor([0, 1, 4095, 65536, 99999, T - 1], device=DEV)
+    want_c, want_s = oracle.quantize_e4m3_rows(x[0, rows], width)
+    assert np.array_equal(codes[0, rows].cpu().numpy(), want_c)
+    assert np.array_equal(scales[0, rows].cpu().numpy(), want_s)
+
+
+def test_packed_prompts_equal_each_prompt_alone():
+    """Three prompts of 16K, 4K and 1K tokens of the 128K workload's operands in one packed
+    call: every output, LSE and index row equals the prompt's own call bit for bit."""
+    base = synth.WORKLOADS["prefill_128k"]
+    lens = [16384, 4096, 1024]
+    per = [synth.group_inputs(base.replace(T=n, S=n, q_pos0=0, wid=40 + i), 4, DEV) for i, n in enumerate(lens)]
+    packed = []
+    for l in range(4):
+        at = dict(per[0][l]["at"])
+        at["q"] = torch.cat([p[l]["at"]["q"] for p in per], dim=1)
+        at["k"] = torch.cat([p[l]["at"]["k"] for p in per], dim=1)
+        ix = None
+        if l == 0:
+            ix = dict(per[0][0]["ix"])
+            for key in ("q", "w", "q_scale", "k", "k_scale"):
+                ix[key] = torch.cat([p[0]["ix"][key] for p in per], dim=1)
+        packed.append(dict(ix=ix, at=at))
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    outs, lses, bufs = dsa.indexshare_group_forward_varlen(packed, "FSSS", base.k, cu, cu, [0, 0, 0])
+    torch.cuda.synchronize()
+    assert dsa.read_device_flags() == 0
+    for i, p in enumerate(per):
+        o1, l1, b1 = dsa.indexshare_group_forward(p, "FSSS", base.k)
+        r0, r1 = cu[i], cu[i + 1]
+        assert torch.equal(bufs[0][:, r0:r1], b1[0])
+        for l in range(4):
+            assert torch.equal(outs[l][:, r0:r1], o1[l]) and torch.equal(lses[l][:, r0:r1], l1[l])
+    del per, packed, outs, lses, bufs
+    torch.cuda.empty_cache()
