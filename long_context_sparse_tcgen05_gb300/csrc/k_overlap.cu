@@ -201,7 +201,9 @@ int device_sms() {
 
 }  // namespace
 
-size_t overlap_matrix_smem(int n, int k) { return (size_t)n * (size_t)(k + (k >> 6) + 1) * sizeof(int32_t); }
+size_t overlap_matrix_smem(int n, int k) {
+  return (size_t)n * ((size_t)k + ((size_t)k >> 6) + 1) * sizeof(int32_t);
+}
 
 cudaError_t launch_overlap_matrix(const OverlapMatrixLaunch& p, double* matrix_dev, cudaStream_t st) {
   TraceScope trace(kTraceOverlap, st);

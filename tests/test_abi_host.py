@@ -339,3 +339,11 @@ def test_varlen_workspace_is_the_largest_sequence_need(lib):
     # malformed sequences fall back to the minimum
     bad = dsa.Varlen(1, (ctypes.c_int64 * 2)(3, 9), (ctypes.c_int64 * 2)(0, 9), (ctypes.c_int64 * 1)(0))
     assert lib.dsa_workspace_size_varlen(ctypes.byref(ix), ctypes.byref(bad), 2048) == 256
+
+
+def test_overlap_matrix_rejects_huge_k_without_overflow(lib):
+    P = ctypes.c_void_p
+    m = (ctypes.c_double * 4)()
+    bufs = (P * 2)(FAKE, FAKE)
+    for k in (2 ** 31 - 1, 2 ** 30, 60000):
+        assert lib.topk_overlap_matrix(bufs, 2, 10, k, None, m, P(FAKE), 1 << 30, None) == UNSUPPORTED
