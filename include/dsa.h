@@ -30,8 +30,8 @@
  *   - Faults found in the data on the device (an index outside [-1, S), a NaN score)
  *     never trap: the element is skipped (attention) or ranked lowest (top-k), and a bit
  *     is OR-ed into the device flag word, read by dsa_read_device_flags.
- *   - Tensors are dense and row-major in the shapes given; "[B,T,H,d]" means the last
- *     index varies fastest.  Query row i of every sequence sits at absolute position
+ *   - Tensors are row-major in the shapes given ("[B,T,H,d]": the last index varies
+ *     fastest) and dense, except where a struct gives strides for its operands.  Query row i of every sequence sits at absolute position
  *     q_pos0 + i and sees the keys s < q_pos0 + i + diag (clipped to [0, S)).  diag = 0 is
  *     the strictly-preceding rule of the pages; diag = 1 also admits the query's own key.
  */
@@ -67,12 +67,20 @@ typedef enum { DSA_BF16 = 0, DSA_E4M3 = 1 } dsa_dtype;
 
 /* Indexer operands of one layer (lightning indexer, "Why The Indexer Becomes Expensive").
  *   q       [B,T,H_I,d_I]  bf16 or e4m3 codes                      (16-byte aligned)
+ *           token (b, t) starts at q + b*q_stride_b + t*q_stride_t (elements); its H_I*d_I
+ *           codes are contiguous, heads of d_I codes each
  *   q_scale [B,T]  fp32 per-token dequantisation scale; required for E4M3, NULL for BF16
- *   w       [B,T,H_I] fp32 head weights (any sign)
+ *   w       [B,T,H_I] fp32 head weights (any sign), dense
  *   k       [B,S,d_I]  same dtype as q                              (16-byte aligned)
- *   k_scale [B,S]  fp32; required for E4M3, NULL for BF16
+ *           key (b, s) starts at k + b*k_stride_b + s*d_I (elements)
+ *   k_scale [B,S]  fp32, dense; required for E4M3, NULL for BF16
  * A dequantised operand is scale * code.  Supported: (H_I, d_I) in {(4,64), (64,128)}
- * for BF16 and {(64,128)} for E4M3. */
+ * for BF16 and {(64,128)} for E4M3.
+ * Strides are in elements; 0 selects the dense value (q_stride_t = H_I*d_I, q_stride_b =
+ * T*q_stride_t, k_stride_b = S*d_I).  Non-zero strides must be multiples of 16 bytes
+ * (the operands are read by TMA) and q_stride_t >= H_I*d_I, else DSA_ERR_MISALIGNED /
+ * DSA_ERR_INVALID_ARG.  A row chunk of a larger batch is a strided view: pass the chunk's
+ * first token as q and the full tensor's strides. */
 typedef struct {
   int32_t B, T, S, H_I, d_I;
   dsa_dtype dtype;
@@ -83,16 +91,23 @@ typedef struct {
   const float* k_scale;
   int64_t q_pos0;
   int32_t diag;
+  int64_t q_stride_b, q_stride_t;
+  int64_t k_stride_b;
 } dsa_indexer_args;
 
 /* Main-attention operands of one layer, multi-query form: every query head attends over
  * the same gathered key/value rows (MLA run over its shared latent KV).
  *   q  [B,T,H,d_qk] bf16                                          (16-byte aligned)
- *   k  [B,S,k_ld] bf16; key row j of sequence b at (b*S + j)*k_ld, first d_qk used
- *   v  [B,S,v_ld] bf16; first d_v columns used.  v may equal k (latent KV: the value is
- *      the first d_v columns of the latent row, so each gathered row serves both).
+ *      query (b, t) starts at q + b*q_stride_b + t*q_stride_t; its H*d_qk values contiguous
+ *   k  [B,S,k_ld] bf16; key row j of sequence b at b*k_stride_b + j*k_ld, first d_qk used
+ *   v  [B,S,v_ld] bf16; row j of sequence b at b*v_stride_b + j*v_ld, first d_v used.  v may
+ *      equal k (latent KV: the value is the first d_v columns of the latent row, so each
+ *      gathered row serves both).
  * out = softmax(scale * q K[idx]^T) V[idx] per head.  Supported (H, d_qk, d_v):
- * (8 or 16, 64, 64) and (64, 576, 512); k_ld and v_ld multiples of 8. */
+ * (8 or 16, 64, 64) and (64, 576, 512); k_ld and v_ld multiples of 8.
+ * Strides are in elements; 0 selects the dense value (q_stride_t = H*d_qk, q_stride_b =
+ * T*q_stride_t, k_stride_b = S*k_ld, v_stride_b = S*v_ld).  Non-zero strides must be
+ * multiples of 8 elements and q_stride_t >= H*d_qk. */
 typedef struct {
   int32_t B, T, S, H, d_qk, d_v;
   float scale;
@@ -101,13 +116,16 @@ typedef struct {
   int64_t k_ld;
   const void* v;
   int64_t v_ld;
+  int64_t q_stride_b, q_stride_t;
+  int64_t k_stride_b, v_stride_b;
 } dsa_attn_args;
 
 typedef enum { DSA_TOPK_FROM_SCORES = 0, DSA_TOPK_FROM_INDEXER = 1 } dsa_topk_kind;
 
 /* Source of a top-k: a materialised fp32 score buffer [B,T,ld] (ld >= S; only the visible
- * prefix of each row is read), or the indexer operands (scores are produced on the fly and
- * never stored as a full matrix). */
+ * prefix of each row is read), or the indexer operands.  From indexer operands the scores
+ * of a chunk of query rows pass through the caller's workspace (fp32, up to 4 GiB per chunk,
+ * see dsa_workspace_size) and are read back by the selection; the caller never sees them. */
 typedef struct {
   dsa_topk_kind kind;
   const float* scores;
@@ -123,15 +141,28 @@ typedef struct {
   float* lse; /* [B,T,H] fp32 natural-log softmax normaliser, or NULL */
 } dsa_layer;
 
-/* Workspace bytes preferred by dsa_topk(FROM_INDEXER) and indexshare_group_forward for
- * this indexer shape: a chunk of fp32 score rows (up to 4 GiB) and, when the chunk has fewer
- * than 256 query rows, room for splitting each row's top-k across CTAs (16 lists of k
- * positions and keys per row).  A smaller workspace also works, down to DSA_WS_MIN plus one
- * score row chunk; without the split room the top-k runs one CTA per row.  dsa_topk over a
- * score buffer uses, beyond DSA_WS_MIN, the same split room when given it.  Calls that need
- * no scratch take DSA_WS_MIN. */
+/* Workspace sizes.  Every size below is the number of bytes with which the call runs its
+ * fastest schedule on the current device (the split of few long rows across CTAs depends on
+ * the device's SM count); the calls accept less, down to the stated minimum, and then take a
+ * slower schedule with identical results.  Calls that need no scratch take DSA_WS_MIN.
+ *
+ * dsa_workspace_size: dsa_topk(FROM_INDEXER) for this indexer shape -- a chunk of fp32 score
+ *   rows (up to 4 GiB; at least DSA_WS_MIN plus one row chunk of B*S*4 bytes is required)
+ *   and, when a chunk has fewer query rows than the device has SMs, room for splitting each
+ *   row's top-k across CTAs.
+ * dsa_topk_workspace_size: dsa_topk(FROM_SCORES) over B*T rows of the given visibility --
+ *   DSA_WS_MIN plus the split room when the rows are few and long (0 extra otherwise).
+ * dsa_attn_workspace_size: dsa_sparse_attn -- DSA_WS_MIN plus, for the 64-head latent shape
+ *   with fewer query rows than half the SMs, room for each row's split parts (fp32 outputs
+ *   and LSEs of up to 8 parts).
+ * indexshare_group_workspace_size: indexshare_group_forward (seqs NULL) or
+ *   indexshare_group_forward_varlen (seqs given) -- the largest of the above over the
+ *   group's layers ('F' layers: indexer and attention; 'S' layers: attention) and, packed,
+ *   over its sequences.  Returns DSA_WS_MIN for arguments that the call would reject. */
 #define DSA_WS_MIN ((size_t)256)
 size_t dsa_workspace_size(const dsa_indexer_args* ix, int32_t k);
+size_t dsa_topk_workspace_size(int32_t B, int32_t T, int32_t S, int64_t q_pos0, int32_t diag, int32_t k);
+size_t dsa_attn_workspace_size(const dsa_attn_args* at, int32_t k);
 
 /* Indexer scores, materialised: scores[b,i,s] (row stride ld >= S, fp32) =
  * sum_h w[b,i,h] * ReLU(q[b,i,h] . k[b,s]) for visible s, -inf for the rest of [0, S). */
@@ -186,13 +217,16 @@ typedef struct {
  * its own rows and keys -- its scores, selections and attention never reach another
  * sequence -- with the results of indexshare_group_forward on that sequence alone.  Every
  * sequence's view is checked (shapes, alignment of its offsets, workspace) before anything
- * launches; sequences with no query rows are skipped.  ws: at least
- * dsa_workspace_size_varlen bytes are preferred (the largest sequence's need). */
+ * launches; sequences with no query rows are skipped.  ws: indexshare_group_workspace_size
+ * (with seqs) bytes are preferred; dsa_workspace_size_varlen gives the indexer part alone
+ * (the largest sequence's need). */
 dsa_status indexshare_group_forward_varlen(const dsa_layer* layers, int32_t n_layers,
                                            const char* schedule, int32_t k,
                                            const dsa_varlen* seqs, int32_t* const* idx_bufs,
                                            void* ws, size_t ws_bytes, void* stream);
 size_t dsa_workspace_size_varlen(const dsa_indexer_args* ix, const dsa_varlen* seqs, int32_t k);
+size_t indexshare_group_workspace_size(const dsa_layer* layers, int32_t n_layers, const char* schedule,
+                                       int32_t k, const dsa_varlen* seqs);
 
 /* Overlap of two index buffers a, b [rows,k] (rows as written by dsa_topk: ascending valid
  * entries, then -1 padding): per_row[r] = |A_r and B_r| / |A_r| over valid entries (1 when
@@ -265,6 +299,16 @@ dsa_status dsa_quantize_e4m3_append(const void* x, int32_t B, int32_t n, int32_t
 /* Reads the device flag word of a workspace into *flags_out (host) and clears it.
  * Synchronises `stream`. */
 dsa_status dsa_read_device_flags(void* ws, uint32_t* flags_out, void* stream);
+
+/* Bound on every wait inside the library's kernels (a wait for a copy, a tensor-core
+ * product or another warp of the same CTA), in SM clock cycles, for the kernels launched
+ * after the call (all threads of the process).  0 restores the default, 2e9 cycles (about
+ * one second).  A wait that runs out stops its CTA's work: the CTA lets the copies and
+ * products it has started finish (those waits keep the default bound), frees its tensor
+ * memory, ORs DSA_FLAG_TIMEOUT into the flag word and exits; the outputs of a call that
+ * raised the flag are unspecified.  It exists to test that path: a bound of a few cycles
+ * makes the waits run out on any input, without touching the GPU's state. */
+void dsa_set_wait_limit(uint64_t cycles);
 
 /* Indexer -> top-k without a caller workspace.  The paper has no counterpart to this call;
  * it exists for callers that cannot allocate device memory where they call the library

@@ -42,13 +42,16 @@ _P = _c.c_void_p
 class IndexerArgs(_c.Structure):
     _fields_ = [("B", _c.c_int32), ("T", _c.c_int32), ("S", _c.c_int32), ("H_I", _c.c_int32),
                 ("d_I", _c.c_int32), ("dtype", _c.c_int), ("q", _P), ("q_scale", _P), ("w", _P),
-                ("k", _P), ("k_scale", _P), ("q_pos0", _c.c_int64), ("diag", _c.c_int32)]
+                ("k", _P), ("k_scale", _P), ("q_pos0", _c.c_int64), ("diag", _c.c_int32),
+                ("q_stride_b", _c.c_int64), ("q_stride_t", _c.c_int64), ("k_stride_b", _c.c_int64)]
 
 
 class AttnArgs(_c.Structure):
     _fields_ = [("B", _c.c_int32), ("T", _c.c_int32), ("S", _c.c_int32), ("H", _c.c_int32),
                 ("d_qk", _c.c_int32), ("d_v", _c.c_int32), ("scale", _c.c_float), ("q", _P),
-                ("k", _P), ("k_ld", _c.c_int64), ("v", _P), ("v_ld", _c.c_int64)]
+                ("k", _P), ("k_ld", _c.c_int64), ("v", _P), ("v_ld", _c.c_int64),
+                ("q_stride_b", _c.c_int64), ("q_stride_t", _c.c_int64), ("k_stride_b", _c.c_int64),
+                ("v_stride_b", _c.c_int64)]
 
 
 class TopkSrc(_c.Structure):
@@ -87,6 +90,16 @@ def load_library(path: str = LIB_PATH):
             S = _c.c_int
             lib.dsa_workspace_size.restype = _c.c_size_t
             lib.dsa_workspace_size.argtypes = [_c.POINTER(IndexerArgs), _c.c_int32]
+            lib.dsa_topk_workspace_size.restype = _c.c_size_t
+            lib.dsa_topk_workspace_size.argtypes = [_c.c_int32, _c.c_int32, _c.c_int32, _c.c_int64, _c.c_int32,
+                                                    _c.c_int32]
+            lib.dsa_attn_workspace_size.restype = _c.c_size_t
+            lib.dsa_attn_workspace_size.argtypes = [_c.POINTER(AttnArgs), _c.c_int32]
+            lib.indexshare_group_workspace_size.restype = _c.c_size_t
+            lib.indexshare_group_workspace_size.argtypes = [_c.POINTER(Layer), _c.c_int32, _c.c_char_p, _c.c_int32,
+                                                            _c.POINTER(Varlen)]
+            lib.dsa_set_wait_limit.restype = None
+            lib.dsa_set_wait_limit.argtypes = [_c.c_uint64]
             lib.dsa_indexer_scores.restype = S
             lib.dsa_indexer_scores.argtypes = [_c.POINTER(IndexerArgs), _P, _c.c_int64, _P,
                                                _c.c_size_t, _P]
@@ -181,28 +194,53 @@ def release_workspace():
 
 # --- struct builders ----------------------------------------------------------------
 
+def _stride(t, dim: int) -> int:
+    """Stride of `dim` in elements, or 0 (the library's dense default) for a dimension of size
+    1, whose stride torch leaves arbitrary."""
+    return t.stride(dim) if t.shape[dim] > 1 else 0
+
+
+def _row_pitch(t) -> int:
+    """Row pitch of a [B,S,width] KV tensor: its row stride, or its width when S == 1."""
+    return t.stride(1) if t.shape[1] > 1 else t.shape[2]
+
+
 def indexer_struct(ix: dict) -> IndexerArgs:
+    """The C struct of an indexer operand dict.  q [B,T,H_I,d_I] and k [B,S,d_I] may be
+    strided views along their token / sequence axes (a token's codes stay contiguous); w and
+    the scales are dense."""
     q, k, w = ix["q"], ix["k"], ix["w"]
     B, T, HI, DI = q.shape
     fp8 = q.dtype == torch.float8_e4m3fn
     for t in (q, k, w):
-        assert t.is_cuda and t.is_contiguous()
+        assert t.is_cuda
+    assert q.stride(3) == 1 and (HI == 1 or q.stride(2) == DI), "the codes of one token must be contiguous"
+    assert k.stride(2) == 1 and (k.shape[1] == 1 or k.stride(1) == DI), "the keys of one sequence must be contiguous"
+    assert w.is_contiguous()
     qs, ks = ix.get("q_scale"), ix.get("k_scale")
+    for t in (qs, ks):
+        assert t is None or t.is_contiguous()
     return IndexerArgs(B, T, k.shape[1], HI, DI, DSA_E4M3 if fp8 else DSA_BF16, q.data_ptr(),
                        qs.data_ptr() if (fp8 and qs is not None) else None, w.data_ptr(),
                        k.data_ptr(), ks.data_ptr() if (fp8 and ks is not None) else None,
-                       int(ix.get("q_pos0", 0)), int(ix.get("diag", 0)))
+                       int(ix.get("q_pos0", 0)), int(ix.get("diag", 0)), _stride(q, 0), _stride(q, 1),
+                       _stride(k, 0))
 
 
 def attn_struct(at: dict) -> AttnArgs:
+    """The C struct of an attention operand dict.  q [B,T,H,d_qk] may be strided along its
+    batch and token axes (a query's heads contiguous); k / v [B,S,*] along their batch axis and
+    row pitch (k_ld / v_ld = the row stride)."""
     q, k = at["q"], at["k"]
     v = at.get("v")
     B, T, H, DQK = q.shape
     for t in (q, k) + ((v,) if v is not None else ()):
-        assert t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16
+        assert t.is_cuda and t.dtype == torch.bfloat16 and t.stride(-1) == 1
+    assert H == 1 or q.stride(2) == DQK, "the heads of one query must be contiguous"
     vv = k if v is None else v
     return AttnArgs(B, T, k.shape[1], H, DQK, int(at["d_v"]), float(at["scale"]), q.data_ptr(),
-                    k.data_ptr(), k.shape[2], vv.data_ptr(), vv.shape[2])
+                    k.data_ptr(), _row_pitch(k), vv.data_ptr(), _row_pitch(vv), _stride(q, 0), _stride(q, 1),
+                    _stride(k, 0), _stride(vv, 0))
 
 
 # --- calls --------------------------------------------------------------------------
@@ -244,8 +282,7 @@ def dsa_topk(k: int, *, ix: dict | None = None, scores: torch.Tensor | None = No
         assert sc.stride(2) == 1 and sc.stride(0) == T * sc.stride(1)
         src = TopkSrc(TOPK_FROM_SCORES, sc.data_ptr(), sc.stride(1), None)
         dev = scores.device
-        # few rows may be split across CTAs: room for up to 16 segment lists per row
-        need = WS_MIN + (B * T * 16 * (k * 8 + 4) if B * T < 256 else 0)
+        need = int(lib.dsa_topk_workspace_size(B, T, S, q_pos0, diag, k))
     if idx is None:
         idx = torch.empty((B, T, k), dtype=torch.int32, device=dev)
     if ws is None:
@@ -256,8 +293,9 @@ def dsa_topk(k: int, *, ix: dict | None = None, scores: torch.Tensor | None = No
 
 
 def dsa_sparse_attn(at: dict, idx: torch.Tensor, out: torch.Tensor | None = None,
-                    lse: torch.Tensor | bool | None = True):
-    """(out [B,T,H,d_v] bf16, lse [B,T,H] fp32 or None)."""
+                    lse: torch.Tensor | bool | None = True, ws: torch.Tensor | None = None):
+    """(out [B,T,H,d_v] bf16, lse [B,T,H] fp32 or None).  `ws`: a workspace to use instead of
+    the cached one (uint8, zero-filled once)."""
     lib = load_library()
     a = attn_struct(at)
     dev = at["q"].device
@@ -268,9 +306,8 @@ def dsa_sparse_attn(at: dict, idx: torch.Tensor, out: torch.Tensor | None = None
         lse = torch.empty((a.B, a.T, a.H), dtype=torch.float32, device=dev)
     elif lse is False:
         lse = None
-    # few rows may be split over CTAs (up to 8 parts per row, fp32 outputs + LSE)
-    rows = a.B * a.T
-    ws = workspace(WS_MIN + (rows * 8 * a.H * (a.d_v + 1) * 4 if rows < 128 else 0), dev)
+    if ws is None:
+        ws = workspace(int(lib.dsa_attn_workspace_size(_c.byref(a), idx.shape[-1])), dev)
     _check(lib.dsa_sparse_attn(_c.byref(a), _ptr(idx), idx.shape[-1], _ptr(out), _ptr(lse),
                                _ptr(ws), ws.numel(), _stream()))
     return out, lse
@@ -294,15 +331,14 @@ def _group_structs(layers, schedule: str, k: int, outs, lses, idx_bufs, with_lse
     if lses is None:
         lses = [torch.empty(l["at"]["q"].shape[:3], dtype=torch.float32, device=dev) if with_lse else None
                 for l in layers]
-    need = WS_MIN
     for i, l in enumerate(layers):
         if i < len(schedule) and schedule[i] == "F" and l.get("ix") is not None:
             arr[i].ix = indexer_struct(l["ix"])
-            need = max(need, int(lib.dsa_workspace_size(_c.byref(arr[i].ix), k)))
         arr[i].at = attn_struct(l["at"])
         arr[i].out = outs[i].data_ptr()
         arr[i].lse = lses[i].data_ptr() if lses[i] is not None else None
     bufs = (_P * max(1, n_full))(*[b.data_ptr() for b in idx_bufs])
+    need = int(lib.indexshare_group_workspace_size(arr, n, schedule.encode(), k, None)) if len(schedule) == n else WS_MIN
     return arr, bufs, need, outs, lses, idx_bufs, dev
 
 
@@ -332,10 +368,7 @@ def indexshare_group_forward_varlen(layers, schedule: str, k: int, cu_q, cu_k, q
     qp = (_c.c_int64 * n_seqs)(*[int(x) for x in q_pos0])
     seqs = Varlen(n_seqs, cq, ck, qp)
     arr, bufs, _, outs, lses, idx_bufs, dev = _group_structs(layers, schedule, k, outs, lses, idx_bufs, with_lse)
-    need = WS_MIN
-    for i, l in enumerate(layers):
-        if schedule[i] == "F" and l.get("ix") is not None:
-            need = max(need, int(lib.dsa_workspace_size_varlen(_c.byref(arr[i].ix), _c.byref(seqs), k)))
+    need = int(lib.indexshare_group_workspace_size(arr, len(layers), schedule.encode(), k, _c.byref(seqs)))
     ws = workspace(need, dev)
     _check(lib.indexshare_group_forward_varlen(arr, len(layers), schedule.encode(), k, _c.byref(seqs), bufs,
                                                _ptr(ws), ws.numel(), _stream()))
@@ -422,6 +455,24 @@ def dsa_quantize_e4m3_append(x: torch.Tensor, codes: torch.Tensor, scales: torch
     return codes, scales
 
 
+def set_wait_limit(cycles: int) -> None:
+    """Bound every wait inside the library's kernels launched from now on to `cycles` SM clock
+    cycles (0: the default, about one second) -- dsa_set_wait_limit, for testing the timeout
+    path."""
+    load_library().dsa_set_wait_limit(int(cycles))
+
+
+def topk_workspace_size(B: int, T: int, S: int, q_pos0: int, diag: int, k: int) -> int:
+    """Workspace bytes dsa_topk over a score buffer uses for its fastest schedule."""
+    return int(load_library().dsa_topk_workspace_size(B, T, S, q_pos0, diag, k))
+
+
+def attn_workspace_size(at: dict, k: int) -> int:
+    """Workspace bytes dsa_sparse_attn uses for its fastest schedule."""
+    a = attn_struct(at)
+    return int(load_library().dsa_attn_workspace_size(_c.byref(a), k))
+
+
 def launch_count() -> int:
     """Kernels launched by the library since it was loaded."""
     return int(load_library().dsa_launch_count())
@@ -465,6 +516,7 @@ __all__ = [
     "indexer_scores", "dsa_topk", "dsa_sparse_attn", "indexshare_group_forward", "topk_overlap",
     "topk_overlap_matrix", "indexshare_schedule_score", "indexshare_schedule_search",
     "dsa_quantize_e4m3_append", "indexshare_group_forward_varlen", "Varlen",
-    "read_device_flags", "workspace", "workspace_size", "load_library", "DsaError",
+    "read_device_flags", "workspace", "workspace_size", "topk_workspace_size", "attn_workspace_size",
+    "set_wait_limit", "load_library", "DsaError",
     "IndexerArgs", "AttnArgs", "TopkSrc", "Layer",
 ]

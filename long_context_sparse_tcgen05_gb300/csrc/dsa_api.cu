@@ -15,6 +15,8 @@
 namespace dsa {
 static std::atomic<uint64_t> g_launches{0};
 void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+static std::atomic<long long> g_wait_limit{kDefaultWaitCycles};
+long long wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
 }  // namespace dsa
 
 namespace {
@@ -65,7 +67,33 @@ dsa_status check_indexer(const dsa_indexer_args* ix) {
   if (!aligned16(ix->w)) return fail(DSA_ERR_MISALIGNED, "indexer w must be 16-byte aligned");
   if (ix->diag < 0 || ix->diag > 1) return fail(DSA_ERR_INVALID_ARG, "diag must be 0 or 1");
   if (ix->q_pos0 < 0) return fail(DSA_ERR_INVALID_ARG, "q_pos0 must be >= 0");
+  if (ix->q_stride_b < 0 || ix->q_stride_t < 0 || ix->k_stride_b < 0)
+    return fail(DSA_ERR_INVALID_ARG, "indexer strides must be >= 0 (0: dense)");
+  if (ix->q_stride_t && ix->q_stride_t < (int64_t)ix->H_I * ix->d_I)
+    return fail(DSA_ERR_INVALID_ARG, "q_stride_t = %lld is smaller than H_I * d_I", (long long)ix->q_stride_t);
+  const int64_t esz = ix->dtype == DSA_E4M3 ? 1 : 2;
+  if ((ix->q_stride_b * esz) % 16 || (ix->q_stride_t * esz) % 16 || (ix->k_stride_b * esz) % 16)
+    return fail(DSA_ERR_MISALIGNED, "indexer strides must be multiples of 16 bytes");
   return DSA_OK;
+}
+
+// Indexer strides with the dense defaults filled in.
+void indexer_strides(const dsa_indexer_args* ix, int64_t* q_sb, int64_t* q_st, int64_t* k_sb) {
+  *q_st = ix->q_stride_t ? ix->q_stride_t : (int64_t)ix->H_I * ix->d_I;
+  *q_sb = ix->q_stride_b ? ix->q_stride_b : (int64_t)ix->T * *q_st;
+  *k_sb = ix->k_stride_b ? ix->k_stride_b : (int64_t)ix->S * ix->d_I;
+}
+
+// The launch description of an indexer call over query rows [t0, t0 + Tc).
+dsa::IndexerLaunch indexer_launch(const dsa_indexer_args* ix, int64_t t0, int Tc) {
+  dsa::IndexerLaunch L{};
+  L.B = ix->B; L.T = ix->T; L.S = ix->S; L.HI = ix->H_I; L.DI = ix->d_I;
+  L.fp8 = ix->dtype == DSA_E4M3;
+  L.q = ix->q; L.q_scale = ix->q_scale; L.w = ix->w; L.k = ix->k; L.k_scale = ix->k_scale;
+  indexer_strides(ix, &L.q_sb, &L.q_st, &L.k_sb);
+  L.q_pos0 = ix->q_pos0; L.diag = ix->diag;
+  L.t0 = (int)t0; L.Tc = Tc;
+  return L;
 }
 
 dsa_status check_attn(const dsa_attn_args* at) {
@@ -80,10 +108,44 @@ dsa_status check_attn(const dsa_attn_args* at) {
   if (at->k_ld < at->d_qk || at->v_ld < at->d_v || at->k_ld % 8 || at->v_ld % 8)
     return fail(DSA_ERR_MISALIGNED, "k_ld/v_ld must cover d_qk/d_v and be multiples of 8 elements");
   if (!(at->scale > 0.f)) return fail(DSA_ERR_INVALID_ARG, "scale must be positive");
+  if (at->q_stride_b < 0 || at->q_stride_t < 0 || at->k_stride_b < 0 || at->v_stride_b < 0)
+    return fail(DSA_ERR_INVALID_ARG, "attention strides must be >= 0 (0: dense)");
+  if (at->q_stride_t && at->q_stride_t < (int64_t)at->H * at->d_qk)
+    return fail(DSA_ERR_INVALID_ARG, "q_stride_t = %lld is smaller than H * d_qk", (long long)at->q_stride_t);
+  if (at->q_stride_b % 8 || at->q_stride_t % 8 || at->k_stride_b % 8 || at->v_stride_b % 8)
+    return fail(DSA_ERR_MISALIGNED, "attention strides must be multiples of 8 elements");
   return DSA_OK;
 }
 
+// The launch description of an attention call (strides resolved, no split planned).
+dsa::AttnLaunch attn_launch(const dsa_attn_args* at, const int32_t* idx, int32_t k, void* out, float* lse) {
+  dsa::AttnLaunch L{};
+  L.B = at->B; L.T = at->T; L.S = at->S; L.H = at->H; L.DQK = at->d_qk; L.DV = at->d_v; L.scale = at->scale;
+  L.q = at->q; L.k = at->k; L.k_ld = at->k_ld; L.v = at->v; L.v_ld = at->v_ld;
+  L.q_st = at->q_stride_t ? at->q_stride_t : (int64_t)at->H * at->d_qk;
+  L.q_sb = at->q_stride_b ? at->q_stride_b : (int64_t)at->T * L.q_st;
+  L.k_sb = at->k_stride_b ? at->k_stride_b : (int64_t)at->S * at->k_ld;
+  L.v_sb = at->v_stride_b ? at->v_stride_b : (int64_t)at->S * at->v_ld;
+  L.idx = idx; L.kk = k; L.out = out; L.lse = lse;
+  return L;
+}
+
+// Workspace bytes beyond DSA_WS_MIN for the parts of a split attention call (0: no split).
+size_t attn_split_bytes(const dsa::AttnLaunch& L) {
+  const int splits = dsa::attn_splits(L);
+  if (splits <= 1) return 0;
+  return (size_t)L.B * L.T * splits * (size_t)L.H * ((size_t)L.DV + 1) * 4;
+}
+
 constexpr int kMaxK = 4096;
+
+// Bytes of the segment lists when `rows` rows of up to n_max scores are split across CTAs
+// (0: no split).
+size_t topk_split_bytes(int64_t rows, int64_t n_max, int k) {
+  const int parts = dsa::topk_parts(rows, n_max);
+  if (parts <= 1) return 0;
+  return (size_t)rows * parts * ((size_t)k * 8 + 4);
+}
 
 // Few long rows: split each across CTAs (dsa::topk_parts) when the workspace from byte `off` on
 // holds the segments' lists; otherwise one CTA per row.
@@ -92,7 +154,7 @@ void plan_topk_parts(dsa::TopkLaunch& P, int64_t rows, int64_t n_max, void* ws, 
   const int parts = dsa::topk_parts(rows, n_max);
   if (parts <= 1) return;
   const size_t per = (size_t)rows * parts;
-  const size_t need = per * ((size_t)P.k * 8 + 4);
+  const size_t need = topk_split_bytes(rows, n_max, P.k);
   if (off > ws_bytes || ws_bytes - off < need) return;
   uint8_t* w = static_cast<uint8_t*>(ws) + off;
   P.parts = parts;
@@ -121,12 +183,7 @@ dsa_status run_indexer_topk(const dsa_indexer_args* ix, int32_t k, int32_t* idx,
   float* sc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + dsa::kWsScratch);
   for (int64_t t0 = 0; t0 < ix->T; t0 += chunk) {
     const int Tc = (int)((ix->T - t0) < chunk ? (ix->T - t0) : chunk);
-    dsa::IndexerLaunch L{};
-    L.B = ix->B; L.T = ix->T; L.S = ix->S; L.HI = ix->H_I; L.DI = ix->d_I;
-    L.fp8 = ix->dtype == DSA_E4M3;
-    L.q = ix->q; L.q_scale = ix->q_scale; L.w = ix->w; L.k = ix->k; L.k_scale = ix->k_scale;
-    L.q_pos0 = ix->q_pos0; L.diag = ix->diag;
-    L.t0 = (int)t0; L.Tc = Tc;
+    dsa::IndexerLaunch L = indexer_launch(ix, t0, Tc);
     L.out = sc; L.ld = ix->S; L.out_bstride = (int64_t)Tc * ix->S; L.write_masked = 0;
     L.flags = ws_flags(ws);
     cudaError_t e = dsa::launch_indexer_scores(L, st);
@@ -148,6 +205,7 @@ dsa_status run_indexer_topk(const dsa_indexer_args* ix, int32_t k, int32_t* idx,
 namespace dsa {
 dsa_status validate_indexer(const dsa_indexer_args* ix) { return check_indexer(ix); }
 dsa_status record_error(dsa_status s, const char* msg) { return fail(s, "%s", msg); }
+IndexerLaunch make_indexer_launch(const dsa_indexer_args* ix, int64_t t0, int Tc) { return indexer_launch(ix, t0, Tc); }
 }  // namespace dsa
 
 extern "C" {
@@ -160,11 +218,20 @@ size_t dsa_workspace_size(const dsa_indexer_args* ix, int32_t k) {
   if (rows < 1) rows = 1;
   if (rows > ix->T) rows = ix->T;
   size_t bytes = dsa::kWsScratch + (size_t)(rows * per_row);
-  // a chunk of few rows may have them split across CTAs: room for the segments' lists
-  const int64_t chunk_rows = rows * ix->B;
-  if (chunk_rows < 256 && k >= 1 && k <= kMaxK)
-    bytes += (size_t)chunk_rows * dsa::kMaxTopkParts * ((size_t)k * 8 + 4);
+  // a chunk of few rows may have them split across CTAs: room for the segments' lists (the
+  // first chunk's rows are the most; the same room serves every later chunk)
+  if (k >= 1 && k <= kMaxK) bytes += topk_split_bytes(rows * ix->B, max_visible(ix->q_pos0, ix->T, ix->diag, ix->S), k);
   return bytes;
+}
+
+size_t dsa_topk_workspace_size(int32_t B, int32_t T, int32_t S, int64_t q_pos0, int32_t diag, int32_t k) {
+  if (B <= 0 || T <= 0 || S <= 0 || q_pos0 < 0 || diag < 0 || diag > 1 || k < 1 || k > kMaxK) return DSA_WS_MIN;
+  return dsa::kWsScratch + topk_split_bytes((int64_t)B * T, max_visible(q_pos0, T, diag, S), k);
+}
+
+size_t dsa_attn_workspace_size(const dsa_attn_args* at, int32_t k) {
+  if (!at || at->B <= 0 || at->T <= 0 || at->S <= 0 || k < 1 || k > kMaxK) return DSA_WS_MIN;
+  return dsa::kWsScratch + attn_split_bytes(attn_launch(at, nullptr, k, nullptr, nullptr));
 }
 
 dsa_status dsa_indexer_scores(const dsa_indexer_args* ix, float* scores, int64_t ld, void* ws, size_t ws_bytes,
@@ -174,12 +241,7 @@ dsa_status dsa_indexer_scores(const dsa_indexer_args* ix, float* scores, int64_t
   if (!scores) return fail(DSA_ERR_INVALID_ARG, "scores is NULL");
   if (ld < ix->S) return fail(DSA_ERR_INVALID_ARG, "ld (%lld) < S (%d)", (long long)ld, ix->S);
   if ((s = check_ws(ws, ws_bytes, DSA_WS_MIN)) != DSA_OK) return s;
-  dsa::IndexerLaunch L{};
-  L.B = ix->B; L.T = ix->T; L.S = ix->S; L.HI = ix->H_I; L.DI = ix->d_I;
-  L.fp8 = ix->dtype == DSA_E4M3;
-  L.q = ix->q; L.q_scale = ix->q_scale; L.w = ix->w; L.k = ix->k; L.k_scale = ix->k_scale;
-  L.q_pos0 = ix->q_pos0; L.diag = ix->diag;
-  L.t0 = 0; L.Tc = ix->T;
+  dsa::IndexerLaunch L = indexer_launch(ix, 0, ix->T);
   L.out = scores; L.ld = ld; L.out_bstride = (int64_t)ix->T * ld; L.write_masked = 1;
   L.flags = ws_flags(ws);
   cudaError_t e = dsa::launch_indexer_scores(L, as_stream(stream));
@@ -224,15 +286,13 @@ dsa_status dsa_sparse_attn(const dsa_attn_args* at, const int32_t* idx, int32_t 
   if (k < 1 || k > kMaxK) return fail(DSA_ERR_UNSUPPORTED, "k=%d outside [1, %d]", k, kMaxK);
   if (!aligned16(out)) return fail(DSA_ERR_MISALIGNED, "out must be 16-byte aligned");
   if ((s = check_ws(ws, ws_bytes, DSA_WS_MIN)) != DSA_OK) return s;
-  dsa::AttnLaunch L{};
-  L.B = at->B; L.T = at->T; L.S = at->S; L.H = at->H; L.DQK = at->d_qk; L.DV = at->d_v; L.scale = at->scale;
-  L.q = at->q; L.k = at->k; L.k_ld = at->k_ld; L.v = at->v; L.v_ld = at->v_ld;
-  L.idx = idx; L.kk = k; L.out = out; L.lse = lse; L.flags = ws_flags(ws);
+  dsa::AttnLaunch L = attn_launch(at, idx, k, out, lse);
+  L.flags = ws_flags(ws);
   // few rows: split each row's blocks over CTAs when the workspace holds the parts
   const int splits = dsa::attn_splits(L);
   if (splits > 1) {
     const size_t parts = (size_t)at->B * at->T * splits;
-    const size_t need = parts * (size_t)at->H * ((size_t)at->d_v + 1) * 4;
+    const size_t need = attn_split_bytes(L);
     if (ws_bytes > dsa::kWsScratch && ws_bytes - dsa::kWsScratch >= need) {
       uint8_t* w = static_cast<uint8_t*>(ws) + dsa::kWsScratch;
       L.splits = splits;
@@ -312,9 +372,11 @@ void varlen_view(const dsa_layer* layers, int32_t n_layers, const char* schedule
   for (int i = 0; i < n_layers; ++i) {
     dsa_layer& L = out[i];
     dsa_attn_args& a = L.at;
+    const int64_t aq_st = a.q_stride_t ? a.q_stride_t : (int64_t)a.H * a.d_qk;
+    a.q_stride_t = aq_st;  // the view's rows keep the packed tensor's row stride
     a.T = T;
     a.S = S;
-    a.q = static_cast<const uint16_t*>(a.q) + q0 * a.H * a.d_qk;
+    a.q = static_cast<const uint16_t*>(a.q) + q0 * aq_st;
     a.k = static_cast<const uint16_t*>(a.k) + k0 * a.k_ld;
     a.v = a.v ? static_cast<const uint16_t*>(a.v) + k0 * a.v_ld : a.v;
     L.out = static_cast<uint16_t*>(L.out) + q0 * a.H * a.d_v;
@@ -322,15 +384,18 @@ void varlen_view(const dsa_layer* layers, int32_t n_layers, const char* schedule
     if (schedule[i] == 'F') {
       dsa_indexer_args& x = L.ix;
       const int64_t elt = x.dtype == DSA_E4M3 ? 1 : 2;
+      const int64_t xq_st = x.q_stride_t ? x.q_stride_t : (int64_t)x.H_I * x.d_I;
+      x.q_stride_t = xq_st;
       x.T = T;
       x.S = S;
-      x.q = static_cast<const uint8_t*>(x.q) + q0 * x.H_I * x.d_I * elt;
+      x.q = static_cast<const uint8_t*>(x.q) + q0 * xq_st * elt;
       if (x.q_scale) x.q_scale += q0;
       x.w += q0 * x.H_I;
       x.k = static_cast<const uint8_t*>(x.k) + k0 * x.d_I * elt;
       if (x.k_scale) x.k_scale += k0;
       x.q_pos0 = v->q_pos0[b];
-      bufs.push_back(idx_bufs[f++] + q0 * k);
+      bufs.push_back(idx_bufs ? idx_bufs[f] + q0 * k : nullptr);
+      ++f;
     }
   }
 }
@@ -383,6 +448,37 @@ dsa_status indexshare_group_forward_varlen(const dsa_layer* layers, int32_t n_la
     if ((s = group_run(view.data(), n_layers, schedule, k, bufs.data(), ws, ws_bytes, stream)) != DSA_OK) return s;
   }
   return DSA_OK;
+}
+
+size_t indexshare_group_workspace_size(const dsa_layer* layers, int32_t n_layers, const char* schedule, int32_t k,
+                                       const dsa_varlen* seqs) {
+  if (!layers || n_layers <= 0 || !schedule || (int32_t)strnlen(schedule, (size_t)n_layers + 1) != n_layers)
+    return DSA_WS_MIN;
+  size_t best = DSA_WS_MIN;
+  auto one_group = [&](const dsa_layer* ls) {
+    for (int i = 0; i < n_layers; ++i) {
+      if (schedule[i] == 'F') best = std::max(best, dsa_workspace_size(&ls[i].ix, k));
+      best = std::max(best, dsa_attn_workspace_size(&ls[i].at, k));
+    }
+  };
+  if (!seqs) {
+    one_group(layers);
+    return best;
+  }
+  if (check_varlen(layers, seqs) != DSA_OK) return DSA_WS_MIN;
+  std::vector<dsa_layer> view;
+  std::vector<int32_t*> bufs;
+  for (int b = 0; b < seqs->n_seqs; ++b) {
+    if (seqs->cu_q[b + 1] == seqs->cu_q[b]) continue;
+    varlen_view(layers, n_layers, schedule, k, seqs, b, nullptr, view, bufs);
+    one_group(view.data());
+  }
+  return best;
+}
+
+void dsa_set_wait_limit(uint64_t cycles) {
+  const long long c = cycles == 0 || cycles > (uint64_t)dsa::kDefaultWaitCycles ? dsa::kDefaultWaitCycles : (long long)cycles;
+  dsa::g_wait_limit.store(c, std::memory_order_relaxed);
 }
 
 size_t dsa_workspace_size_varlen(const dsa_indexer_args* ix, const dsa_varlen* seqs, int32_t k) {

@@ -17,6 +17,10 @@ constexpr size_t kWsScratch = DSA_WS_MIN;
 // Kernel launches issued by this library since load (diagnostics; see dsa_launch_count).
 void count_launches(uint64_t n);
 
+// Bound, in SM clock cycles, on the waits of kernels launched now (dsa_set_wait_limit).
+constexpr long long kDefaultWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
+long long wait_limit();
+
 // Launch tracing (dsa_trace_enable): when on, a scope brackets one launcher's kernels with
 // CUDA events on its stream; durations are read back by dsa_trace_read.
 enum TraceKind { kTraceIndexer = 1, kTraceTopk = 2, kTraceAttention = 3, kTraceOverlap = 4 };
@@ -45,10 +49,15 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 }
 
 // Rows [t0, t0 + Tc) of every sequence of one layer's indexer.
+struct IndexerLaunch;
+IndexerLaunch make_indexer_launch(const dsa_indexer_args* ix, int64_t t0, int Tc);  // strides resolved
+
 struct IndexerLaunch {
   int B, T, S, HI, DI;
   int fp8;
   const void* q;
+  int64_t q_sb, q_st;   // token strides of q in elements (resolved: never 0)
+  int64_t k_sb;         // sequence stride of k in elements
   const float* q_scale;
   const float* w;
   const void* k;
@@ -62,6 +71,7 @@ struct IndexerLaunch {
   int write_masked;     // 1: write -inf over [n_t, S) as well
   uint32_t* flags;      // device flag word (DSA_FLAG_TIMEOUT)
   int ksplit;           // key-range splits per token block (0: chosen by the launcher)
+  long long wait;       // wait bound in cycles (0: wait_limit() at launch)
 };
 cudaError_t launch_indexer_scores(const IndexerLaunch& p, cudaStream_t st);     // tcgen05 path
 
@@ -75,6 +85,7 @@ struct TopkLaunch {
   int diag, k;
   int32_t* idx;
   uint32_t* flags;
+  long long wait;       // wait bound in cycles (0: wait_limit() at launch)
   // few long rows: each row split into `parts` segments (> 1), one CTA each; segment s of row
   // r = b*Tc + tl writes its exact top-k, sorted by position, with the keys, to
   // part_pos / part_key[(r*parts + s)*k ..] and its length to part_cnt[r*parts + s]; a merge
@@ -97,11 +108,14 @@ struct AttnLaunch {
   int64_t k_ld;
   const void* v;
   int64_t v_ld;
+  int64_t q_sb, q_st;   // query strides in elements (resolved: never 0)
+  int64_t k_sb, v_sb;   // sequence strides of k and v in elements
   const int32_t* idx;
   int kk;
   void* out;
   float* lse;
   uint32_t* flags;
+  long long wait;       // wait bound in cycles (0: wait_limit() at launch)
   // few rows (decode): each row's selected blocks split into `splits` (> 1) parts, one CTA
   // each; part s of row r writes its output normalised by its own row sums, fp32,
   // part_o[((r*splits + s)*H + h)*DV ..], and its LSE part_lse[(r*splits + s)*H + h]; a

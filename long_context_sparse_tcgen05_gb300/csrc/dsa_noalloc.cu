@@ -70,12 +70,7 @@ extern "C" dsa_status dsa_topk_indexer_noalloc(const dsa_indexer_args* ix, int32
   const int64_t chunk_max = (int64_t)((kStaticScratchBytes - kFlagBytes) / row_bytes);
   for (int64_t t0 = 0; t0 < ix->T; t0 += chunk_max) {
     const int Tc = (int)((ix->T - t0) < chunk_max ? (ix->T - t0) : chunk_max);
-    dsa::IndexerLaunch L{};
-    L.B = ix->B; L.T = ix->T; L.S = ix->S; L.HI = ix->H_I; L.DI = ix->d_I;
-    L.fp8 = ix->dtype == DSA_E4M3;
-    L.q = ix->q; L.q_scale = ix->q_scale; L.w = ix->w; L.k = ix->k; L.k_scale = ix->k_scale;
-    L.q_pos0 = ix->q_pos0; L.diag = ix->diag;
-    L.t0 = (int)t0; L.Tc = Tc;
+    dsa::IndexerLaunch L = dsa::make_indexer_launch(ix, t0, Tc);
     L.out = sc; L.ld = ix->S; L.out_bstride = (int64_t)Tc * ix->S; L.write_masked = 0;
     L.flags = flag_word;
     cudaError_t e = dsa::launch_indexer_scores(L, st);

@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(AtCfg<HP, DQK, DV, SEPV, NB>::kThreads, 1)
     if (last >= 0) atomicMax(last_s, last);
   }
   // Query tile (heads beyond H are zero).
-  const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q) + (int64_t)row * p.H * DQK;
+  const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q) + (int64_t)b * p.q_sb + (int64_t)(row % p.T) * p.q_st;
   for (int i = threadIdx.x; i < HP * C::kKChunks; i += C::kThreads) {
     const int h = i / C::kKChunks, c16 = i % C::kKChunks;
     uint4 v = make_uint4(0, 0, 0, 0);
@@ -120,8 +120,8 @@ __global__ void __launch_bounds__(AtCfg<HP, DQK, DV, SEPV, NB>::kThreads, 1)
   __syncthreads();
   const int nblocks = (*last_s + NB) / NB;
 
-  const __nv_bfloat16* kbase = static_cast<const __nv_bfloat16*>(p.k) + (int64_t)b * p.S * p.k_ld;
-  const __nv_bfloat16* vbase = static_cast<const __nv_bfloat16*>(p.v) + (int64_t)b * p.S * p.v_ld;
+  const __nv_bfloat16* kbase = static_cast<const __nv_bfloat16*>(p.k) + (int64_t)b * p.k_sb;
+  const __nv_bfloat16* vbase = static_cast<const __nv_bfloat16*>(p.v) + (int64_t)b * p.v_sb;
   auto gather = [&](int jb, int stage) {
     for (int i = threadIdx.x; i < NB * C::kKChunks; i += C::kThreads) {
       const int r = i / C::kKChunks, c16 = i % C::kKChunks;
@@ -302,7 +302,7 @@ cudaError_t launch_cfg(const AttnLaunch& p, cudaStream_t st) {
 cudaError_t launch_sparse_attn(const AttnLaunch& p, cudaStream_t st) {
   if (p.B * p.T <= 0) return cudaSuccess;
   if (sparse_mla_tc_supported(p)) return launch_sparse_mla_tc(p, st);
-  const bool latent = p.v == p.k && p.v_ld == p.k_ld;
+  const bool latent = p.v == p.k && p.v_ld == p.k_ld && p.v_sb == p.k_sb;
   if (p.H == 64 && p.DQK == 576 && p.DV == 512)
     return latent ? launch_cfg<64, 576, 512, false>(p, st) : launch_cfg<64, 576, 512, true>(p, st);
   if (p.H <= 16 && p.DQK == 64 && p.DV == 64)

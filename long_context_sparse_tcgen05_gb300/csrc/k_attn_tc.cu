@@ -103,6 +103,19 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
+// Named barrier that also ORs a predicate over the n participating threads: every thread gets
+// the same answer, so a decision taken on it (leaving the loop after a wait ran out in some
+// warp) is uniform and no warp is left waiting at a later barrier.
+__device__ __forceinline__ bool named_sync_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
@@ -179,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = item / splits;
       const int32_t* irow = p.idx + (int64_t)row * p.kk;
       const int b = row / p.T;
-      const int64_t kvrow0 = (int64_t)b * p.S;
+      const uint8_t* kvb = kvg + (int64_t)b * p.k_sb * 2;  // this sequence's latent rows
       // blocks = 1 + (last entry other than -1) / kNB; all loads of the scan issued together
       int last = -1;
       if (vec) {
@@ -210,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int split = item % splits;
       const int j0 = split * nbr / splits, nb = (split + 1) * nbr / splits - j0;  // this item's blocks
       if (warp == 0) {
-        if (lane == 0) ok = mbar_wait(&bar.info_empty[it & 1], ((it >> 1) & 1) ^ 1, abort_flag);
+        if (lane == 0) ok = mbar_wait(&bar.info_empty[it & 1], ((it >> 1) & 1) ^ 1, abort_flag, p.wait);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (ok && lane == 0) {
           sm->nb[it & 1] = nb;
@@ -223,16 +236,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == 0) {
         const int next_row = (item + (int)gridDim.x) / splits;
         if (lane == 0 && next_row < rows && next_row != row)
-          prefetch_l2(static_cast<const __nv_bfloat16*>(p.q) + (int64_t)next_row * kH * kDQK, kQBytes);
+          prefetch_l2(static_cast<const __nv_bfloat16*>(p.q) + (int64_t)(next_row / p.T) * p.q_sb +
+                          (int64_t)(next_row % p.T) * p.q_st,
+                      kQBytes);
         if (lane == 0) {
-          ok = mbar_wait(&bar.q_empty, (qc & 1) ^ 1, abort_flag);
+          ok = mbar_wait(&bar.q_empty, (qc & 1) ^ 1, abort_flag, p.wait);
           if (ok) {
             mbar_arrive_expect_tx(&bar.q_full, kQBytes);
-            for (int a = 0; a < kAtoms; ++a) tma_load_3d(q_s + a * kAtomQ, &tm_q, &bar.q_full, a * 64, 0, row);
+            for (int a = 0; a < kAtoms; ++a)
+              tma_load_4d(q_s + a * kAtomQ, &tm_q, &bar.q_full, a * 64, 0, row % p.T, row / p.T);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
+      if (!ok) break;  // no Q load was issued for this row
       ++qc;
       for (int j = 0; ok && j < nb; ++j, ++g) {
         const int st = (int)(g % kStages);
@@ -244,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool valid = id >= 0 && id < p.S;
         if (lane < kRowsW && !valid && id != -1) atomicOr(p.flags, DSA_FLAG_BAD_INDEX);
         if (!valid) id = 0;
-        if (!(ok = mbar_wait(&bar.kv_empty[st], (uint32_t)((g / kStages) & 1) ^ 1, abort_flag))) break;
+        if (!(ok = mbar_wait(&bar.kv_empty[st], (uint32_t)((g / kStages) & 1) ^ 1, abort_flag, p.wait))) break;
         uint8_t* stage = kv_s + st * kKVBytes;
         // atom by atom: 8 lanes per row (one 16-byte chunk each), 4 rows per pass, 4 passes
         // cover the warp's 16 rows; the row of each pass is fixed, so its id is fetched once
@@ -263,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r = warp * kRowsW + pass * 4 + (lane >> 3);
             const uint32_t dst = smem_addr(stage + a * kAtomKV + r * 128 + ((cc ^ (r & 7)) << 4));
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
-                         "l"(kvg + (kvrow0 + rid[pass]) * row_bytes + (a * 8 + cc) * 16), "r"(rv[pass] ? 16 : 0)
+                         "l"(kvb + rid[pass] * row_bytes + (a * 8 + cc) * 16), "r"(rv[pass] ? 16 : 0)
                          : "memory");
           }
           asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_addr(&bar.kv_full[st][a]))
@@ -285,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
       int nb = 0;
       if (lane == 0) {
-        ok = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag);
+        ok = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag, p.wait);
         nb = sm->nb[it & 1];
         mbar_arrive(&bar.info_empty[it & 1]);
       }
@@ -294,18 +311,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (nb == 0) continue;
       if (lane == 0) {
-        ok = mbar_wait(&bar.q_full, qc & 1, abort_flag);
+        ok = mbar_wait(&bar.q_full, qc & 1, abort_flag, p.wait);
         for (int j = 0; ok && j < nb; ++j) {
           const long long gs = g + j;
           const int st = (int)(gs % kStages), sb = (int)(gs & 1);
           const uint32_t kvpar = (uint32_t)((gs / kStages) & 1);
-          if (!(ok = mbar_wait(&bar.s_empty[sb], (uint32_t)((gs >> 1) & 1) ^ 1, abort_flag))) break;
+          if (!(ok = mbar_wait(&bar.s_empty[sb], (uint32_t)((gs >> 1) & 1) ^ 1, abort_flag, p.wait))) break;
           // descriptors: base + compile-time offsets in the 16-byte start-address field
           const uint64_t qd = q_desc0, kd = kv_desc0 + (uint64_t)((st * kKVBytes) >> 4);
           const uint32_t d = tmem + kColS + sb * kNB;
 #pragma unroll
           for (int a = 0; a < kAtoms; ++a) {
-            if (!(ok = mbar_wait(&bar.kv_full[st][a], kvpar, abort_flag))) break;
+            if (!(ok = mbar_wait(&bar.kv_full[st][a], kvpar, abort_flag, p.wait))) break;
             fence_async_smem();  // the stage was written by cp.async (generic proxy)
             tc_fence_after();
 #pragma unroll
@@ -337,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
       int nb = 0;
       if (lane == 0) {
-        ok = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag);
+        ok = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag, p.wait);
         nb = sm->nb[it & 1];
         mbar_arrive(&bar.info_empty[it & 1]);
       }
@@ -346,11 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (nb == 0) continue;
       if (lane == 0) {
-        ok = mbar_wait(&bar.o_empty, (oc & 1) ^ 1, abort_flag);
+        ok = mbar_wait(&bar.o_empty, (oc & 1) ^ 1, abort_flag, p.wait);
         for (int j = 0; ok && j < nb; ++j) {
           const long long gp = g + j;
           const int st = (int)(gp % kStages), pb = (int)(gp & 1);
-          if (!(ok = mbar_wait(&bar.p_full[pb], (uint32_t)((gp >> 1) & 1), abort_flag))) break;
+          if (!(ok = mbar_wait(&bar.p_full[pb], (uint32_t)((gp >> 1) & 1), abort_flag, p.wait))) break;
           fence_async_smem();
           tc_fence_after();
           const uint64_t vd = v_desc0 + (uint64_t)((st * kKVBytes) >> 4);
@@ -388,9 +405,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
       const int row = item / splits;
-      if (!(ok = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag))) break;
+      // every wait of these eight warps is followed by a barrier that ORs "it ran out" over
+      // them, so they leave together
+      const bool got_info = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag, p.wait);
+      if (named_sync_or(1, kSmThreads, !got_info)) {
+        ok = false;
+        break;
+      }
       const int nb = sm->nb[it & 1], j0 = sm->j0[it & 1];
-      named_sync(1, kSmThreads);
       if (t == 0) mbar_arrive(&bar.info_empty[it & 1]);
       __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * kH * kDV;
       float* po = splits > 1 ? p.part_o + (int64_t)item * kH * kDV : nullptr;  // this part's output
@@ -408,14 +430,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; ok && j < nb; ++j, ++g) {
         const int sb = (int)(g & 1);
-        if (!(ok = mbar_wait(&bar.s_full[sb], (uint32_t)((g >> 1) & 1), abort_flag))) break;
-        tc_fence_after();
+        const bool got_s = mbar_wait(&bar.s_full[sb], (uint32_t)((g >> 1) & 1), abort_flag, p.wait);
         uint32_t sr[32];
-        tmem_ld32(tmem + lane_base + kColS + sb * kNB + kh * 32, sr);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.s_empty[sb]);
+        if (got_s) {
+          tc_fence_after();
+          tmem_ld32(tmem + lane_base + kColS + sb * kNB + kh * 32, sr);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar.s_empty[sb]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sr[c] = 0u;  // leaving at the barrier below
+        }
         // scores in base-2 units, masked by the validity of each key slot (lane c checks key c)
         const int e = (j0 + j) * kNB + kh * 32 + lane;
         const int id = e < p.kk ? __ldg(irow + e) : -1;
@@ -432,7 +459,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int any = __any_sync(0xffffffffu, need_h);
         if (head_lane) sm->bmax[sb][kh][h] = bmax;
         if (lane == 0) sm->any_rescale[sb][sw] = any;
-        named_sync(1, kSmThreads);
+        if (named_sync_or(1, kSmThreads, !got_s)) {
+          ok = false;
+          break;
+        }
         int anyr = 0;
 #pragma unroll
         for (int w = 0; w < kSmWarps; ++w) anyr |= sm->any_rescale[sb][w];
@@ -443,11 +473,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           // O^T must be complete for the previous block before it is rescaled: the value
           // product of block g-1 releases its stage
           const long long gp = g - 1;
-          if (!(ok = mbar_wait(&bar.kv_empty[gp % kStages], (uint32_t)((gp / kStages) & 1), abort_flag))) break;
+          const bool got_o = mbar_wait(&bar.kv_empty[gp % kStages], (uint32_t)((gp / kStages) & 1), abort_flag, p.wait);
           const float alpha = need ? ex2(m_used - m_new) : 1.f;
           if (head_lane && kh == 0) sm->alpha[h] = alpha;
           l *= alpha;
-          named_sync(1, kSmThreads);
+          if (named_sync_or(1, kSmThreads, !got_o)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
 #pragma unroll 1
           for (int c = 2 * kh; c < 2 * kh + 2; ++c)  // each key half rescales two of the four chunks
@@ -499,8 +532,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (po) p.part_lse[(int64_t)item * kH + h] = lse_v;
         else if (p.lse) p.lse[(int64_t)row * kH + h] = lse_v;
       }
-      if (!(ok = mbar_wait(&bar.o_full, oc & 1, abort_flag))) break;
-      named_sync(1, kSmThreads);
+      const bool got_o = mbar_wait(&bar.o_full, oc & 1, abort_flag, p.wait);
+      if (named_sync_or(1, kSmThreads, !got_o)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
 #pragma unroll 1
       for (int c = 2 * kh; c < 2 * kh + 2; ++c) {
@@ -613,7 +649,7 @@ int num_sms() {
 
 bool sparse_mla_tc_supported(const AttnLaunch& p) {
   return p.H == kH && p.DQK == kDQK && p.DV == kDV && p.v == p.k && p.v_ld == p.k_ld && p.k_ld == kDQK &&
-         (int64_t)p.B * p.S < (1ll << 31);
+         p.v_sb == p.k_sb && p.S < (1 << 30);
 }
 
 cudaError_t launch_sparse_mla_tc(const AttnLaunch& p, cudaStream_t st) {
@@ -623,11 +659,13 @@ cudaError_t launch_sparse_mla_tc(const AttnLaunch& p, cudaStream_t st) {
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tq;
   {
-    cuuint64_t dims[3] = {(cuuint64_t)kDQK, (cuuint64_t)kH, (cuuint64_t)p.B * p.T};
-    cuuint64_t strides[2] = {(cuuint64_t)kDQK * 2, (cuuint64_t)kDQK * 2 * kH};
-    cuuint32_t box[3] = {64, (cuuint32_t)kH, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p.q), dims, strides, box, es,
+    // queries [B][T][H][576] with token strides q_st / q_sb; a box is one swizzle atom (64
+    // columns) of one query's 64 heads
+    cuuint64_t dims[4] = {(cuuint64_t)kDQK, (cuuint64_t)kH, (cuuint64_t)p.T, (cuuint64_t)p.B};
+    cuuint64_t strides[3] = {(cuuint64_t)kDQK * 2, (cuuint64_t)p.q_st * 2, (cuuint64_t)p.q_sb * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)kH, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(p.q), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -637,7 +675,9 @@ cudaError_t launch_sparse_mla_tc(const AttnLaunch& p, cudaStream_t st) {
   const int rows = p.B * p.T;
   const int items = rows * (p.splits > 1 ? p.splits : 1);
   const int grid = items < num_sms() ? items : num_sms();
-  k_sparse_mla_tc<<<grid, kThreads, kSmem, st>>>(tq, p);
+  AttnLaunch q = p;
+  if (q.wait <= 0) q.wait = wait_limit();
+  k_sparse_mla_tc<<<grid, kThreads, kSmem, st>>>(tq, q);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess || p.splits <= 1) return e;
   k_attn_combine<<<rows, 256, 0, st>>>(p);

@@ -149,12 +149,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_k);
       mbar_arrive_expect_tx(q_full, C::kQBytes);
       for (int kb = 0; kb < C::kKBlocks; ++kb)
-        tma_load_3d(q_s + kb * C::kQBlock, &tm_q, q_full, kb * C::kAtomElems, (p.t0 + tl0) * HI, b);
+        tma_load_4d(q_s + kb * C::kQBlock, &tm_q, q_full, kb * C::kAtomElems, 0, p.t0 + tl0, b);
       int issued = 0;
       for (int kt = 0; kt < ktiles; ++kt) {
         const int st = kt % C::kStages;
         const uint32_t ph = (kt / C::kStages) & 1;
-        if (!mbar_wait(k_empty + st, ph ^ 1, abort_flag)) break;
+        if (!mbar_wait(k_empty + st, ph ^ 1, abort_flag, p.wait)) break;
         mbar_arrive_expect_tx(k_full + st, C::kKTile);
         for (int kb = 0; kb < C::kKBlocks; ++kb)
           tma_load_3d(k_s + st * C::kKTile + kb * C::kKBlock, &tm_k, k_full + st, kb * C::kAtomElems,
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0 && ktiles > 0) {
-      bool ok = mbar_wait(q_full, 0, abort_flag);
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.wait);
       int done = 0;
       const uint64_t q_desc0 = desc_sw128(smem_addr(q_s));
       const uint64_t k_desc0 = desc_sw128(smem_addr(k_s));
@@ -178,8 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = kt % C::kStages;
         const uint32_t ph = (kt / C::kStages) & 1;
         const int buf = kt & (kBufs - 1);
-        if (!(ok = mbar_wait(tm_empty + buf, ((kt / kBufs) & 1) ^ 1, abort_flag))) break;
-        if (!(ok = mbar_wait(k_full + st, ph, abort_flag))) break;
+        if (!(ok = mbar_wait(tm_empty + buf, ((kt / kBufs) & 1) ^ 1, abort_flag, p.wait))) break;
+        if (!(ok = mbar_wait(k_full + st, ph, abort_flag, p.wait))) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * kN;
         const uint64_t kd = k_desc0 + (uint64_t)((st * C::kKTile) >> 4);
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int buf = kt & (kBufs - 1);
         const float sk = sk16_next;
         sk16_next = key_scale16(kt + 1);
-        if (!mbar_wait(tm_full + buf, (kt / kBufs) & 1, abort_flag)) break;
+        if (!mbar_wait(tm_full + buf, (kt / kBufs) & 1, abort_flag, p.wait)) break;
         tc_fence_after();
         const uint32_t col0 = tmem + ((uint32_t)(lq * 32) << 16) + buf * kN + ch * C::kCols;
         uint32_t r[2][32];
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int buf = kt & (kBufs - 1);
         const float sk = sk_next;
         sk_next = key_scale(kt + 1);
-        if (!mbar_wait(tm_full + buf, (kt / kBufs) & 1, abort_flag)) break;
+        if (!mbar_wait(tm_full + buf, (kt / kBufs) & 1, abort_flag, p.wait)) break;
         tc_fence_after();
         const uint32_t col0 = t_lane + buf * kN + ch * C::kCols;
         // all of this warp's accumulator columns in one go, then the buffer goes back to the MMA
@@ -386,17 +386,15 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D map over [dim2][dim1][row_elems] with a box of (atom_elems x box_rows x 1), 128-byte swizzle.
-cudaError_t make_map(CUtensorMap* m, const void* base, bool fp8, int row_elems, int64_t dim1, int64_t dim2,
-                     int atom_elems, int box_rows) {
+// Map over a `rank`-dimensional tensor whose innermost dimension holds row_elems contiguous
+// codes: dims[0] = row_elems, dims[1..rank-1] with byte strides strides[0..rank-2]; box
+// (atom_elems x box[1] x ...), 128-byte swizzle.
+cudaError_t make_map(CUtensorMap* m, const void* base, bool fp8, int rank, const cuuint64_t* dims,
+                     const cuuint64_t* strides, const cuuint32_t* box) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  const int esz = fp8 ? 1 : 2;
-  cuuint64_t dims[3] = {(cuuint64_t)row_elems, (cuuint64_t)dim1, (cuuint64_t)dim2};
-  cuuint64_t strides[2] = {(cuuint64_t)row_elems * esz, (cuuint64_t)(row_elems * esz) * (cuuint64_t)dim1};
-  cuuint32_t box[3] = {(cuuint32_t)atom_elems, (cuuint32_t)box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -408,13 +406,23 @@ cudaError_t launch_cfg(const IndexerLaunch& p, cudaStream_t st) {
   TraceScope trace(kTraceIndexer, st);
   using C = Cfg<HI, DI, FP8>;
   CUtensorMap tq, tk;
-  cudaError_t e = make_map(&tq, p.q, FP8, DI, (int64_t)p.T * HI, p.B, C::kAtomElems, kN);
+  const cuuint64_t esz = FP8 ? 1 : 2;
+  // queries [B][T][H_I][d_I] with token strides q_st / q_sb: a box is the block's kTB tokens
+  // x H_I heads x one swizzle atom of d_I, i.e. the [kTB * H_I = kN][atom] tile the MMA reads
+  const cuuint64_t qdims[4] = {(cuuint64_t)DI, (cuuint64_t)HI, (cuuint64_t)p.T, (cuuint64_t)p.B};
+  const cuuint64_t qstr[3] = {(cuuint64_t)DI * esz, (cuuint64_t)p.q_st * esz, (cuuint64_t)p.q_sb * esz};
+  const cuuint32_t qbox[4] = {(cuuint32_t)C::kAtomElems, (cuuint32_t)HI, (cuuint32_t)C::kTB, 1};
+  cudaError_t e = make_map(&tq, p.q, FP8, 4, qdims, qstr, qbox);
   if (e != cudaSuccess) return e;
-  if ((e = make_map(&tk, p.k, FP8, DI, p.S, p.B, C::kAtomElems, kM)) != cudaSuccess) return e;
+  const cuuint64_t kdims[3] = {(cuuint64_t)DI, (cuuint64_t)p.S, (cuuint64_t)p.B};
+  const cuuint64_t kstr[2] = {(cuuint64_t)DI * esz, (cuuint64_t)p.k_sb * esz};
+  const cuuint32_t kbox[3] = {(cuuint32_t)C::kAtomElems, (cuuint32_t)kM, 1};
+  if ((e = make_map(&tk, p.k, FP8, 3, kdims, kstr, kbox)) != cudaSuccess) return e;
   auto kern = k_indexer_tc<HI, DI, FP8>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem)) != cudaSuccess)
     return e;
   IndexerLaunch q = p;
+  if (q.wait <= 0) q.wait = wait_limit();
   const int nblk = (p.Tc + C::kTB - 1) / C::kTB;
   if (q.ksplit <= 0) {
     // split the key range when the token blocks alone would not give about four waves of

@@ -32,7 +32,6 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kPer = 8;                     // consecutive entries per thread per compaction step
-constexpr long long kWaitCycles = 2000000000LL;
 
 // Cap: candidates (and sampled keys) held in shared memory; Ring: bulk-copy slots;
 // Per: consecutive scores per thread per streaming step (a slot holds Per x 512 scores).
@@ -255,18 +254,29 @@ __device__ void ordered_output(Sm& sm, int64_t n, uint32_t tau, uint32_t ties, i
 }
 
 __device__ __forceinline__ uint32_t sa(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
-__device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// Waits for a ring slot's copy; gives up after `limit` cycles (raising *abort) or when another
+// thread has raised *abort.  A bound shorter than the default polls without suspending
+// (try_wait may sleep past a short bound and then report the phase complete).
+__device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, volatile int* abort, long long limit) {
   const long long t0 = clock64();
+  const bool poll = limit < kDefaultWaitCycles;
   while (true) {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(sa(bar)), "r"(parity)
-        : "memory");
+    if (poll)
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(ok)
+          : "r"(sa(bar)), "r"(parity)
+          : "memory");
+    else
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(ok)
+          : "r"(sa(bar)), "r"(parity)
+          : "memory");
     if (ok) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       *abort = 1;
       return false;
     }
@@ -361,9 +371,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
         asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(sa(&sm.full[s])) : "memory");
       }
     };
-    // the stream starts before the sample is taken, so its latency hides behind the select
+    // the stream starts before the sample is taken, so its latency hides behind the select;
+    // chunks [0, issued) have had their copies started (thread 0 keeps the count)
+    int64_t issued = 0;
     if (threadIdx.x == 0)
-      for (int64_t ci = 0; ci < Ring && ci < nchunks; ++ci) issue(ci);
+      for (; issued < Ring && issued < nchunks; ++issued) issue(issued);
     // threshold from a sample of whole 8-score groups (one 32-byte sector each), evenly
     // strided over the row, so the sample touches only every g-th sector
     const int64_t groups = n / 8;
@@ -392,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
       const int s = (int)(ci % Ring);
       // a thread whose copy wait timed out adds 2^16 to the block sum below (a chunk holds at
       // most 8,192 candidates), and the whole block leaves the pass after that sum
-      const bool landed = ring_wait(&sm.full[s], (uint32_t)((ci / Ring) & 1), &sm.abort);
+      const bool landed = ring_wait(&sm.full[s], (uint32_t)((ci / Ring) & 1), &sm.abort, p.wait);
       const int base = (int)ci * kChunk, blen = (int)bulk_len(ci);
       const int q = base + (int)threadIdx.x * Per;
       const float* slot = &sm.ring[s][threadIdx.x * Per];
@@ -424,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
       uint32_t o = count + block_excl_scan1(cnt + (landed ? 0u : 1u << 16), sm.stream_sums[ci & 1], &tot);
       if (tot >> 16) break;
       // every thread has read slot s (the scan synchronised the block): refill it
-      if (threadIdx.x == 0 && ci + Ring < nchunks) issue(ci + Ring);
+      if (threadIdx.x == 0 && ci + Ring < nchunks) issue(issued++);
       if (count + tot > (uint32_t)Cap && count >= (uint32_t)k) {
         // the buffer would overflow: keep only its exact top-k and raise the threshold to the
         // k-th key -- a later key equal to it loses the tie to every kept one -- then recount
@@ -456,12 +468,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
     if (kmax) atomicMax(&sm.kmax, kmax);
     __syncthreads();
     if (sm.abort) {
-      // a copy never completed: let the ones still in flight land before the CTA exits
+      // a wait ran out: let the copies still in flight -- the last Ring chunks issued, one per
+      // ring slot -- land before the CTA exits (with the default bound)
       if (threadIdx.x == 0) {
-        for (int64_t ci = nchunks - Ring > 0 ? nchunks - Ring : 0; ci < nchunks; ++ci) {
+        for (int64_t ci = issued - Ring > 0 ? issued - Ring : 0; ci < issued; ++ci) {
           const long long t0 = clock64();
           uint32_t okw = 0;
-          while (!okw && clock64() - t0 < kWaitCycles)
+          while (!okw && clock64() - t0 < kDefaultWaitCycles)
             asm volatile(
                 "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, "
                 "p;\n}\n"
@@ -561,7 +574,9 @@ cudaError_t launch_rows(const TopkLaunch& p, int rows, cudaStream_t st) {
   cudaError_t e =
       cudaFuncSetAttribute(k_topk_rows<Cap, Ring, Per>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k_topk_rows<Cap, Ring, Per><<<rows * (p.parts > 1 ? p.parts : 1), kThreads, smem, st>>>(p);
+  TopkLaunch q = p;
+  if (q.wait <= 0) q.wait = wait_limit();
+  k_topk_rows<Cap, Ring, Per><<<rows * (p.parts > 1 ? p.parts : 1), kThreads, smem, st>>>(q);
   return cudaGetLastError();
 }
 

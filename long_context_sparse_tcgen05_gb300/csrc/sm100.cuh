@@ -1,6 +1,6 @@
 // Thin inline-PTX wrappers for the sm_100-family features the kernels use: mbarriers,
 // TMA tensor loads, and the 5th-generation tensor core (tcgen05: TMEM allocation, MMA
-// issue/commit, TMEM loads).  Every wait is bounded: after about a second it raises the
+// issue/commit, TMEM loads).  Every wait is bounded: when its bound runs out it raises the
 // CTA's abort word and returns false, so no kernel can spin forever.
 #pragma once
 #include <cuda.h>
@@ -11,7 +11,7 @@
 namespace dsa {
 namespace sm100 {
 
-constexpr long long kWaitTimeoutCycles = 2000000000LL;  // ~1 s at 2 GHz
+constexpr long long kWaitTimeoutCycles = 2000000000LL;  // ~1 s at 2 GHz: the drain bound
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -53,20 +53,34 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase with the given parity to complete.  Gives up (returning false) when
-// another thread has raised *abort, or after kWaitTimeoutCycles, raising *abort itself.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// another thread has raised *abort, or after `limit` cycles, raising *abort itself.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, long long limit) {
+  if (limit < kWaitTimeoutCycles) {
+    // a short bound (tests of the timeout path): poll without suspending, since try_wait may
+    // sleep past the bound and then report the phase complete
+    const long long t0 = clock64();
+    while (!mbar_test(bar, parity)) {
+      if (*abort) return false;
+      if (clock64() - t0 > limit) {
+        *abort = 1;
+        return false;
+      }
+    }
+    return true;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitTimeoutCycles) {
+    if (clock64() - t0 > limit) {
       *abort = 1;
       return false;
     }
   }
 }
-// Same, ignoring the abort word (used to drain copies in flight before a CTA exits).
+// Same, ignoring the abort word, with the default bound (used to drain copies and products
+// in flight before a CTA exits, whatever bound the work's own waits had).
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity))
@@ -83,6 +97,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(
           smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(
+          smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar))
       : "memory");
 }
 

@@ -347,3 +347,99 @@ def test_overlap_matrix_rejects_huge_k_without_overflow(lib):
     bufs = (P * 2)(FAKE, FAKE)
     for k in (2 ** 31 - 1, 2 ** 30, 60000):
         assert lib.topk_overlap_matrix(bufs, 2, 10, k, None, m, P(FAKE), 1 << 30, None) == UNSUPPORTED
+
+
+# --- strides, size queries and the wait bound ---------------------------------------------
+
+@pytest.mark.parametrize("field,value,status", [
+    ("q_stride_t", 64 * 128 - 8, INVALID),   # tokens would overlap
+    ("q_stride_t", 64 * 128 + 4, MISALIGNED),  # 8 bytes of bf16: not a multiple of 16
+    ("q_stride_b", 4, MISALIGNED),
+    ("k_stride_b", 12, MISALIGNED),
+    ("q_stride_b", -16, INVALID),
+    ("k_stride_b", -64, INVALID),
+])
+def test_indexer_stride_validation(lib, field, value, status):
+    assert _topk_ix(lib, _ix(**{field: value})) == status
+
+
+def test_indexer_strides_accepted_when_aligned(lib):
+    # host validation passes; the call then fails only on the workspace it was not given
+    ix = _ix(q_stride_t=64 * 128 + 64, q_stride_b=10 ** 7, k_stride_b=64 * 128 * 3)
+    assert _topk_ix(lib, ix, ws_bytes=300) == WORKSPACE
+    ix8 = _ix(dtype=dsa.DSA_E4M3, q_scale=FAKE, k_scale=FAKE, q_stride_t=64 * 128 + 16, k_stride_b=16)
+    assert _topk_ix(lib, ix8, ws_bytes=300) == WORKSPACE
+    ix8.q_stride_t = 64 * 128 + 8        # 8 bytes of e4m3 codes
+    assert _topk_ix(lib, ix8, ws_bytes=300) == MISALIGNED
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("q_stride_t", 64 * 576 - 8, INVALID), ("q_stride_t", 64 * 576 + 4, MISALIGNED),
+    ("q_stride_b", 12, MISALIGNED), ("k_stride_b", 6, MISALIGNED), ("v_stride_b", -8, INVALID),
+])
+def test_attention_stride_validation(lib, field, value, status):
+    at = _at(**{field: value})
+    r = lib.dsa_sparse_attn(ctypes.byref(at), ctypes.c_void_p(FAKE), 16, ctypes.c_void_p(FAKE), None,
+                            ctypes.c_void_p(FAKE), 256, None)
+    assert r == status
+
+
+def test_topk_workspace_size_query(lib):
+    # many rows: one CTA per row, no scratch beyond the flag word
+    assert lib.dsa_topk_workspace_size(1, 4096, 131072, 0, 0, 2048) == 256
+    # a few long rows: room for the split lists, a whole number of (k positions + k keys + count)
+    # lists per row
+    n = lib.dsa_topk_workspace_size(32, 1, 200000, 200000, 0, 2048)
+    assert n > 256 and (n - 256) % (32 * (2048 * 8 + 4)) == 0
+    # short rows are never split
+    assert lib.dsa_topk_workspace_size(4, 1, 20000, 20000, 0, 2048) == 256
+    # arguments the call would reject
+    for args in ((0, 1, 10, 0, 0, 8), (1, 1, 10, 0, 2, 8), (1, 1, 10, -1, 0, 8), (1, 1, 10, 0, 0, 5000)):
+        assert lib.dsa_topk_workspace_size(*args) == 256
+
+
+def test_attention_workspace_size_query(lib):
+    at = _at(B=32, T=1, S=200000)
+    n = lib.dsa_attn_workspace_size(ctypes.byref(at), 2048)
+    # split parts: fp32 outputs [64 x 512] and 64 LSEs per part, a whole number of parts per row
+    assert n > 256 and (n - 256) % (32 * 64 * 513 * 4) == 0
+    assert lib.dsa_attn_workspace_size(ctypes.byref(_at(B=1, T=4096)), 2048) == 256   # enough rows
+    small = _at(H=8, d_qk=64, d_v=64, k_ld=64, v_ld=64, B=1, T=4)
+    assert lib.dsa_attn_workspace_size(ctypes.byref(small), 64) == 256                # mma.sync shape
+    assert lib.dsa_attn_workspace_size(None, 64) == 256
+    # a short index row is not worth splitting
+    assert lib.dsa_attn_workspace_size(ctypes.byref(at), 64) == 256
+
+
+def test_group_workspace_size_covers_every_layer(lib):
+    arr = (dsa.Layer * 4)()
+    for i in range(4):
+        arr[i].ix = _ix(B=32, T=1, S=200000, q_pos0=200000, dtype=dsa.DSA_E4M3, q_scale=FAKE, k_scale=FAKE)
+        arr[i].at = _at(B=32, T=1, S=200000)
+        arr[i].out = FAKE
+    got = lib.indexshare_group_workspace_size(arr, 4, b"FSSS", 2048, None)
+    want = max(lib.dsa_workspace_size(ctypes.byref(arr[0].ix), 2048),
+               lib.dsa_attn_workspace_size(ctypes.byref(arr[0].at), 2048))
+    assert got == want and got > 256
+    assert lib.indexshare_group_workspace_size(arr, 4, b"FSS", 2048, None) == 256
+    assert lib.indexshare_group_workspace_size(None, 4, b"FSSS", 2048, None) == 256
+    # packed: the largest sequence's group need
+    cu = [0, 1, 2]
+    v = dsa.Varlen(2, (ctypes.c_int64 * 3)(*cu), (ctypes.c_int64 * 3)(0, 200000, 400000), (ctypes.c_int64 * 2)(200000, 200000))
+    pk = (dsa.Layer * 4)()
+    for i in range(4):
+        pk[i].ix = _ix(B=1, T=2, S=400000, dtype=dsa.DSA_E4M3, q_scale=FAKE, k_scale=FAKE)
+        pk[i].at = _at(B=1, T=2, S=400000)
+        pk[i].out = FAKE
+    one = (dsa.Layer * 4)()
+    for i in range(4):
+        one[i].ix = _ix(B=1, T=1, S=200000, q_pos0=200000, dtype=dsa.DSA_E4M3, q_scale=FAKE, k_scale=FAKE)
+        one[i].at = _at(B=1, T=1, S=200000)
+        one[i].out = FAKE
+    assert lib.indexshare_group_workspace_size(pk, 4, b"FSSS", 2048, ctypes.byref(v)) == \
+        lib.indexshare_group_workspace_size(one, 4, b"FSSS", 2048, None)
+
+
+def test_wait_limit_setter_is_callable(lib):
+    lib.dsa_set_wait_limit(100)
+    lib.dsa_set_wait_limit(0)  # back to the default

@@ -1,0 +1,77 @@
+"""The bounded-wait path on the GPU, made to run out on purpose without touching the GPU's
+state: with dsa_set_wait_limit(1) every wait that is not already complete gives up at once,
+so each kernel stops its work, lets the copies and tensor-core products it has started
+finish, frees its tensor memory and raises DSA_FLAG_TIMEOUT.  A normal call on the same
+process afterwards must still match the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import long_context_sparse_tcgen05_gb300 as dsa
+import oracle
+from long_context_sparse_tcgen05_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from long_context_sparse_tcgen05_gb300 import build
+    build.build()
+    dsa.load_library()
+    dsa.read_device_flags()
+    yield
+    dsa.set_wait_limit(0)
+
+
+def _run_all(ix, sc, at, idx, k):
+    """The three kernels that wait on barriers: the indexer (TMA ring, MMA, epilogue), the
+    top-k's bulk-copy ring (rows longer than 4,096 scores) and the tcgen05 attention."""
+    a = dsa.dsa_topk(k, ix=ix)
+    b = dsa.dsa_topk(k, scores=sc[None], q_pos0=sc.shape[1] - sc.shape[0])
+    o, l = dsa.dsa_sparse_attn(at, idx)
+    torch.cuda.synchronize()
+    return a, b, o, l
+
+
+def test_waits_that_run_out_raise_the_flag_and_leave_the_gpu_usable():
+    wl = synth.WORKLOADS["prefill_16k"].replace(T=64, S=8192, q_pos0=8192 - 64, idx_dtype="e4m3",
+                                                values="int", k=256)
+    ix = synth.indexer_inputs(wl, 0, DEV)
+    sc = synth.scores_input(16, 20000, DEV, "int", lo=-50, hi=50)
+    at = synth.attn_inputs(wl.replace(T=160), 0, DEV)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    idx = torch.sort(torch.randint(0, wl.S, (1, 160, wl.k), generator=g, device=DEV, dtype=torch.int32), -1).values
+    try:
+        dsa.set_wait_limit(1)
+        _run_all(ix, sc, at, idx, wl.k)
+        flags = dsa.read_device_flags()
+    finally:
+        dsa.set_wait_limit(0)
+    assert flags & dsa.FLAG_TIMEOUT, hex(flags)
+    # each kernel on its own raises the flag too
+    for call in (lambda: dsa.dsa_topk(wl.k, ix=ix),
+                 lambda: dsa.dsa_topk(wl.k, scores=sc[None], q_pos0=20000 - 16),
+                 lambda: dsa.dsa_sparse_attn(at, idx)):
+        try:
+            dsa.set_wait_limit(1)
+            call()
+            torch.cuda.synchronize()
+        finally:
+            dsa.set_wait_limit(0)
+        assert dsa.read_device_flags() & dsa.FLAG_TIMEOUT
+    # the same calls with the default bound: exact again, no flag
+    a, b, o, l = _run_all(ix, sc, at, idx, wl.k)
+    assert dsa.read_device_flags() == 0
+    rows = [0, 13, 63]
+    ref = oracle.indexer_topk({k: (v.cpu() if torch.is_tensor(v) else v) for k, v in ix.items()}, wl.k, rows)
+    assert np.array_equal(a.reshape(-1, wl.k)[rows].cpu().numpy(), ref)
+    ref_b = oracle.topk_rows(sc.double().cpu().numpy(), np.arange(16) + 20000 - 16, wl.k)
+    assert np.array_equal(b[0].cpu().numpy(), ref_b)
+    host = dict(q_rows=at["q"].reshape(-1, wl.H, wl.DQK)[rows].cpu(), k=at["k"].cpu(), v=None, d_v=wl.DV,
+                scale=wl.scale, T=160)
+    ref_o, _ = oracle.sparse_attn(host, idx.reshape(-1, wl.k)[rows].cpu().numpy(), rows)
+    assert np.abs(o.reshape(-1, wl.H, wl.DV)[rows].float().cpu().numpy() - ref_o).max() <= 2e-2
