@@ -130,6 +130,7 @@ __device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t lbo) 
   return d;
 }
 
+template <bool kPoll>
 __global__ void __launch_bounds__(kThreads, 1)
     k_sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, AttnLaunch p) {
   extern __shared__ uint8_t smem_raw[];
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int split = item % splits;
       const int j0 = split * nbr / splits, nb = (split + 1) * nbr / splits - j0;  // this item's blocks
       if (warp == 0) {
-        if (lane == 0) ok = mbar_wait(&bar.info_empty[it & 1], ((it >> 1) & 1) ^ 1, abort_flag, p.wait);
+        if (lane == 0) ok = mbar_wait<kPoll>(&bar.info_empty[it & 1], ((it >> 1) & 1) ^ 1, abort_flag, p.wait);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (ok && lane == 0) {
           sm->nb[it & 1] = nb;
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           (int64_t)(next_row % p.T) * p.q_st,
                       kQBytes);
         if (lane == 0) {
-          ok = mbar_wait(&bar.q_empty, (qc & 1) ^ 1, abort_flag, p.wait);
+          ok = mbar_wait<kPoll>(&bar.q_empty, (qc & 1) ^ 1, abort_flag, p.wait);
           if (ok) {
             mbar_arrive_expect_tx(&bar.q_full, kQBytes);
             for (int a = 0; a < kAtoms; ++a)
@@ -261,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool valid = id >= 0 && id < p.S;
         if (lane < kRowsW && !valid && id != -1) atomicOr(p.flags, DSA_FLAG_BAD_INDEX);
         if (!valid) id = 0;
-        if (!(ok = mbar_wait(&bar.kv_empty[st], (uint32_t)((g / kStages) & 1) ^ 1, abort_flag, p.wait))) break;
+        if (!(ok = mbar_wait<kPoll>(&bar.kv_empty[st], (uint32_t)((g / kStages) & 1) ^ 1, abort_flag, p.wait))) break;
         uint8_t* stage = kv_s + st * kKVBytes;
         // atom by atom: 8 lanes per row (one 16-byte chunk each), 4 rows per pass, 4 passes
         // cover the warp's 16 rows; the row of each pass is fixed, so its id is fetched once
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
       int nb = 0;
       if (lane == 0) {
-        ok = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag, p.wait);
+        ok = mbar_wait<kPoll>(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag, p.wait);
         nb = sm->nb[it & 1];
         mbar_arrive(&bar.info_empty[it & 1]);
       }
@@ -311,18 +312,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (nb == 0) continue;
       if (lane == 0) {
-        ok = mbar_wait(&bar.q_full, qc & 1, abort_flag, p.wait);
+        ok = mbar_wait<kPoll>(&bar.q_full, qc & 1, abort_flag, p.wait);
         for (int j = 0; ok && j < nb; ++j) {
           const long long gs = g + j;
           const int st = (int)(gs % kStages), sb = (int)(gs & 1);
           const uint32_t kvpar = (uint32_t)((gs / kStages) & 1);
-          if (!(ok = mbar_wait(&bar.s_empty[sb], (uint32_t)((gs >> 1) & 1) ^ 1, abort_flag, p.wait))) break;
+          if (!(ok = mbar_wait<kPoll>(&bar.s_empty[sb], (uint32_t)((gs >> 1) & 1) ^ 1, abort_flag, p.wait))) break;
           // descriptors: base + compile-time offsets in the 16-byte start-address field
           const uint64_t qd = q_desc0, kd = kv_desc0 + (uint64_t)((st * kKVBytes) >> 4);
           const uint32_t d = tmem + kColS + sb * kNB;
 #pragma unroll
           for (int a = 0; a < kAtoms; ++a) {
-            if (!(ok = mbar_wait(&bar.kv_full[st][a], kvpar, abort_flag, p.wait))) break;
+            if (!(ok = mbar_wait<kPoll>(&bar.kv_full[st][a], kvpar, abort_flag, p.wait))) break;
             fence_async_smem();  // the stage was written by cp.async (generic proxy)
             tc_fence_after();
 #pragma unroll
@@ -354,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
       int nb = 0;
       if (lane == 0) {
-        ok = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag, p.wait);
+        ok = mbar_wait<kPoll>(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag, p.wait);
         nb = sm->nb[it & 1];
         mbar_arrive(&bar.info_empty[it & 1]);
       }
@@ -363,11 +364,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (nb == 0) continue;
       if (lane == 0) {
-        ok = mbar_wait(&bar.o_empty, (oc & 1) ^ 1, abort_flag, p.wait);
+        ok = mbar_wait<kPoll>(&bar.o_empty, (oc & 1) ^ 1, abort_flag, p.wait);
         for (int j = 0; ok && j < nb; ++j) {
           const long long gp = g + j;
           const int st = (int)(gp % kStages), pb = (int)(gp & 1);
-          if (!(ok = mbar_wait(&bar.p_full[pb], (uint32_t)((gp >> 1) & 1), abort_flag, p.wait))) break;
+          if (!(ok = mbar_wait<kPoll>(&bar.p_full[pb], (uint32_t)((gp >> 1) & 1), abort_flag, p.wait))) break;
           fence_async_smem();
           tc_fence_after();
           const uint64_t vd = v_desc0 + (uint64_t)((st * kKVBytes) >> 4);
@@ -407,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = item / splits;
       // every wait of these eight warps is followed by a barrier that ORs "it ran out" over
       // them, so they leave together
-      const bool got_info = mbar_wait(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag, p.wait);
+      const bool got_info = mbar_wait<kPoll>(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag, p.wait);
       if (named_sync_or(1, kSmThreads, !got_info)) {
         ok = false;
         break;
@@ -430,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; ok && j < nb; ++j, ++g) {
         const int sb = (int)(g & 1);
-        const bool got_s = mbar_wait(&bar.s_full[sb], (uint32_t)((g >> 1) & 1), abort_flag, p.wait);
+        const bool got_s = mbar_wait<kPoll>(&bar.s_full[sb], (uint32_t)((g >> 1) & 1), abort_flag, p.wait);
         uint32_t sr[32];
         if (got_s) {
           tc_fence_after();
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // O^T must be complete for the previous block before it is rescaled: the value
           // product of block g-1 releases its stage
           const long long gp = g - 1;
-          const bool got_o = mbar_wait(&bar.kv_empty[gp % kStages], (uint32_t)((gp / kStages) & 1), abort_flag, p.wait);
+          const bool got_o = mbar_wait<kPoll>(&bar.kv_empty[gp % kStages], (uint32_t)((gp / kStages) & 1), abort_flag, p.wait);
           const float alpha = need ? ex2(m_used - m_new) : 1.f;
           if (head_lane && kh == 0) sm->alpha[h] = alpha;
           l *= alpha;
@@ -532,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (po) p.part_lse[(int64_t)item * kH + h] = lse_v;
         else if (p.lse) p.lse[(int64_t)row * kH + h] = lse_v;
       }
-      const bool got_o = mbar_wait(&bar.o_full, oc & 1, abort_flag, p.wait);
+      const bool got_o = mbar_wait<kPoll>(&bar.o_full, oc & 1, abort_flag, p.wait);
       if (named_sync_or(1, kSmThreads, !got_o)) {
         ok = false;
         break;
@@ -670,14 +671,15 @@ cudaError_t launch_sparse_mla_tc(const AttnLaunch& p, cudaStream_t st) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(k_sparse_mla_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  AttnLaunch q = p;
+  if (q.wait <= 0) q.wait = wait_limit();
+  auto kern = q.wait < kDefaultWaitCycles ? k_sparse_mla_tc<true> : k_sparse_mla_tc<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (e != cudaSuccess) return e;
   const int rows = p.B * p.T;
   const int items = rows * (p.splits > 1 ? p.splits : 1);
   const int grid = items < num_sms() ? items : num_sms();
-  AttnLaunch q = p;
-  if (q.wait <= 0) q.wait = wait_limit();
-  k_sparse_mla_tc<<<grid, kThreads, kSmem, st>>>(tq, q);
+  kern<<<grid, kThreads, kSmem, st>>>(tq, q);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess || p.splits <= 1) return e;
   k_attn_combine<<<rows, 256, 0, st>>>(p);

@@ -78,7 +78,7 @@ __device__ __forceinline__ int64_t visible_keys(const IndexerLaunch& p, int t_lo
   return n < 0 ? 0 : (n > p.S ? (int64_t)p.S : n);
 }
 
-template <int HI, int DI, bool FP8>
+template <int HI, int DI, bool FP8, bool kPoll>
 __global__ void __launch_bounds__(kThreads, 1)
     k_indexer_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  IndexerLaunch p) {
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kt = 0; kt < ktiles; ++kt) {
         const int st = kt % C::kStages;
         const uint32_t ph = (kt / C::kStages) & 1;
-        if (!mbar_wait(k_empty + st, ph ^ 1, abort_flag, p.wait)) break;
+        if (!mbar_wait<kPoll>(k_empty + st, ph ^ 1, abort_flag, p.wait)) break;
         mbar_arrive_expect_tx(k_full + st, C::kKTile);
         for (int kb = 0; kb < C::kKBlocks; ++kb)
           tma_load_3d(k_s + st * C::kKTile + kb * C::kKBlock, &tm_k, k_full + st, kb * C::kAtomElems,
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0 && ktiles > 0) {
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.wait);
+      bool ok = mbar_wait<kPoll>(q_full, 0, abort_flag, p.wait);
       int done = 0;
       const uint64_t q_desc0 = desc_sw128(smem_addr(q_s));
       const uint64_t k_desc0 = desc_sw128(smem_addr(k_s));
@@ -178,8 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = kt % C::kStages;
         const uint32_t ph = (kt / C::kStages) & 1;
         const int buf = kt & (kBufs - 1);
-        if (!(ok = mbar_wait(tm_empty + buf, ((kt / kBufs) & 1) ^ 1, abort_flag, p.wait))) break;
-        if (!(ok = mbar_wait(k_full + st, ph, abort_flag, p.wait))) break;
+        if (!(ok = mbar_wait<kPoll>(tm_empty + buf, ((kt / kBufs) & 1) ^ 1, abort_flag, p.wait))) break;
+        if (!(ok = mbar_wait<kPoll>(k_full + st, ph, abort_flag, p.wait))) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * kN;
         const uint64_t kd = k_desc0 + (uint64_t)((st * C::kKTile) >> 4);
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int buf = kt & (kBufs - 1);
         const float sk = sk16_next;
         sk16_next = key_scale16(kt + 1);
-        if (!mbar_wait(tm_full + buf, (kt / kBufs) & 1, abort_flag, p.wait)) break;
+        if (!mbar_wait<kPoll>(tm_full + buf, (kt / kBufs) & 1, abort_flag, p.wait)) break;
         tc_fence_after();
         const uint32_t col0 = tmem + ((uint32_t)(lq * 32) << 16) + buf * kN + ch * C::kCols;
         uint32_t r[2][32];
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int buf = kt & (kBufs - 1);
         const float sk = sk_next;
         sk_next = key_scale(kt + 1);
-        if (!mbar_wait(tm_full + buf, (kt / kBufs) & 1, abort_flag, p.wait)) break;
+        if (!mbar_wait<kPoll>(tm_full + buf, (kt / kBufs) & 1, abort_flag, p.wait)) break;
         tc_fence_after();
         const uint32_t col0 = t_lane + buf * kN + ch * C::kCols;
         // all of this warp's accumulator columns in one go, then the buffer goes back to the MMA
@@ -418,11 +418,11 @@ cudaError_t launch_cfg(const IndexerLaunch& p, cudaStream_t st) {
   const cuuint64_t kstr[2] = {(cuuint64_t)DI * esz, (cuuint64_t)p.k_sb * esz};
   const cuuint32_t kbox[3] = {(cuuint32_t)C::kAtomElems, (cuuint32_t)kM, 1};
   if ((e = make_map(&tk, p.k, FP8, 3, kdims, kstr, kbox)) != cudaSuccess) return e;
-  auto kern = k_indexer_tc<HI, DI, FP8>;
-  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem)) != cudaSuccess)
-    return e;
   IndexerLaunch q = p;
   if (q.wait <= 0) q.wait = wait_limit();
+  auto kern = q.wait < kDefaultWaitCycles ? k_indexer_tc<HI, DI, FP8, true> : k_indexer_tc<HI, DI, FP8, false>;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem)) != cudaSuccess)
+    return e;
   const int nblk = (p.Tc + C::kTB - 1) / C::kTB;
   if (q.ksplit <= 0) {
     // split the key range when the token blocks alone would not give about four waves of

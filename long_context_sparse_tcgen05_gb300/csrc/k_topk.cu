@@ -255,14 +255,15 @@ __device__ void ordered_output(Sm& sm, int64_t n, uint32_t tau, uint32_t ties, i
 
 __device__ __forceinline__ uint32_t sa(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 // Waits for a ring slot's copy; gives up after `limit` cycles (raising *abort) or when another
-// thread has raised *abort.  A bound shorter than the default polls without suspending
-// (try_wait may sleep past a short bound and then report the phase complete).
+// thread has raised *abort.  kPoll (the instantiation for a bound shorter than the default,
+// used to test the timeout path) polls with test_wait, which never suspends (try_wait may
+// sleep until the copy lands and so hide a short bound).
+template <bool kPoll>
 __device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, volatile int* abort, long long limit) {
   const long long t0 = clock64();
-  const bool poll = limit < kDefaultWaitCycles;
   while (true) {
     uint32_t ok;
-    if (poll)
+    if constexpr (kPoll)
       asm volatile(
           "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}\n"
           : "=r"(ok)
@@ -283,7 +284,7 @@ __device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-template <int Cap, int Ring, int Per>
+template <int Cap, int Ring, int Per, bool kPoll>
 __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
   using Sm = TopkSmem<Cap, Ring, Per>;
   constexpr int kChunk = kThreads * Per;
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
       const int s = (int)(ci % Ring);
       // a thread whose copy wait timed out adds 2^16 to the block sum below (a chunk holds at
       // most 8,192 candidates), and the whole block leaves the pass after that sum
-      const bool landed = ring_wait(&sm.full[s], (uint32_t)((ci / Ring) & 1), &sm.abort, p.wait);
+      const bool landed = ring_wait<kPoll>(&sm.full[s], (uint32_t)((ci / Ring) & 1), &sm.abort, p.wait);
       const int base = (int)ci * kChunk, blen = (int)bulk_len(ci);
       const int q = base + (int)threadIdx.x * Per;
       const float* slot = &sm.ring[s][threadIdx.x * Per];
@@ -571,12 +572,12 @@ template <int Cap, int Ring, int Per>
 cudaError_t launch_rows(const TopkLaunch& p, int rows, cudaStream_t st) {
   TraceScope trace(kTraceTopk, st);
   const int smem = (int)sizeof(TopkSmem<Cap, Ring, Per>);
-  cudaError_t e =
-      cudaFuncSetAttribute(k_topk_rows<Cap, Ring, Per>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
   TopkLaunch q = p;
   if (q.wait <= 0) q.wait = wait_limit();
-  k_topk_rows<Cap, Ring, Per><<<rows * (p.parts > 1 ? p.parts : 1), kThreads, smem, st>>>(q);
+  auto kern = q.wait < kDefaultWaitCycles ? k_topk_rows<Cap, Ring, Per, true> : k_topk_rows<Cap, Ring, Per, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<rows * (p.parts > 1 ? p.parts : 1), kThreads, smem, st>>>(q);
   return cudaGetLastError();
 }
 

@@ -54,10 +54,12 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 }
 // Wait for the phase with the given parity to complete.  Gives up (returning false) when
 // another thread has raised *abort, or after `limit` cycles, raising *abort itself.
+// kPoll (the kernels' instantiation for a bound shorter than the default, used to test the
+// timeout path) polls with test_wait, which never suspends: try_wait may sleep until the
+// phase completes and so hide a short bound.  The default instantiation suspends in try_wait.
+template <bool kPoll = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, long long limit) {
-  if (limit < kWaitTimeoutCycles) {
-    // a short bound (tests of the timeout path): poll without suspending, since try_wait may
-    // sleep past the bound and then report the phase complete
+  if constexpr (kPoll) {
     const long long t0 = clock64();
     while (!mbar_test(bar, parity)) {
       if (*abort) return false;
@@ -67,15 +69,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       }
     }
     return true;
-  }
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
+  } else {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (clock64() - t0 > limit) {
-      *abort = 1;
-      return false;
+    const long long t0 = clock64();
+    while (true) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if (*abort) return false;
+      if (clock64() - t0 > limit) {
+        *abort = 1;
+        return false;
+      }
     }
   }
 }

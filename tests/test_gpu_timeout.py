@@ -53,21 +53,21 @@ def test_waits_that_run_out_raise_the_flag_and_leave_the_gpu_usable():
         dsa.set_wait_limit(0)
     assert flags & dsa.FLAG_TIMEOUT, hex(flags)
     # each kernel on its own raises the flag too
-    for call in (lambda: dsa.dsa_topk(wl.k, ix=ix),
-                 lambda: dsa.dsa_topk(wl.k, scores=sc[None], q_pos0=20000 - 16),
-                 lambda: dsa.dsa_sparse_attn(at, idx)):
+    for name, call in (("indexer + top-k", lambda: dsa.dsa_topk(wl.k, ix=ix)),
+                       ("top-k over scores", lambda: dsa.dsa_topk(wl.k, scores=sc[None], q_pos0=20000 - 16)),
+                       ("attention", lambda: dsa.dsa_sparse_attn(at, idx))):
         try:
             dsa.set_wait_limit(1)
             call()
             torch.cuda.synchronize()
         finally:
             dsa.set_wait_limit(0)
-        assert dsa.read_device_flags() & dsa.FLAG_TIMEOUT
+        assert dsa.read_device_flags() & dsa.FLAG_TIMEOUT, name
     # the same calls with the default bound: exact again, no flag
     a, b, o, l = _run_all(ix, sc, at, idx, wl.k)
     assert dsa.read_device_flags() == 0
     rows = [0, 13, 63]
-    ref = oracle.indexer_topk({k: (v.cpu() if torch.is_tensor(v) else v) for k, v in ix.items()}, wl.k, rows)
+    ref = oracle.indexer_topk(ix, wl.k, rows)
     assert np.array_equal(a.reshape(-1, wl.k)[rows].cpu().numpy(), ref)
     ref_b = oracle.topk_rows(sc.double().cpu().numpy(), np.arange(16) + 20000 - 16, wl.k)
     assert np.array_equal(b[0].cpu().numpy(), ref_b)
