@@ -291,7 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
     (void)leader;
-    if (*abort_flag && warp == 0 && lane == 0 && qc > 0) mbar_wait_drain(&bar.q_full, (uint32_t)((qc - 1) & 1));
+    // the last query tile issued has landed before the CTA can exit (whichever wait ran out)
+    if (warp == 0 && lane == 0 && qc > 0) mbar_wait_drain(&bar.q_full, (uint32_t)((qc - 1) & 1));
   } else if (warp == kMmaWarp) {
     // ================= score product issuer (one thread) =================
     const uint32_t id_s = idesc_mn(1, 1, kH, kNB);  // S: M=64 heads, N=64 keys
@@ -431,6 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; ok && j < nb; ++j, ++g) {
         const int sb = (int)(g & 1);
+        // this lane's key slot, loaded before the wait so that its latency hides behind it
+        const int e = (j0 + j) * kNB + kh * 32 + lane;
+        const int id = e < p.kk ? __ldg(irow + e) : -1;
         const bool got_s = mbar_wait<kPoll>(&bar.s_full[sb], (uint32_t)((g >> 1) & 1), abort_flag, p.wait);
         uint32_t sr[32];
         if (got_s) {
@@ -445,8 +449,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 32; ++c) sr[c] = 0u;  // leaving at the barrier below
         }
         // scores in base-2 units, masked by the validity of each key slot (lane c checks key c)
-        const int e = (j0 + j) * kNB + kh * 32 + lane;
-        const int id = e < p.kk ? __ldg(irow + e) : -1;
         const uint32_t vm = __ballot_sync(0xffffffffu, id >= 0 && id < p.S);
         float s[32];
         float bmax = -INFINITY;

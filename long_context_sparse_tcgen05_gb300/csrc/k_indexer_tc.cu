@@ -161,11 +161,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (kt_lo + kt) * kM, b);
         issued = kt + 1;
       }
-      if (*abort_flag) {  // let every copy still in flight land before the CTA can exit
-        mbar_wait_drain(q_full, 0);
-        for (int kt = issued > C::kStages ? issued - C::kStages : 0; kt < issued; ++kt)
-          mbar_wait_drain(k_full + kt % C::kStages, (kt / C::kStages) & 1);
-      }
+      // every copy issued lands before the CTA can exit: a wait elsewhere in the CTA may run
+      // out after this loop has ended (in a normal run these phases are long complete)
+      mbar_wait_drain(q_full, 0);
+      for (int kt = issued > C::kStages ? issued - C::kStages : 0; kt < issued; ++kt)
+        mbar_wait_drain(k_full + kt % C::kStages, (kt / C::kStages) & 1);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -199,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(tm_full + buf);
         done = kt + 1;
       }
-      if (*abort_flag && done > 0) mbar_wait_drain(tm_full + ((done - 1) & (kBufs - 1)), ((done - 1) / kBufs) & 1);
+      // the products issued are complete before TMEM can be freed, whichever wait ran out
+      if (done > 0) mbar_wait_drain(tm_full + ((done - 1) & (kBufs - 1)), ((done - 1) / kBufs) & 1);
     }
   } else if (((warp - 2) >> 2) < active_ch) {
     // ---------------- epilogue ----------------
