@@ -123,9 +123,14 @@ typedef struct {
 typedef enum { DSA_TOPK_FROM_SCORES = 0, DSA_TOPK_FROM_INDEXER = 1 } dsa_topk_kind;
 
 /* Source of a top-k: a materialised fp32 score buffer [B,T,ld] (ld >= S; only the visible
- * prefix of each row is read), or the indexer operands.  From indexer operands the scores
- * of a chunk of query rows pass through the caller's workspace (fp32, up to 4 GiB per chunk,
- * see dsa_workspace_size) and are read back by the selection; the caller never sees them. */
+ * prefix of each row is read), or the indexer operands.  From indexer operands with 64 indexer
+ * heads, k <= 2048 and enough query rows to fill the GPU, the scores are never stored: the
+ * indexer keeps, per query row, only the keys whose score reaches a threshold set from a sample
+ * of the row (a few thousand (score, position) pairs in the workspace), and an exact top-k runs
+ * over them; a row whose candidates could not hold its top-k (rare: a badly sampled or heavily
+ * tied row) is recomputed through a score buffer in the workspace.  Other shapes (decode's few
+ * rows, 4 indexer heads, larger k) pass the scores of a chunk of rows through that buffer (fp32,
+ * up to 4 GiB per chunk).  Either way the result is the exact top-k. */
 typedef struct {
   dsa_topk_kind kind;
   const float* scores;
@@ -146,10 +151,12 @@ typedef struct {
  * the device's SM count); the calls accept less, down to the stated minimum, and then take a
  * slower schedule with identical results.  Calls that need no scratch take DSA_WS_MIN.
  *
- * dsa_workspace_size: dsa_topk(FROM_INDEXER) for this indexer shape -- a chunk of fp32 score
- *   rows (up to 4 GiB; at least DSA_WS_MIN plus one row chunk of B*S*4 bytes is required)
- *   and, when a chunk has fewer query rows than the device has SMs, room for splitting each
- *   row's top-k across CTAs.
+ * dsa_workspace_size: dsa_topk(FROM_INDEXER) for this indexer shape -- the candidate lists of
+ *   the path that stores no scores when it applies (at most 1 GiB: 8,192 (score, position)
+ *   pairs per row of a chunk of rows), a score buffer of fp32 rows (up to 4 GiB; at least
+ *   DSA_WS_MIN plus one row of B*S*4 bytes is required) and, when a chunk has fewer query rows
+ *   than the device has SMs, room for splitting each row's top-k across CTAs.  Without room
+ *   for the candidate lists the call stores the scores of every row.
  * dsa_topk_workspace_size: dsa_topk(FROM_SCORES) over B*T rows of the given visibility --
  *   DSA_WS_MIN plus the split room when the rows are few and long (0 extra otherwise).
  * dsa_attn_workspace_size: dsa_sparse_attn -- DSA_WS_MIN plus, for the 64-head latent shape

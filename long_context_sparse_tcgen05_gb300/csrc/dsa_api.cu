@@ -168,7 +168,8 @@ int64_t max_visible(int64_t q_pos0, int T, int diag, int S) {
   return n < 0 ? 0 : (n > S ? S : n);
 }
 
-// Query rows per chunk of the materialised score buffer that `ws_bytes` can hold.
+// Query rows per chunk of the materialised score buffer that `bytes` of scratch (after the
+// 256-byte header) can hold.
 int64_t score_chunk_rows(const dsa_indexer_args* ix, size_t ws_bytes) {
   if (ws_bytes <= dsa::kWsScratch) return 0;
   const int64_t per_row = (int64_t)ix->B * ix->S * 4;
@@ -176,28 +177,114 @@ int64_t score_chunk_rows(const dsa_indexer_args* ix, size_t ws_bytes) {
   return rows > ix->T ? ix->T : rows;
 }
 
-dsa_status run_indexer_topk(const dsa_indexer_args* ix, int32_t k, int32_t* idx, void* ws, size_t ws_bytes,
-                            cudaStream_t st) {
-  const int64_t chunk = score_chunk_rows(ix, ws_bytes);
-  if (chunk < 1) return fail(DSA_ERR_WORKSPACE, "workspace too small for one row of indexer scores (%zu bytes)", ws_bytes);
-  float* sc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + dsa::kWsScratch);
-  for (int64_t t0 = 0; t0 < ix->T; t0 += chunk) {
-    const int Tc = (int)((ix->T - t0) < chunk ? (ix->T - t0) : chunk);
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0)
+    sms = 148;
+  return sms;
+}
+
+// The selecting path (scores never stored): a pass of the indexer keeps, per query row, the keys
+// whose score reaches a threshold set from a sample of the row (about `target` of them, at most
+// `cap` stored), an exact top-k runs over those candidates, and only rows whose candidates could
+// not hold their top-k are recomputed through the score buffer.  It needs 64 indexer heads,
+// k <= kCandMaxK, and enough 4-token blocks in a chunk to fill the GPU from one CTA per block.
+constexpr size_t kCandBytes = (size_t)1 << 30;  // candidate lists of one chunk of rows
+int cand_cap(int k) {
+  int c = 4 * k < 2048 ? 2048 : 4 * k;
+  return (c + 127) / 128 * 128;
+}
+// the largest number of candidates a row's threshold aims at: 60% of the room, so that a
+// segment (a quarter of the room, a quarter of the keys) rarely overflows
+int cand_target(int k) { return cand_cap(k) * 3 / 5; }
+size_t cand_area(int64_t rows, int cap) {  // key + position lists, four counts, fail flags
+  const size_t b = (size_t)rows * ((size_t)cap * 8 + 16 + 1);
+  return (b + 255) & ~(size_t)255;
+}
+bool select_blocks_ok(int64_t B, int64_t Tc) { return B * ((Tc + 3) / 4) >= 4LL * device_sms(); }
+// Query rows per chunk of the selecting path (0: the path does not apply).
+int64_t select_chunk_rows(const dsa_indexer_args* ix, int k) {
+  if (ix->H_I != 64 || k < 1 || k > dsa::kCandMaxK) return 0;
+  int64_t rows = (int64_t)(kCandBytes / ((size_t)ix->B * ((size_t)cand_cap(k) * 8 + 17))) / 256 * 256;
+  if (rows > ix->T) rows = ix->T;
+  if (rows < 1 || !select_blocks_ok(ix->B, rows)) return 0;
+  return rows;
+}
+
+dsa_status run_materialised(const dsa_indexer_args* ix, int32_t k, int32_t* idx, void* ws, float* sc, size_t sc_bytes,
+                            size_t split_off, size_t ws_bytes, int64_t t_begin, int64_t t_end, const uint8_t* gate,
+                            int64_t gate_bstride, cudaStream_t st) {
+  const int64_t per_row = (int64_t)ix->B * ix->S * 4;
+  int64_t chunk = (int64_t)(sc_bytes / per_row);
+  if (chunk > t_end - t_begin) chunk = t_end - t_begin;
+  if (chunk < 1) return fail(DSA_ERR_WORKSPACE, "workspace too small for one row of indexer scores");
+  for (int64_t t0 = t_begin; t0 < t_end; t0 += chunk) {
+    const int Tc = (int)((t_end - t0) < chunk ? (t_end - t0) : chunk);
     dsa::IndexerLaunch L = indexer_launch(ix, t0, Tc);
     L.out = sc; L.ld = ix->S; L.out_bstride = (int64_t)Tc * ix->S; L.write_masked = 0;
     L.flags = ws_flags(ws);
+    if (gate) { L.gate = gate + (t0 - t_begin); L.gate_bstride = gate_bstride; }
     cudaError_t e = dsa::launch_indexer_scores(L, st);
     if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
     dsa::TopkLaunch P{};
     P.scores = sc; P.ld = ix->S; P.bstride = (int64_t)Tc * ix->S;
     P.B = ix->B; P.T = ix->T; P.S = ix->S; P.t0 = (int)t0; P.Tc = Tc;
     P.q_pos0 = ix->q_pos0; P.diag = ix->diag; P.k = k; P.idx = idx; P.flags = ws_flags(ws);
-    plan_topk_parts(P, (int64_t)ix->B * Tc, max_visible(ix->q_pos0, ix->T, ix->diag, ix->S), ws,
-                    dsa::kWsScratch + (size_t)(chunk * ix->B * ix->S * 4), ws_bytes);
+    if (gate) { P.gate = gate + (t0 - t_begin); P.gate_bstride = gate_bstride; }
+    else plan_topk_parts(P, (int64_t)ix->B * Tc, max_visible(ix->q_pos0, ix->T, ix->diag, ix->S), ws, split_off, ws_bytes);
     e = dsa::launch_topk_rows(P, st);
     if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
   }
   return DSA_OK;
+}
+
+dsa_status run_indexer_topk(const dsa_indexer_args* ix, int32_t k, int32_t* idx, void* ws, size_t ws_bytes,
+                            cudaStream_t st) {
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  const int64_t per_row = (int64_t)ix->B * ix->S * 4;
+  const int64_t fchunk = select_chunk_rows(ix, k);
+  const int cap = cand_cap(k);
+  const size_t farea = fchunk > 0 ? cand_area((int64_t)ix->B * fchunk, cap) : 0;
+  if (fchunk > 0 && ws_bytes >= dsa::kWsScratch + farea + (size_t)per_row) {
+    // candidate lists first, the score buffer of the recomputing pass after them
+    uint8_t* a = w8 + dsa::kWsScratch;
+    const int64_t rows_max = (int64_t)ix->B * fchunk;
+    uint2* cand = reinterpret_cast<uint2*>(a);
+    int32_t* ccnt = reinterpret_cast<int32_t*>(a + (size_t)rows_max * cap * 8);
+    uint8_t* fl = a + (size_t)rows_max * (cap * 8 + 16);
+    float* sc = reinterpret_cast<float*>(a + farea);
+    const size_t sc_bytes = ws_bytes - dsa::kWsScratch - farea;
+    for (int64_t t0 = 0; t0 < ix->T; t0 += fchunk) {
+      const int Tc = (int)((ix->T - t0) < fchunk ? (ix->T - t0) : fchunk);
+      if (!select_blocks_ok(ix->B, Tc)) {  // a short tail chunk: the scores of its few rows
+        dsa_status s = run_materialised(ix, k, idx, ws, sc, sc_bytes, ws_bytes, ws_bytes, t0, t0 + Tc, nullptr, 0, st);
+        if (s != DSA_OK) return s;
+        continue;
+      }
+      dsa::IndexerLaunch L = indexer_launch(ix, t0, Tc);
+      L.flags = ws_flags(ws);
+      L.select = 1; L.cap = cap; L.target = cand_target(k); L.topk = k;
+      L.cand = cand; L.cand_cnt = ccnt;
+      cudaError_t e = dsa::launch_indexer_scores(L, st);
+      if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
+      dsa::CandLaunch C{};
+      C.B = ix->B; C.T = ix->T; C.S = ix->S; C.t0 = (int)t0; C.Tc = Tc;
+      C.q_pos0 = ix->q_pos0; C.diag = ix->diag; C.k = k; C.cap = cap;
+      C.cand = cand; C.cand_cnt = ccnt; C.fail = fl; C.idx = idx;
+      if ((e = dsa::launch_topk_cand(C, st)) != cudaSuccess) return cuda_fail(e, "top-k launch");
+      // rows whose candidates could not hold their top-k: scores and top-k again, through
+      // the score buffer (each launch leaves at once unless one of its rows is marked)
+      dsa_status s = run_materialised(ix, k, idx, ws, sc, sc_bytes, ws_bytes, ws_bytes, t0, t0 + Tc, fl, Tc, st);
+      if (s != DSA_OK) return s;
+    }
+    return DSA_OK;
+  }
+  const int64_t chunk = score_chunk_rows(ix, ws_bytes);
+  if (chunk < 1) return fail(DSA_ERR_WORKSPACE, "workspace too small for one row of indexer scores (%zu bytes)", ws_bytes);
+  float* sc = reinterpret_cast<float*>(w8 + dsa::kWsScratch);
+  return run_materialised(ix, k, idx, ws, sc, (size_t)(chunk * per_row), dsa::kWsScratch + (size_t)(chunk * per_row),
+                          ws_bytes, 0, ix->T, nullptr, 0, st);
 }
 
 }  // namespace
@@ -218,6 +305,10 @@ size_t dsa_workspace_size(const dsa_indexer_args* ix, int32_t k) {
   if (rows < 1) rows = 1;
   if (rows > ix->T) rows = ix->T;
   size_t bytes = dsa::kWsScratch + (size_t)(rows * per_row);
+  // the selecting path's candidate lists (rows of the chunk x (cap keys + cap positions + count
+  // + fail flag)) come first when it applies
+  const int64_t fchunk = select_chunk_rows(ix, k);
+  if (fchunk > 0) bytes += cand_area((int64_t)ix->B * fchunk, cand_cap(k));
   // a chunk of few rows may have them split across CTAs: room for the segments' lists (the
   // first chunk's rows are the most; the same room serves every later chunk)
   if (k >= 1 && k <= kMaxK) bytes += topk_split_bytes(rows * ix->B, max_visible(ix->q_pos0, ix->T, ix->diag, ix->S), k);

@@ -72,6 +72,20 @@ struct IndexerLaunch {
   uint32_t* flags;      // device flag word (DSA_FLAG_TIMEOUT)
   int ksplit;           // key-range splits per token block (0: chosen by the launcher)
   long long wait;       // wait bound in cycles (0: wait_limit() at launch)
+  // selecting mode (select != 0; H_I = 64, one CTA per token block): instead of writing scores,
+  // row r = b*Tc + (t - t0) keeps every key whose score reaches a threshold set from a sample of
+  // its tiles (enough keys to hold the top k of them with high probability, at most `target`):
+  // (score bits, position) pairs go to one of four segments of
+  // cand[r*cap ..] (one per lane quarter of the key tiles, cap/4 each), the segment's count to
+  // cand_cnt[r*4 + q]
+  int select;
+  int cap, target, topk;
+  uint2* cand;
+  int32_t* cand_cnt;
+  // recomputing mode: when gate is set, only token blocks holding a row (b, t) whose flag
+  // gate[b*gate_bstride + t - t0] is non-zero run
+  const uint8_t* gate;
+  int64_t gate_bstride;
 };
 cudaError_t launch_indexer_scores(const IndexerLaunch& p, cudaStream_t st);     // tcgen05 path
 
@@ -86,6 +100,10 @@ struct TopkLaunch {
   int32_t* idx;
   uint32_t* flags;
   long long wait;       // wait bound in cycles (0: wait_limit() at launch)
+  // recomputing mode: when gate is set, only rows (b, t) whose flag gate[b*gate_bstride + t - t0]
+  // is non-zero run
+  const uint8_t* gate;
+  int64_t gate_bstride;
   // few long rows: each row split into `parts` segments (> 1), one CTA each; segment s of row
   // r = b*Tc + tl writes its exact top-k, sorted by position, with the keys, to
   // part_pos / part_key[(r*parts + s)*k ..] and its length to part_cnt[r*parts + s]; a merge
@@ -97,6 +115,25 @@ struct TopkLaunch {
 };
 cudaError_t launch_topk_rows(const TopkLaunch& p, cudaStream_t st);
 constexpr int kMaxTopkParts = 16;
+
+// Top-k of rows [t0, t0 + Tc) of every sequence from the candidates of a selecting indexer pass
+// (IndexerLaunch::select): row r = b*Tc + (t - t0) holds four segments of candidates (fp32 score
+// bits, position), segment q at cand[r*cap + q*cap/4 ..] with cand_cnt[r*4 + q] entries (more
+// than cap/4 means it overflowed).  A row whose candidates cannot hold its top-k (fewer than
+// min(k, visible) of them, or more than cap) gets fail[r] = 1 and is left for the recomputing
+// pass; every other row gets fail[r] = 0 and its idx row.
+struct CandLaunch {
+  int B, T, S, t0, Tc;
+  int64_t q_pos0;
+  int diag, k, cap;
+  const uint2* cand;
+  const int32_t* cand_cnt;
+  uint8_t* fail;
+  int32_t* idx;
+};
+constexpr int kCandMaxK = 2048;     // selecting path: k up to this
+constexpr int kCandMaxCap = 8192;   // candidates per row held in shared memory
+cudaError_t launch_topk_cand(const CandLaunch& p, cudaStream_t st);
 // Segments per row for `rows` rows of up to `n` visible scores (1: no split).
 int topk_parts(int64_t rows, int64_t n);
 

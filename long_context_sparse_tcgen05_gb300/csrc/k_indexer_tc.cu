@@ -19,6 +19,14 @@
 //     16 heads: its 16 head weights stay in registers for the whole CTA (re-reading them from
 //     shared memory every tile saturated the LSU pipe), and a 3-shuffle reduce-scatter over
 //     the 4 threads that share the keys leaves each thread one key's sum.
+// Selecting mode (the top-k path that stores no scores): a CTA whose rows are longer than the
+// candidate room first scores an evenly spread sample of its key tiles and records each
+// sampled score's top 16 order-key bits; each token's four warps then set its threshold (the
+// sample's quantile that about `enough` of the row's keys should exceed); every tile is then
+// scored in order and each score at or above the threshold is kept as a (score, position) pair
+// in the warp's quarter of the row's candidate list -- a ballot and popc per tile, a store only
+// for the few that qualify.  The sampled tiles are scored twice (1/64 of the tiles, at least
+// 16), which keeps the main pass in plain tile order.
 // Every wait is bounded; a timeout raises DSA_FLAG_TIMEOUT, drains the copies in flight,
 // frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -39,6 +47,126 @@ constexpr int kBufs = 2;       // TMEM accumulator buffers of kN columns (512 co
 constexpr int kEpiWarps = 16;  // four per TMEM lane quarter, one per 64-column quarter of N
 constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr uint32_t kTmemCols = kBufs * kN;
+// Selecting mode: at most kSampMax sampled key tiles per CTA, their scores' top 16 key bits
+// kept per token in shared memory, two 8-bit histogram passes per token for the threshold.
+constexpr int kSampMax = 64;
+constexpr int kThBins = 512;  // bins of the threshold histogram (a window of sampled key prefixes)
+template <int SAMP>
+struct SelSmem {
+  uint16_t samp[4][SAMP * kM];
+  uint32_t hist[4][kThBins];
+  uint32_t part[4][4]; // per token: each warp's bin total
+  int mvis[4];         // visible sampled keys per token
+  uint32_t lo[4], hi[4];  // smallest and largest sampled key prefix per token
+  uint32_t theta[4];   // per-token threshold key
+  int tile[SAMP];      // key tile of each sample step
+};
+
+// Sampled tiles of a CTA whose rows are longer than the candidate capacity: 1/64 of its tiles,
+// between 16 and `most` (at most all of them).
+__host__ __device__ inline int sample_tiles(int ktiles, int most) {
+  int ns = ktiles / 64;
+  ns = ns < 16 ? 16 : (ns > most ? most : ns);
+  return ns < ktiles ? ns : ktiles;
+}
+// Tile processed at step i of a CTA that first scores nsamp evenly spread sample tiles (their
+// tiles listed in `tiles`), then every tile in order.
+__device__ __forceinline__ int tile_at(int i, int nsamp, const int* tiles) { return i < nsamp ? tiles[i] : i - nsamp; }
+__device__ __forceinline__ void token_sync(int tok) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(1 + tok), "r"(128) : "memory");
+}
+
+// The threshold key of token `tok` from its recorded sample, computed by the token's four
+// epilogue warps (thread tt of 128; every one must call it): the sample's need-th largest
+// score, need = ceil(target * sampled / visible), so that about `target` of the row's keys reach
+// it, rounded down to a bin of a histogram of the sampled 16-bit key prefixes over the window
+// [smallest, largest] (one pass; a row's scores span a narrow range of prefixes).  A threshold
+// of 1 keeps every visible non-NaN key (the sample suggests about all of them).
+// The target is the least number of keys whose estimate from need sampled ones stays 4.5
+// standard deviations (relative error about 1/sqrt(need)) above k: sqrt(target) = (a +
+// sqrt(a^2 + 4k)) / 2 with a = 4.5 sqrt(visible / sampled), capped at `most` (the candidate
+// room the row has, with margin).
+template <class SelSmem>
+__device__ __noinline__ uint32_t token_threshold(SelSmem* ss, int tok, int tt, int nsamp, int mv, int64_t n_vis,
+                                                 int k, int most) {
+  uint32_t* hist = ss->hist[tok];
+  const uint16_t* sp = ss->samp[tok];
+  const int total = nsamp * kM;
+  const int lane = tt & 31, w = tt >> 5;
+  token_sync(tok);  // every warp of the token has recorded its sample entries
+  uint32_t lo = 0xffffu, hi = 0u;
+  for (int i = tt; i < total; i += 128) {
+    const uint32_t k = sp[i];
+    if (k) {
+      lo = k < lo ? k : lo;
+      hi = k > hi ? k : hi;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if (lane == 0) {
+    atomicMin(&ss->lo[tok], lo);
+    atomicMax(&ss->hi[tok], hi);
+  }
+  atomicAdd(&ss->mvis[tok], mv);
+  for (int i = tt; i < kThBins; i += 128) hist[i] = 0;
+  token_sync(tok);
+  const int m = ss->mvis[tok];
+  int64_t need = 0;
+  if (n_vis > 0 && m > 0) {
+    const double a = 4.5 * sqrt((double)n_vis / (double)m);
+    const double r = 0.5 * (a + sqrt(a * a + 4.0 * k));
+    double target = r * r;
+    if (target > most) target = most;
+    need = (int64_t)ceil(target * (double)m / (double)n_vis);
+  }
+  if (need < 1 || need >= m) return 1u;  // (the same decision in every thread)
+  const uint32_t wlo = ss->lo[tok], span = ss->hi[tok] - wlo;
+  int sh = 0;
+  while ((span >> sh) >= (uint32_t)kThBins) ++sh;
+  for (int i = tt; i < total; i += 128) {
+    const uint32_t k = sp[i];
+    const uint32_t bin = (k - wlo) >> sh;  // every recorded non-zero prefix lies in the window
+    if (k && bin < (uint32_t)kThBins) atomicAdd(&hist[bin], 1u);
+  }
+  token_sync(tok);
+  // thread tt owns the four bins 4tt .. 4tt+3 counted from the top; a scan over the token's
+  // threads gives the count above them
+  constexpr int kPer = kThBins / 128;
+  uint32_t c[kPer], sum = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    c[j] = hist[kThBins - 1 - (kPer * tt + j)];
+    sum += c[j];
+  }
+  uint32_t inc = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) ss->part[tok][w] = inc;
+  token_sync(tok);
+  uint32_t above = inc - sum;
+  for (int q = 0; q < w; ++q) above += ss->part[tok][q];
+  if (above < (uint32_t)need && (uint32_t)need <= above + sum) {
+    uint32_t acc = above;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      if (acc + c[j] >= (uint32_t)need) {
+        const uint32_t bin = (uint32_t)(kThBins - 1 - (kPer * tt + j));
+        ss->theta[tok] = (wlo + (bin << sh)) << 16;
+        break;
+      }
+      acc += c[j];
+    }
+  }
+  token_sync(tok);
+  return ss->theta[tok];
+}
 
 template <int HI, int DI, bool FP8>
 struct Cfg {
@@ -56,6 +184,9 @@ struct Cfg {
   static constexpr int kBarOff = kQBytes + kStages * kKTile;
   static constexpr size_t kSmem = 1024 + kBarOff + 256 + (size_t)kTB * HI * 4;
   static constexpr uint32_t kIdesc = idesc_mn(FP8 ? 0u : 1u, FP8 ? 0u : 1u, kM, kN);
+  // selecting mode: sampled tiles whose score prefixes fit beside the stages (FP8: 64; the
+  // bf16 stages are twice as large, so 16)
+  static constexpr int kSamp = FP8 ? kSampMax : 16;
   static_assert(kRowBytes % 128 == 0, "d_I must fill whole 128-byte rows");
   static_assert(kN % HI == 0, "heads must tile the N columns");
 };
@@ -78,11 +209,12 @@ __device__ __forceinline__ int64_t visible_keys(const IndexerLaunch& p, int t_lo
   return n < 0 ? 0 : (n > p.S ? (int64_t)p.S : n);
 }
 
-template <int HI, int DI, bool FP8, bool kPoll>
+template <int HI, int DI, bool FP8, bool kPoll, bool SEL>
 __global__ void __launch_bounds__(kThreads, 1)
     k_indexer_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  IndexerLaunch p) {
   using C = Cfg<HI, DI, FP8>;
+  static_assert(!SEL || HI == 64, "the selecting epilogue is written for 64 heads (one token per warp)");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = smem;
@@ -95,6 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tm_empty + kBufs);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* w_s = reinterpret_cast<float*>(smem + C::kBarOff + 256);
+  using Sel = SelSmem<C::kSamp>;
+  Sel* ss = reinterpret_cast<Sel*>(smem + C::kBarOff + 256 + (size_t)C::kTB * HI * 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nblk = (p.Tc + C::kTB - 1) / C::kTB;
@@ -103,6 +237,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = blockIdx.y;
   const int tl0 = tb * C::kTB;
   const int ntok = min(C::kTB, p.Tc - tl0);
+  if (p.gate) {
+    // recomputing only the rows a selecting pass could not finish: leave unless one of this
+    // block's rows is marked (before any barrier, copy or tensor memory is touched)
+    bool any = false;
+    for (int i = 0; i < ntok; ++i) any |= p.gate[(int64_t)b * p.gate_bstride + tl0 + i] != 0;
+    if (!any) return;
+  }
   // epilogue warps own one column quarter each; quarters that hold none of this block's
   // tokens (decode: one token per block) have no work, so they sit the tiles out and the
   // accumulator buffers wait only for the others
@@ -117,6 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ktiles = max(0, min(kt_vis, kt_lo + tps) - kt_lo);
   const int key_hi = min(p.S, (kt_lo + tps) * kM);  // end of this CTA's key range
   const int64_t row0 = (int64_t)b * p.T + p.t0 + tl0;  // flat (b, t) of the block's first token
+  // selecting mode: rows longer than the candidate capacity first score a sample of tiles
+  const int nsamp = (SEL && nmax > p.cap) ? sample_tiles(ktiles, C::kSamp) : 0;
+  const int nproc = nsamp + ktiles;  // tiles the producer, the MMA and the epilogue walk
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
@@ -129,8 +273,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tm_empty + i, 4 * active_ch);
     }
     *abort_flag = 0;
+    if constexpr (SEL)
+      for (int i = 0; i < 4; ++i) {
+        ss->mvis[i] = 0;
+        ss->lo[i] = 0xffffu;
+        ss->hi[i] = 0u;
+        ss->theta[i] = 1u;
+      }
     fence_barrier_init();
   }
+  if constexpr (SEL)  // the sample tiles, evenly spread over the CTA's tiles
+    for (int s2 = threadIdx.x; s2 < nsamp; s2 += kThreads) ss->tile[s2] = ((2 * s2 + 1) * ktiles) / (2 * nsamp);
   for (int i = threadIdx.x; i < C::kTB * HI; i += kThreads)
     w_s[i] = (i / HI < ntok) ? __ldg(p.w + row0 * HI + i) : 0.f;
   if (warp == 1) {
@@ -151,15 +304,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < C::kKBlocks; ++kb)
         tma_load_4d(q_s + kb * C::kQBlock, &tm_q, q_full, kb * C::kAtomElems, 0, p.t0 + tl0, b);
       int issued = 0;
-      for (int kt = 0; kt < ktiles; ++kt) {
-        const int st = kt % C::kStages;
-        const uint32_t ph = (kt / C::kStages) & 1;
+      for (int i = 0; i < nproc; ++i) {
+        const int kt = SEL ? tile_at(i, nsamp, ss->tile) : i;
+        const int st = i % C::kStages;
+        const uint32_t ph = (i / C::kStages) & 1;
         if (!mbar_wait<kPoll>(k_empty + st, ph ^ 1, abort_flag, p.wait)) break;
         mbar_arrive_expect_tx(k_full + st, C::kKTile);
         for (int kb = 0; kb < C::kKBlocks; ++kb)
           tma_load_3d(k_s + st * C::kKTile + kb * C::kKBlock, &tm_k, k_full + st, kb * C::kAtomElems,
                       (kt_lo + kt) * kM, b);
-        issued = kt + 1;
+        issued = i + 1;
       }
       // every copy issued lands before the CTA can exit: a wait elsewhere in the CTA may run
       // out after this loop has ended (in a normal run these phases are long complete)
@@ -174,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int done = 0;
       const uint64_t q_desc0 = desc_sw128(smem_addr(q_s));
       const uint64_t k_desc0 = desc_sw128(smem_addr(k_s));
-      for (int kt = 0; ok && kt < ktiles; ++kt) {
+      for (int kt = 0; ok && kt < nproc; ++kt) {  // kt: processing step (the tile itself is the producer's)
         const int st = kt % C::kStages;
         const uint32_t ph = (kt / C::kStages) & 1;
         const int buf = kt & (kBufs - 1);
@@ -242,16 +396,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         wp[j] = pack2(0.5f * w_warp[8 * j + 2 * m], 0.5f * w_warp[8 * j + 2 * m + 1]);
-      auto key_scale16 = [&](int kt) -> float {
+      auto key_scale16 = [&](int kt) -> float {  // key scale of this thread's key in tile kt
         const int key = (kt_lo + kt) * kM + my_key;
         return (FP8 && kt < ktiles && key < p.S) ? __ldg(skg + key) : 1.f;
       };
-      float sk16_next = key_scale16(0);
-      for (int kt = 0; kt < ktiles; ++kt) {
-        const int buf = kt & (kBufs - 1);
-        const float sk = sk16_next;
-        sk16_next = key_scale16(kt + 1);
-        if (!mbar_wait<kPoll>(tm_full + buf, (kt / kBufs) & 1, abort_flag, p.wait)) break;
+      // The head-weighted ReLU sum of this thread's key for the accumulator of step i (false:
+      // a wait ran out).  The buffer goes back to the MMA right after the TMEM loads.
+      auto score_step = [&](int i, float& v) -> bool {
+        const int buf = i & (kBufs - 1);
+        if (!mbar_wait<kPoll>(tm_full + buf, (i / kBufs) & 1, abort_flag, p.wait)) return false;
         tc_fence_after();
         const uint32_t col0 = tmem + ((uint32_t)(lq * 32) << 16) + buf * kN + ch * C::kCols;
         uint32_t r[2][32];
@@ -268,29 +421,92 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int a = 0; a < 2; ++a)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float y0 = __uint_as_float(r[a][4 * j + 2 * e]);
-              const float y1 = __uint_as_float(r[a][4 * j + 2 * e + 1]);
-              acc[2 * a + e] = fma2(pack2(y0 + fabsf(y0), y1 + fabsf(y1)), wp[j], acc[2 * a + e]);
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const float y0 = __uint_as_float(r[a][4 * j + 2 * e2]);
+              const float y1 = __uint_as_float(r[a][4 * j + 2 * e2 + 1]);
+              acc[2 * a + e2] = fma2(pack2(y0 + fabsf(y0), y1 + fabsf(y1)), wp[j], acc[2 * a + e2]);
             }
         float v4[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v4[i] = lo2(acc[i]) + hi2(acc[i]);
+        for (int q = 0; q < 4; ++q) v4[q] = lo2(acc[q]) + hi2(acc[q]);
         // reduce-scatter over the 4 threads of a key group: thread m ends with key index m
         const bool hi1 = (m & 2) != 0, hi0 = (m & 1) != 0;
         const float s0 = hi1 ? v4[0] : v4[2], s1 = hi1 ? v4[1] : v4[3];
         const float k0 = hi1 ? v4[2] : v4[0], k1 = hi1 ? v4[3] : v4[1];
         const float u0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 2);
         const float u1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 2);
-        float v = (hi0 ? u1 : u0) + __shfl_xor_sync(0xffffffffu, hi0 ? u0 : u1, 1);
-        const int key = (kt_lo + kt) * kM + my_key;
-        if (ntok > ch && key < p.S) {
-          float* dst = out_b + (int64_t)(tl0 + ch) * p.ld + key;
-          if (key < nvis[0]) {
-            if constexpr (FP8) v *= sq[0] * sk;
-            *dst = v;
-          } else if (p.write_masked) {
-            *dst = -INFINITY;
+        v = (hi0 ? u1 : u0) + __shfl_xor_sync(0xffffffffu, hi0 ? u0 : u1, 1);
+        return true;
+      };
+      if constexpr (SEL) {
+        // selecting mode.  Sample steps record the top 16 key bits of each sampled score; the
+        // token's four warps then set its threshold (every visible non-NaN key when the row is
+        // short enough to keep whole); the main steps keep (key, position) of every score that
+        // reaches it, each warp in its own quarter of the row's list with a register count
+        // (ballot + popc: no atomics on the way).
+        bool dead = false;
+        int mv = 0;  // visible sampled keys seen by this thread
+        for (int i = 0; i < nsamp; ++i) {
+          if (dead) continue;  // still meet the threshold barriers below
+          const int kt = ss->tile[i];
+          const float sk = key_scale16(kt);
+          float v;
+          if (!score_step(i, v)) {
+            dead = true;
+            continue;
+          }
+          const int key = (kt_lo + kt) * kM + my_key;
+          const bool vis = key < nvis[0];
+          if constexpr (FP8) v *= sq[0] * sk;
+          ss->samp[ch][i * kM + my_key] = vis ? (uint16_t)(score_key(v) >> 16) : (uint16_t)0;
+          mv += vis;
+        }
+        const uint32_t theta =
+            nsamp > 0 ? token_threshold(ss, ch, (e & 3) * 32 + lane, nsamp, mv, nvis[0], p.topk, p.target) : 1u;
+        const int64_t crow = (int64_t)b * p.Tc + tl0 + ch;  // chunk-local row of this token
+        const int cap4 = p.cap / 4;
+        uint2* cand = p.cand + crow * p.cap + lq * cap4;
+        // the threshold as a float: scores v >= thf are exactly those whose order key reaches
+        // theta (-inf keeps every non-NaN score)
+        const float thf = theta == 1u ? -INFINITY : __uint_as_float((theta & 0x80000000u) ? (theta & 0x7fffffffu) : ~theta);
+        const int nv = (int)nvis[0];
+        uint32_t wcnt = 0;  // this warp's candidates so far (the same in every lane)
+        const uint32_t below = (1u << lane) - 1u;
+        float sk16_next = key_scale16(0);
+        int key = kt_lo * kM + my_key;
+        for (int kt = 0; !dead && kt < ktiles; ++kt, key += kM) {
+          const float sk = sk16_next;
+          sk16_next = key_scale16(kt + 1);
+          float v;
+          if (!score_step(nsamp + kt, v)) break;
+          if constexpr (FP8) v *= sq[0] * sk;
+          const bool take = key < nv && v >= thf;
+          const uint32_t bal = __ballot_sync(0xffffffffu, take);
+          if (bal) {
+            if (take) {
+              const uint32_t slot = wcnt + __popc(bal & below);
+              if (slot < (uint32_t)cap4) cand[slot] = make_uint2(__float_as_uint(v), (uint32_t)key);
+            }
+            wcnt += __popc(bal);
+          }
+        }
+        if (lane == 0) p.cand_cnt[crow * 4 + lq] = (int32_t)wcnt;
+      } else {
+        float sk16_next = key_scale16(0);
+        for (int kt = 0; kt < ktiles; ++kt) {
+          const float sk = sk16_next;
+          sk16_next = key_scale16(kt + 1);
+          float v;
+          if (!score_step(kt, v)) break;
+          const int key = (kt_lo + kt) * kM + my_key;
+          if (ntok > ch && key < p.S) {
+            float* dst = out_b + (int64_t)(tl0 + ch) * p.ld + key;
+            if (key < nvis[0]) {
+              if constexpr (FP8) v *= sq[0] * sk;
+              *dst = v;
+            } else if (p.write_masked) {
+              *dst = -INFINITY;
+            }
           }
         }
       }
@@ -365,6 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+
   if (threadIdx.x == 0 && *abort_flag && p.flags) atomicOr(p.flags, DSA_FLAG_TIMEOUT);
 }
 
@@ -402,7 +619,7 @@ cudaError_t make_map(CUtensorMap* m, const void* base, bool fp8, int rank, const
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int HI, int DI, bool FP8>
+template <int HI, int DI, bool FP8, bool SEL>
 cudaError_t launch_cfg(const IndexerLaunch& p, cudaStream_t st) {
   TraceScope trace(kTraceIndexer, st);
   using C = Cfg<HI, DI, FP8>;
@@ -421,10 +638,12 @@ cudaError_t launch_cfg(const IndexerLaunch& p, cudaStream_t st) {
   if ((e = make_map(&tk, p.k, FP8, 3, kdims, kstr, kbox)) != cudaSuccess) return e;
   IndexerLaunch q = p;
   if (q.wait <= 0) q.wait = wait_limit();
-  auto kern = q.wait < kDefaultWaitCycles ? k_indexer_tc<HI, DI, FP8, true> : k_indexer_tc<HI, DI, FP8, false>;
-  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem)) != cudaSuccess)
+  auto kern = q.wait < kDefaultWaitCycles ? k_indexer_tc<HI, DI, FP8, true, SEL> : k_indexer_tc<HI, DI, FP8, false, SEL>;
+  const size_t smem = C::kSmem + (SEL ? sizeof(SelSmem<C::kSamp>) : 0);
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
     return e;
   const int nblk = (p.Tc + C::kTB - 1) / C::kTB;
+  if (SEL) q.ksplit = 1;  // a row's candidates come from one CTA
   if (q.ksplit <= 0) {
     // split the key range when the token blocks alone would not give about four waves of
     // CTAs, keeping at least 16 key tiles per split
@@ -438,7 +657,7 @@ cudaError_t launch_cfg(const IndexerLaunch& p, cudaStream_t st) {
     q.ksplit = (int)(want < most ? want : most);
   }
   dim3 grid((unsigned)(nblk * q.ksplit), p.B);
-  kern<<<grid, kThreads, C::kSmem, st>>>(tq, tk, q);
+  kern<<<grid, kThreads, smem, st>>>(tq, tk, q);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -447,8 +666,12 @@ cudaError_t launch_cfg(const IndexerLaunch& p, cudaStream_t st) {
 
 cudaError_t launch_indexer_scores(const IndexerLaunch& p, cudaStream_t st) {
   if (p.B <= 0 || p.Tc <= 0 || p.S <= 0) return cudaSuccess;
-  if (p.HI == 64 && p.DI == 128) return p.fp8 ? launch_cfg<64, 128, true>(p, st) : launch_cfg<64, 128, false>(p, st);
-  if (p.HI == 4 && p.DI == 64 && !p.fp8) return launch_cfg<4, 64, false>(p, st);
+  if (p.HI == 64 && p.DI == 128) {
+    if (p.select)
+      return p.fp8 ? launch_cfg<64, 128, true, true>(p, st) : launch_cfg<64, 128, false, true>(p, st);
+    return p.fp8 ? launch_cfg<64, 128, true, false>(p, st) : launch_cfg<64, 128, false, false>(p, st);
+  }
+  if (p.HI == 4 && p.DI == 64 && !p.fp8 && !p.select) return launch_cfg<4, 64, false, false>(p, st);
   return cudaErrorInvalidValue;
 }
 

@@ -21,8 +21,16 @@
 //   * Fewer rows than SMs (decode): each row is split into segments of at least 32K scores,
 //     one CTA each; a segment writes its exact top-k with the keys, sorted by position, and
 //     k_topk_merge selects the row's top-k from the concatenated lists.
-// If the sample overestimates the threshold (fewer than k candidates), the CTA falls back to
-// histogram passes over the row in global memory and a final ordered compaction pass.
+// If the sample overestimates the threshold (fewer than k candidates), or one chunk brings more
+// candidates than the buffer holds, the CTA falls back to histogram passes over the row in
+// global memory and a final ordered compaction pass.
+//
+// k_topk_cand is the top-k of the path that stores no scores: a row's candidates (score,
+// position) from the selecting indexer are loaded into shared memory, a radix select (starting
+// at the first bit where the smallest and largest candidate keys differ) finds the k-th key and
+// the positions of its ties, and the selected positions are written in order by marking them
+// in a bitmap of the row and compacting it (rows up to 262,144 keys; longer rows sort the k
+// positions bitonically).
 #include "dsa_internal.cuh"
 
 namespace dsa {
@@ -294,6 +302,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
   __shared__ int s_nan;
   const int parts = p.parts > 1 ? p.parts : 1;
   const int row = (int)(blockIdx.x / parts), part = (int)(blockIdx.x % parts);
+  // recomputing pass: only rows the selection left over
+  if (p.gate && !p.gate[(int64_t)(row / p.Tc) * p.gate_bstride + row % p.Tc]) return;
   const int b = row / p.Tc, tl = row % p.Tc, t = p.t0 + tl;
   const float* x = p.scores + (int64_t)b * p.bstride + (int64_t)tl * p.ld;
   int32_t* out = p.idx + ((int64_t)b * p.T + t) * p.k;
@@ -400,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
     const int n32 = (int)n;
     uint32_t count = 0, kmax = 0;
     bool nan_seen = false;
+    bool overflow = false;  // a chunk brought more candidates than the buffer can hold
 #pragma unroll 1
     for (int64_t ci = 0; ci < nchunks; ++ci) {
       const int s = (int)(ci % Ring);
@@ -450,6 +461,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
         for (int j = 0; j < Per; ++j) cnt += q + j < n32 && key[j] >= theta;
         o = count + block_excl_scan(cnt, sm.warp_sums, &tot);
       }
+      if (count + tot > (uint32_t)Cap) {
+        // even compacted the buffer cannot hold this chunk's candidates (a threshold far below
+        // the k-th key, e.g. a row of equal scores): leave the row to the exact passes below
+        overflow = true;
+        break;
+      }
       if (cnt) {
 #pragma unroll
         for (int j = 0; j < Per; ++j) {
@@ -468,9 +485,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
     if (nan_seen) s_nan = 1;
     if (kmax) atomicMax(&sm.kmax, kmax);
     __syncthreads();
-    if (sm.abort) {
-      // a wait ran out: let the copies still in flight -- the last Ring chunks issued, one per
-      // ring slot -- land before the CTA exits (with the default bound)
+    if (sm.abort || overflow) {
+      // the pass ended early (a wait ran out, or the buffer overflowed): let the copies still in
+      // flight -- the last Ring chunks issued, one per ring slot -- land before the CTA goes on
+      // or exits (with the default bound)
       if (threadIdx.x == 0) {
         for (int64_t ci = issued - Ring > 0 ? issued - Ring : 0; ci < issued; ++ci) {
           const long long t0 = clock64();
@@ -483,12 +501,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_rows(TopkLaunch p) {
                 : "r"(sa(&sm.full[ci % Ring])), "r"((uint32_t)((ci / Ring) & 1))
                 : "memory");
         }
-        atomicOr(p.flags, DSA_FLAG_TIMEOUT);
+        if (sm.abort) atomicOr(p.flags, DSA_FLAG_TIMEOUT);
       }
-      return;
+      if (sm.abort) return;
+      __syncthreads();
     }
     c = count;
-    ok = count >= (uint32_t)k && count <= (uint32_t)Cap;
+    ok = !overflow && count >= (uint32_t)k && count <= (uint32_t)Cap;
   }
   __syncthreads();
   if (s_nan && threadIdx.x == 0) atomicOr(p.flags, DSA_FLAG_NAN_SCORE);
@@ -568,6 +587,205 @@ __global__ void __launch_bounds__(kThreads) k_topk_merge(TopkLaunch p) {
   });
 }
 
+constexpr int kBitmapKeys = 262144;  // rows this long or shorter are ordered through a bitmap
+struct CandSmem {
+  uint32_t key[kCandMaxCap];
+  int32_t pos[kCandMaxCap];
+  union {
+    int32_t sel[2 * kCandMaxK];           // longer rows: the k positions, bitonic-sorted
+    uint32_t bits[kBitmapKeys / 32];      // shorter rows: one bit per position
+  };
+  uint32_t hist[kBins];
+  uint32_t warp_sums[kWarps];
+  uint32_t sel_bin, sel_above;
+  uint32_t eq;                  // candidates whose key equals the k-th key
+  uint32_t kmin, kmax;          // smallest and largest candidate key
+  uint32_t pmin, pmax;          // smallest and largest inverted position among those equal to tau
+};
+
+// One row's exact top-k from its candidates (see CandLaunch): the k-th key tau by radix
+// select; when more candidates equal tau than the row can take, the lowest positions among them
+// (a radix select on inverted positions); the k selected positions are then sorted ascending
+// (bitonic) and written.
+__global__ void __launch_bounds__(kThreads, 2) k_topk_cand(CandLaunch p) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  CandSmem& sm = *reinterpret_cast<CandSmem*>(smem_raw);
+  const int row = blockIdx.x;
+  const int b = row / p.Tc, tl = row % p.Tc, t = p.t0 + tl;
+  int32_t* out = p.idx + ((int64_t)b * p.T + t) * p.k;
+  int64_t n = p.q_pos0 + t + p.diag;
+  n = n < 0 ? 0 : (n > p.S ? p.S : n);
+  const int k = p.k;
+  if (n <= k) {  // every visible key
+    for (int j = threadIdx.x; j < k; j += kThreads) out[j] = j < n ? j : -1;
+    if (threadIdx.x == 0) p.fail[row] = 0;
+    return;
+  }
+  // the row's list is four segments of cap/4 (one per epilogue warp of the indexer)
+  const int cap4 = p.cap / 4;
+  int cs[4], pre[4], cnt = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    cs[q] = __ldg(p.cand_cnt + (int64_t)row * 4 + q);
+    pre[q] = cnt;
+    cnt += cs[q];
+  }
+  if (cnt < k || cs[0] > cap4 || cs[1] > cap4 || cs[2] > cap4 || cs[3] > cap4) {
+    if (threadIdx.x == 0) p.fail[row] = 1;
+    return;
+  }
+  const uint2* cd = p.cand + (int64_t)row * p.cap;
+  if (threadIdx.x == 0) {
+    sm.eq = 0;
+    sm.kmin = 0xffffffffu;
+    sm.kmax = 0u;
+    sm.pmin = 0xffffffffu;
+    sm.pmax = 0u;
+  }
+  __syncthreads();
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  {
+    // every load of the four segments in flight at once, then into shared memory contiguously
+    constexpr int kU = kCandMaxCap / 4 / kThreads;  // entries per thread and segment
+    uint2 cv[4][kU];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = u * kThreads + (int)threadIdx.x;
+        cv[q][u] = i < cs[q] ? __ldg(cd + q * cap4 + i) : make_uint2(0u, 0u);
+      }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = u * kThreads + (int)threadIdx.x;
+        if (i < cs[q]) {
+          const uint32_t kk = score_key(__uint_as_float(cv[q][u].x));
+          sm.key[pre[q] + i] = kk;
+          sm.pos[pre[q] + i] = (int32_t)cv[q][u].y;
+          lo = kk < lo ? kk : lo;
+          hi = kk > hi ? kk : hi;
+        }
+      }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicMin(&sm.kmin, lo);
+    atomicMax(&sm.kmax, hi);
+  }
+  __syncthreads();
+  // every candidate shares the bits of kmin and kmax above their highest differing bit: the
+  // radix passes start there (a row's candidates sit in a narrow range of scores, so the
+  // leading digits would put them all in one histogram bin)
+  auto common = [](uint32_t a, uint32_t b, uint32_t* prefix) {
+    const uint32_t d = a ^ b;
+    const int top = d ? 32 - __clz(d) : 0;
+    *prefix = top >= 32 ? 0u : (b & ~((1u << top) - 1u));
+    return top;
+  };
+  uint32_t ties, prefix;
+  int top = common(sm.kmin, sm.kmax, &prefix);
+  const uint32_t tau =
+      radix_select(sm, (int64_t)cnt, (uint32_t)k, [&](int64_t i) { return sm.key[i]; }, &ties, prefix, top, 0);
+  uint32_t eq_local = 0, plo = 0xffffffffu, phi = 0u;
+  for (int i = threadIdx.x; i < cnt; i += kThreads)
+    if (sm.key[i] == tau) {
+      ++eq_local;
+      const uint32_t ip = ~(uint32_t)sm.pos[i];
+      plo = ip < plo ? ip : plo;
+      phi = ip > phi ? ip : phi;
+    }
+  if (eq_local) {
+    atomicAdd(&sm.eq, eq_local);
+    atomicMin(&sm.pmin, plo);
+    atomicMax(&sm.pmax, phi);
+  }
+  __syncthreads();
+  // the ties lowest positions among the keys equal to tau: those up to pi (a radix select of
+  // the ties-th largest inverted position; entries of other keys map to 0, below every one)
+  int32_t pi = INT32_MAX;
+  if (sm.eq > ties) {
+    uint32_t t2, pprefix;
+    const int ptop = common(sm.pmin, sm.pmax, &pprefix);
+    const uint32_t inv = radix_select(sm, (int64_t)cnt, ties,
+                                      [&](int64_t i) { return sm.key[i] == tau ? ~(uint32_t)sm.pos[i] : 0u; }, &t2,
+                                      pprefix, ptop, 0);
+    pi = (int32_t)~inv;
+  }
+  auto selected = [&](int i) { return sm.key[i] > tau || (sm.key[i] == tau && sm.pos[i] <= pi); };
+  if (n <= kBitmapKeys) {
+    // mark the selected positions in a bitmap of the row, then one ordered compaction of its
+    // words (each thread a contiguous run of words; a block scan places the runs)
+    const int words = (int)((n + 31) / 32);
+    for (int w = threadIdx.x; w < words; w += kThreads) sm.bits[w] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < cnt; i += kThreads)
+      if (selected(i) && (uint32_t)sm.pos[i] < (uint32_t)n) atomicOr(&sm.bits[sm.pos[i] >> 5], 1u << (sm.pos[i] & 31));
+    __syncthreads();
+    const int per = (words + kThreads - 1) / kThreads;
+    const int w0 = (int)threadIdx.x * per, w1 = min(words, w0 + per);
+    uint32_t c = 0;
+    for (int w = w0; w < w1; ++w) c += __popc(sm.bits[w]);
+    uint32_t tot;
+    uint32_t o = block_excl_scan(c, sm.warp_sums, &tot);
+    for (int w = w0; w < w1 && o < (uint32_t)k; ++w) {
+      uint32_t m = sm.bits[w];
+      while (m && o < (uint32_t)k) {
+        out[o++] = w * 32 + (__ffs(m) - 1);
+        m &= m - 1;
+      }
+    }
+    for (int j = (int)tot + threadIdx.x; j < k; j += kThreads) out[j] = -1;  // (tot == k)
+    if (threadIdx.x == 0) p.fail[row] = 0;
+    return;
+  }
+  // compact the k selected positions (any order), then sort them
+  int P = 1;
+  while (P < k) P <<= 1;
+  uint32_t out_base = 0;
+  for (int base = 0; base < cnt; base += kThreads * kPer) {
+    const int q = base + (int)threadIdx.x * kPer;
+    uint32_t c = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = q + j;
+      c += i < cnt && (sm.key[i] > tau || (sm.key[i] == tau && sm.pos[i] <= pi));
+    }
+    uint32_t tot;
+    uint32_t o = out_base + block_excl_scan(c, sm.warp_sums, &tot);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = q + j;
+      if (i < cnt && (sm.key[i] > tau || (sm.key[i] == tau && sm.pos[i] <= pi)) && o < (uint32_t)k) sm.sel[o++] = sm.pos[i];
+    }
+    out_base += tot;
+  }
+  for (int i = k + threadIdx.x; i < P; i += kThreads) sm.sel[i] = INT32_MAX;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int tt = threadIdx.x; tt < P / 2; tt += kThreads) {
+        const int lo = 2 * tt - (tt & (stride - 1));
+        const int hi = lo + stride;
+        const bool asc = (lo & size) == 0;
+        const int32_t a = sm.sel[lo], c = sm.sel[hi];
+        if ((a > c) == asc) {
+          sm.sel[lo] = c;
+          sm.sel[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int j = threadIdx.x; j < k; j += kThreads) out[j] = sm.sel[j];
+  if (threadIdx.x == 0) p.fail[row] = 0;
+}
+
 template <int Cap, int Ring, int Per>
 cudaError_t launch_rows(const TopkLaunch& p, int rows, cudaStream_t st) {
   TraceScope trace(kTraceTopk, st);
@@ -593,6 +811,19 @@ int topk_parts(int64_t rows, int64_t n) {
   if (parts > by_len) parts = by_len;
   if (parts > kMaxTopkParts) parts = kMaxTopkParts;
   return parts < 2 ? 1 : (int)parts;
+}
+
+cudaError_t launch_topk_cand(const CandLaunch& p, cudaStream_t st) {
+  const int rows = p.B * p.Tc;
+  if (rows <= 0) return cudaSuccess;
+  if (p.k < 1 || p.k > kCandMaxK || p.cap > kCandMaxCap || p.cap < p.k) return cudaErrorInvalidValue;
+  TraceScope trace(kTraceTopk, st);
+  const int smem = (int)sizeof(CandSmem);
+  cudaError_t e = cudaFuncSetAttribute(k_topk_cand, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  k_topk_cand<<<rows, kThreads, smem, st>>>(p);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_topk_rows(const TopkLaunch& p, cudaStream_t st) {

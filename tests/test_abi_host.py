@@ -198,7 +198,14 @@ def test_overlap_validation(lib):
 def test_workspace_size_plan(lib):
     ix = _ix(T=131072, S=131072)
     n = lib.dsa_workspace_size(ctypes.byref(ix), 2048)
-    assert n >= 256 + 131072 * 4 and n <= 256 + (4 << 30)
+    # a score chunk of at most 4 GiB, plus the candidate lists of the selecting path (at most
+    # 1 GiB: 8,192 keys and positions per row of a chunk)
+    assert n >= 256 + 131072 * 4 and n <= 256 + (4 << 30) + (1 << 30)
+    assert n > 256 + (4 << 30)  # 64 heads, k = 2,048, many rows: the selecting path applies
+    # k beyond the selecting path, or 4 indexer heads: the score chunk alone
+    assert lib.dsa_workspace_size(ctypes.byref(ix), 4096) <= 256 + (4 << 30)
+    small = _ix(T=131072, S=131072, H_I=4, d_I=64)
+    assert lib.dsa_workspace_size(ctypes.byref(small), 64) <= 256 + (4 << 30)
     assert lib.dsa_workspace_size(None, 16) == 256
 
 

@@ -512,3 +512,71 @@ def test_group_forward_varlen_equals_each_sequence_alone(base, shapes, k):
             ref_o, _ = oracle.sparse_attn(per_seq[i][l]["at"], got, rows)
             o = o1[l].reshape(wl.T, wl.H, wl.DV)[rows].float().cpu().numpy()
             assert np.abs(o - ref_o).max() <= ATOL_OUT
+
+
+# --- the selecting path (scores never stored) ---------------------------------------------
+
+def _launches(fn):
+    torch.cuda.synchronize()
+    n0 = dsa.launch_count()
+    out = fn()
+    torch.cuda.synchronize()
+    return out, dsa.launch_count() - n0
+
+
+@pytest.mark.parametrize("dtype,values,B,T,S,diag", [
+    ("e4m3", "gauss", 1, 3072, 40000, 0),   # every row sampled (about 2.5k candidates each)
+    ("e4m3", "int", 1, 2560, 30000, 0),     # integer scores: ties at the threshold and the k-th key
+    ("bf16", "gauss", 1, 2560, 24000, 1),
+    ("e4m3", "int", 2, 1300, 20000, 0),     # two sequences
+    ("bf16", "int", 1, 12000, 12000, 0),    # a prefill from 0: rows with n <= k, n <= 4k (all
+                                            # their keys kept) and n > 4k (sampled)
+])
+def test_selecting_path_equals_materialised_path(dtype, values, B, T, S, diag):
+    """dsa_topk from indexer operands (the selecting path: an indexer pass keeping the keys
+    above a sampled threshold, exact top-k over them, recompute of rows it could not finish)
+    against dsa_indexer_scores followed by dsa_topk over the stored scores: both select
+    exactly over identical fp32 scores, so every row must agree bit for bit; integer rows are
+    also checked against the oracle."""
+    wl = _wl(64, 128, dtype, values, T, S=S, k=2048, q_pos0=S - T, diag=diag, B=B)
+    ix = synth.indexer_inputs(wl, 0, DEV)
+    sel, n_sel = _launches(lambda: dsa.dsa_topk(2048, ix=ix))
+    assert n_sel == 4, n_sel  # selecting indexer, candidate top-k, gated recompute (indexer, top-k)
+    sc = dsa.indexer_scores(ix)  # [B, T, S], the same fp32 scores, stored
+    mat = dsa.dsa_topk(2048, scores=sc, q_pos0=S - T, diag=diag)
+    assert torch.equal(sel, mat)
+    del sc
+    assert dsa.read_device_flags() == 0
+    if values == "int":
+        rows = synth.sample_rows(wl, 12)
+        ref = oracle.indexer_topk(ix, 2048, rows)
+        assert np.array_equal(sel.reshape(-1, 2048)[rows].cpu().numpy(), ref)
+
+
+def test_selecting_path_recomputes_rows_whose_candidates_overflow():
+    """Head weights of zero make every score 0: each row's threshold admits all its keys, the
+    candidate lists overflow, and every row is recomputed through the score buffer -- the
+    result is the lowest k positions of each row, as the oracle gives for all-equal scores."""
+    wl = _wl(64, 128, "e4m3", "gauss", 2560, S=30000, k=2048, q_pos0=30000 - 2560)
+    ix = synth.indexer_inputs(wl, 0, DEV)
+    ix["w"] = torch.zeros_like(ix["w"])
+    sel = dsa.dsa_topk(2048, ix=ix)
+    torch.cuda.synchronize()
+    assert dsa.read_device_flags() == 0
+    want = torch.arange(2048, dtype=torch.int32, device=DEV).expand(1, 2560, 2048)
+    assert torch.equal(sel, want)
+    rows = [0, 1000, 2559]
+    assert np.array_equal(sel.reshape(-1, 2048)[rows].cpu().numpy(), oracle.indexer_topk(ix, 2048, rows))
+
+
+@pytest.mark.parametrize("R,n,k", [(40, 30000, 2048), (4, 200000, 2048), (160, 9000, 3000), (24, 131072, 1)])
+def test_topk_from_scores_equal_long_rows(R, n, k):
+    """Rows of one repeated score: the sampled threshold admits every key, a single streamed
+    chunk brings more candidates than the buffer holds, and the row must take the exact passes
+    over global memory (one CTA per row, and rows split across CTAs) -- the lowest k positions."""
+    sc = torch.full((1, R, n), 0.25, dtype=torch.float32, device=DEV)
+    idx = dsa.dsa_topk(k, scores=sc, q_pos0=n - R)
+    torch.cuda.synchronize()
+    assert dsa.read_device_flags() == 0
+    want = torch.arange(k, dtype=torch.int32, device=DEV).expand(1, R, k)
+    assert torch.equal(idx, want)

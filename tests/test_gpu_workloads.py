@@ -176,3 +176,28 @@ def test_packed_prompts_equal_each_prompt_alone():
             assert torch.equal(outs[l][:, r0:r1], o1[l]) and torch.equal(lses[l][:, r0:r1], l1[l])
     del per, packed, outs, lses, bufs
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,dtype,n_rows", [("prefill_128k", "e4m3", 24), ("prefill_128k", "bf16", 12),
+                                               ("decode_b32_200k", "e4m3", 32), ("chunked_prefill_1m", "e4m3", 10)])
+def test_indexer_topk_bit_exact_at_full_size_on_integer_operands(name, dtype, n_rows):
+    """The indexer -> top-k path at each workload's full shape, in the launch configuration the
+    group call uses (row chunks of the score workspace at 128K, the key-range split of the
+    decode indexer with the split top-k over 200,000-key rows, 1M-key rows), on small-integer
+    operands: q_I, k_I in [-3, 3], w in [1, 4], so every score is an integer of magnitude at most
+    64 * 4 * 128 * 9 = 294,912 < 2^24 and exact in fp32.  Sampled index rows must equal the
+    oracle's bit for bit, ties to the lower position included."""
+    wl = synth.WORKLOADS[name].replace(values="int", idx_dtype=dtype)
+    ix = synth.indexer_inputs(wl, 0, DEV)
+    idx = dsa.dsa_topk(wl.k, ix=ix)
+    torch.cuda.synchronize()
+    assert dsa.read_device_flags() == 0
+    rows = synth.sample_rows(wl, n_rows) if wl.B == 1 else list(range(wl.B))
+    # row chunks of the 128K workspace hold 8,192 rows: include rows on both sides of a seam
+    if name == "prefill_128k":
+        rows = sorted(set(rows) | {8191, 8192, 65535, 65536})
+    got = idx.reshape(wl.B * wl.T, wl.k)[torch.as_tensor(rows, device=DEV)].cpu().numpy()
+    ref = oracle.indexer_topk(ix, wl.k, rows)
+    assert np.array_equal(got, ref)
+    del ix, idx
+    torch.cuda.empty_cache()
