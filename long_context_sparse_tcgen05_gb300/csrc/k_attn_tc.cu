@@ -100,6 +100,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// Thread t of the warp receives, for each of the x4 repetitions j, TMEM lanes base + t/4 and
+// base + t/4 + 8 at columns 8j + 2(t%4) and 8j + 2(t%4) + 1, in that order (r[4j .. 4j+3]).
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
@@ -397,8 +406,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q4 = warp & 3;                    // TMEM lane quarter
     const int sw = warp - kSmWarp0;             // softmax warp index 0..7
     const int kh = sw >> 2;                     // key half: columns 32 * kh .. + 31 of each block
-    const bool head_lane = lane < 16;           // M=64 rows live in lanes 0..15 of each quarter
-    const int h = q4 * 16 + lane;               // head of this lane (valid when head_lane)
+    // The M = 64 score rows sit in lanes 0..15 of each lane quarter; the 16x256b TMEM shape
+    // spreads them over all 32 threads: thread t holds heads hd[0] = 16 q4 + t/4 and hd[1] =
+    // hd[0] + 8, each at the 8 keys 8j + 2m + {0, 1} (m = t % 4, j < 4) of the warp's key half;
+    // a head's four threads (one quad) combine their maxima and sums with two shuffles.
+    const int m = lane & 3;
+    const int hd[2] = {q4 * 16 + (lane >> 2), q4 * 16 + (lane >> 2) + 8};
+    const bool quad_lead = m == 0;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const float sl2 = p.scale * kLog2e;
     const int t = threadIdx.x - kSmWarp0 * 32;  // 0..255
@@ -429,38 +443,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      float m_used = -INFINITY, l = 0.f;
+      float m_used[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
       for (int j = 0; ok && j < nb; ++j, ++g) {
         const int sb = (int)(g & 1);
         // this lane's key slot, loaded before the wait so that its latency hides behind it
         const int e = (j0 + j) * kNB + kh * 32 + lane;
         const int id = e < p.kk ? __ldg(irow + e) : -1;
         const bool got_s = mbar_wait<kPoll>(&bar.s_full[sb], (uint32_t)((g >> 1) & 1), abort_flag, p.wait);
-        uint32_t sr[32];
+        uint32_t sr[16];
         if (got_s) {
           tc_fence_after();
-          tmem_ld32(tmem + lane_base + kColS + sb * kNB + kh * 32, sr);
+          tmem_ld_16x256b_x4(tmem + lane_base + kColS + sb * kNB + kh * 32, sr);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bar.s_empty[sb]);
         } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) sr[c] = 0u;  // leaving at the barrier below
+          for (int c = 0; c < 16; ++c) sr[c] = 0u;  // leaving at the barrier below
         }
         // scores in base-2 units, masked by the validity of each key slot (lane c checks key c)
         const uint32_t vm = __ballot_sync(0xffffffffu, id >= 0 && id < p.S);
-        float s[32];
-        float bmax = -INFINITY;
+        float s[2][8];
+        float bmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float x = __uint_as_float(sr[c]) * sl2;
-          s[c] = ((vm >> c) & 1u) ? x : -INFINITY;
-          bmax = fmaxf(bmax, s[c]);
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+          for (int hs = 0; hs < 2; ++hs)
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const float x = __uint_as_float(sr[4 * jj + 2 * hs + e2]) * sl2;
+              const float y = ((vm >> (8 * jj + 2 * m + e2)) & 1u) ? x : -INFINITY;
+              s[hs][2 * jj + e2] = y;
+              bmax[hs] = fmaxf(bmax[hs], y);
+            }
+#pragma unroll
+        for (int hs = 0; hs < 2; ++hs) {
+          bmax[hs] = fmaxf(bmax[hs], __shfl_xor_sync(0xffffffffu, bmax[hs], 1));
+          bmax[hs] = fmaxf(bmax[hs], __shfl_xor_sync(0xffffffffu, bmax[hs], 2));
         }
-        const bool need_h = head_lane && bmax > m_used + kRescaleLog2;
+        const bool need_h = bmax[0] > m_used[0] + kRescaleLog2 || bmax[1] > m_used[1] + kRescaleLog2;
         const int any = __any_sync(0xffffffffu, need_h);
-        if (head_lane) sm->bmax[sb][kh][h] = bmax;
+        if (quad_lead) {
+          sm->bmax[sb][kh][hd[0]] = bmax[0];
+          sm->bmax[sb][kh][hd[1]] = bmax[1];
+        }
         if (lane == 0) sm->any_rescale[sb][sw] = any;
         if (named_sync_or(1, kSmThreads, !got_s)) {
           ok = false;
@@ -469,17 +496,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         int anyr = 0;
 #pragma unroll
         for (int w = 0; w < kSmWarps; ++w) anyr |= sm->any_rescale[sb][w];
-        const float bm = head_lane ? fmaxf(sm->bmax[sb][0][h], sm->bmax[sb][1][h]) : -INFINITY;
-        const bool need = head_lane && bm > m_used + kRescaleLog2;  // same decision in both halves
-        const float m_new = need ? bm : m_used;
+        float m_new[2];
+        bool need[2];
+#pragma unroll
+        for (int hs = 0; hs < 2; ++hs) {
+          const float bm = fmaxf(sm->bmax[sb][0][hd[hs]], sm->bmax[sb][1][hd[hs]]);
+          need[hs] = bm > m_used[hs] + kRescaleLog2;  // the same decision in both key halves
+          m_new[hs] = need[hs] ? bm : m_used[hs];
+        }
         if (j > 0 && anyr) {
           // O^T must be complete for the previous block before it is rescaled: the value
           // product of block g-1 releases its stage
           const long long gp = g - 1;
           const bool got_o = mbar_wait<kPoll>(&bar.kv_empty[gp % kStages], (uint32_t)((gp / kStages) & 1), abort_flag, p.wait);
-          const float alpha = need ? ex2(m_used - m_new) : 1.f;
-          if (head_lane && kh == 0) sm->alpha[h] = alpha;
-          l *= alpha;
+#pragma unroll
+          for (int hs = 0; hs < 2; ++hs) {
+            const float alpha = need[hs] ? ex2(m_used[hs] - m_new[hs]) : 1.f;
+            if (quad_lead && kh == 0) sm->alpha[hd[hs]] = alpha;
+            l[hs] *= alpha;
+          }
           if (named_sync_or(1, kSmThreads, !got_o)) {
             ok = false;
             break;
@@ -500,24 +535,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
           tc_fence_before();
         }
-        m_used = m_new;
-        const float mu = m_used == -INFINITY ? 0.f : m_used;
-        if (head_lane) {
-          // this half of the head's P row: 32 keys of bf16 = four 16-byte chunks of the 128-byte
-          // swizzled K-major row in the block's rope atom, which S(g) -- now complete -- was the
-          // last to read
-          uint8_t* prow = kv_s + (size_t)(g % kStages) * kKVBytes + kPAtom * kAtomKV + h * 128;
+        // P rows (bf16) of this thread's two heads, in the block's rope atom, which S(g) -- now
+        // complete -- was the last to read: key 8j + 2m + {0, 1} of the key half is the 4-byte
+        // word m of 16-byte chunk 4kh + j of the head's 128-byte swizzled row
+        uint8_t* patom = kv_s + (size_t)(g % kStages) * kKVBytes + kPAtom * kAtomKV;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t w[4];
+        for (int hs = 0; hs < 2; ++hs) {
+          m_used[hs] = m_new[hs];
+          const float mu = m_used[hs] == -INFINITY ? 0.f : m_used[hs];
+          uint8_t* prow = patom + hd[hs] * 128 + m * 4;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float a = ex2(s[ch * 8 + 2 * i] - mu), bq = ex2(s[ch * 8 + 2 * i + 1] - mu);
-              l += a + bq;
-              __nv_bfloat162 v2 = __floats2bfloat162_rn(a, bq);
-              w[i] = *reinterpret_cast<uint32_t*>(&v2);
-            }
-            *reinterpret_cast<uint4*>(prow + (((kh * 4 + ch) ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int jj = 0; jj < 4; ++jj) {
+            const float a = ex2(s[hs][2 * jj] - mu), bq = ex2(s[hs][2 * jj + 1] - mu);
+            l[hs] += a + bq;
+            __nv_bfloat162 v2 = __floats2bfloat162_rn(a, bq);
+            *reinterpret_cast<uint32_t*>(prow + (((kh * 4 + jj) ^ (hd[hs] & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&v2);
           }
         }
         fence_async_smem();
@@ -526,14 +558,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue: O = O^T / l, LSE ----
-      if (head_lane) sm->lpart[kh][h] = l;
+#pragma unroll
+      for (int hs = 0; hs < 2; ++hs) {
+        l[hs] += __shfl_xor_sync(0xffffffffu, l[hs], 1);
+        l[hs] += __shfl_xor_sync(0xffffffffu, l[hs], 2);
+        if (quad_lead) sm->lpart[kh][hd[hs]] = l[hs];
+      }
       named_sync(1, kSmThreads);
-      if (head_lane && kh == 0) {
-        const float lt = sm->lpart[0][h] + sm->lpart[1][h];
-        sm->lsum[h] = lt > 0.f ? 1.f / lt : 0.f;  // reciprocal row sums
-        const float lse_v = lt > 0.f ? (m_used + log2f(lt)) * kLn2 : -INFINITY;
-        if (po) p.part_lse[(int64_t)item * kH + h] = lse_v;
-        else if (p.lse) p.lse[(int64_t)row * kH + h] = lse_v;
+      if (quad_lead && kh == 0) {
+#pragma unroll
+        for (int hs = 0; hs < 2; ++hs) {
+          const int hh = hd[hs];
+          const float lt = sm->lpart[0][hh] + sm->lpart[1][hh];
+          sm->lsum[hh] = lt > 0.f ? 1.f / lt : 0.f;  // reciprocal row sums
+          const float lse_v = lt > 0.f ? (m_used[hs] + log2f(lt)) * kLn2 : -INFINITY;
+          if (po) p.part_lse[(int64_t)item * kH + hh] = lse_v;
+          else if (p.lse) p.lse[(int64_t)row * kH + hh] = lse_v;
+        }
       }
       const bool got_o = mbar_wait<kPoll>(&bar.o_full, oc & 1, abort_flag, p.wait);
       if (named_sync_or(1, kSmThreads, !got_o)) {
