@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--workload", default="prefill_128k")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the other configurations after the headline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle CPU time")
     ap.add_argument("--kernel", choices=["attn", "indexer", "topk", "ixtopk", "quant"], default=None,
                     help="time one call on a single-kernel case instead of the group step "
@@ -165,14 +166,22 @@ def indexer_flops(wl) -> float:
     return float(np.sum(visible_counts(wl).astype(np.float64)) * 2 * wl.HI * wl.DI)
 
 
+def stores_scores(wl) -> bool:
+    """Whether dsa_topk from indexer operands passes this workload's scores through a score
+    buffer (few query rows, 4 indexer heads or k > 2,048) rather than keeping candidates only."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+    return wl.HI != 64 or wl.k > 2048 or wl.B * ((wl.T + 3) // 4) < 4 * sms
+
+
 def indexer_bytes(wl) -> float:
-    """Algorithmic HBM bytes of one indexer call as built here (scores materialised): the key
-    cache and its scales, the queries, head weights and scales, and the fp32 score of every
-    visible pair written once."""
+    """Algorithmic HBM bytes of one indexer call: the key cache and its scales, the queries, head
+    weights and scales, and -- where the path stores scores (decode's few rows) -- the fp32 score
+    of every visible pair written once."""
     elt = 1 if wl.idx_dtype == "e4m3" else 2
     keys = wl.B * wl.S * (wl.DI * elt + 4)
     queries = wl.B * wl.T * (wl.HI * wl.DI * elt + wl.HI * 4 + 4)
-    return float(keys + queries + np.sum(visible_counts(wl).astype(np.float64)) * 4)
+    scores = np.sum(visible_counts(wl).astype(np.float64)) * 4 if stores_scores(wl) else 0.0
+    return float(keys + queries + scores)
 
 
 def captured_traffic(kernel: str, units: int):
@@ -435,7 +444,73 @@ def run_ours(args, rank, world, local):
         line["e2e"] = run_e2e(dsa, wl, layers, group, outs, lses, bufs, args, world)
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(wl, layers[0]["ix"], [g["at"] for g in group], args.cpu_seconds)
+    if not args.no_workloads:
+        del layers, group, ffff, outs, lses, bufs
+        torch.cuda.empty_cache()
+        line["workloads"] = run_workloads(dsa, dev, peaks, fp8_peak_tf, world)
     return line
+
+
+def run_workloads(dsa, dev, peaks, fp8_tf, world, steps=3):
+    """The project's other configurations after the headline step, a few steps each through the
+    same call (one F,S,S,S group of the workload's first four layers): group ms and tokens/s;
+    for the three large ones also the all-full (F,F,F,F) group and the speedup of F,S,S,S over
+    it, and the roofline fraction of the kernel that dominates the F,S,S,S step (attention
+    against measured HBM; the indexer against the tensor peak of its dtype -- FP8 measured in
+    this run, bf16 from the measured peaks -- or HBM where its arithmetic intensity is below the
+    ridge, as in decode)."""
+    res = {}
+    for name in ("tiny_l1k", "prefill_16k", "decode_b32_200k", "chunked_prefill_1m"):
+        wl = synth.WORKLOADS[name]
+        layers = synth.group_inputs(wl, 4, dev, with_indexer=True)
+        fsss = [dict(ix=layers[0]["ix"], at=layers[l]["at"]) for l in range(4)]
+        ffff = [dict(ix=layers[l]["ix"], at=layers[l]["at"]) for l in range(4)]
+        outs = [torch.empty(wl.B, wl.T, wl.H, wl.DV, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+        lses = [torch.empty(wl.B, wl.T, wl.H, dtype=torch.float32, device=dev) for _ in range(4)]
+        bufs = [torch.empty(wl.B, wl.T, wl.k, dtype=torch.int32, device=dev) for _ in range(4)]
+
+        def step():
+            dsa.indexshare_group_forward(fsss, "FSSS", wl.k, outs=outs, lses=lses, idx_bufs=bufs[:1])
+
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        dsa.trace_enable(256 * steps + 64)
+        ms = time_loop(step, steps, 0, world)
+        trace = dsa.trace_read()
+        dsa.trace_disable()
+        by_kind = {}
+        for kind, t in trace:
+            by_kind[kind] = by_kind.get(kind, 0.0) + t / steps
+        ent = {"group_ms": round(ms, 3), "tokens_per_s": round(wl.B * wl.T * world / (ms / 1e3), 1),
+               "kernel_ms_per_step": {k: round(v, 3) for k, v in sorted(by_kind.items())}}
+        if name != "tiny_l1k":
+            ffff_ms = time_loop(lambda: dsa.indexshare_group_forward(ffff, "FFFF", wl.k, outs=outs, lses=lses,
+                                                                      idx_bufs=bufs), 2, 1, world)
+            ent["ffff_ms"] = round(ffff_ms, 3)
+            ent["fsss_vs_ffff"] = round(ffff_ms / ms, 3)
+            att, ixt = by_kind.get("attention", 0.0), by_kind.get("indexer", 0.0) + by_kind.get("topk", 0.0)
+            if att >= ixt:
+                gbs = 4 * attn_bytes(wl) / (att / 1e3) / 1e9
+                ent["roofline"] = {"kernel": "sparse MLA attention", "bound": "hbm", "achieved": round(gbs, 1),
+                                   "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4)}
+            else:
+                ix_ms = by_kind.get("indexer", 0.0)
+                fp8 = wl.idx_dtype == "e4m3"
+                tpeak = fp8_tf if fp8 else peaks["bf16_tflops"]
+                kern = "indexer (%s)" % ("FP8" if fp8 else "bf16")
+                if indexer_flops(wl) / indexer_bytes(wl) >= tpeak * 1e12 / (peaks["hbm_gbs"] * 1e9):
+                    tf = indexer_flops(wl) / (ix_ms / 1e3) / 1e12
+                    ent["roofline"] = {"kernel": kern, "bound": "tensor", "achieved": round(tf, 1),
+                                       "peak": tpeak, "unit": "TFLOP/s", "frac": round(tf / tpeak, 4)}
+                else:
+                    gbs = indexer_bytes(wl) / (ix_ms / 1e3) / 1e9
+                    ent["roofline"] = {"kernel": kern, "bound": "hbm", "achieved": round(gbs, 1),
+                                       "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4)}
+        res[name] = ent
+        del layers, fsss, ffff, outs, lses, bufs
+        torch.cuda.empty_cache()
+    return res
 
 
 def _indexer_kernel_line(wl, by_kind, steps, fp8_tf):

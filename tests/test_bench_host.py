@@ -58,3 +58,6 @@ def test_decode_indexer_bytes_and_its_bound(bench):
     assert 100 < bench.indexer_flops(wl) / bench.indexer_bytes(wl) < 140
     prefill = synth.WORKLOADS["prefill_128k"]
     assert bench.indexer_flops(prefill) / bench.indexer_bytes(prefill) > 570
+    # prefill keeps candidates only: no score bytes in its count
+    assert not bench.stores_scores(prefill) and bench.stores_scores(wl)
+    assert bench.indexer_bytes(prefill) == 131072 * (128 + 4) + 131072 * (64 * 128 + 64 * 4 + 4)
