@@ -510,7 +510,51 @@ def run_workloads(dsa, dev, peaks, fp8_tf, world, steps=3):
         res[name] = ent
         del layers, fsss, ffff, outs, lses, bufs
         torch.cuda.empty_cache()
+    res["mtp_draft_b32_200k"] = run_draft(dsa, dev, world, steps)
     return res
+
+
+def run_draft(dsa, dev, world, steps=3):
+    """The four draft steps of a multi-token-prediction layer over the batch-32 200K decode
+    cache: one indexshare_draft_forward call (the first step's indexer + top-k, then one
+    attention launch for all steps over its index row) against the same steps run as an
+    F,S,S,S group (one attention launch per step); ms of each and the speedup."""
+    wl = synth.WORKLOADS["mtp_draft_b32_200k"]
+    layers = synth.group_inputs(wl, 4, dev, with_indexer=True)
+    group = [dict(ix=layers[0]["ix"], at=layers[l]["at"]) for l in range(4)]
+    at = dict(layers[0]["at"])
+    at["q"] = torch.cat([l["at"]["q"] for l in layers], dim=1).contiguous()
+    out = torch.empty(wl.B, 4, wl.H, wl.DV, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(wl.B, 4, wl.H, dtype=torch.float32, device=dev)
+    idx = torch.empty(wl.B, 1, wl.k, dtype=torch.int32, device=dev)
+    outs = [torch.empty(wl.B, 1, wl.H, wl.DV, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    lses = [torch.empty(wl.B, 1, wl.H, dtype=torch.float32, device=dev) for _ in range(4)]
+    bufs = [torch.empty(wl.B, 1, wl.k, dtype=torch.int32, device=dev)]
+
+    def draft():
+        dsa.indexshare_draft_forward(layers[0]["ix"], at, wl.k, out=out, lse=lse, idx=idx)
+
+    def walk():
+        dsa.indexshare_group_forward(group, "FSSS", wl.k, outs=outs, lses=lses, idx_bufs=bufs)
+
+    for _ in range(3):
+        draft()
+        walk()
+    torch.cuda.synchronize()
+    dsa.trace_enable(64 * steps + 64)
+    d_ms = time_loop(draft, steps, 0, world)
+    trace = dsa.trace_read()
+    dsa.trace_disable()
+    g_ms = time_loop(walk, steps, 0, world)
+    by_kind = {}
+    for kind, t in trace:
+        by_kind[kind] = by_kind.get(kind, 0.0) + t / steps
+    ent = {"draft_ms": round(d_ms, 3), "group_ms": round(g_ms, 3), "draft_vs_group": round(g_ms / d_ms, 3),
+           "draft_kernel_ms": {k: round(v, 3) for k, v in sorted(by_kind.items())},
+           "tokens_per_s": round(wl.B * 4 * world / (d_ms / 1e3), 1)}
+    del layers, group, at, out, lse, idx, outs, lses, bufs
+    torch.cuda.empty_cache()
+    return ent
 
 
 def _indexer_kernel_line(wl, by_kind, steps, fp8_tf):

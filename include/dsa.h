@@ -203,6 +203,27 @@ dsa_status indexshare_group_forward(const dsa_layer* layers, int32_t n_layers,
                                     const char* schedule, int32_t k, int32_t* const* idx_bufs,
                                     void* ws, size_t ws_bytes, void* stream);
 
+/* Draft-step index reuse in the multi-token-prediction layer (GLM-5.2 article, "Reuse in the
+ * MTP layer": the first draft step computes the indices; the later draft steps reuse those
+ * indices and the earlier KV cache).  One call: the first step's indexer + top-k, then ONE
+ * attention launch in which the n = at->T draft queries of every sequence attend over that
+ * sequence's single index row.
+ *   ix   the first draft step's indexer: B sequences, T = 1 query each, keys k / k_scale
+ *        [B,S,...] (the layer's shared indexer-key cache).
+ *   at   the draft queries as T = n query positions: q [B,n,H,d_qk] (step s of sequence b
+ *        at q + b*q_stride_b + s*q_stride_t), k / v the shared latent cache [B,S,...]; B and
+ *        S equal the indexer's.
+ *   idx  [B,k] int32, written: the first step's selection (ascending, -1 padded); every
+ *        step of sequence b reads row b (index-row stride 0 between steps).
+ *   out  [B,n,H,d_v] bf16; lse [B,n,H] fp32 or NULL.
+ * Results equal dsa_topk(FROM_INDEXER) on ix followed, for each step s, by dsa_sparse_attn
+ * of step s's queries over idx (up to the summation order of a decode split).
+ * ws: indexshare_draft_workspace_size bytes are preferred.  Errors as the two calls. */
+dsa_status indexshare_draft_forward(const dsa_indexer_args* ix, const dsa_attn_args* at, int32_t k,
+                                    int32_t* idx, void* out, float* lse, void* ws, size_t ws_bytes,
+                                    void* stream);
+size_t indexshare_draft_workspace_size(const dsa_indexer_args* ix, const dsa_attn_args* at, int32_t k);
+
 /* Variable-length sequences packed along the row axis (host arrays).  Sequence b owns the
  * packed query rows cu_q[b] .. cu_q[b+1]-1 and the packed key rows cu_k[b] .. cu_k[b+1]-1;
  * its first query row sits at absolute position q_pos0[b] (a full prefill: q_pos0 = 0 with

@@ -11,6 +11,8 @@ Calls (same names as the C ABI):
   dsa_sparse_attn(at, idx)                -> (out [B,T,H,d_v] bf16, lse [B,T,H] fp32)
   indexshare_group_forward(layers, schedule, k) -> (outs, lses, idx_bufs)
   indexshare_group_forward_varlen(layers, schedule, k, cu_q, cu_k, q_pos0) -> same, packed rows
+  indexshare_draft_forward(ix, at, k)     -> (out [B,n,H,d_v], lse [B,n,H], idx [B,1,k]): n draft
+                                             steps over the first step's selection, one launch
   topk_overlap(a, b)                      -> (per_row fp32, mean float)
   topk_overlap_matrix(bufs)               -> (n x n mean overlaps, counts [rows,n,n] or None)
   indexshare_schedule_score(M, schedule)  -> float (host only)
@@ -113,6 +115,12 @@ def load_library(path: str = LIB_PATH):
             lib.indexshare_group_forward.argtypes = [_c.POINTER(Layer), _c.c_int32, _c.c_char_p,
                                                      _c.c_int32, _c.POINTER(_P), _P, _c.c_size_t,
                                                      _P]
+            lib.indexshare_draft_forward.restype = S
+            lib.indexshare_draft_forward.argtypes = [_c.POINTER(IndexerArgs), _c.POINTER(AttnArgs), _c.c_int32,
+                                                     _P, _P, _P, _P, _c.c_size_t, _P]
+            lib.indexshare_draft_workspace_size.restype = _c.c_size_t
+            lib.indexshare_draft_workspace_size.argtypes = [_c.POINTER(IndexerArgs), _c.POINTER(AttnArgs),
+                                                            _c.c_int32]
             lib.indexshare_group_forward_varlen.restype = S
             lib.indexshare_group_forward_varlen.argtypes = [_c.POINTER(Layer), _c.c_int32, _c.c_char_p, _c.c_int32,
                                                             _c.POINTER(Varlen), _c.POINTER(_P), _P, _c.c_size_t, _P]
@@ -311,6 +319,31 @@ def dsa_sparse_attn(at: dict, idx: torch.Tensor, out: torch.Tensor | None = None
     _check(lib.dsa_sparse_attn(_c.byref(a), _ptr(idx), idx.shape[-1], _ptr(out), _ptr(lse),
                                _ptr(ws), ws.numel(), _stream()))
     return out, lse
+
+
+def indexshare_draft_forward(ix: dict, at: dict, k: int, out: torch.Tensor | None = None,
+                             lse: torch.Tensor | bool | None = True, idx: torch.Tensor | None = None):
+    """Draft steps of a multi-token-prediction layer in one call: `ix` is the first step's
+    indexer (T = 1 query per sequence, the layer's key cache), `at` holds the n steps' queries
+    as q [B,n,H,d_qk] over the shared KV.  Returns (out [B,n,H,d_v] bf16, lse [B,n,H] fp32 or
+    None, idx [B,1,k] int32: the first step's selection, read by every step)."""
+    lib = load_library()
+    a = attn_struct(at)
+    x = indexer_struct(ix)
+    dev = at["q"].device
+    if idx is None:
+        idx = torch.empty((a.B, 1, k), dtype=torch.int32, device=dev)
+    assert idx.dtype == torch.int32 and idx.is_contiguous() and idx.numel() == a.B * k
+    if out is None:
+        out = torch.empty((a.B, a.T, a.H, a.d_v), dtype=torch.bfloat16, device=dev)
+    if lse is True:
+        lse = torch.empty((a.B, a.T, a.H), dtype=torch.float32, device=dev)
+    elif lse is False:
+        lse = None
+    ws = workspace(int(lib.indexshare_draft_workspace_size(_c.byref(x), _c.byref(a), k)), dev)
+    _check(lib.indexshare_draft_forward(_c.byref(x), _c.byref(a), k, _ptr(idx), _ptr(out), _ptr(lse), _ptr(ws),
+                                        ws.numel(), _stream()))
+    return out, lse, idx
 
 
 def _group_structs(layers, schedule: str, k: int, outs, lses, idx_bufs, with_lse: bool):

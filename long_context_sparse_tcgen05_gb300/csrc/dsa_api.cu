@@ -127,6 +127,7 @@ dsa::AttnLaunch attn_launch(const dsa_attn_args* at, const int32_t* idx, int32_t
   L.k_sb = at->k_stride_b ? at->k_stride_b : (int64_t)at->S * at->k_ld;
   L.v_sb = at->v_stride_b ? at->v_stride_b : (int64_t)at->S * at->v_ld;
   L.idx = idx; L.kk = k; L.out = out; L.lse = lse;
+  L.idx_st = k; L.idx_sb = (int64_t)at->T * k;
   return L;
 }
 
@@ -369,30 +370,79 @@ dsa_status dsa_topk(const dsa_topk_src* src, int32_t B, int32_t T, int32_t S, in
   return run_indexer_topk(ix, k, idx, ws, ws_bytes, st);
 }
 
-dsa_status dsa_sparse_attn(const dsa_attn_args* at, const int32_t* idx, int32_t k, void* out, float* lse, void* ws,
-                           size_t ws_bytes, void* stream) {
-  dsa_status s = check_attn(at);
-  if (s != DSA_OK) return s;
+namespace {
+
+// Checks shared by the attention entry points (the attention args themselves checked before).
+dsa_status check_attn_call(const int32_t* idx, int32_t k, const void* out, void* ws, size_t ws_bytes) {
   if (!idx || !out) return fail(DSA_ERR_INVALID_ARG, "idx and out must be non-NULL");
   if (k < 1 || k > kMaxK) return fail(DSA_ERR_UNSUPPORTED, "k=%d outside [1, %d]", k, kMaxK);
   if (!aligned16(out)) return fail(DSA_ERR_MISALIGNED, "out must be 16-byte aligned");
-  if ((s = check_ws(ws, ws_bytes, DSA_WS_MIN)) != DSA_OK) return s;
-  dsa::AttnLaunch L = attn_launch(at, idx, k, out, lse);
+  return check_ws(ws, ws_bytes, DSA_WS_MIN);
+}
+
+// Launch of a described attention call: with few rows each row's blocks are split over CTAs
+// when the workspace holds the parts.
+dsa_status run_attn(dsa::AttnLaunch L, void* ws, size_t ws_bytes, void* stream) {
   L.flags = ws_flags(ws);
-  // few rows: split each row's blocks over CTAs when the workspace holds the parts
   const int splits = dsa::attn_splits(L);
   if (splits > 1) {
-    const size_t parts = (size_t)at->B * at->T * splits;
+    const size_t parts = (size_t)L.B * L.T * splits;
     const size_t need = attn_split_bytes(L);
     if (ws_bytes > dsa::kWsScratch && ws_bytes - dsa::kWsScratch >= need) {
       uint8_t* w = static_cast<uint8_t*>(ws) + dsa::kWsScratch;
       L.splits = splits;
       L.part_o = reinterpret_cast<float*>(w);
-      L.part_lse = reinterpret_cast<float*>(w + parts * (size_t)at->H * at->d_v * 4);
+      L.part_lse = reinterpret_cast<float*>(w + parts * (size_t)L.H * L.DV * 4);
     }
   }
   cudaError_t e = dsa::launch_sparse_attn(L, as_stream(stream));
   return e == cudaSuccess ? DSA_OK : cuda_fail(e, "attention launch");
+}
+
+// The draft steps of a sequence read its one index row: T query positions, row stride 0.
+dsa::AttnLaunch draft_launch(const dsa_attn_args* at, const int32_t* idx, int32_t k, void* out, float* lse) {
+  dsa::AttnLaunch L = attn_launch(at, idx, k, out, lse);
+  L.idx_st = 0;
+  L.idx_sb = k;
+  return L;
+}
+
+dsa_status check_draft(const dsa_indexer_args* ix, const dsa_attn_args* at) {
+  dsa_status s = check_indexer(ix);
+  if (s != DSA_OK) return s;
+  if ((s = check_attn(at)) != DSA_OK) return s;
+  if (ix->T != 1)
+    return fail(DSA_ERR_INVALID_ARG, "the first draft step's indexer has T=%d queries per sequence (1 expected)", ix->T);
+  if (ix->B != at->B || ix->S != at->S)
+    return fail(DSA_ERR_INVALID_ARG, "indexer B/S (%d/%d) differ from the attention's (%d/%d)", ix->B, ix->S, at->B, at->S);
+  return DSA_OK;
+}
+
+}  // namespace
+
+dsa_status dsa_sparse_attn(const dsa_attn_args* at, const int32_t* idx, int32_t k, void* out, float* lse, void* ws,
+                           size_t ws_bytes, void* stream) {
+  dsa_status s = check_attn(at);
+  if (s != DSA_OK) return s;
+  if ((s = check_attn_call(idx, k, out, ws, ws_bytes)) != DSA_OK) return s;
+  return run_attn(attn_launch(at, idx, k, out, lse), ws, ws_bytes, stream);
+}
+
+dsa_status indexshare_draft_forward(const dsa_indexer_args* ix, const dsa_attn_args* at, int32_t k, int32_t* idx,
+                                    void* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  dsa_status s = check_draft(ix, at);
+  if (s != DSA_OK) return s;
+  if ((s = check_attn_call(idx, k, out, ws, ws_bytes)) != DSA_OK) return s;
+  // the first step's indexer + top-k, then every step over that one index row
+  if ((s = run_indexer_topk(ix, k, idx, ws, ws_bytes, as_stream(stream))) != DSA_OK) return s;
+  return run_attn(draft_launch(at, idx, k, out, lse), ws, ws_bytes, stream);
+}
+
+size_t indexshare_draft_workspace_size(const dsa_indexer_args* ix, const dsa_attn_args* at, int32_t k) {
+  if (!ix || !at || at->B <= 0 || at->T <= 0 || at->S <= 0 || k < 1 || k > kMaxK) return DSA_WS_MIN;
+  const size_t a = dsa::kWsScratch + attn_split_bytes(draft_launch(at, nullptr, k, nullptr, nullptr));
+  const size_t t = dsa_workspace_size(ix, k);
+  return a > t ? a : t;
 }
 
 namespace {

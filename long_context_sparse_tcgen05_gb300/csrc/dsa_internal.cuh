@@ -149,6 +149,9 @@ struct AttnLaunch {
   int64_t k_sb, v_sb;   // sequence strides of k and v in elements
   const int32_t* idx;
   int kk;
+  // index-row strides in elements: row (b, t) reads idx + b*idx_sb + t*idx_st (dense rows:
+  // kk and T*kk; the draft steps of a sequence sharing its one row: 0 and kk)
+  int64_t idx_st, idx_sb;
   void* out;
   float* lse;
   uint32_t* flags;
@@ -161,6 +164,10 @@ struct AttnLaunch {
   float* part_o;
   float* part_lse;
 };
+// The index row of flat query row `row` = b*T + t.
+__host__ __device__ inline const int32_t* attn_idx_row(const AttnLaunch& p, int row) {
+  return p.idx + (int64_t)(row / p.T) * p.idx_sb + (int64_t)(row % p.T) * p.idx_st;
+}
 cudaError_t launch_sparse_attn(const AttnLaunch& p, cudaStream_t st);
 constexpr int kMaxAttnSplits = 8;
 int attn_splits(const AttnLaunch& p);  // parts per row the 64-head MLA kernel would use (1: none)

@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(AtCfg<HP, DQK, DV, SEPV, NB>::kThreads, 1)
 
   const int row = blockIdx.x;  // flat b*T + t
   const int b = row / p.T;
-  const int32_t* irow = p.idx + (int64_t)row * p.kk;
+  const int32_t* irow = attn_idx_row(p, row);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wm = warp / C::kWN, wn = warp % C::kWN;
   const int g = lane >> 2, c = lane & 3;

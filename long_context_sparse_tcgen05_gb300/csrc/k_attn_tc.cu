@@ -6,18 +6,21 @@
 //
 // Persistent CTAs (one per SM) walk query rows.  For each row:
 //   * warps 0..3 load the query tile with TMA and gather the selected KV rows, 64 per block,
-//     with 16-byte cp.async copies into two 128-byte-swizzled stages.  A stage lands atom by
-//     atom (64 columns of all 64 rows), each atom with its own barrier, so the score product
-//     starts on the first columns while the rest are still in flight;
-//   * warp 4 issues  S = Q K^T  (M = 64 heads, N = 64 keys, K = 576) into TMEM, atom by atom;
+//     with 16-byte cp.async copies into two 128-byte-swizzled stages.  A stage lands in three
+//     groups of three atoms (an atom: 64 columns of all 64 rows), each group with its own
+//     barrier, so the score product starts on the first columns while the rest are still in
+//     flight.  Every copying thread arrives on a group's barrier, and those arrivals pace the
+//     gather: one barrier per atom moved about 17% fewer bytes per second than one per stage
+//     (and 32-row stages, with twice the arrivals per byte, half as many);
+//   * warp 4 issues  S = Q K^T  (M = 64 heads, N = 64 keys, K = 576) into TMEM, group by group;
 //   * warp 5 issues  O^T += V^T P^T  (M = 128 value dims x 4, N = 64 heads, K = 64 keys) -- the
 //     transposed value product keeps the 64 x 512 fp32 accumulator in 256 TMEM columns.  Two
 //     issuing threads let the tensor pipe interleave the two products (a single issuer stalls
 //     in the 36-instruction score chain while a value product is ready);
 //   * warps 6..13 run the online softmax, two warps per TMEM lane quarter, each on 32 of the
-//     block's 64 keys (one head per TMEM lane, base-2 exponent, fp32 row sums; the two halves
-//     of a head exchange block maxima and partial sums through shared memory; bf16 P is written
-//     into the block's rope columns, free once S is done).  The running maximum is raised only
+//     block's 64 keys (base-2 exponent, fp32 row sums; the two halves of a head exchange block
+//     maxima and partial sums through shared memory; bf16 P is written into the block's rope
+//     columns, free once S is done).  The running maximum is raised only
 //     when a block exceeds it by more than 2^8; then O^T is rescaled in TMEM.  At the end
 //     they normalise O, write bf16 O and the natural-log LSE.
 // With fewer rows than SMs (decode) a row's blocks are split over several CTAs: each writes
@@ -38,15 +41,22 @@ namespace {
 using namespace sm100;
 
 constexpr int kH = 64, kDQK = 576, kDV = 512;
-constexpr int kNB = 64;                    // keys per block (N of the S product, K of the PV product)
-constexpr int kStages = 2;                 // gathered KV blocks in flight
+// Keys per block (N of the S product, K of the PV product) and blocks in flight.  64 x 2 fills
+// shared memory beside the query tile; 32 x 4 (the same bytes, shorter per-block steps) was
+// measured 1.55x slower (5.98 against 3.87 ms over 8,192 rows of 2,048 keys).
+constexpr int kNB = 64;
+constexpr int kStages = 2;
+static_assert(kNB == 64 || kNB == 32, "P rows are 128- or 64-byte swizzled");
+constexpr int kHalf = kNB / 2;             // keys of a block per softmax warp
 constexpr int kAtoms = kDQK / 64;          // 9 swizzle atoms of 64 bf16 per row
 constexpr uint32_t kAtomQ = kH * 128;      // 8 KB
-constexpr uint32_t kAtomKV = kNB * 128;    // 8 KB
+constexpr uint32_t kAtomKV = kNB * 128;    // kNB rows of 128 bytes
 constexpr uint32_t kQBytes = kAtoms * kAtomQ;
 constexpr uint32_t kKVBytes = kAtoms * kAtomKV;
 constexpr int kPAtom = kAtoms - 1;         // P(g) overwrites block g's rope atom once S(g) is done
-constexpr int kGroups = kAtoms;            // a stage lands atom by atom
+constexpr int kBarAtoms = 3;               // atoms per landing barrier (a group of atoms lands together)
+constexpr int kGroups = kAtoms / kBarAtoms;
+static_assert(kAtoms % kBarAtoms == 0, "landing groups must tile the atoms");
 constexpr int kProdWarps = 4;              // cp.async gather warps
 constexpr int kMmaWarp = kProdWarps;       // warp 4: score product issuer (and TMEM owner)
 constexpr int kPvWarp = kProdWarps + 1;    // warp 5: value product issuer
@@ -56,7 +66,7 @@ constexpr int kSmThreads = kSmWarps * 32;
 constexpr int kThreads = (kProdWarps + 2 + kSmWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;              // O^T: 4 chunks x 64 columns
-constexpr uint32_t kColS = 256;            // S: 2 buffers x 64 columns
+constexpr uint32_t kColS = 256;            // S: 2 buffers x kNB columns
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;
@@ -100,9 +110,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
-// Thread t of the warp receives, for each of the x4 repetitions j, TMEM lanes base + t/4 and
-// base + t/4 + 8 at columns 8j + 2(t%4) and 8j + 2(t%4) + 1, in that order (r[4j .. 4j+3]).
-__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+// Thread t of the warp receives, for each of the x2 / x4 repetitions j, TMEM lanes base + t/4
+// and base + t/4 + 8 at columns 8j + 2(t%4) and 8j + 2(t%4) + 1, in that order (r[4j .. 4j+3]).
+__device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
@@ -197,10 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0, qc = 0;
     long long g = 0;  // global block counter
     bool ok = true;
-    const bool vec = (p.kk & 3) == 0;
+    const bool vec = ((p.kk | p.idx_st | p.idx_sb) & 3) == 0 && (reinterpret_cast<uintptr_t>(p.idx) & 15u) == 0;
     for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
       const int row = item / splits;
-      const int32_t* irow = p.idx + (int64_t)row * p.kk;
+      const int32_t* irow = attn_idx_row(p, row);
       const int b = row / p.T;
       const uint8_t* kvb = kvg + (int64_t)b * p.k_sb * 2;  // this sequence's latent rows
       // blocks = 1 + (last entry other than -1) / kNB; all loads of the scan issued together
@@ -293,8 +308,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                          "l"(kvb + rid[pass] * row_bytes + (a * 8 + cc) * 16), "r"(rv[pass] ? 16 : 0)
                          : "memory");
           }
-          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_addr(&bar.kv_full[st][a]))
-                       : "memory");
+          if (a % kBarAtoms == kBarAtoms - 1)
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(
+                             smem_addr(&bar.kv_full[st][a / kBarAtoms]))
+                         : "memory");
         }
       }
     }
@@ -304,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0 && qc > 0) mbar_wait_drain(&bar.q_full, (uint32_t)((qc - 1) & 1));
   } else if (warp == kMmaWarp) {
     // ================= score product issuer (one thread) =================
-    const uint32_t id_s = idesc_mn(1, 1, kH, kNB);  // S: M=64 heads, N=64 keys
+    const uint32_t id_s = idesc_mn(1, 1, kH, kNB);  // S: M=64 heads, N=32 keys
     const uint64_t q_desc0 = desc_sw128(smem_addr(q_s));
     const uint64_t kv_desc0 = desc_sw128(smem_addr(kv_s));
     int it = 0, qc = 0;
@@ -333,7 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d = tmem + kColS + sb * kNB;
 #pragma unroll
           for (int a = 0; a < kAtoms; ++a) {
-            if (!(ok = mbar_wait<kPoll>(&bar.kv_full[st][a], kvpar, abort_flag, p.wait))) break;
+            if (a % kBarAtoms == 0 && !(ok = mbar_wait<kPoll>(&bar.kv_full[st][a / kBarAtoms], kvpar, abort_flag, p.wait)))
+              break;
             fence_async_smem();  // the stage was written by cp.async (generic proxy)
             tc_fence_after();
 #pragma unroll
@@ -357,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kPvWarp) {
     // ================= value product issuer (one thread) =================
     const uint32_t id_o = idesc_mn(1, 1, 128, kH) | (1u << 15);  // O^T: M=128 dims (MN-major A), N=64 heads
-    const uint64_t kv_desc0 = desc_sw128(smem_addr(kv_s));
+    // P: 64 rows (heads) of kNB keys, 128- or 64-byte swizzled rows
+    const uint64_t p_desc0 = kNB == 64 ? desc_sw128(smem_addr(kv_s)) : desc_sw64(smem_addr(kv_s));
     const uint64_t v_desc0 = desc_sw128_mn(smem_addr(kv_s), kAtomKV);
     int it = 0, oc = 0;
     long long g = 0;
@@ -382,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_async_smem();
           tc_fence_after();
           const uint64_t vd = v_desc0 + (uint64_t)((st * kKVBytes) >> 4);
-          const uint64_t pd = kv_desc0 + (uint64_t)((st * kKVBytes + kPAtom * kAtomKV) >> 4);
+          const uint64_t pd = p_desc0 + (uint64_t)((st * kKVBytes + kPAtom * kAtomKV) >> 4);
 #pragma unroll
           for (int k = 0; k < kNB / 16; ++k)
 #pragma unroll
@@ -408,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kh = sw >> 2;                     // key half: columns 32 * kh .. + 31 of each block
     // The M = 64 score rows sit in lanes 0..15 of each lane quarter; the 16x256b TMEM shape
     // spreads them over all 32 threads: thread t holds heads hd[0] = 16 q4 + t/4 and hd[1] =
-    // hd[0] + 8, each at the 8 keys 8j + 2m + {0, 1} (m = t % 4, j < 4) of the warp's key half;
-    // a head's four threads (one quad) combine their maxima and sums with two shuffles.
+    // hd[0] + 8, each at the 4 keys 8j + 2m + {0, 1} (m = t % 4, j < 2) of the warp's 16-key
+    // half; a head's four threads (one quad) combine their maxima and sums with two shuffles.
     const int m = lane & 3;
     const int hd[2] = {q4 * 16 + (lane >> 2), q4 * 16 + (lane >> 2) + 8};
     const bool quad_lead = m == 0;
@@ -432,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t == 0) mbar_arrive(&bar.info_empty[it & 1]);
       __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * kH * kDV;
       float* po = splits > 1 ? p.part_o + (int64_t)item * kH * kDV : nullptr;  // this part's output
-      const int32_t* irow = p.idx + (int64_t)row * p.kk;
+      const int32_t* irow = attn_idx_row(p, row);
       if (nb == 0) {  // nothing visible: O = 0, LSE = -inf
         if (po) {
           for (int i = t; i < kH * kDV / 4; i += kSmThreads) reinterpret_cast<float4*>(po)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -446,28 +465,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_used[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
       for (int j = 0; ok && j < nb; ++j, ++g) {
         const int sb = (int)(g & 1);
-        // this lane's key slot, loaded before the wait so that its latency hides behind it
-        const int e = (j0 + j) * kNB + kh * 32 + lane;
+        // this lane's key slot (lanes 16..31 repeat 0..15), loaded before the wait so that its
+        // latency hides behind it
+        const int e = (j0 + j) * kNB + kh * kHalf + (lane & (kHalf - 1));
         const int id = e < p.kk ? __ldg(irow + e) : -1;
         const bool got_s = mbar_wait<kPoll>(&bar.s_full[sb], (uint32_t)((g >> 1) & 1), abort_flag, p.wait);
-        uint32_t sr[16];
+        uint32_t sr[kHalf / 2];
         if (got_s) {
           tc_fence_after();
-          tmem_ld_16x256b_x4(tmem + lane_base + kColS + sb * kNB + kh * 32, sr);
+          tmem_ld_16x256b(tmem + lane_base + kColS + sb * kNB + kh * kHalf, sr);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bar.s_empty[sb]);
         } else {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) sr[c] = 0u;  // leaving at the barrier below
+          for (int c = 0; c < kHalf / 2; ++c) sr[c] = 0u;  // leaving at the barrier below
         }
         // scores in base-2 units, masked by the validity of each key slot (lane c checks key c)
         const uint32_t vm = __ballot_sync(0xffffffffu, id >= 0 && id < p.S);
-        float s[2][8];
+        float s[2][kHalf / 4];
         float bmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
+        for (int jj = 0; jj < kHalf / 8; ++jj)
 #pragma unroll
           for (int hs = 0; hs < 2; ++hs)
 #pragma unroll
@@ -537,19 +557,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // P rows (bf16) of this thread's two heads, in the block's rope atom, which S(g) -- now
         // complete -- was the last to read: key 8j + 2m + {0, 1} of the key half is the 4-byte
-        // word m of 16-byte chunk 4kh + j of the head's 128-byte swizzled row
+        // word m of 16-byte chunk (kHalf / 8) kh + j of the head's 2 kNB-byte row, whose chunks
+        // the swizzle permutes (128-byte rows: by head mod 8; 64-byte rows: by (head / 2) mod 4)
         uint8_t* patom = kv_s + (size_t)(g % kStages) * kKVBytes + kPAtom * kAtomKV;
 #pragma unroll
         for (int hs = 0; hs < 2; ++hs) {
           m_used[hs] = m_new[hs];
           const float mu = m_used[hs] == -INFINITY ? 0.f : m_used[hs];
-          uint8_t* prow = patom + hd[hs] * 128 + m * 4;
+          uint8_t* prow = patom + hd[hs] * (2 * kNB) + m * 4;
+          const int perm = kNB == 64 ? (hd[hs] & 7) : ((hd[hs] >> 1) & 3);
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
+          for (int jj = 0; jj < kHalf / 8; ++jj) {
             const float a = ex2(s[hs][2 * jj] - mu), bq = ex2(s[hs][2 * jj + 1] - mu);
             l[hs] += a + bq;
             __nv_bfloat162 v2 = __floats2bfloat162_rn(a, bq);
-            *reinterpret_cast<uint32_t*>(prow + (((kh * 4 + jj) ^ (hd[hs] & 7)) << 4)) = *reinterpret_cast<uint32_t*>(&v2);
+            *reinterpret_cast<uint32_t*>(prow + (((kh * (kHalf / 8) + jj) ^ perm) << 4)) =
+                *reinterpret_cast<uint32_t*>(&v2);
           }
         }
         fence_async_smem();
@@ -735,7 +758,7 @@ int attn_splits(const AttnLaunch& p) {
   const int rows = p.B * p.T, sms = num_sms();
   if (rows <= 0 || rows * 2 > sms) return 1;
   int s = sms / rows;                                       // about one CTA per SM
-  const int by_len = (p.kk + 4 * kNB - 1) / (4 * kNB);      // parts of at least 4 blocks
+  const int by_len = (p.kk + 255) / 256;                    // parts of at least 256 keys
   if (s > by_len) s = by_len;
   if (s > kMaxAttnSplits) s = kMaxAttnSplits;
   return s < 2 ? 1 : s;

@@ -171,6 +171,18 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same for rows of 64 bytes (32 bf16 of K) in the 64-byte swizzle: 8-row groups 512 bytes
+// apart (tile base 512-byte aligned).
+__device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(512 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;                    // 64-byte swizzle
+  return d;
+}
+
 // Instruction descriptor: fp32 accumulator, both operands K-major, shape M x N.
 // a_fmt/b_fmt: kind::f16 -> 1 = bf16; kind::f8f6f4 -> 0 = e4m3.
 __host__ __device__ constexpr uint32_t idesc_mn(uint32_t a_fmt, uint32_t b_fmt, int M, int N) {

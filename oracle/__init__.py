@@ -14,6 +14,8 @@ What it follows:
     S layers reuse the nearest preceding F layer's top-k.
   * GLM-5.2 IndexShare article, "What IndexShare reuses": the pattern is F,S,S,S and the
     shared layers keep their own queries, attention weights and outputs.
+  * same article, "Reuse in the MTP layer": the first draft step of the multi-token-prediction
+    layer computes the indices; the later draft steps reuse those indices and the KV cache.
   * The score formula I[t,s] = sum_h w[t,h] * ReLU(q_I[t,h] . k_I[s]) is the project's
     statement of the indexer (the pages do not print one).
   * IndexCache notes, section 1: the indexer runs in FP8; its operands are e4m3 codes with one
@@ -299,6 +301,19 @@ def group_forward(layers, schedule: str, k: int, rows=None):
         out, lse = sparse_attn(layer["at"], cur, rows)
         res.append(dict(idx=cur, out=out, lse=lse))
     return res
+
+
+def draft_forward(ix: dict, at: dict, k: int, seqs=None):
+    """Draft steps of a multi-token-prediction layer: the first step's indexer + top-k picks
+    each sequence's positions (``ix``: one query per sequence), then every draft step s of
+    sequence b (``at["q"]`` [B, n, H, DQK], one shared KV) attends over those positions.
+    Returns (idx [m, k], out [m, n, H, DV], lse [m, n, H]) for the m sequences ``seqs``."""
+    B, n = at["q"].shape[:2]
+    seqs = list(range(B)) if seqs is None else [int(b) for b in seqs]
+    idx = indexer_topk(ix, k, seqs)  # flat row b*1 + 0 of the one-query indexer
+    rows = [b * n + s for b in seqs for s in range(n)]
+    out, lse = sparse_attn(at, np.repeat(idx, n, axis=0), rows)
+    return idx, out.reshape(len(seqs), n, *out.shape[1:]), lse.reshape(len(seqs), n, lse.shape[1])
 
 
 # --- overlap ------------------------------------------------------------------------

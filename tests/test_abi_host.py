@@ -450,3 +450,32 @@ def test_group_workspace_size_covers_every_layer(lib):
 def test_wait_limit_setter_is_callable(lib):
     lib.dsa_set_wait_limit(100)
     lib.dsa_set_wait_limit(0)  # back to the default
+
+
+def _draft(lib, ix, at, k=16, idx=FAKE, out=FAKE):
+    return lib.indexshare_draft_forward(ctypes.byref(ix) if ix is not None else None, ctypes.byref(at), k,
+                                        ctypes.c_void_p(idx) if idx else None,
+                                        ctypes.c_void_p(out) if out else None, None, ctypes.c_void_p(FAKE), 256,
+                                        None)
+
+
+def test_draft_forward_validation(lib):
+    ix, at = _ix(T=1), _at(T=4)
+    assert _draft(lib, None, at) == INVALID
+    assert _draft(lib, _ix(T=2), at) == INVALID      # the first step has one query per sequence
+    assert _draft(lib, _ix(T=1, B=2), at) == INVALID  # sequences differ
+    assert _draft(lib, _ix(T=1, S=32), at) == INVALID  # caches differ
+    assert _draft(lib, ix, _at(T=4, H=32)) == UNSUPPORTED
+    assert _draft(lib, ix, at, idx=0) == INVALID
+    assert _draft(lib, ix, at, k=0) == UNSUPPORTED
+    assert _draft(lib, ix, at, out=FAKE + 2) == MISALIGNED
+
+
+def test_draft_workspace_size_covers_topk_and_attention(lib):
+    ix = _ix(B=32, T=1, S=200000, q_pos0=200000, dtype=dsa.DSA_E4M3, q_scale=FAKE, k_scale=FAKE)
+    at = _at(B=32, T=4, S=200000)
+    n = lib.indexshare_draft_workspace_size(ctypes.byref(ix), ctypes.byref(at), 2048)
+    assert n >= lib.dsa_workspace_size(ctypes.byref(ix), 2048)
+    # the 128 draft rows fill the GPU without a decode split; one step alone splits its 32 rows
+    assert n >= lib.dsa_attn_workspace_size(ctypes.byref(at), 2048)
+    assert lib.indexshare_draft_workspace_size(None, ctypes.byref(at), 2048) == 256

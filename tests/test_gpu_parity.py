@@ -580,3 +580,26 @@ def test_topk_from_scores_equal_long_rows(R, n, k):
     assert dsa.read_device_flags() == 0
     want = torch.arange(k, dtype=torch.int32, device=DEV).expand(1, R, k)
     assert torch.equal(idx, want)
+
+
+@pytest.mark.parametrize("base,B,S,k,n_steps", [
+    ("mtp_draft_b32_200k", 3, 5000, 256, 4),   # tcgen05 attention, FP8 indexer, ragged last block
+    ("mtp_draft_b32_200k", 2, 777, 2048, 3),   # k beyond the visible keys: -1 padding
+    ("tiny_l1k", 2, 1000, 64, 4),              # the 8-head shapes (mma.sync attention), bf16 indexer
+])
+def test_draft_forward_matches_oracle(base, B, S, k, n_steps):
+    """indexshare_draft_forward: the first draft step's indexer + top-k, then one attention
+    launch for every draft step over that one index row, against the oracle's draft walk
+    (integer indexer operands: index rows bit for bit; outputs within 2e-2, LSE within 1e-3)."""
+    wl = synth.WORKLOADS[base].replace(B=B, T=1, S=S, q_pos0=S, k=k, values="int", shared_cache=True)
+    layers = synth.group_inputs(wl, n_steps, DEV, with_indexer=True)
+    at = dict(layers[0]["at"])
+    at["q"] = torch.cat([l["at"]["q"] for l in layers], dim=1).contiguous()
+    out, lse, idx = dsa.indexshare_draft_forward(layers[0]["ix"], at, k)
+    torch.cuda.synchronize()
+    assert dsa.read_device_flags() == 0
+    ref_idx, ref_o, ref_l = oracle.draft_forward(layers[0]["ix"], at, k)
+    assert np.array_equal(idx.reshape(B, k).cpu().numpy(), ref_idx)
+    assert np.abs(out.float().cpu().numpy() - ref_o).max() <= 2e-2
+    gl, fin = lse.cpu().numpy(), np.isfinite(ref_l)
+    assert np.array_equal(np.isfinite(gl), fin) and np.abs(gl[fin] - ref_l[fin]).max() <= 1e-3

@@ -88,6 +88,39 @@ def test_workload_group_sampled_rows(name, n_rows):
     torch.cuda.empty_cache()
 
 
+def test_draft_steps_in_one_launch_at_full_size():
+    """indexshare_draft_forward at the 32 x 200,000 draft shape: the first step's indexer +
+    top-k, then one attention launch in which the four draft queries of each sequence attend
+    over its one index row.  Integer indexer operands make the selection exact, so sampled
+    sequences are compared with the oracle's draft walk directly (index rows bit for bit,
+    outputs within 2e-2, LSE within 1e-3); the selection equals dsa_topk on the first step and
+    every step equals its own attention call over it (within 1e-2, the decode split of a
+    single step sums in another order)."""
+    wl = synth.WORKLOADS["mtp_draft_b32_200k"].replace(values="int")
+    layers = synth.group_inputs(wl, 4, DEV, with_indexer=True)
+    at = dict(layers[0]["at"])
+    at["q"] = torch.cat([l["at"]["q"] for l in layers], dim=1).contiguous()
+    out, lse, idx = dsa.indexshare_draft_forward(layers[0]["ix"], at, wl.k)
+    torch.cuda.synchronize()
+    assert dsa.read_device_flags() == 0
+    idx_f = dsa.dsa_topk(wl.k, ix=layers[0]["ix"])
+    assert torch.equal(idx_f.reshape(wl.B, wl.k), idx.reshape(wl.B, wl.k))
+    for s in range(4):
+        o_s, l_s = dsa.dsa_sparse_attn(layers[s]["at"], idx_f)
+        assert (o_s[:, 0].float() - out[:, s].float()).abs().max().item() <= 1e-2
+        assert (l_s[:, 0] - lse[:, s]).abs().max().item() <= 1e-3
+    bsel = [0, 13, 31]
+    ix = _subset_batches(layers[0]["ix"], ["q", "w", "q_scale", "k", "k_scale"], bsel)
+    ats = _subset_batches(at, ["q", "k", "v"], bsel)
+    ref_idx, ref_o, ref_l = oracle.draft_forward(ix, ats, wl.k)
+    assert np.array_equal(idx.reshape(wl.B, wl.k)[bsel].cpu().numpy(), ref_idx)
+    assert np.abs(out[bsel].float().cpu().numpy() - ref_o).max() <= 2e-2
+    gl, fin = lse[bsel].cpu().numpy(), np.isfinite(ref_l)
+    assert np.array_equal(np.isfinite(gl), fin) and np.abs(gl[fin] - ref_l[fin]).max() <= 1e-3
+    del layers, at, out, lse, idx, idx_f
+    torch.cuda.empty_cache()
+
+
 def test_heatmap_all_full_pass_and_overlap_matrix_sampled_rows():
     """The launch configuration of bench.py --heatmap: 16 layers of the 128K clustered
     workload, each with its own indexer + top-k, then the all-pairs overlap matrix.  Per layer

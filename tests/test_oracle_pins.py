@@ -312,6 +312,26 @@ def test_group_all_full_equals_independent_layers_and_fsss_with_equal_indexers()
     assert mean == 1.0
 
 
+def test_draft_steps_equal_an_fsss_walk_over_the_steps():
+    """Draft-step reuse restated as an IndexShare schedule: the n draft steps are n layers of
+    one query each, the first F (its indexer) and the rest S, all on the one shared cache; the
+    stacked-query form must give the same positions and, step by step, the same outputs."""
+    wl = synth.WORKLOADS["mtp_draft_b32_200k"].replace(B=3, S=300, q_pos0=300, k=24)
+    layers = synth.group_inputs(wl, 4, with_indexer=True)
+    walk = oracle.group_forward(layers, "FSSS", wl.k)
+    at = dict(layers[0]["at"])
+    at["q"] = torch.cat([l["at"]["q"] for l in layers], dim=1)  # [B, 4, H, DQK]
+    idx, out, lse = oracle.draft_forward(layers[0]["ix"], at, wl.k)
+    assert np.array_equal(idx, walk[0]["idx"])
+    for s in range(4):
+        assert np.array_equal(out[:, s], walk[s]["out"]) and np.array_equal(lse[:, s], walk[s]["lse"])
+    # a subset of sequences gives those sequences' rows
+    idx2, out2, _ = oracle.draft_forward(layers[0]["ix"], at, wl.k, seqs=[2, 0])
+    assert np.array_equal(idx2, idx[[2, 0]]) and np.array_equal(out2, out[[2, 0]])
+    # the steps keep their own queries: their outputs differ
+    assert not np.allclose(out[:, 0], out[:, 1])
+
+
 @pytest.mark.parametrize("bad", ["SFSS", "FSS", "FSSSF", "FSXS", ""])
 def test_group_rejects_bad_schedules(bad):
     with pytest.raises(ValueError):
