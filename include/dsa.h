@@ -344,8 +344,10 @@ void dsa_set_wait_limit(uint64_t cycles);
  * code that must not grow its footprint after start-up).  Results are identical to
  * dsa_topk with a DSA_TOPK_FROM_INDEXER source.
  *   ix, k, idx  as for dsa_topk; idx [B,T,k] int32 is the caller's output buffer.
- *   flags       device uint32 the kernels OR DSA_FLAG_* bits into, or NULL to use a word
- *               inside the library's array (cleared at the start of every call).
+ *   flags       device uint32 the kernels OR DSA_FLAG_* bits into, or NULL: the bits that
+ *               call raises (a wait that ran out, NaN scores) then go to a word inside the
+ *               library's array that nothing reads back and the next call clears, so they
+ *               are lost -- pass a word to observe them.
  * Scratch: a file-scope device array of 64 MiB, held by every GPU that loads the library
  * until the process exits.  B*S*4 must not exceed 64 MiB - 256 B (DSA_ERR_UNSUPPORTED
  * otherwise); no cudaMalloc/cudaFree or allocating library routine is called.  The first

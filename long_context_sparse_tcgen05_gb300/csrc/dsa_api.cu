@@ -294,6 +294,10 @@ namespace dsa {
 dsa_status validate_indexer(const dsa_indexer_args* ix) { return check_indexer(ix); }
 dsa_status record_error(dsa_status s, const char* msg) { return fail(s, "%s", msg); }
 IndexerLaunch make_indexer_launch(const dsa_indexer_args* ix, int64_t t0, int Tc) { return indexer_launch(ix, t0, Tc); }
+void plan_topk_split(TopkLaunch& P, int64_t rows, int64_t n_max, void* ws, size_t off, size_t ws_bytes) {
+  plan_topk_parts(P, rows, n_max, ws, off, ws_bytes);
+}
+int64_t max_visible_keys(int64_t q_pos0, int T, int diag, int S) { return max_visible(q_pos0, T, diag, S); }
 }  // namespace dsa
 
 extern "C" {

@@ -113,6 +113,10 @@ struct TopkLaunch {
   uint32_t* part_key;
   int32_t* part_cnt;
 };
+// Few long rows: split each row of a top-k launch across CTAs when ws + off .. ws + ws_bytes
+// holds the segments' lists (P.parts stays 1 otherwise); n_max: the longest row's keys.
+void plan_topk_split(TopkLaunch& P, int64_t rows, int64_t n_max, void* ws, size_t off, size_t ws_bytes);
+int64_t max_visible_keys(int64_t q_pos0, int T, int diag, int S);  // of the call's last row
 cudaError_t launch_topk_rows(const TopkLaunch& p, cudaStream_t st);
 constexpr int kMaxTopkParts = 16;
 

@@ -79,6 +79,12 @@ extern "C" dsa_status dsa_topk_indexer_noalloc(const dsa_indexer_args* ix, int32
     P.scores = sc; P.ld = ix->S; P.bstride = (int64_t)Tc * ix->S;
     P.B = ix->B; P.T = ix->T; P.S = ix->S; P.t0 = (int)t0; P.Tc = Tc;
     P.q_pos0 = ix->q_pos0; P.diag = ix->diag; P.k = k; P.idx = idx; P.flags = flag_word;
+    // few long rows (decode): split each over CTAs when the array's tail, after this chunk's
+    // scores, holds the segments' lists (B = 32 rows of 200,000 keys: 25.6 MB of scores and
+    // 8.4 MB of lists)
+    const size_t lists_off = (kFlagBytes + (size_t)Tc * row_bytes + 255) & ~(size_t)255;
+    dsa::plan_topk_split(P, (int64_t)ix->B * Tc, dsa::max_visible_keys(ix->q_pos0, ix->T, ix->diag, ix->S), base,
+                         lists_off, kStaticScratchBytes);
     e = dsa::launch_topk_rows(P, st);
     if (e != cudaSuccess) return dsa::record_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   }

@@ -69,6 +69,23 @@ def test_noalloc_matches_workspace_entry_point_twice(lib, name, over, k):
     assert torch.equal(second, ref)
 
 
+def test_noalloc_splits_few_long_rows_like_the_workspace_path(lib):
+    """Decode shape (32 sequences x one query over 200,000 keys): the fixed array holds the
+    25.6 MB of scores and, after them, the segment lists of rows split over several CTAs, so
+    the call launches the indexer, the split top-k and its merge -- and equals dsa_topk."""
+    wl = synth.WORKLOADS["decode_b32_200k"].replace(values="gauss")
+    ix = synth.indexer_inputs(wl, 0, DEV)
+    ref = dsa.dsa_topk(wl.k, ix=ix)
+    torch.cuda.synchronize()
+    n0 = dsa.launch_count()
+    got = _noalloc(lib, ix, wl.k)
+    torch.cuda.synchronize()
+    assert dsa.launch_count() - n0 == 3  # indexer, top-k segments, merge
+    assert torch.equal(got, ref)
+    del ix
+    torch.cuda.empty_cache()
+
+
 def test_noalloc_reports_flags_into_caller_word(lib):
     wl = synth.WORKLOADS["tiny_l1k"].replace(T=200, S=200)
     ix = synth.indexer_inputs(wl, 0, DEV)
