@@ -196,9 +196,10 @@ int cand_cap(int k) {
   int c = 4 * k < 2048 ? 2048 : 4 * k;
   return (c + 127) / 128 * 128;
 }
-// the largest number of candidates a row's threshold aims at: 60% of the room, so that a
-// segment (a quarter of the room, a quarter of the keys) rarely overflows
-int cand_target(int k) { return cand_cap(k) * 3 / 5; }
+// the largest number of candidates a row's threshold aims at: half the room, so that a
+// segment (a quarter of the room, a quarter of the keys) rarely overflows (at 60%, 5 of 4,096
+// rows of a 1M-key chunk overflowed a segment, each then recomputed over its million keys)
+int cand_target(int k) { return cand_cap(k) / 2; }
 size_t cand_area(int64_t rows, int cap) {  // key + position lists, four counts, fail flags
   const size_t b = (size_t)rows * ((size_t)cap * 8 + 16 + 1);
   return (b + 255) & ~(size_t)255;
@@ -225,7 +226,14 @@ dsa_status run_materialised(const dsa_indexer_args* ix, int32_t k, int32_t* idx,
     dsa::IndexerLaunch L = indexer_launch(ix, t0, Tc);
     L.out = sc; L.ld = ix->S; L.out_bstride = (int64_t)Tc * ix->S; L.write_masked = 0;
     L.flags = ws_flags(ws);
-    if (gate) { L.gate = gate + (t0 - t_begin); L.gate_bstride = gate_bstride; }
+    // a recomputing pass runs only the few flagged token blocks: with long rows, split their
+    // key ranges over at least 4,096 CTAs (the others leave at once) -- a flagged 1M-key row
+    // took 1.6 ms on three CTAs, 0.33 this way
+    if (gate) {
+      L.gate = gate + (t0 - t_begin);
+      L.gate_bstride = gate_bstride;
+      if (ix->S >= (1 << 18)) L.ctas_min = 4096;
+    }
     cudaError_t e = dsa::launch_indexer_scores(L, st);
     if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
     dsa::TopkLaunch P{};

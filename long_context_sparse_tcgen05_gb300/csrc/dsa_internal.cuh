@@ -71,6 +71,7 @@ struct IndexerLaunch {
   int write_masked;     // 1: write -inf over [n_t, S) as well
   uint32_t* flags;      // device flag word (DSA_FLAG_TIMEOUT)
   int ksplit;           // key-range splits per token block (0: chosen by the launcher)
+  int ctas_min;         // launcher's split: at least this many CTAs (0: four waves)
   long long wait;       // wait bound in cycles (0: wait_limit() at launch)
   // selecting mode (select != 0; H_I = 64, one CTA per token block): instead of writing scores,
   // row r = b*Tc + (t - t0) keeps every key whose score reaches a threshold set from a sample of

@@ -698,13 +698,14 @@ cudaError_t launch_cfg(const IndexerLaunch& p, cudaStream_t st) {
   if (SEL) q.ksplit = 1;  // a row's candidates come from one CTA
   if (q.ksplit <= 0) {
     // split the key range when the token blocks alone would not give about four waves of
-    // CTAs, keeping at least 16 key tiles per split
+    // CTAs (or ctas_min), keeping at least 16 key tiles per split
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long ctas = (long long)nblk * p.B;
     const int tiles_all = (p.S + kM - 1) / kM;
-    long long want = ctas >= 4LL * sms ? 1 : (4LL * sms + ctas - 1) / ctas;
+    const long long goal = p.ctas_min > 4LL * sms ? (long long)p.ctas_min : 4LL * sms;
+    long long want = ctas >= goal ? 1 : (goal + ctas - 1) / ctas;
     const long long most = tiles_all / 16 > 0 ? tiles_all / 16 : 1;
     q.ksplit = (int)(want < most ? want : most);
   }

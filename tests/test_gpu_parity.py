@@ -569,6 +569,34 @@ def test_selecting_path_recomputes_rows_whose_candidates_overflow():
     assert np.array_equal(sel.reshape(-1, 2048)[rows].cpu().numpy(), oracle.indexer_topk(ix, 2048, rows))
 
 
+def test_selecting_path_recomputes_long_rows_split_over_key_ranges():
+    """Rows of 300,000 keys whose candidates overflow are recomputed with their key range split
+    over several CTAs.  The key codes are zero except at 120 positions spread over the whole
+    row, so every other score is 0: each row's threshold admits all its keys, every row is
+    recomputed, and its top-k holds the spread positions (scores > 0) from every key range plus
+    the lowest positions scoring 0.  It must equal the stored-scores path bit for bit and the
+    oracle on sampled rows."""
+    S, T = 300000, 4096
+    wl = _wl(64, 128, "e4m3", "gauss", T, S=S, k=2048, q_pos0=S - T)
+    ix = synth.indexer_inputs(wl, 0, DEV)
+    special = torch.linspace(3, S - T - 7, 120).long().to(DEV)
+    kc = ix["k"].view(torch.uint8)
+    keep = kc[:, special].clone()
+    kc.zero_()
+    kc[:, special] = keep
+    sel = dsa.dsa_topk(2048, ix=ix)
+    # the stored-scores path: a workspace too small for the candidate lists
+    small = torch.zeros(256 + (200 << 20), dtype=torch.uint8, device=DEV)
+    ref = dsa.dsa_topk(2048, ix=ix, ws=small)
+    torch.cuda.synchronize()
+    assert dsa.read_device_flags() == 0
+    assert torch.equal(sel, ref)
+    rows = [0, 2047, 4095]
+    got = sel.reshape(-1, 2048)[rows].cpu().numpy()
+    assert np.array_equal(got, oracle.indexer_topk(ix, 2048, rows))
+    assert np.isin(special.cpu().numpy(), got[0]).sum() >= 60  # spread positions were selected
+
+
 @pytest.mark.parametrize("R,n,k", [(40, 30000, 2048), (4, 200000, 2048), (160, 9000, 3000), (24, 131072, 1)])
 def test_topk_from_scores_equal_long_rows(R, n, k):
     """Rows of one repeated score: the sampled threshold admits every key, a single streamed
