@@ -548,9 +548,15 @@ struct MergeSmem {
 };
 
 // One split row: the exact top-k of its segments' lists, concatenated in segment order (so in
-// position order).
+// position order).  kSmemKeys: the row's keys are first gathered densely into shared memory
+// (at most kMergeSmemKeys), the radix passes start at the first bit where the smallest and
+// largest key differ, and only entries at or above the k-th key fetch their position; otherwise
+// every pass reads the lists in global memory.
+constexpr int kMergeSmemKeys = 40960;  // 160 KB
+template <bool kSmemKeys>
 __global__ void __launch_bounds__(kThreads) k_topk_merge(TopkLaunch p) {
   __shared__ MergeSmem sm;
+  extern __shared__ uint32_t mkeys[];
   const int row = blockIdx.x, parts = p.parts, k = p.k;
   if (threadIdx.x == 0) {
     int acc = 0;
@@ -578,13 +584,59 @@ __global__ void __launch_bounds__(kThreads) k_topk_merge(TopkLaunch p) {
     return;
   }
   uint32_t ties;
-  const uint32_t tau =
-      radix_select(sm, n, (uint32_t)k, [&](int64_t i) { return p.part_key[locate(i)]; }, &ties, 0u, 32, 0);
-  ordered_output(sm, n, tau, ties, k, out, [&](int64_t i, uint32_t& key, int32_t& ps) {
-    const int64_t o = locate(i);
-    key = p.part_key[o];
-    ps = p.part_pos[o];
-  });
+  if constexpr (kSmemKeys) {
+    uint32_t lo = 0xffffffffu, hi = 0u;
+    for (int s = 0; s < parts; ++s) {
+      const int c = sm.pre[s + 1] - sm.pre[s];
+      const uint32_t* src = p.part_key + base + (int64_t)s * k;
+      for (int j = threadIdx.x; j < c; j += kThreads) {
+        const uint32_t kk = __ldg(src + j);
+        mkeys[sm.pre[s] + j] = kk;
+        lo = kk < lo ? kk : lo;
+        hi = kk > hi ? kk : hi;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if ((threadIdx.x & 31) == 0) sm.warp_sums[threadIdx.x >> 5] = lo;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t m = 0xffffffffu;
+      for (int w = 0; w < kWarps; ++w) m = sm.warp_sums[w] < m ? sm.warp_sums[w] : m;
+      sm.sel_bin = m;
+    }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) sm.warp_sums[threadIdx.x >> 5] = hi;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t m = 0u;
+      for (int w = 0; w < kWarps; ++w) m = sm.warp_sums[w] > m ? sm.warp_sums[w] : m;
+      sm.sel_above = m;
+    }
+    __syncthreads();
+    // every key shares the bits of the smallest and largest above their highest differing bit
+    const uint32_t kmin = sm.sel_bin, kmax = sm.sel_above, d = kmin ^ kmax;
+    const int top = d ? 32 - __clz(d) : 0;
+    const uint32_t prefix = top >= 32 ? 0u : (kmax & ~((1u << top) - 1u));
+    __syncthreads();
+    const uint32_t tau =
+        radix_select(sm, n, (uint32_t)k, [&](int64_t i) { return mkeys[i]; }, &ties, prefix, top, 0);
+    ordered_output(sm, n, tau, ties, k, out, [&](int64_t i, uint32_t& key, int32_t& ps) {
+      key = mkeys[i];
+      ps = key >= tau ? p.part_pos[locate(i)] : 0;  // only taken entries need their position
+    });
+  } else {
+    const uint32_t tau =
+        radix_select(sm, n, (uint32_t)k, [&](int64_t i) { return p.part_key[locate(i)]; }, &ties, 0u, 32, 0);
+    ordered_output(sm, n, tau, ties, k, out, [&](int64_t i, uint32_t& key, int32_t& ps) {
+      const int64_t o = locate(i);
+      key = p.part_key[o];
+      ps = p.part_pos[o];
+    });
+  }
 }
 
 constexpr int kBitmapKeys = 262144;  // rows this long or shorter are ordered through a bitmap
@@ -837,7 +889,14 @@ cudaError_t launch_topk_rows(const TopkLaunch& p, cudaStream_t st) {
   count_launches(1);
   if (e != cudaSuccess || p.parts <= 1) return e;
   TraceScope trace(kTraceTopk, st);
-  k_topk_merge<<<rows, kThreads, 0, st>>>(p);
+  if ((int64_t)p.parts * p.k <= kMergeSmemKeys) {
+    const int smem = (int)((size_t)p.parts * p.k * sizeof(uint32_t));
+    if ((e = cudaFuncSetAttribute(k_topk_merge<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+      return e;
+    k_topk_merge<true><<<rows, kThreads, smem, st>>>(p);
+  } else {
+    k_topk_merge<false><<<rows, kThreads, 0, st>>>(p);
+  }
   count_launches(1);
   return cudaGetLastError();
 }
