@@ -135,7 +135,7 @@ dsa::AttnLaunch attn_launch(const dsa_attn_args* at, const int32_t* idx, int32_t
 size_t attn_split_bytes(const dsa::AttnLaunch& L) {
   const int splits = dsa::attn_splits(L);
   if (splits <= 1) return 0;
-  return (size_t)L.B * L.T * splits * (size_t)L.H * ((size_t)L.DV + 1) * 4;
+  return (size_t)L.B * L.T * (L.layers > 1 ? L.layers : 1) * splits * (size_t)L.H * ((size_t)L.DV + 1) * 4;
 }
 
 constexpr int kMaxK = 4096;
@@ -398,7 +398,7 @@ dsa_status run_attn(dsa::AttnLaunch L, void* ws, size_t ws_bytes, void* stream) 
   L.flags = ws_flags(ws);
   const int splits = dsa::attn_splits(L);
   if (splits > 1) {
-    const size_t parts = (size_t)L.B * L.T * splits;
+    const size_t parts = (size_t)L.B * L.T * (L.layers > 1 ? L.layers : 1) * splits;
     const size_t need = attn_split_bytes(L);
     if (ws_bytes > dsa::kWsScratch && ws_bytes - dsa::kWsScratch >= need) {
       uint8_t* w = static_cast<uint8_t*>(ws) + dsa::kWsScratch;
@@ -493,6 +493,40 @@ dsa_status group_check(const dsa_layer* layers, int32_t n_layers, const char* sc
   return check_ws(ws, ws_bytes, DSA_WS_MIN);
 }
 
+// Layers a .. end-1 of a run of layers that read one index buffer (a full layer and the shared
+// layers after it), attended in one launch: consecutive layers of the tcgen05 shape with equal
+// scale and strides, when a single layer has too few query rows to fill the GPU (decode: a
+// layer's 32 rows would be split over CTAs and merged; four layers' 128 rows fill it without
+// splitting), at most kMaxAttnLayers.  Layer a alone otherwise.
+int attn_batch_end(const dsa_layer* ls, int a, int run_end, int32_t k) {
+  const dsa::AttnLaunch A = attn_launch(&ls[a].at, nullptr, k, nullptr, nullptr);
+  if (!dsa::sparse_mla_tc_supported(A) || dsa::attn_splits(A) <= 1) return a + 1;
+  int c = a + 1;
+  while (c < run_end && c - a < dsa::kMaxAttnLayers) {
+    const dsa::AttnLaunch C = attn_launch(&ls[c].at, nullptr, k, nullptr, nullptr);
+    if (!dsa::sparse_mla_tc_supported(C) || C.scale != A.scale || C.q_st != A.q_st || C.q_sb != A.q_sb ||
+        C.k_sb != A.k_sb || C.v_sb != A.v_sb || C.k_ld != A.k_ld)
+      break;
+    ++c;
+  }
+  return c;
+}
+
+// The attention launch of layers a .. c-1 over idx.
+dsa::AttnLaunch batch_launch(const dsa_layer* ls, int a, int c, const int32_t* idx, int32_t k) {
+  dsa::AttnLaunch L = attn_launch(&ls[a].at, idx, k, ls[a].out, ls[a].lse);
+  if (c - a > 1) {
+    L.layers = c - a;
+    for (int l = 0; l < L.layers; ++l) {
+      L.lq[l] = ls[a + l].at.q;
+      L.lk[l] = ls[a + l].at.k;
+      L.lout[l] = ls[a + l].out;
+      L.llse[l] = ls[a + l].lse;
+    }
+  }
+  return L;
+}
+
 // The schedule walk of a checked group.
 dsa_status group_run(const dsa_layer* layers, int32_t n_layers, const char* schedule, int32_t k,
                      int32_t* const* idx_bufs, void* ws, size_t ws_bytes, void* stream) {
@@ -500,15 +534,22 @@ dsa_status group_run(const dsa_layer* layers, int32_t n_layers, const char* sche
   cudaStream_t st = as_stream(stream);
   const int32_t* cur = nullptr;
   int f = 0;
-  for (int i = 0; i < n_layers; ++i) {
-    const dsa_layer& L = layers[i];
+  for (int i = 0; i < n_layers;) {
     if (schedule[i] == 'F') {
       // Full layer: indexer + top-k, positions kept in this F layer's buffer.
-      if ((s = run_indexer_topk(&L.ix, k, idx_bufs[f], ws, ws_bytes, st)) != DSA_OK) return s;
+      if ((s = run_indexer_topk(&layers[i].ix, k, idx_bufs[f], ws, ws_bytes, st)) != DSA_OK) return s;
       cur = idx_bufs[f++];
     }
-    // Every layer (full or shared) attends with its own operands over `cur`.
-    if ((s = dsa_sparse_attn(&L.at, cur, k, L.out, L.lse, ws, ws_bytes, stream)) != DSA_OK) return s;
+    // Every layer (full or shared) up to the next full one attends with its own operands over
+    // `cur`, several layers per launch where that fills the GPU better.
+    int run_end = i + 1;
+    while (run_end < n_layers && schedule[run_end] != 'F') ++run_end;
+    for (int a = i; a < run_end;) {
+      const int c = attn_batch_end(layers, a, run_end, k);
+      if ((s = run_attn(batch_launch(layers, a, c, cur, k), ws, ws_bytes, stream)) != DSA_OK) return s;
+      a = c;
+    }
+    i = run_end;
   }
   return DSA_OK;
 }
@@ -612,6 +653,17 @@ size_t indexshare_group_workspace_size(const dsa_layer* layers, int32_t n_layers
     for (int i = 0; i < n_layers; ++i) {
       if (schedule[i] == 'F') best = std::max(best, dsa_workspace_size(&ls[i].ix, k));
       best = std::max(best, dsa_attn_workspace_size(&ls[i].at, k));
+    }
+    if (k < 1 || k > kMaxK) return;
+    for (int i = 0; i < n_layers;) {  // the split parts of the launches group_run makes
+      int run_end = i + 1;
+      while (run_end < n_layers && schedule[run_end] != 'F') ++run_end;
+      for (int a = i; a < run_end;) {
+        const int c = attn_batch_end(ls, a, run_end, k);
+        best = std::max(best, dsa::kWsScratch + attn_split_bytes(batch_launch(ls, a, c, nullptr, k)));
+        a = c;
+      }
+      i = run_end;
     }
   };
   if (!seqs) {

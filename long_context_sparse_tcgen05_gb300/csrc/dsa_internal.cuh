@@ -142,6 +142,7 @@ cudaError_t launch_topk_cand(const CandLaunch& p, cudaStream_t st);
 // Segments per row for `rows` rows of up to `n` visible scores (1: no split).
 int topk_parts(int64_t rows, int64_t n);
 
+constexpr int kMaxAttnLayers = 8;
 struct AttnLaunch {
   int B, T, S, H, DQK, DV;
   float scale;
@@ -168,6 +169,14 @@ struct AttnLaunch {
   int splits;
   float* part_o;
   float* part_lse;
+  // several layers of one group in one launch (0 or 1: the one layer above): layer l has its
+  // own queries, latent KV, output and LSE (same shapes and strides) and reads the same index
+  // rows; work items run over layers x rows x parts, part_o / part_lse by that flat item
+  int layers;
+  const void* lq[kMaxAttnLayers];
+  const void* lk[kMaxAttnLayers];
+  void* lout[kMaxAttnLayers];
+  float* llse[kMaxAttnLayers];
 };
 // The index row of flat query row `row` = b*T + t.
 __host__ __device__ inline const int32_t* attn_idx_row(const AttnLaunch& p, int row) {

@@ -302,6 +302,7 @@ cudaError_t launch_cfg(const AttnLaunch& p, cudaStream_t st) {
 cudaError_t launch_sparse_attn(const AttnLaunch& p, cudaStream_t st) {
   if (p.B * p.T <= 0) return cudaSuccess;
   if (sparse_mla_tc_supported(p)) return launch_sparse_mla_tc(p, st);
+  if (p.layers > 1) return cudaErrorInvalidValue;  // several layers per launch: the tcgen05 kernel only
   const bool latent = p.v == p.k && p.v_ld == p.k_ld && p.v_sb == p.k_sb;
   if (p.H == 64 && p.DQK == 576 && p.DV == 512)
     return latent ? launch_cfg<64, 576, 512, false>(p, st) : launch_cfg<64, 576, 512, true>(p, st);

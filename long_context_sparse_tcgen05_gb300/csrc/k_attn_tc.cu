@@ -154,9 +154,14 @@ __device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t lbo) 
   return d;
 }
 
+// One query tensor map per layer of the launch.
+struct QMaps {
+  CUtensorMap m[kMaxAttnLayers];
+};
+
 template <bool kPoll>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, AttnLaunch p) {
+    k_sparse_mla_tc(const __grid_constant__ QMaps qm, AttnLaunch p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = base;
@@ -166,8 +171,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &sm->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rows = p.B * p.T;
-  const int splits = p.splits > 1 ? p.splits : 1;  // work item = (row, part of its blocks)
+  const int rows1 = p.B * p.T;                     // query rows of one layer
+  const int rows = rows1 * (p.layers > 1 ? p.layers : 1);
+  const int splits = p.splits > 1 ? p.splits : 1;  // work item = (layer x row, part of its blocks)
   const int items = rows * splits;
 
   if (threadIdx.x == 0) {
@@ -206,7 +212,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // each atom every copying thread arms an asynchronous arrive on that atom's kv_full
     // barrier, which fires once its own copies have landed, so the producer never waits for
     // its copies and all stages stay in flight.
-    const uint8_t* kvg = static_cast<const uint8_t*>(p.k);
     const int64_t row_bytes = p.k_ld * 2;
     const bool leader = warp == 0 && lane == 0;
     int it = 0, qc = 0;
@@ -214,10 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     const bool vec = ((p.kk | p.idx_st | p.idx_sb) & 3) == 0 && (reinterpret_cast<uintptr_t>(p.idx) & 15u) == 0;
     for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
-      const int row = item / splits;
+      const int lrow = item / splits, layer = lrow / rows1, row = lrow % rows1;  // row within its layer
       const int32_t* irow = attn_idx_row(p, row);
       const int b = row / p.T;
-      const uint8_t* kvb = kvg + (int64_t)b * p.k_sb * 2;  // this sequence's latent rows
+      const uint8_t* kvb = static_cast<const uint8_t*>(p.lk[layer]) + (int64_t)b * p.k_sb * 2;  // its latent rows
       // blocks = 1 + (last entry other than -1) / kNB; all loads of the scan issued together
       int last = -1;
       if (vec) {
@@ -259,17 +264,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok || *abort_flag) break;
       if (nb == 0) continue;
       if (warp == 0) {
-        const int next_row = (item + (int)gridDim.x) / splits;
-        if (lane == 0 && next_row < rows && next_row != row)
-          prefetch_l2(static_cast<const __nv_bfloat16*>(p.q) + (int64_t)(next_row / p.T) * p.q_sb +
-                          (int64_t)(next_row % p.T) * p.q_st,
+        const int next = (item + (int)gridDim.x) / splits;
+        if (lane == 0 && next < rows && next != lrow) {
+          const int nr = next % rows1;
+          prefetch_l2(static_cast<const __nv_bfloat16*>(p.lq[next / rows1]) + (int64_t)(nr / p.T) * p.q_sb +
+                          (int64_t)(nr % p.T) * p.q_st,
                       kQBytes);
+        }
         if (lane == 0) {
           ok = mbar_wait<kPoll>(&bar.q_empty, (qc & 1) ^ 1, abort_flag, p.wait);
           if (ok) {
             mbar_arrive_expect_tx(&bar.q_full, kQBytes);
             for (int a = 0; a < kAtoms; ++a)
-              tma_load_4d(q_s + a * kAtomQ, &tm_q, &bar.q_full, a * 64, 0, row % p.T, row / p.T);
+              tma_load_4d(q_s + a * kAtomQ, &qm.m[layer], &bar.q_full, a * 64, 0, row % p.T, row / p.T);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -433,10 +440,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= softmax + epilogue (warps 6..13) =================
     const int q4 = warp & 3;                    // TMEM lane quarter
     const int sw = warp - kSmWarp0;             // softmax warp index 0..7
-    const int kh = sw >> 2;                     // key half: columns 32 * kh .. + 31 of each block
+    const int kh = sw >> 2;                     // key half: columns kHalf * kh .. + kHalf - 1 of each block
     // The M = 64 score rows sit in lanes 0..15 of each lane quarter; the 16x256b TMEM shape
     // spreads them over all 32 threads: thread t holds heads hd[0] = 16 q4 + t/4 and hd[1] =
-    // hd[0] + 8, each at the 4 keys 8j + 2m + {0, 1} (m = t % 4, j < 2) of the warp's 16-key
+    // hd[0] + 8, each at the keys 8j + 2m + {0, 1} (m = t % 4, j < kHalf / 8) of the warp's key
     // half; a head's four threads (one quad) combine their maxima and sums with two shuffles.
     const int m = lane & 3;
     const int hd[2] = {q4 * 16 + (lane >> 2), q4 * 16 + (lane >> 2) + 8};
@@ -448,7 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long g = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
-      const int row = item / splits;
+      const int lrow = item / splits, layer = lrow / rows1, row = lrow % rows1;
+      float* const lse_out = p.llse[layer];
       // every wait of these eight warps is followed by a barrier that ORs "it ran out" over
       // them, so they leave together
       const bool got_info = mbar_wait<kPoll>(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag, p.wait);
@@ -458,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int nb = sm->nb[it & 1], j0 = sm->j0[it & 1];
       if (t == 0) mbar_arrive(&bar.info_empty[it & 1]);
-      __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * kH * kDV;
+      __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.lout[layer]) + (int64_t)row * kH * kDV;
       float* po = splits > 1 ? p.part_o + (int64_t)item * kH * kDV : nullptr;  // this part's output
       const int32_t* irow = attn_idx_row(p, row);
       if (nb == 0) {  // nothing visible: O = 0, LSE = -inf
@@ -467,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t < kH) p.part_lse[(int64_t)item * kH + t] = -INFINITY;
         } else {
           for (int i = t; i < kH * kDV / 8; i += kSmThreads) reinterpret_cast<uint4*>(og)[i] = make_uint4(0, 0, 0, 0);
-          if (p.lse && t < kH) p.lse[(int64_t)row * kH + t] = -INFINITY;
+          if (lse_out && t < kH) lse_out[(int64_t)row * kH + t] = -INFINITY;
         }
         continue;
       }
@@ -605,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           sm->lsum[hh] = lt > 0.f ? 1.f / lt : 0.f;  // reciprocal row sums
           const float lse_v = lt > 0.f ? (m_used[hs] + log2f(lt)) * kLn2 : -INFINITY;
           if (po) p.part_lse[(int64_t)item * kH + hh] = lse_v;
-          else if (p.lse) p.lse[(int64_t)row * kH + hh] = lse_v;
+          else if (lse_out) lse_out[(int64_t)row * kH + hh] = lse_v;
         }
       }
       const bool got_o = mbar_wait<kPoll>(&bar.o_full, oc & 1, abort_flag, p.wait);
@@ -659,8 +667,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kCombHeads = 4;
 __global__ void __launch_bounds__(128) k_attn_combine(AttnLaunch p) {
   __shared__ float wgt[kMaxAttnSplits][kCombHeads];
-  const int row = blockIdx.x, h0 = blockIdx.y * kCombHeads, S = p.splits;
-  const float* pl = p.part_lse + (int64_t)row * S * kH;
+  // blockIdx.x: flat (layer, row); parts of flat row r are items r*S .. r*S + S - 1
+  const int lrow = blockIdx.x, h0 = blockIdx.y * kCombHeads, S = p.splits;
+  const int rows1 = p.B * p.T, layer = lrow / rows1, row = lrow % rows1;
+  float* const lse_out = p.llse[layer];
+  const float* pl = p.part_lse + (int64_t)lrow * S * kH;
   if (threadIdx.x < kCombHeads) {
     const int h = h0 + threadIdx.x;
     float mx = -INFINITY;
@@ -672,12 +683,12 @@ __global__ void __launch_bounds__(128) k_attn_combine(AttnLaunch p) {
       sum += w;
     }
     for (int s = 0; s < S; ++s) wgt[s][threadIdx.x] = sum > 0.f ? wgt[s][threadIdx.x] / sum : 0.f;
-    if (p.lse) p.lse[(int64_t)row * kH + h] = sum > 0.f ? mx + logf(sum) : -INFINITY;
+    if (lse_out) lse_out[(int64_t)row * kH + h] = sum > 0.f ? mx + logf(sum) : -INFINITY;
   }
   __syncthreads();
   const int64_t first = (int64_t)h0 * kDV / 4;  // this CTA's first float4 within a part
-  const float4* po = reinterpret_cast<const float4*>(p.part_o + (int64_t)row * S * kH * kDV) + first;
-  __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * kH * kDV;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + (int64_t)lrow * S * kH * kDV) + first;
+  __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.lout[layer]) + (int64_t)row * kH * kDV;
   for (int i = threadIdx.x; i < kCombHeads * kDV / 4; i += 128) {
     const int hl = (i * 4) / kDV;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -734,41 +745,51 @@ bool sparse_mla_tc_supported(const AttnLaunch& p) {
 
 cudaError_t launch_sparse_mla_tc(const AttnLaunch& p, cudaStream_t st) {
   if (p.splits > kMaxAttnSplits || (p.splits > 1 && !(p.part_o && p.part_lse))) return cudaErrorInvalidValue;
+  if (p.layers > kMaxAttnLayers) return cudaErrorInvalidValue;
   TraceScope trace(kTraceAttention, st);
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  CUtensorMap tq;
-  {
+  // a single-layer call describes its layer in q / k / out / lse
+  AttnLaunch q = p;
+  if (q.layers <= 1) {
+    q.layers = 1;
+    q.lq[0] = p.q;
+    q.lk[0] = p.k;
+    q.lout[0] = p.out;
+    q.llse[0] = p.lse;
+  }
+  QMaps qm;
+  for (int l = 0; l < q.layers; ++l) {
     // queries [B][T][H][576] with token strides q_st / q_sb; a box is one swizzle atom (64
     // columns) of one query's 64 heads
     cuuint64_t dims[4] = {(cuuint64_t)kDQK, (cuuint64_t)kH, (cuuint64_t)p.T, (cuuint64_t)p.B};
     cuuint64_t strides[3] = {(cuuint64_t)kDQK * 2, (cuuint64_t)p.q_st * 2, (cuuint64_t)p.q_sb * 2};
     cuuint32_t box[4] = {64, (cuuint32_t)kH, 1, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
-    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(p.q), dims, strides, box, es,
+    if (enc(&qm.m[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q.lq[l]), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  AttnLaunch q = p;
   if (q.wait <= 0) q.wait = wait_limit();
   auto kern = q.wait < kDefaultWaitCycles ? k_sparse_mla_tc<true> : k_sparse_mla_tc<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (e != cudaSuccess) return e;
-  const int rows = p.B * p.T;
+  const int rows = p.B * p.T * q.layers;
   const int items = rows * (p.splits > 1 ? p.splits : 1);
   const int grid = items < num_sms() ? items : num_sms();
-  kern<<<grid, kThreads, kSmem, st>>>(tq, q);
+  kern<<<grid, kThreads, kSmem, st>>>(qm, q);
   count_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess || p.splits <= 1) return e;
-  k_attn_combine<<<dim3((unsigned)rows, kH / kCombHeads), 128, 0, st>>>(p);
+  k_attn_combine<<<dim3((unsigned)rows, kH / kCombHeads), 128, 0, st>>>(q);
   count_launches(1);
   return cudaGetLastError();
 }
 
+
 int attn_splits(const AttnLaunch& p) {
   if (!sparse_mla_tc_supported(p)) return 1;
-  const int rows = p.B * p.T, sms = num_sms();
+  const int rows = p.B * p.T * (p.layers > 1 ? p.layers : 1), sms = num_sms();
   if (rows <= 0 || rows * 2 > sms) return 1;
   int s = sms / rows;                                       // about one CTA per SM
   const int by_len = (p.kk + 255) / 256;                    // parts of at least 256 keys

@@ -631,3 +631,44 @@ def test_draft_forward_matches_oracle(base, B, S, k, n_steps):
     assert np.abs(out.float().cpu().numpy() - ref_o).max() <= 2e-2
     gl, fin = lse.cpu().numpy(), np.isfinite(ref_l)
     assert np.array_equal(np.isfinite(gl), fin) and np.abs(gl[fin] - ref_l[fin]).max() <= 1e-3
+
+
+@pytest.mark.parametrize("schedule", ["FSSS", "FSSSSSSSSS", "FSFSSS"])
+def test_group_batches_decode_layers_into_one_attention_launch(schedule):
+    """A decode group's layers that read one index buffer attend in one launch (few rows per
+    layer: 8 sequences x one query).  Runs of up to eight layers share a launch, which here
+    still splits each row over CTAs and merges the parts; every layer must equal its own
+    attention call over the same buffer (within 1e-2: another split, another summation
+    order) and the oracle (2e-2, LSE 1e-3)."""
+    n = len(schedule)
+    wl = synth.WORKLOADS["decode_b32_200k"].replace(B=8, S=5000, q_pos0=5000, k=512)
+    layers = synth.group_inputs(wl, n, DEV, with_indexer=True)
+    n0 = dsa.launch_count()
+    outs, lses, bufs = dsa.indexshare_group_forward(layers, schedule, wl.k)
+    torch.cuda.synchronize()
+    launches = dsa.launch_count() - n0
+    assert dsa.read_device_flags() == 0
+    f_of = []
+    f = -1
+    for c in schedule:
+        f += c == "F"
+        f_of.append(f)
+    runs = sum(1 for i, c in enumerate(schedule) if c == "F")
+    for l in range(n):
+        o1, l1 = dsa.dsa_sparse_attn(layers[l]["at"], bufs[f_of[l]])
+        assert (o1.float() - outs[l].float()).abs().max().item() <= 1e-2
+        assert (l1 - lses[l]).abs().max().item() <= 1e-3
+        ref_o, ref_l = oracle.sparse_attn(layers[l]["at"], bufs[f_of[l]].reshape(wl.B, wl.k).cpu().numpy())
+        assert np.abs(outs[l].reshape(wl.B, wl.H, wl.DV).float().cpu().numpy() - ref_o).max() <= 2e-2
+        fin = np.isfinite(ref_l)
+        assert np.abs(lses[l].reshape(wl.B, wl.H).cpu().numpy()[fin] - ref_l[fin]).max() <= 1e-3
+    # fewer attention launches than layers: one (split + merge) per run of at most 8 layers
+    batches = 0
+    i = 0
+    while i < n:
+        j = i + 1
+        while j < n and schedule[j] == "S":
+            j += 1
+        batches += (j - i + 7) // 8
+        i = j
+    assert launches <= runs * 3 + batches * 2
