@@ -158,6 +158,15 @@ __device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t lbo) 
 struct QMaps {
   CUtensorMap m[kMaxAttnLayers];
 };
+// Entry l of a per-layer array of the launch parameters, selected with constant indices (a
+// runtime index into a parameter array makes the compiler copy the array to local memory).
+template <class T>
+__device__ __forceinline__ T layer_pick(const T (&a)[kMaxAttnLayers], int l) {
+  T r = a[0];
+#pragma unroll
+  for (int i = 1; i < kMaxAttnLayers; ++i) r = l == i ? a[i] : r;
+  return r;
+}
 
 template <bool kPoll>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -222,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lrow = item / splits, layer = lrow / rows1, row = lrow % rows1;  // row within its layer
       const int32_t* irow = attn_idx_row(p, row);
       const int b = row / p.T;
-      const uint8_t* kvb = static_cast<const uint8_t*>(p.lk[layer]) + (int64_t)b * p.k_sb * 2;  // its latent rows
+      const uint8_t* kvb = static_cast<const uint8_t*>(layer_pick(p.lk, layer)) + (int64_t)b * p.k_sb * 2;  // its latent rows
       // blocks = 1 + (last entry other than -1) / kNB; all loads of the scan issued together
       int last = -1;
       if (vec) {
@@ -267,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int next = (item + (int)gridDim.x) / splits;
         if (lane == 0 && next < rows && next != lrow) {
           const int nr = next % rows1;
-          prefetch_l2(static_cast<const __nv_bfloat16*>(p.lq[next / rows1]) + (int64_t)(nr / p.T) * p.q_sb +
+          prefetch_l2(static_cast<const __nv_bfloat16*>(layer_pick(p.lq, next / rows1)) + (int64_t)(nr / p.T) * p.q_sb +
                           (int64_t)(nr % p.T) * p.q_st,
                       kQBytes);
         }
@@ -456,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
       const int lrow = item / splits, layer = lrow / rows1, row = lrow % rows1;
-      float* const lse_out = p.llse[layer];
+      float* const lse_out = layer_pick(p.llse, layer);
       // every wait of these eight warps is followed by a barrier that ORs "it ran out" over
       // them, so they leave together
       const bool got_info = mbar_wait<kPoll>(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag, p.wait);
@@ -466,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int nb = sm->nb[it & 1], j0 = sm->j0[it & 1];
       if (t == 0) mbar_arrive(&bar.info_empty[it & 1]);
-      __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.lout[layer]) + (int64_t)row * kH * kDV;
+      __nv_bfloat16* og = static_cast<__nv_bfloat16*>(layer_pick(p.lout, layer)) + (int64_t)row * kH * kDV;
       float* po = splits > 1 ? p.part_o + (int64_t)item * kH * kDV : nullptr;  // this part's output
       const int32_t* irow = attn_idx_row(p, row);
       if (nb == 0) {  // nothing visible: O = 0, LSE = -inf
@@ -670,7 +679,7 @@ __global__ void __launch_bounds__(128) k_attn_combine(AttnLaunch p) {
   // blockIdx.x: flat (layer, row); parts of flat row r are items r*S .. r*S + S - 1
   const int lrow = blockIdx.x, h0 = blockIdx.y * kCombHeads, S = p.splits;
   const int rows1 = p.B * p.T, layer = lrow / rows1, row = lrow % rows1;
-  float* const lse_out = p.llse[layer];
+  float* const lse_out = layer_pick(p.llse, layer);
   const float* pl = p.part_lse + (int64_t)lrow * S * kH;
   if (threadIdx.x < kCombHeads) {
     const int h = h0 + threadIdx.x;
@@ -688,7 +697,7 @@ __global__ void __launch_bounds__(128) k_attn_combine(AttnLaunch p) {
   __syncthreads();
   const int64_t first = (int64_t)h0 * kDV / 4;  // this CTA's first float4 within a part
   const float4* po = reinterpret_cast<const float4*>(p.part_o + (int64_t)lrow * S * kH * kDV) + first;
-  __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.lout[layer]) + (int64_t)row * kH * kDV;
+  __nv_bfloat16* og = static_cast<__nv_bfloat16*>(layer_pick(p.lout, layer)) + (int64_t)row * kH * kDV;
   for (int i = threadIdx.x; i < kCombHeads * kDV / 4; i += 128) {
     const int hl = (i * 4) / kDV;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
