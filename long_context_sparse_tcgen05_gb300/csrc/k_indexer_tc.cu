@@ -187,6 +187,7 @@ struct Cfg {
   static constexpr int kBarOff = kQBytes + kStages * kKTile;
   static constexpr size_t kSmem = 1024 + kBarOff + 256 + (size_t)kTB * HI * 4;
   static constexpr uint32_t kIdesc = idesc_mn(FP8 ? 0u : 1u, FP8 ? 0u : 1u, kM, kN);
+  static constexpr uint32_t kIdescTok = idesc_mn(FP8 ? 0u : 1u, FP8 ? 0u : 1u, kM, HI);  // one token's heads
   // selecting mode: sampled tiles whose score prefixes fit beside the stages (FP8: 64; the
   // bf16 stages are twice as large, so 16)
   static constexpr int kSamp = FP8 ? kSampMax : 16;
@@ -212,12 +213,17 @@ __device__ __forceinline__ int64_t visible_keys(const IndexerLaunch& p, int t_lo
   return n < 0 ? 0 : (n > p.S ? (int64_t)p.S : n);
 }
 
-template <int HI, int DI, bool FP8, bool kPoll, bool SEL>
+template <int HI, int DI, bool FP8, bool kPoll, bool SEL, bool DEC>
 __global__ void __launch_bounds__(kThreads, 1)
     k_indexer_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  IndexerLaunch p) {
   using C = Cfg<HI, DI, FP8>;
   static_assert(!SEL || HI == 64, "the selecting epilogue is written for 64 heads (one token per warp)");
+  // DEC (one query token per block, as in decode): each step's four products cover four key
+  // tiles (N = 64, the token's heads) in the four 64-column groups of the accumulator, so all
+  // sixteen epilogue warps work, one key tile per column group, where one token alone would
+  // leave twelve of them idle
+  static_assert(!DEC || (HI == 64 && !SEL), "the one-token layout is written for 64 heads, scores stored");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = smem;
@@ -251,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // tokens (decode: one token per block) have no work, so they sit the tiles out and the
   // accumulator buffers wait only for the others
   constexpr int kTokWarp = C::kCols / HI > 0 ? C::kCols / HI : 1;
-  const int active_ch = min(kEpiWarps / 4, (ntok + kTokWarp - 1) / kTokWarp);
+  const int active_ch = DEC ? kEpiWarps / 4 : min(kEpiWarps / 4, (ntok + kTokWarp - 1) / kTokWarp);
   const int64_t nmax = visible_keys(p, tl0 + ntok - 1);
   // this CTA's key tiles: [kt_lo, kt_lo + ktiles) of the ceil(S / kM) tiles of the row
   const int tiles_all = (p.S + kM - 1) / kM;
@@ -263,7 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t row0 = (int64_t)b * p.T + p.t0 + tl0;  // flat (b, t) of the block's first token
   // selecting mode: rows longer than the candidate capacity first score a sample of tiles
   const int nsamp = (SEL && nmax > p.cap) ? sample_tiles(ktiles, C::kSamp) : 0;
-  const int nproc = nsamp + ktiles;  // tiles the producer, the MMA and the epilogue walk
+  const int nproc = DEC ? (ktiles + 3) / 4 : nsamp + ktiles;  // steps of the MMA and the epilogue
+  const int nload = DEC ? ktiles : nproc;                      // tiles the producer streams
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
@@ -307,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < C::kKBlocks; ++kb)
         tma_load_4d(q_s + kb * C::kQBlock, &tm_q, q_full, kb * C::kAtomElems, 0, p.t0 + tl0, b);
       int issued = 0;
-      for (int i = 0; i < nproc; ++i) {
+      for (int i = 0; i < nload; ++i) {
         const int kt = SEL ? tile_at(i, nsamp, ss->tile) : i;
         const int st = i % C::kStages;
         const uint32_t ph = (i / C::kStages) & 1;
@@ -332,29 +339,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t q_desc0 = desc_sw128(smem_addr(q_s));
       const uint64_t k_desc0 = desc_sw128(smem_addr(k_s));
       for (int kt = 0; ok && kt < nproc; ++kt) {  // kt: processing step (the tile itself is the producer's)
-        const int st = kt % C::kStages;
-        const uint32_t ph = (kt / C::kStages) & 1;
         const int buf = kt & (kBufs - 1);
         if (!(ok = mbar_wait<kPoll>(tm_empty + buf, ((kt / kBufs) & 1) ^ 1, abort_flag, p.wait))) break;
-        if (!(ok = mbar_wait<kPoll>(k_full + st, ph, abort_flag, p.wait))) break;
-        tc_fence_after();
-        const uint32_t d = tmem + buf * kN;
-        const uint64_t kd = k_desc0 + (uint64_t)((st * C::kKTile) >> 4);
+        // one tile (N = 256: the block's tokens x heads), or DEC: up to four tiles, one per
+        // 64-column group (N = 64: the token's heads)
+        const int ntile = DEC ? min(4, ktiles - 4 * kt) : 1;
+        int issued_c = 0;
+        for (int c = 0; ok && c < ntile; ++c) {
+          const int ti = DEC ? 4 * kt + c : kt;  // the tile's place in the producer's stream
+          const int st = ti % C::kStages;
+          if (!(ok = mbar_wait<kPoll>(k_full + st, (ti / C::kStages) & 1, abort_flag, p.wait))) break;
+          tc_fence_after();
+          const uint32_t d = tmem + buf * kN + (DEC ? c * 64 : 0);
+          const uint64_t kd = k_desc0 + (uint64_t)((st * C::kKTile) >> 4);
 #pragma unroll
-        for (int kb = 0; kb < C::kKBlocks; ++kb)
+          for (int kb = 0; kb < C::kKBlocks; ++kb)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            // base descriptors + compile-time offsets in the 16-byte start-address field
-            const uint64_t ad = kd + (uint64_t)((kb * C::kKBlock + j * 32) >> 4);
-            const uint64_t bd = q_desc0 + (uint64_t)((kb * C::kQBlock + j * 32) >> 4);
-            if constexpr (FP8)
-              mma_fp8(d, ad, bd, C::kIdesc, (kb | j) != 0);
-            else
-              mma_bf16(d, ad, bd, C::kIdesc, (kb | j) != 0);
-          }
-        mma_commit(k_empty + st);
-        mma_commit(tm_full + buf);
-        done = kt + 1;
+            for (int j = 0; j < 4; ++j) {
+              // base descriptors + compile-time offsets in the 16-byte start-address field
+              const uint64_t ad = kd + (uint64_t)((kb * C::kKBlock + j * 32) >> 4);
+              const uint64_t bd = q_desc0 + (uint64_t)((kb * C::kQBlock + j * 32) >> 4);
+              constexpr uint32_t id = DEC ? C::kIdescTok : C::kIdesc;
+              if constexpr (FP8)
+                mma_fp8(d, ad, bd, id, (kb | j) != 0);
+              else
+                mma_bf16(d, ad, bd, id, (kb | j) != 0);
+            }
+          mma_commit(k_empty + st);
+          ++issued_c;
+        }
+        // the accumulator's commit also covers a step cut short by a wait that ran out, so the
+        // drain below waits for every product issued
+        if (issued_c > 0) {
+          mma_commit(tm_full + buf);
+          done = kt + 1;
+        }
+        if (!ok) break;
       }
       // the products issued are complete before TMEM can be freed, whichever wait ran out
       if (done > 0) mbar_wait_drain(tm_full + ((done - 1) & (kBufs - 1)), ((done - 1) / kBufs) & 1);
@@ -364,20 +384,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int e = warp - 2;
     const int lq = warp & 3;                 // TMEM lane quarter this warp may read
     const int ch = e >> 2;                   // column quarter (one 64-column slice of N)
+    const int wtok = DEC ? 0 : ch;           // HI = 64: the token of this warp's columns
     const int key_in_tile = lq * 32 + lane;  // TMEM lane = key
     const uint32_t t_lane = tmem + ((uint32_t)(lq * 32) << 16);
     float* out_b = p.out + (int64_t)b * p.out_bstride;
     const float* skg = FP8 ? p.k_scale + (int64_t)b * p.S : nullptr;
 
     constexpr int kTokW = C::kCols / HI > 0 ? C::kCols / HI : 1;  // tokens per epilogue warp
-    const float* w_warp = w_s + ch * C::kCols;                      // this warp's columns' weights
+    const float* w_warp = w_s + (DEC ? 0 : ch * C::kCols);          // this warp's columns' weights
 
     // per-token constants of this warp's tokens, held in registers
     int64_t nvis[kTokW];
     float sq[kTokW];
 #pragma unroll
     for (int tk = 0; tk < kTokW; ++tk) {
-      const int tok = ch * kTokW + tk;
+      const int tok = DEC ? 0 : ch * kTokW + tk;
       nvis[tk] = tok < ntok ? visible_keys(p, tl0 + tok) : 0;
       sq[tk] = (FP8 && tok < ntok) ? __ldg(p.q_scale + row0 + tok) : 1.f;
     }
@@ -544,15 +565,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) p.cand_cnt[crow * 4 + lq] = (int32_t)wcnt;
       } else {
-        float sk16_next = key_scale16(0);
-        for (int kt = 0; kt < ktiles; ++kt) {
+        // step i holds tile i (the block's tokens in the column groups), or DEC: tiles 4i .. 4i+3,
+        // tile 4i + ch in this warp's column group
+        auto tile_of = [&](int i) { return DEC ? 4 * i + ch : i; };
+        float sk16_next = key_scale16(tile_of(0));
+        for (int kt = 0; kt < nproc; ++kt) {
           const float sk = sk16_next;
-          sk16_next = key_scale16(kt + 1);
+          sk16_next = key_scale16(tile_of(kt + 1));
           float v;
           if (!score_step(kt, v)) break;
-          const int key = (kt_lo + kt) * kM + my_key;
-          if (ntok > ch && key < p.S) {
-            float* dst = out_b + (int64_t)(tl0 + ch) * p.ld + key;
+          const int ti = tile_of(kt);
+          const int key = (kt_lo + ti) * kM + my_key;
+          if ((DEC ? ti < ktiles : ntok > ch) && key < p.S) {
+            float* dst = out_b + (int64_t)(tl0 + wtok) * p.ld + key;
             if (key < nvis[0]) {
               if constexpr (FP8) v *= sq[0] * sk;
               *dst = v;
@@ -671,7 +696,7 @@ cudaError_t make_map(CUtensorMap* m, const void* base, bool fp8, int rank, const
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int HI, int DI, bool FP8, bool SEL>
+template <int HI, int DI, bool FP8, bool SEL, bool DEC = false>
 cudaError_t launch_cfg(const IndexerLaunch& p, cudaStream_t st) {
   TraceScope trace(kTraceIndexer, st);
   using C = Cfg<HI, DI, FP8>;
@@ -690,7 +715,8 @@ cudaError_t launch_cfg(const IndexerLaunch& p, cudaStream_t st) {
   if ((e = make_map(&tk, p.k, FP8, 3, kdims, kstr, kbox)) != cudaSuccess) return e;
   IndexerLaunch q = p;
   if (q.wait <= 0) q.wait = wait_limit();
-  auto kern = q.wait < kDefaultWaitCycles ? k_indexer_tc<HI, DI, FP8, true, SEL> : k_indexer_tc<HI, DI, FP8, false, SEL>;
+  auto kern = q.wait < kDefaultWaitCycles ? k_indexer_tc<HI, DI, FP8, true, SEL, DEC>
+                                          : k_indexer_tc<HI, DI, FP8, false, SEL, DEC>;
   const size_t smem = C::kSmem + (SEL ? sizeof(SelSmem<C::kSamp>) : 0);
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
     return e;
@@ -722,6 +748,8 @@ cudaError_t launch_indexer_scores(const IndexerLaunch& p, cudaStream_t st) {
   if (p.HI == 64 && p.DI == 128) {
     if (p.select)
       return p.fp8 ? launch_cfg<64, 128, true, true>(p, st) : launch_cfg<64, 128, false, true>(p, st);
+    if (p.Tc == 1)  // one query token per block (decode): four key tiles per step
+      return p.fp8 ? launch_cfg<64, 128, true, false, true>(p, st) : launch_cfg<64, 128, false, false, true>(p, st);
     return p.fp8 ? launch_cfg<64, 128, true, false>(p, st) : launch_cfg<64, 128, false, false>(p, st);
   }
   if (p.HI == 4 && p.DI == 64 && !p.fp8 && !p.select) return launch_cfg<4, 64, false, false>(p, st);
