@@ -6,12 +6,14 @@
 //
 // Persistent CTAs (one per SM) walk query rows.  For each row:
 //   * warps 0..3 load the query tile with TMA and gather the selected KV rows, 64 per block,
-//     with 16-byte cp.async copies into two 128-byte-swizzled stages (prefetching the rows of
-//     the block two ahead into L2).  A stage lands in three groups of three atoms (an atom: 64
-//     columns of all 64 rows), each group with its own barrier, so the score product starts on
-//     the first columns while the rest are still in flight.  Every copying thread arrives on a group's barrier, and those arrivals pace the
-//     gather: one barrier per atom moved about 17% fewer bytes per second than one per stage
-//     (and 32-row stages, with twice the arrivals per byte, half as many);
+//     with 16-byte cp.async copies into two 128-byte-swizzled stages, prefetching the rows of
+//     the block two ahead into L2 (the stage's fill latency, mostly DRAM misses, paces the
+//     ring).  A stage lands in three groups of three atoms (an atom: 64 columns of all 64
+//     rows), each group with its own barrier, so the score product starts on the first columns
+//     while the rest are still in flight.  Every copying thread arrives on a group's barrier,
+//     and those arrivals pace the gather: one barrier per atom moved about 17% fewer bytes per
+//     second than one per stage (and 32-row stages, with twice the arrivals per byte, half as
+//     many);
 //   * warp 4 issues  S = Q K^T  (M = 64 heads, N = 64 keys, K = 576) into TMEM, group by group;
 //   * warp 5 issues  O^T += V^T P^T  (M = 128 value dims x 4, N = 64 heads, K = 64 keys) -- the
 //     transposed value product keeps the 64 x 512 fp32 accumulator in 256 TMEM columns.  Two
@@ -20,12 +22,14 @@
 //   * warps 6..13 run the online softmax, two warps per TMEM lane quarter, each on 32 of the
 //     block's 64 keys (base-2 exponent, fp32 row sums; the two halves of a head exchange block
 //     maxima and partial sums through shared memory; bf16 P is written into the block's rope
-//     columns, free once S is done).  The running maximum is raised only
-//     when a block exceeds it by more than 2^8; then O^T is rescaled in TMEM.  At the end
-//     they normalise O, write bf16 O and the natural-log LSE.
-// With fewer rows than SMs (decode) a row's blocks are split over several CTAs: each writes
-// its part normalised by its own row sums, in fp32, with its LSE, and k_attn_combine merges
-// the parts (weights exp(LSE_part - LSE_row)).
+//     columns, free once S is done).  The running maximum is raised only when a block exceeds
+//     it by more than 2^8; then O^T is rescaled in TMEM.  At the end they normalise O, write
+//     bf16 O and the natural-log LSE.
+// One launch may cover several layers that read the same index rows (each with its own
+// queries, latent KV, output and LSE): work items run over layers x rows.  With fewer rows
+// than SMs (decode) a row's blocks are split over several CTAs: each writes its part
+// normalised by its own row sums, in fp32, with its LSE, and k_attn_combine merges the parts
+// (weights exp(LSE_part - LSE_row)).
 // Entries of -1 are skipped (masked), out-of-range entries raise DSA_FLAG_BAD_INDEX and are
 // skipped.  Every wait is bounded (DSA_FLAG_TIMEOUT); TMEM is freed on every exit path.
 #include <cuda_bf16.h>

@@ -22,12 +22,16 @@
 // Selecting mode (the top-k path that stores no scores): a CTA whose rows are longer than the
 // candidate room first scores an evenly spread sample of its key tiles and records each
 // sampled score's top 16 order-key bits; each token's four warps then set its threshold (the
-// sample's quantile that about `enough` of the row's keys should exceed); every tile is then
+// sample's quantile that about `target` of the row's keys should exceed); every tile is then
 // scored in order and each score at or above the threshold is kept as a (score, position) pair
-// in the warp's quarter of the row's candidate list: per tile a lane only parks its score in
-// shared memory and sets a bit; once per 32 tiles (8 for bf16) the warp scans its lanes' counts
-// and each lane appends its own.  The sampled tiles are scored twice (1/64 of the tiles, at
-// least 16), which keeps the main pass in plain tile order.
+// in the warp's quarter of the row's candidate list: where over half a score per warp and tile
+// qualifies, a lane parks each tile's score in shared memory and sets a bit, and once per 32
+// tiles (8 for bf16) the warp scans its lanes' counts and each lane appends its own; sparser
+// rows append under a per-tile ballot.  The sampled tiles are scored twice (1/64 of the tiles,
+// at least 16), which keeps the main pass in plain tile order.
+// One-token mode (one query token per block, as in decode): each step's four products cover
+// four key tiles (N = 64: the token's heads), one per 64-column group, so all sixteen epilogue
+// warps work.
 // Every wait is bounded; a timeout raises DSA_FLAG_TIMEOUT, drains the copies in flight,
 // frees TMEM and returns.
 #include <cuda_bf16.h>
