@@ -517,8 +517,9 @@ def run_workloads(dsa, dev, peaks, fp8_tf, world, steps=3):
 def run_draft(dsa, dev, world, steps=3):
     """The four draft steps of a multi-token-prediction layer over the batch-32 200K decode
     cache: one indexshare_draft_forward call (the first step's indexer + top-k, then one
-    attention launch for all steps over its index row) against the same steps run as an
-    F,S,S,S group (one attention launch per step); ms of each and the speedup."""
+    attention launch for all steps over its index row) beside the same steps run as an F,S,S,S
+    group (whose layers reading one index buffer also share an attention launch when they have
+    few rows); ms of each and their ratio."""
     wl = synth.WORKLOADS["mtp_draft_b32_200k"]
     layers = synth.group_inputs(wl, 4, dev, with_indexer=True)
     group = [dict(ix=layers[0]["ix"], at=layers[l]["at"]) for l in range(4)]
