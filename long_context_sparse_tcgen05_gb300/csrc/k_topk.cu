@@ -838,6 +838,135 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk_cand(CandLaunch p) {
   if (threadIdx.x == 0) p.fail[row] = 0;
 }
 
+// ---- few long rows of stored scores: a sampled threshold, one filtering pass, candidate top-k ----
+// (decode: 32 rows of 200,000 scores.)  k_row_threshold estimates, from an evenly spread sample
+// of each row, the key that about `target` of its scores reach; k_row_filter streams every
+// score once over many CTAs and appends those at or above it, as (score, position) pairs, to
+// the row's candidate list (the format of the selecting indexer, one quarter per warp of four);
+// k_topk_cand then selects the exact top-k.  A row whose candidates are fewer than k or overflow
+// a quarter is recomputed by the one-CTA-per-row pass, gated on its flag.
+constexpr int kFiltSamples = 8192;  // sampled scores per row
+constexpr int kFiltChunk = 8192;    // scores per filtering CTA
+constexpr int kFiltThreads = 256;
+struct ThreshSmem {
+  uint32_t key[kFiltSamples];
+  uint32_t hist[kBins];
+  uint32_t warp_sums[kWarps];
+  uint32_t sel_bin, sel_above;
+};
+
+__device__ __forceinline__ int64_t launch_row_visible(const TopkLaunch& p, int tl) {
+  const int64_t n = p.q_pos0 + p.t0 + tl + p.diag;
+  return n < 0 ? 0 : (n > p.S ? (int64_t)p.S : n);
+}
+
+// One row per CTA: the sample's need-th largest key, need = ceil(target' m / n) for m sampled of
+// n visible scores, where target' (at most `target`) stays 4.5 standard deviations of the
+// estimate above k; 0 (keep every visible score) when the sample cannot tell.  Also clears the
+// row's four counts.
+__global__ void __launch_bounds__(kThreads) k_row_threshold(TopkLaunch p, int target, uint32_t* tau, int32_t* cnt) {
+  __shared__ ThreshSmem sm;
+  const int row = blockIdx.x, b = row / p.Tc, tl = row % p.Tc;
+  if (threadIdx.x < 4) cnt[row * 4 + threadIdx.x] = 0;
+  const int64_t n = launch_row_visible(p, tl);
+  const int m = n < kFiltSamples ? (int)n : kFiltSamples;
+  int64_t need = 0;
+  if (n > p.k && m > 0) {
+    const float ratio = (float)n / (float)m;
+    const float a = 4.5f * sqrtf(ratio);
+    const float r = 0.5f * (a + sqrtf(a * a + 4.0f * (float)p.k));
+    need = (int64_t)ceilf(fminf(r * r, (float)target) / ratio);
+  }
+  if (need < 1 || need >= m) {  // (the same decision in every thread)
+    if (threadIdx.x == 0) tau[row] = 0u;
+    return;
+  }
+  const float* sr = p.scores + (int64_t)b * p.bstride + (int64_t)tl * p.ld;
+  // all of a thread's sample loads in flight at once (one scattered sector each)
+  constexpr int kPerT = kFiltSamples / kThreads;
+  float v[kPerT];
+#pragma unroll
+  for (int u = 0; u < kPerT; ++u) {
+    const int i = u * kThreads + (int)threadIdx.x;
+    v[u] = i < m ? __ldg(sr + (int64_t)i * n / m) : 0.f;
+  }
+#pragma unroll
+  for (int u = 0; u < kPerT; ++u) {
+    const int i = u * kThreads + (int)threadIdx.x;
+    if (i < m) sm.key[i] = score_key(v[u]);
+  }
+  __syncthreads();
+  uint32_t ties;
+  const uint32_t t = radix_select(sm, (int64_t)m, (uint32_t)need, [&](int64_t i) { return sm.key[i]; }, &ties, 0u, 32, 0);
+  if (threadIdx.x == 0) tau[row] = t;
+}
+
+// Grid (chunks, rows): chunk c streams scores [c kFiltChunk, (c + 1) kFiltChunk) of the row's
+// visible range and gathers those at or above the row's threshold in shared memory (a
+// block-local count: one atomic per warp and pass on the same global counter serialised the
+// whole pass); then entry i of the CTA's gathered list goes to quarter i % 4 of the row's list,
+// after one global atomic per quarter reserves the room.  NaN scores raise DSA_FLAG_NAN_SCORE.
+constexpr int kFiltBuf = 2048;  // gathered entries per CTA (8,192 scores: about 2% qualify)
+constexpr int kFiltUnroll = 8;  // scores per thread per pass, loaded together
+__global__ void __launch_bounds__(kFiltThreads) k_row_filter(TopkLaunch p, const uint32_t* tau, int cap, uint2* cand,
+                                                             int32_t* cnt) {
+  __shared__ uint2 buf[kFiltBuf];
+  __shared__ int nbuf, over;
+  __shared__ int qbase[4];
+  const int row = blockIdx.y, b = row / p.Tc, tl = row % p.Tc;
+  const int64_t n = launch_row_visible(p, tl);
+  const int64_t c0 = (int64_t)blockIdx.x * kFiltChunk;
+  if (c0 >= n) return;
+  const int64_t c1 = n < c0 + kFiltChunk ? n : c0 + kFiltChunk;
+  const float* sr = p.scores + (int64_t)b * p.bstride + (int64_t)tl * p.ld;
+  const uint32_t th = tau[row];
+  const int lane = threadIdx.x & 31, cap4 = cap / 4;
+  const uint32_t below = (1u << lane) - 1u;
+  if (threadIdx.x == 0) nbuf = 0, over = 0;
+  __syncthreads();
+  bool nan = false;
+  for (int64_t base = c0; base < c1; base += (int64_t)kFiltThreads * kFiltUnroll) {
+    float v[kFiltUnroll];
+#pragma unroll
+    for (int u = 0; u < kFiltUnroll; ++u) {
+      const int64_t i = base + u * kFiltThreads + threadIdx.x;
+      v[u] = i < c1 ? __ldg(sr + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kFiltUnroll; ++u) {
+      const int64_t i = base + u * kFiltThreads + threadIdx.x;
+      const bool valid = i < c1;
+      nan |= valid && v[u] != v[u];
+      const bool take = valid && score_key(v[u]) >= th;
+      const uint32_t bal = __ballot_sync(0xffffffffu, take);
+      if (bal) {
+        int slot0 = 0;
+        if (lane == 0) slot0 = atomicAdd(&nbuf, __popc(bal));
+        slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+        if (take) {
+          const int slot = slot0 + __popc(bal & below);
+          if (slot < kFiltBuf) buf[slot] = make_uint2(__float_as_uint(v[u]), (uint32_t)i);
+          else over = 1;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int m = nbuf < kFiltBuf ? nbuf : kFiltBuf;
+  if (threadIdx.x < 4) {
+    // an overflowing CTA claims more than a quarter holds, so the row is recomputed exactly
+    const int add = over ? cap4 + 1 : (m - (int)threadIdx.x + 3) / 4;
+    qbase[threadIdx.x] = atomicAdd(cnt + row * 4 + threadIdx.x, add);
+  }
+  __syncthreads();
+  if (!over)
+    for (int i = threadIdx.x; i < m; i += kFiltThreads) {
+      const int q = i & 3, slot = qbase[q] + (i >> 2);
+      if (slot < cap4) cand[(int64_t)row * cap + q * cap4 + slot] = buf[i];
+    }
+  if (nan) atomicOr(p.flags, DSA_FLAG_NAN_SCORE);
+}
+
 template <int Cap, int Ring, int Per>
 cudaError_t launch_rows(const TopkLaunch& p, int rows, cudaStream_t st) {
   TraceScope trace(kTraceTopk, st);
@@ -883,6 +1012,50 @@ cudaError_t launch_topk_rows(const TopkLaunch& p, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   if (p.parts > kMaxTopkParts || (p.parts > 1 && !(p.part_pos && p.part_key && p.part_cnt)))
     return cudaErrorInvalidValue;
+  if (p.parts > 1 && !p.gate && p.k <= kCandMaxK) {
+    // few long rows: threshold, filter and candidate top-k in the room planned for the segment
+    // lists, when it holds the candidate lists (decode: 67 -> about 30 us for 32 rows of 200K)
+    const int cap = ((p.k * 4 < 2048 ? 2048 : p.k * 4) + 127) / 128 * 128;
+    // (the room starts wherever the caller's score chunk ends: 4-byte aligned; the pairs want 8)
+    const uintptr_t at = reinterpret_cast<uintptr_t>(p.part_pos), at16 = (at + 15) & ~(uintptr_t)15;
+    const size_t room = (size_t)rows * p.parts * ((size_t)p.k * 8 + 4) - (size_t)(at16 - at);
+    const size_t cand_b = (size_t)rows * cap * 8, cnt_b = (size_t)rows * 16, tau_b = (size_t)rows * 4;
+    if (cap <= kCandMaxCap && cand_b + cnt_b + tau_b + rows <= room) {
+      uint8_t* w = reinterpret_cast<uint8_t*>(at16);
+      uint2* cand = reinterpret_cast<uint2*>(w);
+      int32_t* cnt = reinterpret_cast<int32_t*>(w + cand_b);
+      uint32_t* tau = reinterpret_cast<uint32_t*>(w + cand_b + cnt_b);
+      uint8_t* fail = w + cand_b + cnt_b + tau_b;
+      int64_t n_max = p.q_pos0 + p.t0 + p.Tc - 1 + p.diag;
+      n_max = n_max < 0 ? 0 : (n_max > p.S ? p.S : n_max);
+      {
+        TraceScope trace(kTraceTopk, st);
+        k_row_threshold<<<rows, kThreads, 0, st>>>(p, cap / 2, tau, cnt);
+        count_launches(1);
+        const unsigned chunks = (unsigned)((n_max + kFiltChunk - 1) / kFiltChunk);
+        if (chunks > 0) {
+          k_row_filter<<<dim3(chunks, (unsigned)rows), kFiltThreads, 0, st>>>(p, tau, cap, cand, cnt);
+          count_launches(1);
+        }
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+      }
+      CandLaunch C{};
+      C.B = p.B; C.T = p.T; C.S = p.S; C.t0 = p.t0; C.Tc = p.Tc;
+      C.q_pos0 = p.q_pos0; C.diag = p.diag; C.k = p.k; C.cap = cap;
+      C.cand = cand; C.cand_cnt = cnt; C.fail = fail; C.idx = p.idx;
+      cudaError_t e = launch_topk_cand(C, st);
+      if (e != cudaSuccess) return e;
+      // rows the candidates could not finish: the one-CTA-per-row pass over their scores
+      TopkLaunch g = p;
+      g.parts = 1;
+      g.gate = fail;
+      g.gate_bstride = p.Tc;
+      e = p.k <= 2560 ? launch_rows<4096, 2, 16>(g, rows, st) : launch_rows<8192, 2, 8>(g, rows, st);
+      count_launches(1);
+      return e;
+    }
+  }
   // about 1.25k + 16 n / Cap candidates are expected: 4096 slots hold them for k <= 2560
   cudaError_t e =
       p.k <= 2560 ? launch_rows<4096, 2, 16>(p, rows, st) : launch_rows<8192, 2, 8>(p, rows, st);

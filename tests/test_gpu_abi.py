@@ -100,7 +100,7 @@ def _launches(fn):
 
 
 def test_topk_workspace_query_selects_the_split_path():
-    # 12 long rows: split across CTAs only with the queried room
+    # 12 long rows: the few-long-rows path only with the queried room
     R, n, k = 12, 200000, 2048
     sc = synth.scores_input(R, n, DEV, "int", lo=-40, hi=40)
     q_pos0 = n - R
@@ -109,7 +109,9 @@ def test_topk_workspace_query_selects_the_split_path():
     ref = oracle.topk_rows(sc.double().cpu().numpy(), np.clip(np.arange(R) + q_pos0, 0, n), k)
     ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
     idx, nl = _launches(lambda: dsa.dsa_topk(k, scores=sc[None], q_pos0=q_pos0, ws=ws))
-    assert nl == 2  # segments, then the merge
+    # few long rows in the queried room: sampled threshold, filter, candidate top-k, and the
+    # gated pass for rows the candidates could not finish
+    assert nl == 4
     assert np.array_equal(idx[0].cpu().numpy(), ref)
     ws_min = torch.zeros(dsa.WS_MIN, dtype=torch.uint8, device=DEV)
     idx2, nl2 = _launches(lambda: dsa.dsa_topk(k, scores=sc[None], q_pos0=q_pos0, ws=ws_min))

@@ -71,8 +71,9 @@ def test_noalloc_matches_workspace_entry_point_twice(lib, name, over, k):
 
 def test_noalloc_splits_few_long_rows_like_the_workspace_path(lib):
     """Decode shape (32 sequences x one query over 200,000 keys): the fixed array holds the
-    25.6 MB of scores and, after them, the segment lists of rows split over several CTAs, so
-    the call launches the indexer, the split top-k and its merge -- and equals dsa_topk."""
+    25.6 MB of scores and, after them, the room of the few-long-rows top-k, so the call launches
+    the indexer, the sampled threshold, the filter, the candidate top-k and the gated pass for
+    rows the candidates could not finish -- and equals dsa_topk."""
     wl = synth.WORKLOADS["decode_b32_200k"].replace(values="gauss")
     ix = synth.indexer_inputs(wl, 0, DEV)
     ref = dsa.dsa_topk(wl.k, ix=ix)
@@ -80,7 +81,7 @@ def test_noalloc_splits_few_long_rows_like_the_workspace_path(lib):
     n0 = dsa.launch_count()
     got = _noalloc(lib, ix, wl.k)
     torch.cuda.synchronize()
-    assert dsa.launch_count() - n0 == 3  # indexer, top-k segments, merge
+    assert dsa.launch_count() - n0 == 5
     assert torch.equal(got, ref)
     del ix
     torch.cuda.empty_cache()
