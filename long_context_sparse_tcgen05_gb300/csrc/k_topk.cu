@@ -925,29 +925,49 @@ __global__ void __launch_bounds__(kFiltThreads) k_row_filter(TopkLaunch p, const
   if (threadIdx.x == 0) nbuf = 0, over = 0;
   __syncthreads();
   bool nan = false;
-  for (int64_t base = c0; base < c1; base += (int64_t)kFiltThreads * kFiltUnroll) {
-    float v[kFiltUnroll];
-#pragma unroll
-    for (int u = 0; u < kFiltUnroll; ++u) {
-      const int64_t i = base + u * kFiltThreads + threadIdx.x;
-      v[u] = i < c1 ? __ldg(sr + i) : 0.f;
+  auto consider = [&](float v, int64_t i, bool valid) {  // warp-uniform call
+    nan |= valid && v != v;
+    const bool take = valid && score_key(v) >= th;
+    const uint32_t bal = __ballot_sync(0xffffffffu, take);
+    if (bal) {
+      int slot0 = 0;
+      if (lane == 0) slot0 = atomicAdd(&nbuf, __popc(bal));
+      slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+      if (take) {
+        const int slot = slot0 + __popc(bal & below);
+        if (slot < kFiltBuf) buf[slot] = make_uint2(__float_as_uint(v), (uint32_t)i);
+        else over = 1;
+      }
     }
+  };
+  if (c1 - c0 == kFiltChunk && (reinterpret_cast<uintptr_t>(sr + c0) & 15u) == 0) {
+    // a whole 16-byte-aligned chunk: 16-byte loads, two per thread and pass in flight
+    const float4* s4 = reinterpret_cast<const float4*>(sr + c0);
+    for (int base = 0; base < kFiltChunk / 4; base += 2 * kFiltThreads) {
+      float4 w[2];
 #pragma unroll
-    for (int u = 0; u < kFiltUnroll; ++u) {
-      const int64_t i = base + u * kFiltThreads + threadIdx.x;
-      const bool valid = i < c1;
-      nan |= valid && v[u] != v[u];
-      const bool take = valid && score_key(v[u]) >= th;
-      const uint32_t bal = __ballot_sync(0xffffffffu, take);
-      if (bal) {
-        int slot0 = 0;
-        if (lane == 0) slot0 = atomicAdd(&nbuf, __popc(bal));
-        slot0 = __shfl_sync(0xffffffffu, slot0, 0);
-        if (take) {
-          const int slot = slot0 + __popc(bal & below);
-          if (slot < kFiltBuf) buf[slot] = make_uint2(__float_as_uint(v[u]), (uint32_t)i);
-          else over = 1;
-        }
+      for (int u = 0; u < 2; ++u) w[u] = __ldg(s4 + base + u * kFiltThreads + threadIdx.x);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int64_t i = c0 + 4 * (int64_t)(base + u * kFiltThreads + threadIdx.x);
+        consider(w[u].x, i, true);
+        consider(w[u].y, i + 1, true);
+        consider(w[u].z, i + 2, true);
+        consider(w[u].w, i + 3, true);
+      }
+    }
+  } else {
+    for (int64_t base = c0; base < c1; base += (int64_t)kFiltThreads * kFiltUnroll) {
+      float v[kFiltUnroll];
+#pragma unroll
+      for (int u = 0; u < kFiltUnroll; ++u) {
+        const int64_t i = base + u * kFiltThreads + threadIdx.x;
+        v[u] = i < c1 ? __ldg(sr + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kFiltUnroll; ++u) {
+        const int64_t i = base + u * kFiltThreads + threadIdx.x;
+        consider(v[u], i, i < c1);
       }
     }
   }
