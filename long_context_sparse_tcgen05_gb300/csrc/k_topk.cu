@@ -852,6 +852,7 @@ struct ThreshSmem {
   uint32_t key[kFiltSamples];
   uint32_t hist[kBins];
   uint32_t warp_sums[kWarps];
+  uint32_t key_hi[kWarps];
   uint32_t sel_bin, sel_above;
 };
 
@@ -862,7 +863,9 @@ __device__ __forceinline__ int64_t launch_row_visible(const TopkLaunch& p, int t
 
 // One row per CTA: the sample's need-th largest key, need = ceil(target' m / n) for m sampled of
 // n visible scores, where target' (at most `target`) stays 4.5 standard deviations of the
-// estimate above k; 0 (keep every visible score) when the sample cannot tell.  Also clears the
+// estimate above k; 0 (keep every visible score) when the sample cannot tell.  The sample is 64
+// runs of 128 consecutive scores spread evenly over the row (coalesced loads), and the radix
+// passes start at the first bit where its smallest and largest keys differ.  Also clears the
 // row's four counts.
 __global__ void __launch_bounds__(kThreads) k_row_threshold(TopkLaunch p, int target, uint32_t* tau, int32_t* cnt) {
   __shared__ ThreshSmem sm;
@@ -877,27 +880,57 @@ __global__ void __launch_bounds__(kThreads) k_row_threshold(TopkLaunch p, int ta
     const float r = 0.5f * (a + sqrtf(a * a + 4.0f * (float)p.k));
     need = (int64_t)ceilf(fminf(r * r, (float)target) / ratio);
   }
-  if (need < 1 || need >= m) {  // (the same decision in every thread)
+  // (the same decision in every thread; a row of at most kFiltSamples scores keeps them all)
+  if (need < 1 || need >= m || n <= kFiltSamples) {
     if (threadIdx.x == 0) tau[row] = 0u;
     return;
   }
   const float* sr = p.scores + (int64_t)b * p.bstride + (int64_t)tl * p.ld;
-  // all of a thread's sample loads in flight at once (one scattered sector each)
-  constexpr int kPerT = kFiltSamples / kThreads;
+  // sample i: element i % 128 of run i / 128, the runs starting evenly over the row (n > m =
+  // 8,192 here, so they do not overlap); all of a thread's loads in flight at once
+  constexpr int kRun = 128, kRuns = kFiltSamples / kRun, kPerT = kFiltSamples / kThreads;
   float v[kPerT];
 #pragma unroll
   for (int u = 0; u < kPerT; ++u) {
-    const int i = u * kThreads + (int)threadIdx.x;
-    v[u] = i < m ? __ldg(sr + (int64_t)i * n / m) : 0.f;
+    const int i = u * kThreads + (int)threadIdx.x, r = i / kRun;
+    const int64_t start = (int64_t)r * (n - kRun) / (kRuns - 1);
+    v[u] = __ldg(sr + start + (i % kRun));
   }
+  uint32_t lo = 0xffffffffu, hi = 0u;
 #pragma unroll
   for (int u = 0; u < kPerT; ++u) {
-    const int i = u * kThreads + (int)threadIdx.x;
-    if (i < m) sm.key[i] = score_key(v[u]);
+    const uint32_t key = score_key(v[u]);
+    sm.key[u * kThreads + (int)threadIdx.x] = key;
+    lo = key < lo ? key : lo;
+    hi = key > hi ? key : hi;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    sm.warp_sums[threadIdx.x >> 5] = lo;
+    sm.key_hi[threadIdx.x >> 5] = hi;
   }
   __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t a = 0xffffffffu, z = 0u;
+    for (int w = 0; w < kWarps; ++w) {
+      a = sm.warp_sums[w] < a ? sm.warp_sums[w] : a;
+      z = sm.key_hi[w] > z ? sm.key_hi[w] : z;
+    }
+    sm.sel_bin = a;
+    sm.sel_above = z;
+  }
+  __syncthreads();
+  const uint32_t d = sm.sel_bin ^ sm.sel_above;
+  const int top = d ? 32 - __clz(d) : 0;
+  const uint32_t prefix = top >= 32 ? 0u : (sm.sel_above & ~((1u << top) - 1u));
+  __syncthreads();
   uint32_t ties;
-  const uint32_t t = radix_select(sm, (int64_t)m, (uint32_t)need, [&](int64_t i) { return sm.key[i]; }, &ties, 0u, 32, 0);
+  const uint32_t t =
+      radix_select(sm, (int64_t)kFiltSamples, (uint32_t)need, [&](int64_t i) { return sm.key[i]; }, &ties, prefix, top, 0);
   if (threadIdx.x == 0) tau[row] = t;
 }
 
