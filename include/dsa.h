@@ -155,17 +155,20 @@ typedef struct {
  *   the path that stores no scores when it applies (at most 1 GiB: 8,192 (score, position)
  *   pairs per row of a chunk of rows), a score buffer of fp32 rows (up to 4 GiB; at least
  *   DSA_WS_MIN plus one row of B*S*4 bytes is required) and, when a chunk has fewer query rows
- *   than the device has SMs, room for splitting each row's top-k across CTAs.  Without room
- *   for the candidate lists the call stores the scores of every row.
+ *   than the device has SMs, room for spreading each row's top-k over CTAs (a sampled
+ *   threshold, a filtering pass and a candidate select; or, for k > 2,048, segments and a
+ *   merge).  Without room for the candidate lists the call stores the scores of every row.
  * dsa_topk_workspace_size: dsa_topk(FROM_SCORES) over B*T rows of the given visibility --
- *   DSA_WS_MIN plus the split room when the rows are few and long (0 extra otherwise).
+ *   DSA_WS_MIN plus that room when the rows are few and long (0 extra otherwise).
  * dsa_attn_workspace_size: dsa_sparse_attn -- DSA_WS_MIN plus, for the 64-head latent shape
  *   with fewer query rows than half the SMs, room for each row's split parts (fp32 outputs
  *   and LSEs of up to 8 parts).
  * indexshare_group_workspace_size: indexshare_group_forward (seqs NULL) or
  *   indexshare_group_forward_varlen (seqs given) -- the largest of the above over the
- *   group's layers ('F' layers: indexer and attention; 'S' layers: attention) and, packed,
- *   over its sequences.  Returns DSA_WS_MIN for arguments that the call would reject. */
+ *   group's layers ('F' layers: indexer and attention; 'S' layers: attention), including the
+ *   split parts of the launches that attend several layers at once (the layers that read one
+ *   index buffer, when each has few rows), and, packed, over its sequences.  Returns
+ *   DSA_WS_MIN for arguments that the call would reject. */
 #define DSA_WS_MIN ((size_t)256)
 size_t dsa_workspace_size(const dsa_indexer_args* ix, int32_t k);
 size_t dsa_topk_workspace_size(int32_t B, int32_t T, int32_t S, int64_t q_pos0, int32_t diag, int32_t k);
@@ -197,8 +200,11 @@ dsa_status dsa_sparse_attn(const dsa_attn_args* at, const int32_t* idx, int32_t 
 /* IndexShare group forward ("How IndexShare Works"; "What IndexShare reuses").
  * schedule: one 'F' or 'S' per layer, starting with 'F' (e.g. "FSSS").  For each 'F'
  * layer number f (0-based count of F layers so far), indexer + top-k write idx_bufs[f]
- * ([B,T,k] int32, caller-owned).  Every layer then runs dsa_sparse_attn with its own
- * operands over the most recent F layer's buffer.  All layers share B, T, S. */
+ * ([B,T,k] int32, caller-owned).  Every layer then attends with its own operands over the
+ * most recent F layer's buffer, as dsa_sparse_attn would; the layers that read one buffer
+ * share one attention launch when each has too few rows to fill the GPU (decode) and their
+ * attention operands have the 64-head latent shape with equal scale and strides (results as
+ * per-layer calls, up to the summation order of a decode split).  All layers share B, T, S. */
 dsa_status indexshare_group_forward(const dsa_layer* layers, int32_t n_layers,
                                     const char* schedule, int32_t k, int32_t* const* idx_bufs,
                                     void* ws, size_t ws_bytes, void* stream);
