@@ -116,7 +116,8 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 // Thread t of the warp receives, for each of the x2 / x4 repetitions j, TMEM lanes base + t/4
 // and base + t/4 + 8 at columns 8j + 2(t%4) and 8j + 2(t%4) + 1, in that order (r[4j .. 4j+3]).
-__device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[8]) {
+// (x2: the 32-key block width, which the kernel keeps buildable.)
+[[maybe_unused]] __device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[8]) {
   asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                : "r"(taddr));
@@ -226,7 +227,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barrier, which fires once its own copies have landed, so the producer never waits for
     // its copies and all stages stay in flight.
     const int64_t row_bytes = p.k_ld * 2;
-    const bool leader = warp == 0 && lane == 0;
     int it = 0, qc = 0;
     long long g = 0;  // global block counter
     bool ok = true;
@@ -345,7 +345,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
-    (void)leader;
     // the last query tile issued has landed before the CTA can exit (whichever wait ran out)
     if (warp == 0 && lane == 0 && qc > 0) mbar_wait_drain(&bar.q_full, (uint32_t)((qc - 1) & 1));
   } else if (warp == kMmaWarp) {
