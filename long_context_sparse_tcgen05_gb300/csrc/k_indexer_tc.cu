@@ -217,6 +217,25 @@ __device__ __forceinline__ int64_t visible_keys(const IndexerLaunch& p, int t_lo
   return n < 0 ? 0 : (n > p.S ? (int64_t)p.S : n);
 }
 
+// Out-of-line append of one batch (see the selecting main loop): returns the warp's new count.
+__device__ __noinline__ uint32_t sel_flush(uint32_t mask, const float* vbuf, int lane, uint32_t wcnt, int cap4,
+                                           uint2* cand, int key0) {
+  const uint32_t c = __popc(mask);
+  uint32_t inc = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  const uint32_t total = __shfl_sync(0xffffffffu, inc, 31);
+  uint32_t slot = wcnt + inc - c;
+  for (uint32_t mm = mask; mm; mm &= mm - 1, ++slot) {
+    const int tb = __ffs(mm) - 1;
+    if (slot < (uint32_t)cap4) cand[slot] = make_uint2(__float_as_uint(vbuf[tb * 32 + lane]), (uint32_t)(key0 + tb * kM));
+  }
+  return wcnt + total;
+}
+
 template <int HI, int DI, bool FP8, bool kPoll, bool SEL, bool DEC>
 __global__ void __launch_bounds__(kThreads, 1)
     k_indexer_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -505,29 +524,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // token's sample area, no longer read once its threshold is set) and one bit per tile in
         // a lane mask; once per batch of kBatch tiles the warp scans the lanes' counts and each
         // lane appends its own qualifying scores.  The list is unordered; the top-k orders its
-        // selection by position.  (On 4,096 rows x 128K keys: this form 4.90 ms, a per-tile
-        // ballot with a divergent store 4.92, a staging ring in shared memory 5.08, a predicated
-        // store every tile 5.24; a count alone, storing nothing, 4.03.)
+        // selection by position.  (On 4,096 rows x 128K keys: this form 4.74 ms with the batch's
+        // append out of line, 4.90 inlined, a per-tile ballot with a divergent store 4.92, a
+        // staging ring in shared memory 5.08, a predicated store every tile 5.24; a count alone,
+        // storing nothing, 4.03.)
         constexpr int kBatch = FP8 ? 32 : 8;
         static_assert(sizeof(ss->samp[0]) >= 4 * kBatch * 32 * sizeof(float), "batch exceeds the token's sample area");
         float* vbuf = reinterpret_cast<float*>(ss->samp[ch]) + (e & 3) * kBatch * 32;
         uint32_t mask = 0;  // bit i: this lane's score of the batch's tile i qualifies
         auto flush = [&](int kt0) {  // append the batch starting at tile kt0
-          const uint32_t c = __popc(mask);
-          uint32_t inc = c;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += y;
-          }
-          const uint32_t total = __shfl_sync(0xffffffffu, inc, 31);
-          uint32_t slot = wcnt + inc - c;
-          for (uint32_t mm = mask; mm; mm &= mm - 1, ++slot) {
-            const int tb = __ffs(mm) - 1;
-            if (slot < (uint32_t)cap4)
-              cand[slot] = make_uint2(__float_as_uint(vbuf[tb * 32 + lane]), (uint32_t)((kt_lo + kt0 + tb) * kM + my_key));
-          }
-          wcnt += total;
+          wcnt = sel_flush(mask, vbuf, lane, wcnt, cap4, cand, (kt_lo + kt0) * kM + my_key);
           mask = 0;
         };
         // Rows whose threshold keeps under half a score per warp and tile (long rows: 0.15 at
