@@ -162,7 +162,9 @@ typedef struct {
  *   DSA_WS_MIN plus that room when the rows are few and long (0 extra otherwise).
  * dsa_attn_workspace_size: dsa_sparse_attn -- DSA_WS_MIN plus, for the 64-head latent shape
  *   with fewer query rows than half the SMs, room for each row's split parts (fp32 outputs
- *   and LSEs of up to 8 parts).
+ *   and LSEs of up to 8 parts); with more rows, one byte per row (rounded up to 256) that
+ *   marks the rows a fixed-reference softmax pass leaves to a running-maximum recompute
+ *   (without it every row takes the running-maximum softmax; same results either way).
  * indexshare_group_workspace_size: indexshare_group_forward (seqs NULL) or
  *   indexshare_group_forward_varlen (seqs given) -- the largest of the above over the
  *   group's layers ('F' layers: indexer and attention; 'S' layers: attention), including the

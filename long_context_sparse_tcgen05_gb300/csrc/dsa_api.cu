@@ -138,6 +138,17 @@ size_t attn_split_bytes(const dsa::AttnLaunch& L) {
   return (size_t)L.B * L.T * (L.layers > 1 ? L.layers : 1) * splits * (size_t)L.H * ((size_t)L.DV + 1) * 4;
 }
 
+// Bytes of the fixed-reference pass's row marks (one per flat row; 0 where the call splits rows
+// or takes the other kernel).
+size_t attn_mark_bytes(const dsa::AttnLaunch& L) {
+  if (!dsa::sparse_mla_tc_supported(L) || dsa::attn_splits(L) > 1) return 0;
+  const size_t rows = (size_t)L.B * L.T * (L.layers > 1 ? L.layers : 1);
+  return (rows + 255) & ~(size_t)255;
+}
+
+// All the workspace an attention call uses beyond DSA_WS_MIN.
+size_t attn_extra_bytes(const dsa::AttnLaunch& L) { return attn_split_bytes(L) + attn_mark_bytes(L); }
+
 constexpr int kMaxK = 4096;
 
 // Bytes of the segment lists when `rows` rows of up to n_max scores are split across CTAs
@@ -335,7 +346,7 @@ size_t dsa_topk_workspace_size(int32_t B, int32_t T, int32_t S, int64_t q_pos0, 
 
 size_t dsa_attn_workspace_size(const dsa_attn_args* at, int32_t k) {
   if (!at || at->B <= 0 || at->T <= 0 || at->S <= 0 || k < 1 || k > kMaxK) return DSA_WS_MIN;
-  return dsa::kWsScratch + attn_split_bytes(attn_launch(at, nullptr, k, nullptr, nullptr));
+  return dsa::kWsScratch + attn_extra_bytes(attn_launch(at, nullptr, k, nullptr, nullptr));
 }
 
 dsa_status dsa_indexer_scores(const dsa_indexer_args* ix, float* scores, int64_t ld, void* ws, size_t ws_bytes,
@@ -406,6 +417,11 @@ dsa_status run_attn(dsa::AttnLaunch L, void* ws, size_t ws_bytes, void* stream) 
       L.part_o = reinterpret_cast<float*>(w);
       L.part_lse = reinterpret_cast<float*>(w + parts * (size_t)L.H * L.DV * 4);
     }
+  } else {
+    // the fixed-reference softmax when the workspace holds its row marks (else the running one)
+    const size_t marks = attn_mark_bytes(L);
+    if (marks > 0 && ws_bytes > dsa::kWsScratch && ws_bytes - dsa::kWsScratch >= marks)
+      L.redo = static_cast<uint8_t*>(ws) + dsa::kWsScratch;
   }
   cudaError_t e = dsa::launch_sparse_attn(L, as_stream(stream));
   return e == cudaSuccess ? DSA_OK : cuda_fail(e, "attention launch");
@@ -452,7 +468,7 @@ dsa_status indexshare_draft_forward(const dsa_indexer_args* ix, const dsa_attn_a
 
 size_t indexshare_draft_workspace_size(const dsa_indexer_args* ix, const dsa_attn_args* at, int32_t k) {
   if (!ix || !at || at->B <= 0 || at->T <= 0 || at->S <= 0 || k < 1 || k > kMaxK) return DSA_WS_MIN;
-  const size_t a = dsa::kWsScratch + attn_split_bytes(draft_launch(at, nullptr, k, nullptr, nullptr));
+  const size_t a = dsa::kWsScratch + attn_extra_bytes(draft_launch(at, nullptr, k, nullptr, nullptr));
   const size_t t = dsa_workspace_size(ix, k);
   return a > t ? a : t;
 }
@@ -660,7 +676,7 @@ size_t indexshare_group_workspace_size(const dsa_layer* layers, int32_t n_layers
       while (run_end < n_layers && schedule[run_end] != 'F') ++run_end;
       for (int a = i; a < run_end;) {
         const int c = attn_batch_end(ls, a, run_end, k);
-        best = std::max(best, dsa::kWsScratch + attn_split_bytes(batch_launch(ls, a, c, nullptr, k)));
+        best = std::max(best, dsa::kWsScratch + attn_extra_bytes(batch_launch(ls, a, c, nullptr, k)));
         a = c;
       }
       i = run_end;

@@ -173,6 +173,11 @@ struct AttnLaunch {
   // own queries, latent KV, output and LSE (same shapes and strides) and reads the same index
   // rows; work items run over layers x rows x parts, part_o / part_lse by that flat item
   int layers;
+  // fixed-reference pass (redo set, no split): redo[r] = 1 for flat row r (layer x row) whose
+  // row sums left the range the fixed reference keeps exact; a recomputing pass (gate set)
+  // then runs only the marked rows
+  uint8_t* redo;
+  const uint8_t* gate;
   const void* lq[kMaxAttnLayers];
   const void* lk[kMaxAttnLayers];
   void* lout[kMaxAttnLayers];

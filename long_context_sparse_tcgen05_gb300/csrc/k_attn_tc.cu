@@ -96,6 +96,7 @@ struct Small {
   float bmax[2][2][kH];           // [block parity][key half][head]: block maxima of the two halves
   float lpart[2][kH];             // [key half][head]: partial row sums at the end of a row
   int any_rescale[2][kSmWarps];   // by block parity, so a fast warp never overwrites an unread flag
+  int bad;                        // fixed reference: a row sum of this row left the exact range
 };
 
 constexpr size_t kSmem = 1024 + kQBytes + kStages * kKVBytes + sizeof(Small);
@@ -173,7 +174,12 @@ __device__ __forceinline__ T layer_pick(const T (&a)[kMaxAttnLayers], int l) {
   return r;
 }
 
-template <bool kPoll>
+// kFixed: the softmax uses a fixed reference maximum of 0 (base-2 units) instead of a running
+// one, so a block needs no exchange of maxima between the warps that share a head and O^T is
+// never rescaled; exact while every row sum stays within [2^-64, 2^64] (P <= 2^64 in bf16, O^T
+// and the sums in fp32).  A row outside that range is marked in p.redo and recomputed by the
+// running-maximum kernel, which then runs only the marked rows (p.gate).
+template <bool kPoll, bool kFixed>
 __global__ void __launch_bounds__(kThreads, 1)
     k_sparse_mla_tc(const __grid_constant__ QMaps qm, AttnLaunch p) {
   extern __shared__ uint8_t smem_raw[];
@@ -189,6 +195,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rows = rows1 * (p.layers > 1 ? p.layers : 1);
   const int splits = p.splits > 1 ? p.splits : 1;  // work item = (layer x row, part of its blocks)
   const int items = rows * splits;
+  // items in order, skipping rows that a recomputing pass (p.gate) does not run; every role walks
+  // the same sequence, so the barriers they share stay in step (a warp-uniform call)
+  auto next_item = [&](int i) -> int {
+    if (!p.gate) return i;
+    const int G = (int)gridDim.x, ln = (int)(threadIdx.x & 31);
+    for (int base = i; base < items; base += 32 * G) {
+      const int cand = base + ln * G;
+      const bool f = cand < items && p.gate[cand / splits] != 0;
+      const uint32_t bal = __ballot_sync(0xffffffffu, f);
+      if (bal) return base + (__ffs(bal) - 1) * G;
+    }
+    return items;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&bar.q_full, 1);
@@ -208,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar.o_full, 1);
     mbar_init(&bar.o_empty, kSmWarps);
     sm->abort = 0;
+    sm->bad = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -231,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long g = 0;  // global block counter
     bool ok = true;
     const bool vec = ((p.kk | p.idx_st | p.idx_sb) & 3) == 0 && (reinterpret_cast<uintptr_t>(p.idx) & 15u) == 0;
-    for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
+    for (int item = next_item(blockIdx.x); ok && item < items; item = next_item(item + (int)gridDim.x), ++it) {
       const int lrow = item / splits, layer = lrow / rows1, row = lrow % rows1;  // row within its layer
       const int32_t* irow = attn_idx_row(p, row);
       const int b = row / p.T;
@@ -355,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0, qc = 0;
     long long g = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
+    for (int item = next_item(blockIdx.x); ok && item < items; item = next_item(item + (int)gridDim.x), ++it) {
       int nb = 0;
       if (lane == 0) {
         ok = mbar_wait<kPoll>(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag, p.wait);
@@ -409,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0, oc = 0;
     long long g = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
+    for (int item = next_item(blockIdx.x); ok && item < items; item = next_item(item + (int)gridDim.x), ++it) {
       int nb = 0;
       if (lane == 0) {
         ok = mbar_wait<kPoll>(&bar.info_full[it & 1], (it >> 1) & 1, abort_flag, p.wait);
@@ -466,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0, oc = 0;
     long long g = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < items; item += gridDim.x, ++it) {
+    for (int item = next_item(blockIdx.x); ok && item < items; item = next_item(item + (int)gridDim.x), ++it) {
       const int lrow = item / splits, layer = lrow / rows1, row = lrow % rows1;
       float* const lse_out = layer_pick(p.llse, layer);
       // every wait of these eight warps is followed by a barrier that ORs "it ran out" over
@@ -489,9 +509,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = t; i < kH * kDV / 8; i += kSmThreads) reinterpret_cast<uint4*>(og)[i] = make_uint4(0, 0, 0, 0);
           if (lse_out && t < kH) lse_out[(int64_t)row * kH + t] = -INFINITY;
         }
+        if (kFixed && t == 0 && p.redo) p.redo[lrow] = 0;
         continue;
       }
       float m_used[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+      bool failed = false;  // kFixed: a wait ran out; the warp goes to the row's end barrier
       for (int j = 0; ok && j < nb; ++j, ++g) {
         const int sb = (int)(g & 1);
         // this lane's key slot (lanes 16..31 repeat 0..15), loaded before the wait so that its
@@ -526,63 +548,71 @@ __global__ void __launch_bounds__(kThreads, 1)
               s[hs][2 * jj + e2] = y;
               bmax[hs] = fmaxf(bmax[hs], y);
             }
-#pragma unroll
-        for (int hs = 0; hs < 2; ++hs) {
-          bmax[hs] = fmaxf(bmax[hs], __shfl_xor_sync(0xffffffffu, bmax[hs], 1));
-          bmax[hs] = fmaxf(bmax[hs], __shfl_xor_sync(0xffffffffu, bmax[hs], 2));
-        }
-        const bool need_h = bmax[0] > m_used[0] + kRescaleLog2 || bmax[1] > m_used[1] + kRescaleLog2;
-        const int any = __any_sync(0xffffffffu, need_h);
-        if (quad_lead) {
-          sm->bmax[sb][kh][hd[0]] = bmax[0];
-          sm->bmax[sb][kh][hd[1]] = bmax[1];
-        }
-        if (lane == 0) sm->any_rescale[sb][sw] = any;
-        if (named_sync_or(1, kSmThreads, !got_s)) {
-          ok = false;
-          break;
-        }
-        int anyr = 0;
-#pragma unroll
-        for (int w = 0; w < kSmWarps; ++w) anyr |= sm->any_rescale[sb][w];
         float m_new[2];
-        bool need[2];
-#pragma unroll
-        for (int hs = 0; hs < 2; ++hs) {
-          const float bm = fmaxf(sm->bmax[sb][0][hd[hs]], sm->bmax[sb][1][hd[hs]]);
-          need[hs] = bm > m_used[hs] + kRescaleLog2;  // the same decision in both key halves
-          m_new[hs] = need[hs] ? bm : m_used[hs];
-        }
-        if (j > 0 && anyr) {
-          // O^T must be complete for the previous block before it is rescaled: the value
-          // product of block g-1 releases its stage
-          const long long gp = g - 1;
-          const bool got_o = mbar_wait<kPoll>(&bar.kv_empty[gp % kStages], (uint32_t)((gp / kStages) & 1), abort_flag, p.wait);
-#pragma unroll
-          for (int hs = 0; hs < 2; ++hs) {
-            const float alpha = need[hs] ? ex2(m_used[hs] - m_new[hs]) : 1.f;
-            if (quad_lead && kh == 0) sm->alpha[hd[hs]] = alpha;
-            l[hs] *= alpha;
+        if constexpr (kFixed) {
+          if (!got_s) {
+            failed = true;
+            break;
           }
-          if (named_sync_or(1, kSmThreads, !got_o)) {
+          m_new[0] = m_new[1] = 0.f;
+        } else {
+  #pragma unroll
+          for (int hs = 0; hs < 2; ++hs) {
+            bmax[hs] = fmaxf(bmax[hs], __shfl_xor_sync(0xffffffffu, bmax[hs], 1));
+            bmax[hs] = fmaxf(bmax[hs], __shfl_xor_sync(0xffffffffu, bmax[hs], 2));
+          }
+          const bool need_h = bmax[0] > m_used[0] + kRescaleLog2 || bmax[1] > m_used[1] + kRescaleLog2;
+          const int any = __any_sync(0xffffffffu, need_h);
+          if (quad_lead) {
+            sm->bmax[sb][kh][hd[0]] = bmax[0];
+            sm->bmax[sb][kh][hd[1]] = bmax[1];
+          }
+          if (lane == 0) sm->any_rescale[sb][sw] = any;
+          if (named_sync_or(1, kSmThreads, !got_s)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 2 * kh; c < 2 * kh + 2; ++c)  // each key half rescales two of the four chunks
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-              uint32_t r[32];
-              const uint32_t ta = tmem + lane_base + kColO + c * kH + half * 32;
-              tmem_ld32(ta, r);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * sm->alpha[half * 32 + i]);
-              tmem_st32(ta, r);
+          int anyr = 0;
+  #pragma unroll
+          for (int w = 0; w < kSmWarps; ++w) anyr |= sm->any_rescale[sb][w];
+          bool need[2];
+  #pragma unroll
+          for (int hs = 0; hs < 2; ++hs) {
+            const float bm = fmaxf(sm->bmax[sb][0][hd[hs]], sm->bmax[sb][1][hd[hs]]);
+            need[hs] = bm > m_used[hs] + kRescaleLog2;  // the same decision in both key halves
+            m_new[hs] = need[hs] ? bm : m_used[hs];
+          }
+          if (j > 0 && anyr) {
+            // O^T must be complete for the previous block before it is rescaled: the value
+            // product of block g-1 releases its stage
+            const long long gp = g - 1;
+            const bool got_o = mbar_wait<kPoll>(&bar.kv_empty[gp % kStages], (uint32_t)((gp / kStages) & 1), abort_flag, p.wait);
+  #pragma unroll
+            for (int hs = 0; hs < 2; ++hs) {
+              const float alpha = need[hs] ? ex2(m_used[hs] - m_new[hs]) : 1.f;
+              if (quad_lead && kh == 0) sm->alpha[hd[hs]] = alpha;
+              l[hs] *= alpha;
             }
-          tmem_wait_st();
-          tc_fence_before();
+            if (named_sync_or(1, kSmThreads, !got_o)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+  #pragma unroll 1
+            for (int c = 2 * kh; c < 2 * kh + 2; ++c)  // each key half rescales two of the four chunks
+  #pragma unroll 1
+              for (int half = 0; half < 2; ++half) {
+                uint32_t r[32];
+                const uint32_t ta = tmem + lane_base + kColO + c * kH + half * 32;
+                tmem_ld32(ta, r);
+                tmem_wait_ld();
+  #pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * sm->alpha[half * 32 + i]);
+                tmem_st32(ta, r);
+              }
+            tmem_wait_st();
+            tc_fence_before();
+          }
         }
         // P rows (bf16) of this thread's two heads, in the block's rope atom, which S(g) -- now
         // complete -- was the last to read: key 8j + 2m + {0, 1} of the key half is the 4-byte
@@ -616,12 +646,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         l[hs] += __shfl_xor_sync(0xffffffffu, l[hs], 2);
         if (quad_lead) sm->lpart[kh][hd[hs]] = l[hs];
       }
-      named_sync(1, kSmThreads);
+      if (named_sync_or(1, kSmThreads, failed)) {
+        ok = false;
+        break;
+      }
       if (quad_lead && kh == 0) {
 #pragma unroll
         for (int hs = 0; hs < 2; ++hs) {
           const int hh = hd[hs];
           const float lt = sm->lpart[0][hh] + sm->lpart[1][hh];
+          if (kFixed && !(lt >= 0x1p-64f && lt <= 0x1p64f)) sm->bad = 1;  // (also inf, NaN)
           sm->lsum[hh] = lt > 0.f ? 1.f / lt : 0.f;  // reciprocal row sums
           const float lse_v = lt > 0.f ? (m_used[hs] + log2f(lt)) * kLn2 : -INFINITY;
           if (po) p.part_lse[(int64_t)item * kH + hh] = lse_v;
@@ -661,6 +695,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.o_empty);
       named_sync(1, kSmThreads);  // lsum and lpart are reused by the next row
+      if (kFixed && t == 0) {
+        if (p.redo) p.redo[lrow] = (uint8_t)sm->bad;
+        sm->bad = 0;
+      }
       ++oc;
     }
   }
@@ -784,7 +822,13 @@ cudaError_t launch_sparse_mla_tc(const AttnLaunch& p, cudaStream_t st) {
       return cudaErrorInvalidValue;
   }
   if (q.wait <= 0) q.wait = wait_limit();
-  auto kern = q.wait < kDefaultWaitCycles ? k_sparse_mla_tc<true> : k_sparse_mla_tc<false>;
+  const bool poll = q.wait < kDefaultWaitCycles;
+  // with room for the row marks and no split: the fixed-reference pass, then the running-maximum
+  // pass over the rows it marked (its CTAs skip every other row)
+  const bool fixed = q.redo != nullptr && q.splits <= 1;
+  if (!fixed) q.redo = nullptr;
+  auto kern_exact = poll ? k_sparse_mla_tc<true, false> : k_sparse_mla_tc<false, false>;
+  auto kern = fixed ? (poll ? k_sparse_mla_tc<true, true> : k_sparse_mla_tc<false, true>) : kern_exact;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (e != cudaSuccess) return e;
   const int rows = p.B * p.T * q.layers;
@@ -792,7 +836,18 @@ cudaError_t launch_sparse_mla_tc(const AttnLaunch& p, cudaStream_t st) {
   const int grid = items < num_sms() ? items : num_sms();
   kern<<<grid, kThreads, kSmem, st>>>(qm, q);
   count_launches(1);
-  if ((e = cudaGetLastError()) != cudaSuccess || p.splits <= 1) return e;
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (fixed) {
+    AttnLaunch r = q;
+    r.redo = nullptr;
+    r.gate = q.redo;
+    if ((e = cudaFuncSetAttribute(kern_exact, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem)) != cudaSuccess)
+      return e;
+    kern_exact<<<grid, kThreads, kSmem, st>>>(qm, r);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (p.splits <= 1) return e;
   k_attn_combine<<<dim3((unsigned)rows, kH / kCombHeads), 128, 0, st>>>(q);
   count_launches(1);
   return cudaGetLastError();

@@ -410,12 +410,14 @@ def test_attention_workspace_size_query(lib):
     n = lib.dsa_attn_workspace_size(ctypes.byref(at), 2048)
     # split parts: fp32 outputs [64 x 512] and 64 LSEs per part, a whole number of parts per row
     assert n > 256 and (n - 256) % (32 * 64 * 513 * 4) == 0
-    assert lib.dsa_attn_workspace_size(ctypes.byref(_at(B=1, T=4096)), 2048) == 256   # enough rows
+    # enough rows: no split, one byte per row for the fixed-reference pass's row marks
+    assert lib.dsa_attn_workspace_size(ctypes.byref(_at(B=1, T=4096)), 2048) == 256 + 4096
+    assert lib.dsa_attn_workspace_size(ctypes.byref(_at(B=1, T=4000)), 2048) == 256 + 4096  # rounded to 256
     small = _at(H=8, d_qk=64, d_v=64, k_ld=64, v_ld=64, B=1, T=4)
     assert lib.dsa_attn_workspace_size(ctypes.byref(small), 64) == 256                # mma.sync shape
     assert lib.dsa_attn_workspace_size(None, 64) == 256
-    # a short index row is not worth splitting
-    assert lib.dsa_attn_workspace_size(ctypes.byref(at), 64) == 256
+    # a short index row is not worth splitting: the row marks of its 32 rows
+    assert lib.dsa_attn_workspace_size(ctypes.byref(at), 64) == 256 + 256
 
 
 def test_group_workspace_size_covers_every_layer(lib):

@@ -223,6 +223,30 @@ def test_sparse_attn_matches_oracle(H, DQK, DV, latent, T, S, k):
     assert np.abs(gl[fin] - ref_l[fin]).max() <= ATOL_LSE
 
 
+def test_sparse_attn_rows_outside_fixed_range_recomputed():
+    """Rows whose softmax sums leave the range a fixed reference maximum keeps exact (every
+    base-2 score far below 0, so P underflows to 0, or far above, so P overflows) come out
+    as the running-maximum softmax gives them, beside ordinary rows of the same call."""
+    T, S, k = 160, 900, 256
+    at, idx = _attn_case(64, 576, 512, True, T, S, k, seed=5)
+    q = at["q"].float()
+    q[:, 1::3] *= 40.0                               # base-2 scores past 64, most past 128
+    kv = at["k"].float()
+    kv[:, :, -1] = 8.0                               # a shift common to a row's keys (a
+    q[:, 2::3, :, -1] = -1200.0                      # key-only column); base-2 scores near -577
+    at["q"] = q.to(torch.bfloat16).contiguous()
+    at["k"] = kv.to(torch.bfloat16).contiguous()
+    out, lse = dsa.dsa_sparse_attn(at, idx)
+    ref_o, ref_l = oracle.sparse_attn(at, idx.reshape(T, k).cpu().numpy())
+    got = out.reshape(T, 64, 512).float().cpu().numpy()
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref_o).max() <= ATOL_OUT
+    gl = lse.reshape(T, 64).cpu().numpy()
+    assert np.isfinite(gl).all() and np.isfinite(ref_l).all()
+    # lse grows to ~200 on the scaled rows: the tolerance is relative there
+    assert (np.abs(gl - ref_l) <= ATOL_LSE * np.maximum(1.0, np.abs(ref_l))).all()
+
+
 def test_sparse_attn_bad_index_is_skipped_and_flagged():
     at, idx = _attn_case(64, 576, 512, True, 8, 500, 64)
     bad = idx.clone()
