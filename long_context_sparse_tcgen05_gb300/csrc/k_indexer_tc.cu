@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kt = SEL ? tile_at(i, nsamp, ss->tile) : i;
         const int st = i % C::kStages;
         const uint32_t ph = (i / C::kStages) & 1;
-        if (!mbar_wait<kPoll>(k_empty + st, ph ^ 1, abort_flag, p.wait)) break;
+        if (!mbar_wait<kPoll, true>(k_empty + st, ph ^ 1, abort_flag, p.wait)) break;
         mbar_arrive_expect_tx(k_full + st, C::kKTile);
         for (int kb = 0; kb < C::kKBlocks; ++kb)
           tma_load_3d(k_s + st * C::kKTile + kb * C::kKBlock, &tm_k, k_full + st, kb * C::kAtomElems,
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t k_desc0 = desc_sw128(smem_addr(k_s));
       for (int kt = 0; ok && kt < nproc; ++kt) {  // kt: processing step (the tile itself is the producer's)
         const int buf = kt & (kBufs - 1);
-        if (!(ok = mbar_wait<kPoll>(tm_empty + buf, ((kt / kBufs) & 1) ^ 1, abort_flag, p.wait))) break;
+        if (!(ok = mbar_wait<kPoll, true>(tm_empty + buf, ((kt / kBufs) & 1) ^ 1, abort_flag, p.wait))) break;
         // one tile (N = 256: the block's tokens x heads), or DEC: up to four tiles, one per
         // 64-column group (N = 64: the token's heads)
         const int ntile = DEC ? min(4, ktiles - 4 * kt) : 1;
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; ok && c < ntile; ++c) {
           const int ti = DEC ? 4 * kt + c : kt;  // the tile's place in the producer's stream
           const int st = ti % C::kStages;
-          if (!(ok = mbar_wait<kPoll>(k_full + st, (ti / C::kStages) & 1, abort_flag, p.wait))) break;
+          if (!(ok = mbar_wait<kPoll, true>(k_full + st, (ti / C::kStages) & 1, abort_flag, p.wait))) break;
           tc_fence_after();
           const uint32_t d = tmem + buf * kN + (DEC ? c * 64 : 0);
           const uint64_t kd = k_desc0 + (uint64_t)((st * C::kKTile) >> 4);
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // a wait ran out).  The buffer goes back to the MMA right after the TMEM loads.
       auto score_step = [&](int i, float& v) -> bool {
         const int buf = i & (kBufs - 1);
-        if (!mbar_wait<kPoll>(tm_full + buf, (i / kBufs) & 1, abort_flag, p.wait)) return false;
+        if (!mbar_wait<kPoll, true>(tm_full + buf, (i / kBufs) & 1, abort_flag, p.wait)) return false;
         tc_fence_after();
         const uint32_t col0 = tmem + ((uint32_t)(lq * 32) << 16) + buf * kN + ch * C::kCols;
         uint32_t r[2][32];
@@ -602,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int buf = kt & (kBufs - 1);
         const float sk = sk_next;
         sk_next = key_scale(kt + 1);
-        if (!mbar_wait<kPoll>(tm_full + buf, (kt / kBufs) & 1, abort_flag, p.wait)) break;
+        if (!mbar_wait<kPoll, true>(tm_full + buf, (kt / kBufs) & 1, abort_flag, p.wait)) break;
         tc_fence_after();
         const uint32_t col0 = t_lane + buf * kN + ch * C::kCols;
         // all of this warp's accumulator columns in one go, then the buffer goes back to the MMA

@@ -41,6 +41,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Same, with a suspend-time hint: a thread whose phase is not complete sleeps until it
+// completes or `ns` nanoseconds pass, instead of returning after the short default time and
+// taking issue slots from the warps that share its scheduler on every retry.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kSuspendNs = 1000000;  // 1 ms: a wait's abort word and bound are read this often
 // Non-blocking probe of a phase (never suspends the thread, unlike try_wait).
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -56,8 +70,10 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // another thread has raised *abort, or after `limit` cycles, raising *abort itself.
 // kPoll (the kernels' instantiation for a bound shorter than the default, used to test the
 // timeout path) polls with test_wait, which never suspends: try_wait may sleep until the
-// phase completes and so hide a short bound.  The default instantiation suspends in try_wait.
-template <bool kPoll = false>
+// phase completes and so hide a short bound.  The default instantiation suspends in try_wait
+// for the short default time; kSleep asks it to sleep until the phase completes (the hint
+// above), for warps whose retries would take issue slots from warps doing the work.
+template <bool kPoll = false, bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, long long limit) {
   if constexpr (kPoll) {
     const long long t0 = clock64();
@@ -70,10 +86,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
     return true;
   } else {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto try_once = [&]() { return kSleep ? mbar_try_wait_sleep(bar, parity, kSuspendNs) : mbar_try_wait(bar, parity); };
+    if (try_once()) return true;
     const long long t0 = clock64();
     while (true) {
-      if (mbar_try_wait(bar, parity)) return true;
+      if (try_once()) return true;
       if (*abort) return false;
       if (clock64() - t0 > limit) {
         *abort = 1;
