@@ -447,6 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int key = (kt_lo + kt) * kM + my_key;
         return (FP8 && kt < ktiles && key < p.S) ? __ldg(skg + key) : 1.f;
       };
+      // the same by key, clamped to the last key (a key past the row's end is never kept)
+      auto key_scale_at = [&](int key) -> float { return FP8 ? __ldg(skg + min(key, p.S - 1)) : 1.f; };
       // The head-weighted ReLU sum of this thread's key for the accumulator of step i (false:
       // a wait ran out).  The buffer goes back to the MMA right after the TMEM loads.
       auto score_step = [&](int i, float& v) -> bool {
@@ -518,8 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float thf = theta == 1u ? -INFINITY : __uint_as_float((theta & 0x80000000u) ? (theta & 0x7fffffffu) : ~theta);
         const int nv = (int)nvis[0];
         uint32_t wcnt = 0;  // this warp's candidates so far (the same in every lane)
-        float sk16_next = key_scale16(0);
         int key = kt_lo * kM + my_key;
+        float sk16_next = key_scale_at(key);
         // Batched append: every tile only records each lane's score in shared memory (the
         // token's sample area, no longer read once its threshold is set) and one bit per tile in
         // a lane mask; once per batch of kBatch tiles the warp scans the lanes' counts and each
@@ -531,6 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kBatch = FP8 ? 32 : 8;
         static_assert(sizeof(ss->samp[0]) >= 4 * kBatch * 32 * sizeof(float), "batch exceeds the token's sample area");
         float* vbuf = reinterpret_cast<float*>(ss->samp[ch]) + (e & 3) * kBatch * 32;
+        const uint32_t vb_lane = smem_addr(vbuf + lane);  // this lane's slot of tile 0
         uint32_t mask = 0;  // bit i: this lane's score of the batch's tile i qualifies
         auto flush = [&](int kt0) {  // append the batch starting at tile kt0
           wcnt = sel_flush(mask, vbuf, lane, wcnt, cap4, cand, (kt_lo + kt0) * kM + my_key);
@@ -544,12 +547,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (batched) {
           for (; !dead && kt < ktiles; ++kt, key += kM) {
             const float sk = sk16_next;
-            sk16_next = key_scale16(kt + 1);
+            sk16_next = key_scale_at(key + kM);
             float v;
             if (!score_step(nsamp + kt, v)) break;
             if constexpr (FP8) v *= sq[0] * sk;
             const int tb = kt & (kBatch - 1);
-            vbuf[tb * 32 + lane] = v;
+            asm volatile("st.shared.f32 [%0], %1;\n" ::"r"(vb_lane + (uint32_t)tb * 128u), "f"(v) : "memory");
             mask |= (key < nv && v >= thf ? 1u : 0u) << tb;
             if (tb == kBatch - 1) flush(kt - tb);
           }
@@ -558,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t below = (1u << lane) - 1u;
           for (; !dead && kt < ktiles; ++kt, key += kM) {
             const float sk = sk16_next;
-            sk16_next = key_scale16(kt + 1);
+            sk16_next = key_scale_at(key + kM);
             float v;
             if (!score_step(nsamp + kt, v)) break;
             if constexpr (FP8) v *= sq[0] * sk;
