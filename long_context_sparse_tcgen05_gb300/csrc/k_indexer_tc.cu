@@ -21,14 +21,21 @@
 //     the 4 threads that share the keys leaves each thread one key's sum.
 // Selecting mode (the top-k path that stores no scores): a CTA whose rows are longer than the
 // candidate room first scores an evenly spread sample of its key tiles and records each
-// sampled score's top 16 order-key bits; each token's four warps then set its threshold (the
+// sampled score's top 16 order-key bits; each token's eight warps then set its threshold (the
 // sample's quantile that about `target` of the row's keys should exceed); every tile is then
 // scored in order and each score at or above the threshold is kept as a (score, position) pair
-// in the warp's quarter of the row's candidate list: where over half a score per warp and tile
-// qualifies, a lane parks each tile's score in shared memory and sets a bit, and once per 32
-// tiles (8 for bf16) the warp scans its lanes' counts and each lane appends its own; sparser
-// rows append under a per-tile ballot.  The sampled tiles are scored twice (1/64 of the tiles,
-// at least 16), which keeps the main pass in plain tile order.
+// in the row's candidate list quarter of the warp's TMEM lane quarter: where over half a score
+// per warp and step qualifies, a lane parks each step's score in shared memory and sets a bit,
+// and once per 16 steps (4 for bf16) the warp scans its lanes' counts, claims slots from the
+// quarter's count in shared memory and each lane appends its own; sparser rows append under a
+// per-step ballot.  The sampled tiles are scored twice (1/64 of the tiles, at least 16), which
+// keeps the main pass in plain tile order.  Here the sixteen epilogue warps form two groups of
+// eight that take the steps in turn (group g reads accumulator buffer g), each warp reading
+// two tokens' columns in four 16-lane loads: a warp's fixed work per step (waits, loads,
+// fences, release, key scale, loop) is paid once per two tokens, and every scheduler keeps
+// four warps, two working on each buffer (4,096 rows x 128K keys: 4.19 against 4.33 ms with
+// one token per warp and step; eight warps of two tokens each, with only two warps per
+// scheduler to hide the load latency, took 4.75).
 // One-token mode (one query token per block, as in decode): each step's four products cover
 // four key tiles (N = 64: the token's heads), one per 64-column group, so all sixteen epilogue
 // warps work.
@@ -60,7 +67,8 @@ template <int SAMP>
 struct SelSmem {
   uint16_t samp[4][SAMP * kM];
   uint32_t hist[4][kThBins];
-  uint32_t part[4][4]; // per token: each warp's bin total
+  uint32_t part[4][8]; // per token: each warp's bin total
+  uint32_t claim[4][4];   // per token and TMEM lane quarter: candidate slots claimed
   int mvis[4];         // visible sampled keys per token
   uint32_t lo[4], hi[4];  // smallest and largest sampled key prefix per token
   uint32_t theta[4];   // per-token threshold key
@@ -77,12 +85,14 @@ __host__ __device__ inline int sample_tiles(int ktiles, int most) {
 // Tile processed at step i of a CTA that first scores nsamp evenly spread sample tiles (their
 // tiles listed in `tiles`), then every tile in order.
 __device__ __forceinline__ int tile_at(int i, int nsamp, const int* tiles) { return i < nsamp ? tiles[i] : i - nsamp; }
+// the kTokThreads epilogue threads of token tok (both groups' warps of its column quarter)
+constexpr int kTokThreads = 256;
 __device__ __forceinline__ void token_sync(int tok) {
-  asm volatile("bar.sync %0, %1;\n" ::"r"(1 + tok), "r"(128) : "memory");
+  asm volatile("bar.sync %0, %1;\n" ::"r"(1 + tok), "r"(kTokThreads) : "memory");
 }
 
 // The threshold key of token `tok` from its recorded sample, computed by the token's four
-// epilogue warps (thread tt of 128; every one must call it): the sample's need-th largest
+// epilogue warps (thread tt of kTokThreads; every one must call it): the sample's need-th largest
 // score, need = ceil(target * sampled / visible), so that about `target` of the row's keys reach
 // it, rounded down to a bin of a histogram of the sampled 16-bit key prefixes over the window
 // [smallest, largest] (one pass; a row's scores span a narrow range of prefixes).  A threshold
@@ -100,7 +110,7 @@ __device__ __noinline__ uint32_t token_threshold(SelSmem* ss, int tok, int tt, i
   const int lane = tt & 31, w = tt >> 5;
   token_sync(tok);  // every warp of the token has recorded its sample entries
   uint32_t lo = 0xffffu, hi = 0u;
-  for (int i = tt; i < total; i += 128) {
+  for (int i = tt; i < total; i += kTokThreads) {
     const uint32_t k = sp[i];
     if (k) {
       lo = k < lo ? k : lo;
@@ -117,7 +127,7 @@ __device__ __noinline__ uint32_t token_threshold(SelSmem* ss, int tok, int tt, i
     atomicMax(&ss->hi[tok], hi);
   }
   atomicAdd(&ss->mvis[tok], mv);
-  for (int i = tt; i < kThBins; i += 128) hist[i] = 0;
+  for (int i = tt; i < kThBins; i += kTokThreads) hist[i] = 0;
   token_sync(tok);
   const int m = ss->mvis[tok];
   // (single precision: the threshold is an estimate, any value keeps the result exact, and
@@ -134,15 +144,15 @@ __device__ __noinline__ uint32_t token_threshold(SelSmem* ss, int tok, int tt, i
   const uint32_t wlo = ss->lo[tok], span = ss->hi[tok] - wlo;
   int sh = 0;
   while ((span >> sh) >= (uint32_t)kThBins) ++sh;
-  for (int i = tt; i < total; i += 128) {
+  for (int i = tt; i < total; i += kTokThreads) {
     const uint32_t k = sp[i];
     const uint32_t bin = (k - wlo) >> sh;  // every recorded non-zero prefix lies in the window
     if (k && bin < (uint32_t)kThBins) atomicAdd(&hist[bin], 1u);
   }
   token_sync(tok);
-  // thread tt owns the four bins 4tt .. 4tt+3 counted from the top; a scan over the token's
+  // thread tt owns the kPer bins kPer*tt .. counted from the top; a scan over the token's
   // threads gives the count above them
-  constexpr int kPer = kThBins / 128;
+  constexpr int kPer = kThBins / kTokThreads;
   uint32_t c[kPer], sum = 0;
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
@@ -217,9 +227,12 @@ __device__ __forceinline__ int64_t visible_keys(const IndexerLaunch& p, int t_lo
   return n < 0 ? 0 : (n > p.S ? (int64_t)p.S : n);
 }
 
-// Out-of-line append of one batch (see the selecting main loop): returns the warp's new count.
-__device__ __noinline__ uint32_t sel_flush(uint32_t mask, const float* vbuf, int lane, uint32_t wcnt, int cap4,
-                                           uint2* cand, int key0) {
+// Out-of-line append of one batch (see the selecting main loop): the lanes' qualifying scores
+// (bit t of a lane's mask: its score of the batch's entry t, parked at vbuf[t * 32 + lane], key
+// key0 + t * kstep) go to slots the warp claims from the count it shares with the other group's
+// warp of its list quarter.
+__device__ __noinline__ void sel_flush(uint32_t mask, const float* vbuf, int lane, uint32_t* claim, int cap4,
+                                       uint2* cand, int key0, int kstep) {
   const uint32_t c = __popc(mask);
   uint32_t inc = c;
 #pragma unroll
@@ -228,12 +241,14 @@ __device__ __noinline__ uint32_t sel_flush(uint32_t mask, const float* vbuf, int
     if (lane >= o) inc += y;
   }
   const uint32_t total = __shfl_sync(0xffffffffu, inc, 31);
-  uint32_t slot = wcnt + inc - c;
+  if (total == 0) return;
+  uint32_t base = 0;
+  if (lane == 0) base = atomicAdd(claim, total);
+  uint32_t slot = __shfl_sync(0xffffffffu, base, 0) + inc - c;
   for (uint32_t mm = mask; mm; mm &= mm - 1, ++slot) {
     const int tb = __ffs(mm) - 1;
-    if (slot < (uint32_t)cap4) cand[slot] = make_uint2(__float_as_uint(vbuf[tb * 32 + lane]), (uint32_t)(key0 + tb * kM));
+    if (slot < (uint32_t)cap4) cand[slot] = make_uint2(__float_as_uint(vbuf[tb * 32 + lane]), (uint32_t)(key0 + tb * kstep));
   }
-  return wcnt + total;
 }
 
 template <int HI, int DI, bool FP8, bool kPoll, bool SEL, bool DEC>
@@ -281,6 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // accumulator buffers wait only for the others
   constexpr int kTokWarp = C::kCols / HI > 0 ? C::kCols / HI : 1;
   const int active_ch = DEC ? kEpiWarps / 4 : min(kEpiWarps / 4, (ntok + kTokWarp - 1) / kTokWarp);
+  // selecting mode: the epilogue warps form two groups of eight, group g reading accumulator
+  // buffer g (the steps of its parity); a warp reads the column quarters of a token pair
+  const int active_pairs = (active_ch + 1) / 2;
   const int64_t nmax = visible_keys(p, tl0 + ntok - 1);
   // this CTA's key tiles: [kt_lo, kt_lo + ktiles) of the ceil(S / kM) tiles of the row
   const int tiles_all = (p.S + kM - 1) / kM;
@@ -303,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     for (int i = 0; i < kBufs; ++i) {
       mbar_init(tm_full + i, 1);
-      mbar_init(tm_empty + i, 4 * active_ch);
+      mbar_init(tm_empty + i, SEL ? 4 * active_pairs : 4 * active_ch);  // the warps that read buffer i
     }
     *abort_flag = 0;
     if constexpr (SEL)
@@ -312,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ss->lo[i] = 0xffffu;
         ss->hi[i] = 0u;
         ss->theta[i] = 1u;
+        for (int q = 0; q < 4; ++q) ss->claim[i][q] = 0u;
       }
     fence_barrier_init();
   }
@@ -402,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the products issued are complete before TMEM can be freed, whichever wait ran out
       if (done > 0) mbar_wait_drain(tm_full + ((done - 1) & (kBufs - 1)), ((done - 1) / kBufs) & 1);
     }
-  } else if (((warp - 2) >> 2) < active_ch) {
+  } else if (SEL ? (((warp - 2) >> 2) & 1) < active_pairs : ((warp - 2) >> 2) < active_ch) {
     // ---------------- epilogue ----------------
     const int e = warp - 2;
     const int lq = warp & 3;                 // TMEM lane quarter this warp may read
@@ -449,6 +468,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // the same by key, clamped to the last key (a key past the row's end is never kept)
       auto key_scale_at = [&](int key) -> float { return FP8 ? __ldg(skg + min(key, p.S - 1)) : 1.f; };
+      // Head-weighted ReLU sums over this thread's 16 heads of one token for the two keys of
+      // a 16-lane half a (keys a*16 + {0, 8} + rq), from that half's 32 registers of a 16x256b
+      // load (ra[4j + 2e + {0,1}]: key a*16 + e*8 + rq, heads 8j + 2m + {0,1}), into acc_e0 and
+      // acc_e1 as two partial sums each (even / odd head of each pair).
+      auto accum_half = [&](const uint32_t (&ra)[32], const unsigned long long (&w)[8], unsigned long long& acc_e0,
+                            unsigned long long& acc_e1) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float y0 = __uint_as_float(ra[4 * j]), y1 = __uint_as_float(ra[4 * j + 1]);
+          const float y2 = __uint_as_float(ra[4 * j + 2]), y3 = __uint_as_float(ra[4 * j + 3]);
+          acc_e0 = fma2(pack2(y0 + fabsf(y0), y1 + fabsf(y1)), w[j], acc_e0);
+          acc_e1 = fma2(pack2(y2 + fabsf(y2), y3 + fabsf(y3)), w[j], acc_e1);
+        }
+      };
+      // reduce-scatter of the four keys' sums over the 4 threads of a key group: thread m ends
+      // with key index m's total
+      auto xlane = [&](const unsigned long long (&acc)[4]) -> float {
+        float v4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v4[q] = lo2(acc[q]) + hi2(acc[q]);
+        const bool hi1 = (m & 2) != 0, hi0 = (m & 1) != 0;
+        const float s0 = hi1 ? v4[0] : v4[2], s1 = hi1 ? v4[1] : v4[3];
+        const float k0 = hi1 ? v4[2] : v4[0], k1 = hi1 ? v4[3] : v4[1];
+        const float u0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 2);
+        const float u1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 2);
+        return (hi0 ? u1 : u0) + __shfl_xor_sync(0xffffffffu, hi0 ? u0 : u1, 1);
+      };
       // The head-weighted ReLU sum of this thread's key for the accumulator of step i (false:
       // a wait ran out).  The buffer goes back to the MMA right after the TMEM loads.
       auto score_step = [&](int i, float& v) -> bool {
@@ -463,120 +509,181 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tm_empty + buf);
-        // acc[2a + e]: key a*16 + e*8 + rq, as two partial sums (even / odd head of each pair)
         unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-#pragma unroll
-          for (int a = 0; a < 2; ++a)
-#pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
-              const float y0 = __uint_as_float(r[a][4 * j + 2 * e2]);
-              const float y1 = __uint_as_float(r[a][4 * j + 2 * e2 + 1]);
-              acc[2 * a + e2] = fma2(pack2(y0 + fabsf(y0), y1 + fabsf(y1)), wp[j], acc[2 * a + e2]);
-            }
-        float v4[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) v4[q] = lo2(acc[q]) + hi2(acc[q]);
-        // reduce-scatter over the 4 threads of a key group: thread m ends with key index m
-        const bool hi1 = (m & 2) != 0, hi0 = (m & 1) != 0;
-        const float s0 = hi1 ? v4[0] : v4[2], s1 = hi1 ? v4[1] : v4[3];
-        const float k0 = hi1 ? v4[2] : v4[0], k1 = hi1 ? v4[3] : v4[1];
-        const float u0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 2);
-        const float u1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 2);
-        v = (hi0 ? u1 : u0) + __shfl_xor_sync(0xffffffffu, hi0 ? u0 : u1, 1);
+        accum_half(r[0], wp, acc[0], acc[1]);
+        accum_half(r[1], wp, acc[2], acc[3]);
+        v = xlane(acc);
         return true;
       };
       if constexpr (SEL) {
-        // selecting mode.  Sample steps record the top 16 key bits of each sampled score; the
-        // token's four warps then set its threshold (every visible non-NaN key when the row is
+        // Selecting mode.  Two groups of eight warps take the steps in turn (group g: the steps
+        // of parity g, whose accumulator is buffer g), each warp reading the column quarters of
+        // a token pair, so a warp's fixed work per step (waits, loads, fences, release, key
+        // scale, loop) is paid once per two tokens while each scheduler still holds four
+        // working warps.  Sample steps record the top 16 key bits of each sampled score; each
+        // token's eight warps then set its threshold (every visible non-NaN key when the row is
         // short enough to keep whole); the main steps keep (key, position) of every score that
-        // reaches it, each warp in its own quarter of the row's list with a register count
-        // (ballot + popc: no atomics on the way).
+        // reaches it, in the row's list quarter of the warp's TMEM lane quarter (the two groups'
+        // warps of a quarter claim its slots from a count in shared memory).
+        const int grp = e >> 3;              // this warp's group, and the buffer it reads
+        const int pr = (e >> 2) & 1;         // its token pair
+        const int c0 = 2 * pr;               // the pair's first token (column quarter)
+        const bool has1 = c0 + 1 < ntok;     // the pair's second token exists
+        unsigned long long wq0[8], wq1[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          wq0[j] = pack2(0.5f * w_s[c0 * HI + 8 * j + 2 * m], 0.5f * w_s[c0 * HI + 8 * j + 2 * m + 1]);
+          wq1[j] = pack2(0.5f * w_s[(c0 + 1) * HI + 8 * j + 2 * m], 0.5f * w_s[(c0 + 1) * HI + 8 * j + 2 * m + 1]);
+        }
+        const int nv0 = (int)visible_keys(p, tl0 + c0);
+        const int nv1 = has1 ? (int)visible_keys(p, tl0 + c0 + 1) : 0;
+        const float sq0 = FP8 ? __ldg(p.q_scale + row0 + c0) : 1.f;
+        const float sq1 = (FP8 && has1) ? __ldg(p.q_scale + row0 + c0 + 1) : 1.f;
+        const uint32_t t_pair = tmem + ((uint32_t)(lq * 32) << 16) + grp * kN + c0 * C::kCols;  // in buffer grp
+        // Both tokens' sums for step i (of this group's parity; false: a wait ran out): four
+        // loads of 16 lanes x 64 columns into one set of registers, each summed before the next;
+        // the buffer goes back to the MMA once the last is loaded.
+        auto step2 = [&](int i, float& v0, float& v1) -> bool {
+          if (!mbar_wait<kPoll, true>(tm_full + grp, (i / kBufs) & 1, abort_flag, p.wait)) return false;
+          tc_fence_after();
+          uint32_t r[32];
+          unsigned long long x0[4] = {0ull, 0ull, 0ull, 0ull}, x1[4] = {0ull, 0ull, 0ull, 0ull};
+          tmem_ld_16x256b_x8(t_pair, r);
+          tmem_wait_ld();
+          accum_half(r, wq0, x0[0], x0[1]);
+          tmem_ld_16x256b_x8(t_pair + (16u << 16), r);
+          tmem_wait_ld();
+          accum_half(r, wq0, x0[2], x0[3]);
+          tmem_ld_16x256b_x8(t_pair + C::kCols, r);
+          tmem_wait_ld();
+          accum_half(r, wq1, x1[0], x1[1]);
+          tmem_ld_16x256b_x8(t_pair + C::kCols + (16u << 16), r);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tm_empty + grp);
+          accum_half(r, wq1, x1[2], x1[3]);
+          v0 = xlane(x0);
+          v1 = xlane(x1);
+          return true;
+        };
         bool dead = false;
-        int mv = 0;  // visible sampled keys seen by this thread
-        for (int i = 0; i < nsamp; ++i) {
+        int mv0 = 0, mv1 = 0;  // visible sampled keys seen by this thread, per token
+        for (int i = grp; i < nsamp; i += kBufs) {
           if (dead) continue;  // still meet the threshold barriers below
-          const int kt = ss->tile[i];
-          const float sk = key_scale16(kt);
-          float v;
-          if (!score_step(i, v)) {
+          const int key = (kt_lo + ss->tile[i]) * kM + my_key;
+          const float sk = key_scale_at(key);
+          float v0, v1;
+          if (!step2(i, v0, v1)) {
             dead = true;
             continue;
           }
-          const int key = (kt_lo + kt) * kM + my_key;
-          const bool vis = key < nvis[0];
-          if constexpr (FP8) v *= sq[0] * sk;
-          ss->samp[ch][i * kM + my_key] = vis ? (uint16_t)(score_key(v) >> 16) : (uint16_t)0;
-          mv += vis;
-        }
-        const uint32_t theta =
-            nsamp > 0 ? token_threshold(ss, ch, (e & 3) * 32 + lane, nsamp, mv, nvis[0], p.topk, p.target) : 1u;
-        const int64_t crow = (int64_t)b * p.Tc + tl0 + ch;  // chunk-local row of this token
-        const int cap4 = p.cap / 4;
-        uint2* cand = p.cand + crow * p.cap + lq * cap4;
-        // the threshold as a float: scores v >= thf are exactly those whose order key reaches
-        // theta (-inf keeps every non-NaN score)
-        const float thf = theta == 1u ? -INFINITY : __uint_as_float((theta & 0x80000000u) ? (theta & 0x7fffffffu) : ~theta);
-        const int nv = (int)nvis[0];
-        uint32_t wcnt = 0;  // this warp's candidates so far (the same in every lane)
-        int key = kt_lo * kM + my_key;
-        float sk16_next = key_scale_at(key);
-        // Batched append: every tile only records each lane's score in shared memory (the
-        // token's sample area, no longer read once its threshold is set) and one bit per tile in
-        // a lane mask; once per batch of kBatch tiles the warp scans the lanes' counts and each
-        // lane appends its own qualifying scores.  The list is unordered; the top-k orders its
-        // selection by position.  (On 4,096 rows x 128K keys: this form 4.74 ms with the batch's
-        // append out of line, 4.90 inlined, a per-tile ballot with a divergent store 4.92, a
-        // staging ring in shared memory 5.08, a predicated store every tile 5.24; a count alone,
-        // storing nothing, 4.03.)
-        constexpr int kBatch = FP8 ? 32 : 8;
-        static_assert(sizeof(ss->samp[0]) >= 4 * kBatch * 32 * sizeof(float), "batch exceeds the token's sample area");
-        float* vbuf = reinterpret_cast<float*>(ss->samp[ch]) + (e & 3) * kBatch * 32;
-        const uint32_t vb_lane = smem_addr(vbuf + lane);  // this lane's slot of tile 0
-        uint32_t mask = 0;  // bit i: this lane's score of the batch's tile i qualifies
-        auto flush = [&](int kt0) {  // append the batch starting at tile kt0
-          wcnt = sel_flush(mask, vbuf, lane, wcnt, cap4, cand, (kt_lo + kt0) * kM + my_key);
-          mask = 0;
-        };
-        // Rows whose threshold keeps under half a score per warp and tile (long rows: 0.15 at
-        // 1M keys, 1.2 at 128K) append at once under a ballot instead, which skips most tiles
-        // entirely (1M-key chunk: 39.7 ms that way, 42.5 batched; 128K: 82.2 against 80.3).
-        const bool batched = (float)p.target * 32.f >= 0.5f * (float)(nv > 0 ? nv : 1);
-        int kt = 0;
-        if (batched) {
-          for (; !dead && kt < ktiles; ++kt, key += kM) {
-            const float sk = sk16_next;
-            sk16_next = key_scale_at(key + kM);
-            float v;
-            if (!score_step(nsamp + kt, v)) break;
-            if constexpr (FP8) v *= sq[0] * sk;
-            const int tb = kt & (kBatch - 1);
-            asm volatile("st.shared.f32 [%0], %1;\n" ::"r"(vb_lane + (uint32_t)tb * 128u), "f"(v) : "memory");
-            mask |= (key < nv && v >= thf ? 1u : 0u) << tb;
-            if (tb == kBatch - 1) flush(kt - tb);
+          if constexpr (FP8) {
+            v0 *= sq0 * sk;
+            v1 *= sq1 * sk;
           }
-          if (kt & (kBatch - 1)) flush(kt & ~(kBatch - 1));  // the last, partial batch
-        } else {
-          const uint32_t below = (1u << lane) - 1u;
-          for (; !dead && kt < ktiles; ++kt, key += kM) {
-            const float sk = sk16_next;
-            sk16_next = key_scale_at(key + kM);
-            float v;
-            if (!score_step(nsamp + kt, v)) break;
-            if constexpr (FP8) v *= sq[0] * sk;
-            const bool take = key < nv && v >= thf;
-            const uint32_t bal = __ballot_sync(0xffffffffu, take);
-            if (bal) {
-              if (take) {
-                const uint32_t slot = wcnt + __popc(bal & below);
-                if (slot < (uint32_t)cap4) cand[slot] = make_uint2(__float_as_uint(v), (uint32_t)key);
-              }
-              wcnt += __popc(bal);
+          const bool vis0 = key < nv0, vis1 = key < nv1;
+          ss->samp[c0][i * kM + my_key] = vis0 ? (uint16_t)(score_key(v0) >> 16) : (uint16_t)0;
+          ss->samp[c0 + 1][i * kM + my_key] = vis1 ? (uint16_t)(score_key(v1) >> 16) : (uint16_t)0;
+          mv0 += vis0;
+          mv1 += vis1;
+        }
+        const int tt = (grp * 4 + (e & 3)) * 32 + lane;  // this thread among its tokens' kTokThreads
+        const uint32_t theta0 = nsamp > 0 ? token_threshold(ss, c0, tt, nsamp, mv0, nv0, p.topk, p.target) : 1u;
+        const uint32_t theta1 =
+            (nsamp > 0 && has1) ? token_threshold(ss, c0 + 1, tt, nsamp, mv1, nv1, p.topk, p.target) : 1u;
+        const int64_t crow0 = (int64_t)b * p.Tc + tl0 + c0;  // chunk-local row of the first token
+        const int cap4 = p.cap / 4;
+        uint2* cand0 = p.cand + crow0 * p.cap + lq * cap4;
+        uint2* cand1 = cand0 + p.cap;  // the second token's row (written only when it exists)
+        uint32_t* claim0 = &ss->claim[c0][lq];
+        uint32_t* claim1 = &ss->claim[c0 + 1][lq];
+        // the thresholds as floats: scores v >= thf are exactly those whose order key reaches
+        // theta (-inf keeps every non-NaN score)
+        auto th_float = [](uint32_t th) {
+          return th == 1u ? -INFINITY : __uint_as_float((th & 0x80000000u) ? (th & 0x7fffffffu) : ~th);
+        };
+        const float thf0 = th_float(theta0), thf1 = th_float(theta1);
+        // this group's first main step (parity grp) and its tile's key; a warp steps two tiles on
+        const int i0 = nsamp + ((grp - nsamp) & 1);
+        int key = (kt_lo + i0 - nsamp) * kM + my_key;
+        float sk_next = key_scale_at(key);
+        // Batched append: every step only records each lane's two scores in shared memory (the
+        // tokens' sample areas, no longer read once the thresholds are set) and one bit per step
+        // in a lane mask per token; once per batch of kBatch steps the warp scans the lanes'
+        // counts and each lane appends its own qualifying scores.  The lists are unordered; the
+        // top-k orders its selection by position.
+        constexpr int kBatch = FP8 ? 16 : 4;
+        static_assert(sizeof(ss->samp[0]) >= 8 * kBatch * 32 * sizeof(float), "batch exceeds the token's sample area");
+        const int slice = (grp * 4 + (e & 3)) * kBatch * 32;  // this warp's part of a sample area
+        float* vbuf0 = reinterpret_cast<float*>(ss->samp[c0]) + slice;
+        float* vbuf1 = reinterpret_cast<float*>(ss->samp[c0 + 1]) + slice;
+        const uint32_t vb0 = smem_addr(vbuf0 + lane), vb1 = smem_addr(vbuf1 + lane);  // slots of entry 0
+        // Rows whose threshold keeps under half a score per warp and step (long rows: 0.15 at
+        // 1M keys, 1.2 at 128K) append at once under a ballot instead, which skips most steps
+        // entirely.
+        const bool batched = (float)p.target * 32.f >= 0.5f * (float)(nv0 > 0 ? nv0 : 1);
+        if (batched) {
+          uint32_t mask0 = 0, mask1 = 0;  // bit t: this lane's score of the batch's entry t qualifies
+          int tb = 0, kbase = key;        // entries parked; the key of entry 0
+          auto flush = [&]() {
+            sel_flush(mask0, vbuf0, lane, claim0, cap4, cand0, kbase, kBufs * kM);
+            if (has1) sel_flush(mask1, vbuf1, lane, claim1, cap4, cand1, kbase, kBufs * kM);
+            mask0 = mask1 = 0;
+          };
+          for (int i = i0; !dead && i < nproc; i += kBufs, key += kBufs * kM) {
+            const float sk = sk_next;
+            sk_next = key_scale_at(key + kBufs * kM);
+            float v0, v1;
+            if (!step2(i, v0, v1)) break;
+            if constexpr (FP8) {
+              v0 *= sq0 * sk;
+              v1 *= sq1 * sk;
+            }
+            asm volatile("st.shared.f32 [%0], %1;\n" ::"r"(vb0 + (uint32_t)tb * 128u), "f"(v0) : "memory");
+            asm volatile("st.shared.f32 [%0], %1;\n" ::"r"(vb1 + (uint32_t)tb * 128u), "f"(v1) : "memory");
+            mask0 |= (key < nv0 && v0 >= thf0 ? 1u : 0u) << tb;
+            mask1 |= (key < nv1 && v1 >= thf1 ? 1u : 0u) << tb;
+            if (++tb == kBatch) {
+              flush();
+              tb = 0;
+              kbase = key + kBufs * kM;
             }
           }
+          if (tb) flush();  // the last, partial batch
+        } else {
+          const uint32_t below = (1u << lane) - 1u;
+          auto append = [&](bool take, float v, uint32_t* claim, uint2* cand) {
+            const uint32_t bal = __ballot_sync(0xffffffffu, take);
+            if (bal) {
+              uint32_t base = 0;
+              if (lane == 0) base = atomicAdd(claim, (uint32_t)__popc(bal));
+              base = __shfl_sync(0xffffffffu, base, 0);
+              if (take) {
+                const uint32_t slot = base + __popc(bal & below);
+                if (slot < (uint32_t)cap4) cand[slot] = make_uint2(__float_as_uint(v), (uint32_t)key);
+              }
+            }
+          };
+          for (int i = i0; !dead && i < nproc; i += kBufs, key += kBufs * kM) {
+            const float sk = sk_next;
+            sk_next = key_scale_at(key + kBufs * kM);
+            float v0, v1;
+            if (!step2(i, v0, v1)) break;
+            if constexpr (FP8) {
+              v0 *= sq0 * sk;
+              v1 *= sq1 * sk;
+            }
+            append(key < nv0 && v0 >= thf0, v0, claim0, cand0);
+            append(key < nv1 && v1 >= thf1, v1, claim1, cand1);
+          }
         }
-        if (lane == 0) p.cand_cnt[crow * 4 + lq] = (int32_t)wcnt;
+        // both groups' warps of the pair have claimed their slots; group 0 publishes the counts
+        asm volatile("bar.sync %0, %1;\n" ::"r"(5 + pr), "r"(kTokThreads) : "memory");
+        if (grp == 0 && lane == 0) {
+          p.cand_cnt[crow0 * 4 + lq] = (int32_t)*claim0;
+          if (has1) p.cand_cnt[(crow0 + 1) * 4 + lq] = (int32_t)*claim1;
+        }
       } else {
         // step i holds tile i (the block's tokens in the column groups), or DEC: tiles 4i .. 4i+3,
         // tile 4i + ch in this warp's column group

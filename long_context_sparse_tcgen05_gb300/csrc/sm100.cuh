@@ -89,12 +89,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     auto try_once = [&]() { return kSleep ? mbar_try_wait_sleep(bar, parity, kSuspendNs) : mbar_try_wait(bar, parity); };
     if (try_once()) return true;
     const long long t0 = clock64();
-    while (true) {
+    // a sleeping waiter reads the abort word (a shared-space load) and the bound every 16 tries
+    // only: it wakes often, and each retry takes an issue slot from the warps doing the work
+    const uint32_t abort_s = smem_addr(const_cast<int*>(abort));
+    for (uint32_t n = 1;; ++n) {
       if (try_once()) return true;
-      if (*abort) return false;
-      if (clock64() - t0 > limit) {
-        *abort = 1;
-        return false;
+      if ((n & (kSleep ? 15u : 0u)) == 0) {
+        uint32_t a;
+        asm volatile("ld.volatile.shared.u32 %0, [%1];\n" : "=r"(a) : "r"(abort_s) : "memory");
+        if (a) return false;
+        if (clock64() - t0 > limit) {
+          *abort = 1;
+          return false;
+        }
       }
     }
   }
