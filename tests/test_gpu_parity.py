@@ -555,6 +555,13 @@ def _launches(fn):
     ("e4m3", "int", 2, 1300, 20000, 0),     # two sequences
     ("bf16", "int", 1, 12000, 12000, 0),    # a prefill from 0: rows with n <= k, n <= 4k (all
                                             # their keys kept) and n > 4k (sampled)
+    # a last token block of 1, 2 or 3 tokens: a warp whose pair lacks its second token, a pair
+    # of column quarters without tokens
+    ("e4m3", "int", 1, 2561, 30000, 0),
+    ("bf16", "int", 1, 2562, 24000, 0),
+    ("e4m3", "gauss", 1, 2563, 30000, 1),
+    # 1,094 key tiles: 17 sampled tiles, so the two epilogue groups score unequal shares
+    ("e4m3", "int", 1, 2437, 140000, 0),
 ])
 def test_selecting_path_equals_materialised_path(dtype, values, B, T, S, diag):
     """dsa_topk from indexer operands (the selecting path: an indexer pass keeping the keys
