@@ -67,7 +67,8 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase with the given parity to complete.  Gives up (returning false) when
-// another thread has raised *abort, or after `limit` cycles, raising *abort itself.
+// another thread has raised *abort, or after `limit` cycles, raising *abort itself.  `abort`
+// is a word in the CTA's shared memory (it is read with a shared-space load).
 // kPoll (the kernels' instantiation for a bound shorter than the default, used to test the
 // timeout path) polls with test_wait, which never suspends: try_wait may sleep until the
 // phase completes and so hide a short bound.  The default instantiation suspends in try_wait
