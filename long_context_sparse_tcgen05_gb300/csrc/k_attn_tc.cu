@@ -598,8 +598,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             m_new[hs] = need[hs] ? bm : m_used[hs];
           }
           if (j > 0 && anyr) {
-            // O^T must be complete for the previous block before it is rescaled: the value
-            // product of block g-1 releases its stage
+            // O^T must be complete for the previous block before it is rescaled: the last
+            // chunk of the value product of block g-1 releases its stage's last atoms, and its
+            // commit covers the earlier chunks
             const long long gp = g - 1;
             const bool got_o = mbar_wait<kPoll>(&bar.kv_empty[gp % kStages][kDV / 128 - 1], (uint32_t)((gp / kStages) & 1), abort_flag, p.wait);
   #pragma unroll

@@ -91,7 +91,7 @@ __device__ __forceinline__ void token_sync(int tok) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(1 + tok), "r"(kTokThreads) : "memory");
 }
 
-// The threshold key of token `tok` from its recorded sample, computed by the token's four
+// The threshold key of token `tok` from its recorded sample, computed by the token's eight
 // epilogue warps (thread tt of kTokThreads; every one must call it): the sample's need-th largest
 // score, need = ceil(target * sampled / visible), so that about `target` of the row's keys reach
 // it, rounded down to a bin of a histogram of the sampled 16-bit key prefixes over the window
