@@ -227,13 +227,13 @@ __device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
   return d;
 }
 __device__ __forceinline__ float lo2(unsigned long long v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;\n" : "=f"(lo), "=f"(hi) : "l"(v));
+  float lo;
+  asm("mov.b64 {%0, _}, %1;\n" : "=f"(lo) : "l"(v));
   return lo;
 }
 __device__ __forceinline__ float hi2(unsigned long long v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;\n" : "=f"(lo), "=f"(hi) : "l"(v));
+  float hi;
+  asm("mov.b64 {_, %0}, %1;\n" : "=f"(hi) : "l"(v));
   return hi;
 }
 
