@@ -217,10 +217,22 @@ size_t cand_area(int64_t rows, int cap) {  // key + position lists, four counts,
 }
 bool select_blocks_ok(int64_t B, int64_t Tc) { return B * ((Tc + 3) / 4) >= 4LL * device_sms(); }
 // Query rows per chunk of the selecting path (0: the path does not apply).
+// The rows are split into equal chunks, each a whole number of waves of 4-token blocks (one
+// CTA per block on every SM) where that still fits the candidate room: a chunk's last wave
+// then runs full (128K rows: nine chunks of 14,592 rows, 24 waves each, where chunks of the
+// most rows that fit left a last chunk of 2,048 of the longest rows, 3.4 waves).
 int64_t select_chunk_rows(const dsa_indexer_args* ix, int k) {
   if (ix->H_I != 64 || k < 1 || k > dsa::kCandMaxK) return 0;
-  int64_t rows = (int64_t)(kCandBytes / ((size_t)ix->B * ((size_t)cand_cap(k) * 8 + 17))) / 256 * 256;
-  if (rows > ix->T) rows = ix->T;
+  const int64_t most = (int64_t)(kCandBytes / ((size_t)ix->B * ((size_t)cand_cap(k) * 8 + 17)));
+  int64_t rows = ix->T;
+  if (most < ix->T) {
+    const int64_t n = (ix->T + most - 1) / most;  // chunks
+    const int64_t sms = device_sms();
+    const int64_t unit = 4 * (sms / ix->B > 1 ? sms / ix->B : 1);  // rows of one wave of blocks
+    rows = (ix->T + n - 1) / n;
+    rows = (rows + unit - 1) / unit * unit;
+    if (rows > most) rows = most / unit * unit > 0 ? most / unit * unit : most;
+  }
   if (rows < 1 || !select_blocks_ok(ix->B, rows)) return 0;
   return rows;
 }
