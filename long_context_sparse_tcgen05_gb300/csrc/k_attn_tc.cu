@@ -5,7 +5,7 @@
 // of the same row, so each gathered row feeds both products.
 //
 // Persistent CTAs (one per SM) walk query rows.  For each row:
-//   * warps 0..3 load the query tile with TMA and gather the selected KV rows, 64 per block,
+//   * warps 0..3 gather the selected KV rows, 64 per block,
 //     with 16-byte cp.async copies into two 128-byte-swizzled stages, prefetching the rows of
 //     the block two ahead into L2 (the stage's fill latency, mostly DRAM misses, paces the
 //     ring).  A stage lands in three groups of three atoms (an atom: 64 columns of all 64
@@ -14,7 +14,9 @@
 //     and those arrivals pace the gather: one barrier per atom moved about 17% fewer bytes per
 //     second than one per stage (and 32-row stages, with twice the arrivals per byte, half as
 //     many);
-//   * warp 4 issues  S = Q K^T  (M = 64 heads, N = 64 keys, K = 576) into TMEM, group by group;
+//   * warp 4 loads each row's query tile with TMA, once its own last score product of the
+//     previous row is done with the buffer (so the gathers never wait for it), and issues
+//     S = Q K^T  (M = 64 heads, N = 64 keys, K = 576) into TMEM, group by group;
 //   * warp 5 issues  O^T += V^T P^T  (M = 128 value dims x 4, N = 64 heads, K = 64 keys) -- the
 //     transposed value product keeps the 64 x 512 fp32 accumulator in 256 TMEM columns.  Two
 //     issuing threads let the tensor pipe interleave the two products (a single issuer stalls
@@ -29,7 +31,10 @@
 //     done).  The fixed-reference pass takes a reference maximum of 0 (below); the
 //     running-maximum form raises its maximum only when a block exceeds it by more than 2^8
 //     (the two halves exchange block maxima) and then rescales O^T in TMEM.  At the end they
-//     normalise O, write bf16 O and the natural-log LSE.
+//     normalise O and write bf16 O -- each warp's four 32-head slices of O^T loaded in turn, a
+//     slice landing while the one before it is stored, lane pairs storing two neighbouring
+//     dimensions of a head as one 4-byte word (the epilogue took about 7,450 cycles a row with
+//     one 2-byte store per element, 4,650 this way) -- and the natural-log LSE.
 // One launch may cover several layers that read the same index rows (each with its own
 // queries, latent KV, output and LSE): work items run over layers x rows.  With fewer rows
 // than SMs (decode) a row's blocks are split over several CTAs: each writes its part
@@ -99,7 +104,7 @@ struct Small {
   int nb[2];                       // blocks of the work item in flight (by item parity)
   int j0[2];                       // its first block within the row
   float alpha[kH];
-  float lsum[kH];
+  alignas(16) float lsum[kH];
   float bmax[2][2][kH];           // [block parity][key half][head]: block maxima of the two halves
   float lpart[2][kH];             // [key half][head]: partial row sums at the end of a row
   int any_rescale[2][kSmWarps];   // by block parity, so a fast warp never overwrites an unread flag
@@ -254,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barrier, which fires once its own copies have landed, so the producer never waits for
     // its copies and all stages stay in flight.
     const int64_t row_bytes = p.k_ld * 2;
-    int it = 0, qc = 0;
+    int it = 0;
     long long g = 0;  // global block counter
     bool ok = true;
     const bool vec = ((p.kk | p.idx_st | p.idx_sb) & 3) == 0 && (reinterpret_cast<uintptr_t>(p.idx) & 15u) == 0;
@@ -263,9 +268,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t* irow = attn_idx_row(p, row);
       const int b = row / p.T;
       const uint8_t* kvb = static_cast<const uint8_t*>(layer_pick(p.lk, layer)) + (int64_t)b * p.k_sb * 2;  // its latent rows
-      // blocks = 1 + (last entry other than -1) / kNB; all loads of the scan issued together
+      // blocks = 1 + (last entry other than -1) / kNB: the last 32 entries first (a full row
+      // ends in a valid one), else a scan of the row with all its loads issued together
       int last = -1;
-      if (vec) {
+      {
+        const int e = p.kk - 1 - lane;
+        const int v = e >= 0 ? __ldg(irow + e) : -1;
+        const uint32_t bal = __ballot_sync(0xffffffffu, v != -1);
+        if (bal) last = p.kk - __ffs(bal);  // the lowest such lane holds the highest entry
+      }
+      if (last >= 0) {
+      } else if (vec) {
         const int n4 = p.kk >> 2;
         for (int c0 = 0; c0 < n4; c0 += 32 * 8) {
           int4 v[8];
@@ -311,18 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           (int64_t)(nr % p.T) * p.q_st,
                       kQBytes);
         }
-        if (lane == 0) {
-          ok = mbar_wait<kPoll>(&bar.q_empty, (qc & 1) ^ 1, abort_flag, p.wait);
-          if (ok) {
-            mbar_arrive_expect_tx(&bar.q_full, kQBytes);
-            for (int a = 0; a < kAtoms; ++a)
-              tma_load_4d(q_s + a * kAtomQ, &qm.m[layer], &bar.q_full, a * 64, 0, row % p.T, row / p.T);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      if (!ok) break;  // no Q load was issued for this row
-      ++qc;
       for (int j = 0; ok && j < nb; ++j, ++g) {
         const int st = (int)(g % kStages);
         // ids of this warp's 16 rows
@@ -378,14 +380,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
-    // the last query tile issued has landed before the CTA can exit (whichever wait ran out)
-    if (warp == 0 && lane == 0 && qc > 0) mbar_wait_drain(&bar.q_full, (uint32_t)((qc - 1) & 1));
   } else if (warp == kMmaWarp) {
     // ================= score product issuer (one thread) =================
     const uint32_t id_s = idesc_mn(1, 1, kH, kNB);  // S: M=64 heads, N=32 keys
     const uint64_t q_desc0 = desc_sw128(smem_addr(q_s));
     const uint64_t kv_desc0 = desc_sw128(smem_addr(kv_s));
-    int it = 0, qc = 0;
+    int it = 0, qc = 0, qi = 0;  // rows begun; query tiles loaded
     long long g = 0;
     bool ok = true;
     for (int item = next_item(blockIdx.x); ok && item < items; item = next_item(item + (int)gridDim.x), ++it) {
@@ -400,7 +400,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (nb == 0) continue;
       if (lane == 0) {
-        ok = mbar_wait<kPoll>(&bar.q_full, qc & 1, abort_flag, p.wait);
+        // this row's query tile, once the previous row's last score product (issued by this
+        // thread) is done with the buffer: the gathers never wait for it
+        ok = mbar_wait<kPoll>(&bar.q_empty, (qc & 1) ^ 1, abort_flag, p.wait);
+        if (ok) {
+          const int lrow = item / splits, layer = lrow / rows1, row = lrow % rows1;
+          mbar_arrive_expect_tx(&bar.q_full, kQBytes);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_4d(q_s + a * kAtomQ, &qm.m[layer], &bar.q_full, a * 64, 0, row % p.T, row / p.T);
+          ++qi;
+          ok = mbar_wait<kPoll>(&bar.q_full, qc & 1, abort_flag, p.wait);
+        }
         for (int j = 0; ok && j < nb; ++j) {
           const long long gs = g + j;
           const int st = (int)(gs % kStages), sb = (int)(gs & 1);
@@ -432,6 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {  // wait for this thread's own products before TMEM can be freed
       mma_commit(&bar.drain[0]);
       mbar_wait_drain(&bar.drain[0], 0);
+      // and for the last query tile it loaded (whichever wait ran out)
+      if (qi > 0) mbar_wait_drain(&bar.q_full, (uint32_t)((qi - 1) & 1));
     }
   } else if (warp == kPvWarp) {
     // ================= value product issuer (one thread) =================
@@ -684,28 +696,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-#pragma unroll 1
-      for (int c = 2 * kh; c < 2 * kh + 2; ++c) {
-        const int d = c * 128 + q4 * 32 + lane;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_base + kColO + c * kH + half * 32, r);
-          tmem_wait_ld();
-          if (po) {
+      // this warp's four slices of O^T (dimension chunks 2kh, 2kh + 1; heads 0-31, 32-63), each
+      // loaded while the previous one is stored; the reciprocal row sums are read four at a time
+      {
+        uint32_t ra[32], rb[32];
+        auto slice = [&](int n) {  // TMEM address of slice n
+          return tmem + lane_base + kColO + (uint32_t)((2 * kh + (n >> 1)) * kH + (n & 1) * 32);
+        };
+        auto store = [&](const uint32_t (&r)[32], int n) {
+          const int d = (2 * kh + (n >> 1)) * 128 + q4 * 32 + lane, h0 = (n & 1) * 32;
+          const float4* ls4 = reinterpret_cast<const float4*>(sm->lsum + h0);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int hh = half * 32 + i;
-              po[(int64_t)hh * kDV + d] = __uint_as_float(r[i]) * sm->lsum[hh];
-            }
-          } else {
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 L = ls4[i4];
+            const float lv[4] = {L.x, L.y, L.z, L.w};
+            if (po) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int hh = half * 32 + i;
-              og[(int64_t)hh * kDV + d] = __float2bfloat16_rn(__uint_as_float(r[i]) * sm->lsum[hh]);
+              for (int u = 0; u < 4; ++u)
+                po[(int64_t)(h0 + 4 * i4 + u) * kDV + d] = __uint_as_float(r[4 * i4 + u]) * lv[u];
+            } else {
+              // lane pairs write two neighbouring dimensions of one head as one 4-byte word:
+              // of heads (i, i + 1) the even lane keeps i and takes its partner's value of i,
+              // the odd lane keeps i + 1 and takes its partner's value of i + 1
+              const bool odd = (lane & 1) != 0;
+#pragma unroll
+              for (int u = 0; u < 4; u += 2) {
+                const int i = 4 * i4 + u;
+                const float a = __uint_as_float(r[i]) * lv[u], bq = __uint_as_float(r[i + 1]) * lv[u + 1];
+                const float other = __shfl_xor_sync(0xffffffffu, odd ? a : bq, 1);
+                const __nv_bfloat162 w = odd ? __floats2bfloat162_rn(other, bq) : __floats2bfloat162_rn(a, other);
+                *reinterpret_cast<__nv_bfloat162*>(og + (int64_t)(h0 + i + (odd ? 1 : 0)) * kDV + (d & ~1)) = w;
+              }
             }
           }
-        }
+        };
+        tmem_ld32(slice(0), ra);
+        tmem_wait_ld();
+        tmem_ld32(slice(1), rb);
+        store(ra, 0);
+        tmem_wait_ld();
+        tmem_ld32(slice(2), ra);
+        store(rb, 1);
+        tmem_wait_ld();
+        tmem_ld32(slice(3), rb);
+        store(ra, 2);
+        tmem_wait_ld();
+        store(rb, 3);
       }
       tc_fence_before();
       __syncwarp();
