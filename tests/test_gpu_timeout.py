@@ -45,6 +45,10 @@ def test_waits_that_run_out_raise_the_flag_and_leave_the_gpu_usable():
     # traffic that some copy is still in flight when its consumer first looks
     sc = synth.scores_input(4096, 131072, DEV, "int", lo=-50, hi=50)
     at = synth.attn_inputs(wl.replace(T=160), 0, DEV)
+    # the selecting path (scores never stored): 640 token blocks of rows longer than their
+    # candidate room, so the indexer samples, sets thresholds and appends candidates
+    wl_sel = wl.replace(T=2560, q_pos0=8192 - 2560)
+    ix_sel = synth.indexer_inputs(wl_sel, 0, DEV)
     g = torch.Generator(device=DEV).manual_seed(5)
     idx = torch.sort(torch.randint(0, wl.S, (1, 160, wl.k), generator=g, device=DEV, dtype=torch.int32), -1).values
     try:
@@ -56,6 +60,7 @@ def test_waits_that_run_out_raise_the_flag_and_leave_the_gpu_usable():
     assert flags & dsa.FLAG_TIMEOUT, hex(flags)
     # each kernel on its own raises the flag too
     for name, call in (("indexer + top-k", lambda: dsa.dsa_topk(wl.k, ix=ix)),
+                       ("selecting indexer + top-k", lambda: dsa.dsa_topk(wl.k, ix=ix_sel)),
                        ("top-k over scores", lambda: dsa.dsa_topk(wl.k, scores=sc[None], q_pos0=131072 - 4096)),
                        ("attention", lambda: dsa.dsa_sparse_attn(at, idx))):
         raised = False
@@ -75,6 +80,12 @@ def test_waits_that_run_out_raise_the_flag_and_leave_the_gpu_usable():
     rows = [0, 13, 63]
     ref = oracle.indexer_topk(ix, wl.k, rows)
     assert np.array_equal(a.reshape(-1, wl.k)[rows].cpu().numpy(), ref)
+    sel = dsa.dsa_topk(wl.k, ix=ix_sel)
+    torch.cuda.synchronize()
+    assert dsa.read_device_flags() == 0
+    rows_sel = [0, 1283, 2559]
+    ref_sel = oracle.indexer_topk(ix_sel, wl.k, rows_sel)
+    assert np.array_equal(sel.reshape(-1, wl.k)[rows_sel].cpu().numpy(), ref_sel)
     some = [0, 1777, 4095]
     ref_b = oracle.topk_rows(sc[some].double().cpu().numpy(), np.array(some) + 131072 - 4096, wl.k)
     assert np.array_equal(b[0][some].cpu().numpy(), ref_b)

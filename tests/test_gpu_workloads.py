@@ -226,9 +226,10 @@ def test_indexer_topk_bit_exact_at_full_size_on_integer_operands(name, dtype, n_
     torch.cuda.synchronize()
     assert dsa.read_device_flags() == 0
     rows = synth.sample_rows(wl, n_rows) if wl.B == 1 else list(range(wl.B))
-    # row chunks of the 128K workspace hold 8,192 rows: include rows on both sides of a seam
+    # rows on both sides of seams: the selecting path's row chunks (14,592 rows at 128K on a
+    # 152-SM part) and the score buffer's 8,192-row chunks
     if name == "prefill_128k":
-        rows = sorted(set(rows) | {8191, 8192, 65535, 65536})
+        rows = sorted(set(rows) | {8191, 8192, 14591, 14592, 65535, 65536, 116735, 116736})
     got = idx.reshape(wl.B * wl.T, wl.k)[torch.as_tensor(rows, device=DEV)].cpu().numpy()
     ref = oracle.indexer_topk(ix, wl.k, rows)
     assert np.array_equal(got, ref)
