@@ -164,7 +164,7 @@ typedef struct {
  *   with fewer query rows than half the SMs, room for each row's split parts (fp32 outputs
  *   and LSEs of up to 8 parts); with more rows, one byte per row (rounded up to 256) that
  *   marks the rows a fixed-reference softmax pass leaves to a running-maximum recompute
- *   (without it every row takes the running-maximum softmax; same results either way).
+ *   (without it every row takes the running-maximum softmax; the two agree up to rounding).
  * indexshare_group_workspace_size: indexshare_group_forward (seqs NULL) or
  *   indexshare_group_forward_varlen (seqs given) -- the largest of the above over the
  *   group's layers ('F' layers: indexer and attention; 'S' layers: attention), including the
