@@ -564,17 +564,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vm = __ballot_sync(0xffffffffu, id >= 0 && id < p.S);
         float s[2][kHalf / 4];
         float bmax[2] = {-INFINITY, -INFINITY};
+        if (vm == 0xffffffffu) {  // every key of the half valid (warp-uniform): no mask
 #pragma unroll
-        for (int jj = 0; jj < kHalf / 8; ++jj)
+          for (int jj = 0; jj < kHalf / 8; ++jj)
 #pragma unroll
-          for (int hs = 0; hs < 2; ++hs)
+            for (int hs = 0; hs < 2; ++hs)
 #pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
-              const float x = __uint_as_float(sr[4 * jj + 2 * hs + e2]) * sl2;
-              const float y = ((vm >> (8 * jj + 2 * m + e2)) & 1u) ? x : -INFINITY;
-              s[hs][2 * jj + e2] = y;
-              bmax[hs] = fmaxf(bmax[hs], y);
-            }
+              for (int e2 = 0; e2 < 2; ++e2) {
+                const float x = __uint_as_float(sr[4 * jj + 2 * hs + e2]) * sl2;
+                s[hs][2 * jj + e2] = x;
+                bmax[hs] = fmaxf(bmax[hs], x);
+              }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < kHalf / 8; ++jj)
+#pragma unroll
+            for (int hs = 0; hs < 2; ++hs)
+#pragma unroll
+              for (int e2 = 0; e2 < 2; ++e2) {
+                const float x = __uint_as_float(sr[4 * jj + 2 * hs + e2]) * sl2;
+                const float y = ((vm >> (8 * jj + 2 * m + e2)) & 1u) ? x : -INFINITY;
+                s[hs][2 * jj + e2] = y;
+                bmax[hs] = fmaxf(bmax[hs], y);
+              }
+        }
         float m_new[2];
         if constexpr (kFixed) {
           if (!got_s) {
