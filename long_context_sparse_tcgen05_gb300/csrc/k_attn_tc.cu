@@ -540,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       float m_used[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+      const uint32_t kv_base_s = smem_addr(kv_s);  // the stages' shared-space address
       bool failed = false;  // kFixed: a wait ran out; the warp goes to the row's end barrier
       for (int j = 0; ok && j < nb; ++j, ++g) {
         const int sb = (int)(g & 1);
@@ -659,20 +660,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // complete -- was the last to read: key 8j + 2m + {0, 1} of the key half is the 4-byte
         // word m of 16-byte chunk (kHalf / 8) kh + j of the head's 2 kNB-byte row, whose chunks
         // the swizzle permutes (128-byte rows: by head mod 8; 64-byte rows: by (head / 2) mod 4)
-        uint8_t* patom = kv_s + (size_t)(g % kStages) * kKVBytes + kPAtom * kAtomKV;
+        const uint32_t patom = kv_base_s + (uint32_t)(g % kStages) * kKVBytes + kPAtom * kAtomKV;
 #pragma unroll
         for (int hs = 0; hs < 2; ++hs) {
           m_used[hs] = m_new[hs];
           const float mu = m_used[hs] == -INFINITY ? 0.f : m_used[hs];
-          uint8_t* prow = patom + hd[hs] * (2 * kNB) + m * 4;
+          const uint32_t prow = patom + hd[hs] * (2 * kNB) + m * 4;
           const int perm = kNB == 64 ? (hd[hs] & 7) : ((hd[hs] >> 1) & 3);
 #pragma unroll
           for (int jj = 0; jj < kHalf / 8; ++jj) {
             const float a = ex2(s[hs][2 * jj] - mu), bq = ex2(s[hs][2 * jj + 1] - mu);
             l[hs] += a + bq;
             __nv_bfloat162 v2 = __floats2bfloat162_rn(a, bq);
-            *reinterpret_cast<uint32_t*>(prow + (((kh * (kHalf / 8) + jj) ^ perm) << 4)) =
-                *reinterpret_cast<uint32_t*>(&v2);
+            asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(prow + ((uint32_t)((kh * (kHalf / 8) + jj) ^ perm) << 4)),
+                         "r"(*reinterpret_cast<uint32_t*>(&v2))
+                         : "memory");
           }
         }
         fence_async_smem();
