@@ -703,3 +703,40 @@ def test_group_batches_decode_layers_into_one_attention_launch(schedule):
         batches += (j - i + 7) // 8
         i = j
     assert launches <= runs * 3 + batches * 2
+
+
+def test_group_batched_layers_recompute_the_rows_each_layer_marks():
+    """Four layers of 40 decode sequences attend in one launch (a layer alone would split its
+    rows; together they fill the GPU), so the fixed-reference softmax runs over layers x rows
+    and marks rows by their flat index.  Layer 2's queries are scaled up (scores past 2^7 in
+    base 2) and layer 3's scores all sit near -577 (base 2): both layers' rows leave the range
+    the fixed reference keeps exact and are recomputed, while layers 0 and 1 keep the fixed
+    pass.  Every layer must match the oracle."""
+    # k = 512: one layer's 40 rows would split (two 256-key parts); four layers' 160 do not
+    wl = synth.WORKLOADS["decode_b32_200k"].replace(B=40, S=3000, q_pos0=3000, k=512)
+    layers = synth.group_inputs(wl, 4, DEV, with_indexer=True)
+    at2 = dict(layers[2]["at"])
+    at2["q"] = (at2["q"].float() * 40.0).to(torch.bfloat16).contiguous()
+    layers[2]["at"] = at2
+    at3 = dict(layers[3]["at"])
+    q3, k3 = at3["q"].float(), at3["k"].float()
+    k3[:, :, -1] = 8.0
+    q3[..., -1] = -1200.0
+    at3["q"], at3["k"] = q3.to(torch.bfloat16).contiguous(), k3.to(torch.bfloat16).contiguous()
+    layers[3]["at"] = at3
+    dsa.trace_enable(64)
+    outs, lses, bufs = dsa.indexshare_group_forward(layers, "FSSS", wl.k)
+    torch.cuda.synchronize()
+    kinds = [kind for kind, _ in dsa.trace_read()]
+    dsa.trace_disable()
+    assert kinds.count("attention") == 1, kinds  # the four layers in one attention call
+    assert dsa.read_device_flags() == 0
+    idx = bufs[0].reshape(wl.B, wl.k).cpu().numpy()
+    for l in range(4):
+        ref_o, ref_l = oracle.sparse_attn(layers[l]["at"], idx)
+        got = outs[l].reshape(wl.B, wl.H, wl.DV).float().cpu().numpy()
+        assert np.isfinite(got).all()
+        assert np.abs(got - ref_o).max() <= ATOL_OUT, l
+        gl = lses[l].reshape(wl.B, wl.H).cpu().numpy()
+        assert np.isfinite(gl).all()
+        assert (np.abs(gl - ref_l) <= ATOL_LSE * np.maximum(1.0, np.abs(ref_l))).all(), l
